@@ -1,0 +1,251 @@
+"""Pins of the CPU oracle to facts other than itself.
+
+* Fixed depth with a depth-indexed cache is an unrolled pre-norm transformer of
+  n_core * r_max layers (each loop step uses its own cache slots; §4.2 of the
+  paper), so the oracle's fixed-depth tokens and logits must equal a full-
+  sequence, cache-free causal forward computed with torch's own attention.
+* With early exits, the oracle must equal a recursive, cache-free
+  recomputation that applies the depth-clamp reading directly
+  (tests/brute_force.py), including prelude/coda layers and the adapter.
+* Gate extremes: an always-positive gate exits every token at r_min (§4.3,
+  lookahead: r_min = 2), an always-negative gate reproduces fixed depth.
+* bf16 rounding equals torch's float32 -> bfloat16 conversion.
+* RoPE scores depend only on the relative position.
+* Executed FLOPs equal the closed form used by §5 eq. (1).
+* Exit gaps of the depth-indexed cache are never written.
+"""
+
+import dataclasses
+import math
+
+import numpy as np
+import pytest
+import torch
+import torch.nn.functional as F
+
+from synth import make_requests, make_weights, model_shape, workload
+from oracle.model import OracleModel, decode_sequence, _bf16
+from tests.brute_force import BruteForceLM
+
+
+def micro(**kw):
+    base = dict(name="micro", vocab=64, d_model=32, n_heads=4, head_dim=8, ffn=48,
+                n_prelude=0, n_core=2, n_coda=0, r_max=3, r_min=2,
+                has_adapter=False, dtype="fp32", init_std=0.2, gate_bias=0.0)
+    base.update(kw)
+    return dataclasses.replace(model_shape("tiny"), **base)
+
+
+def prompt_for(shape, n, seed=7):
+    rng = np.random.default_rng(seed)
+    return rng.integers(0, shape.vocab, n).astype(np.int32)
+
+
+# ---------------------------------------------------------------------------
+# fixed depth == unrolled textbook transformer (torch, float64, no cache)
+# ---------------------------------------------------------------------------
+
+def torch_unrolled_logits(shape, weights, tokens):
+    w = {k: torch.from_numpy(v.astype(np.float64)) for k, v in weights.items()}
+    T = len(tokens)
+    d, H, hd = shape.d_model, shape.n_heads, shape.head_dim
+    x = w["embed"][torch.as_tensor(tokens, dtype=torch.long)]
+    inv = shape.rope_theta ** (-torch.arange(0, hd, 2, dtype=torch.float64) / hd)
+    ang = torch.arange(T, dtype=torch.float64)[:, None] * inv[None, :]
+    cos, sin = torch.cos(ang), torch.sin(ang)
+
+    def rope(t):  # [H, T, hd]
+        a, b = t[..., : hd // 2], t[..., hd // 2:]
+        return torch.cat([a * cos - b * sin, b * cos + a * sin], dim=-1)
+
+    def rms(t, g):
+        return F.rms_norm(t, (d,), g, eps=shape.rms_eps)
+
+    for _ in range(shape.r_max):
+        for l in range(shape.n_core):
+            p = f"core.{l}."
+            u = rms(x, w[p + "attn_norm"])
+            q, k, v = F.linear(u, w[p + "wqkv"]).split(d, dim=-1)
+            q = rope(q.view(T, H, hd).transpose(0, 1))
+            k = rope(k.view(T, H, hd).transpose(0, 1))
+            v = v.view(T, H, hd).transpose(0, 1)
+            o = F.scaled_dot_product_attention(q, k, v, is_causal=True)
+            x = x + F.linear(o.transpose(0, 1).reshape(T, d), w[p + "wo"])
+            u = rms(x, w[p + "mlp_norm"])
+            x = x + F.linear(F.silu(F.linear(u, w[p + "wg"])) * F.linear(u, w[p + "wu"]), w[p + "wd"])
+    return F.linear(rms(x, w["final_norm"]), w["lm_head"]).numpy()
+
+
+@pytest.mark.parametrize("r_max", [1, 3])
+def test_fixed_depth_is_unrolled_transformer(r_max):
+    shape = micro(r_max=r_max, r_min=min(2, r_max))
+    wts = make_weights(shape)
+    prompt = prompt_for(shape, 9)
+    gen = 6
+    tr = decode_sequence(OracleModel(shape, wts), prompt, gen, mode="fixed", keep_logits=gen)
+    seq = np.concatenate([prompt, np.array(tr.tokens[:-1], dtype=np.int32)])
+    ref = torch_unrolled_logits(shape, wts, seq)
+    P = len(prompt)
+    for t in range(gen):
+        np.testing.assert_allclose(tr.logits[t], ref[P - 1 + t], atol=2e-5, rtol=0)
+        assert tr.tokens[t] == int(np.argmax(ref[P - 1 + t]))
+    assert tr.exit_depths == [r_max] * (gen - 1)
+
+
+def test_tiny_config_fixed_depth_is_unrolled_transformer():
+    shape = model_shape("tiny")
+    wts = make_weights(shape)
+    req = make_requests(workload("tiny"), shape.vocab)[3]
+    gen = 5
+    tr = decode_sequence(OracleModel(shape, wts), req["prompt"], gen, mode="fixed", keep_logits=gen)
+    seq = np.concatenate([req["prompt"], np.array(tr.tokens[:-1], dtype=np.int32)])
+    ref = torch_unrolled_logits(shape, wts, seq)
+    P = len(req["prompt"])
+    for t in range(gen):
+        np.testing.assert_allclose(tr.logits[t], ref[P - 1 + t], atol=2e-5, rtol=0)
+
+
+# ---------------------------------------------------------------------------
+# early exit + depth clamp == cache-free recursion
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("variant", ["looped", "huginn_like"])
+def test_adaptive_matches_brute_force(variant):
+    if variant == "looped":
+        shape = micro(r_max=4)
+    else:
+        shape = micro(r_max=4, n_prelude=1, n_core=1, n_coda=1, has_adapter=True)
+    wts = make_weights(shape)
+    prompt = prompt_for(shape, 5, seed=11)
+    gen = 7
+    rng = np.random.default_rng(5)
+    depths = rng.integers(2, shape.r_max + 1, gen - 1).astype(np.int8)
+    depths[1] = 2
+    depths[2] = shape.r_max
+    tr = decode_sequence(OracleModel(shape, wts), prompt, gen, mode="adaptive",
+                         force_exit=depths, keep_logits=gen)
+    assert tr.exit_depths == [int(x) for x in depths]
+    bf = BruteForceLM(shape, wts, prompt, gen, lambda t: int(depths[t - 1]))
+    toks, lg = bf.run()
+    assert tr.tokens == toks
+    for t in range(gen):
+        np.testing.assert_allclose(tr.logits[t], lg[t], atol=2e-5, rtol=0)
+
+
+def test_brute_force_detects_wrong_clamp():
+    """Sensitivity: reading exited tokens at the current depth (no clamp) differs."""
+    shape = micro(r_max=4)
+    wts = make_weights(shape)
+    prompt = prompt_for(shape, 5, seed=11)
+    gen = 5
+    depths = np.array([2, 2, 4, 3], dtype=np.int8)
+    tr = decode_sequence(OracleModel(shape, wts), prompt, gen, force_exit=depths, keep_logits=gen)
+    # A schedule that pretends every earlier token ran to full depth reads other states.
+    bf = BruteForceLM(shape, wts, prompt, gen, lambda t: int(depths[t - 1]))
+    bf.exit_depth = lambda i: shape.r_max if i < bf.P else int(depths[i - bf.P])
+    honest = bf.run()[1]
+    wrong = BruteForceLM(shape, wts, prompt, gen, lambda t: int(depths[t - 1]))
+    wrong.exit_depth = lambda i: shape.r_max
+    wrong_lg = wrong.run()[1]
+    np.testing.assert_allclose(tr.logits[-1], honest[-1], atol=2e-5, rtol=0)
+    assert np.max(np.abs(tr.logits[-1] - wrong_lg[-1])) > 1e-3
+
+
+# ---------------------------------------------------------------------------
+# gate special cases, rounding, RoPE, FLOPs, gaps
+# ---------------------------------------------------------------------------
+
+def test_gate_extremes():
+    shape = micro(r_max=5)
+    prompt = prompt_for(shape, 6)
+    gen = 6
+    wts = make_weights(shape)
+    hi = decode_sequence(OracleModel(dataclasses.replace(shape, gate_bias=100.0), wts), prompt, gen)
+    assert hi.exit_depths == [2] * (gen - 1)
+    hi3 = decode_sequence(OracleModel(dataclasses.replace(shape, gate_bias=100.0, r_min=3), wts),
+                          prompt, gen)
+    assert hi3.exit_depths == [3] * (gen - 1)
+    lo = decode_sequence(OracleModel(dataclasses.replace(shape, gate_bias=-100.0), wts), prompt, gen,
+                         keep_logits=gen)
+    fx = decode_sequence(OracleModel(shape, wts), prompt, gen, mode="fixed", keep_logits=gen)
+    assert lo.exit_depths == [5] * (gen - 1)
+    assert lo.tokens == fx.tokens
+    for a, b in zip(lo.logits, fx.logits):
+        np.testing.assert_array_equal(a, b)
+
+
+def test_gate_threshold_is_strict_and_in_logit_space():
+    shape = micro(r_max=4, gate_q=0.5)
+    om = OracleModel(shape, make_weights(shape))
+    assert om.theta == 0.0
+    assert OracleModel(micro(gate_q=0.2), make_weights(shape)).theta == pytest.approx(math.log(0.25))
+
+
+def test_bf16_rounding_matches_torch():
+    rng = np.random.default_rng(0)
+    x = np.concatenate([rng.normal(0, 1, 10000), rng.normal(0, 1e-3, 1000),
+                        # exact ties between two bf16 neighbours
+                        (np.arange(1, 200) * 2 + 1).astype(np.float64) * 2.0 ** -8 + 1.0])
+    x32 = x.astype(np.float32)
+    ref = torch.from_numpy(x32).to(torch.bfloat16).to(torch.float32).numpy()
+    np.testing.assert_array_equal(_bf16(x32.astype(np.float64)).astype(np.float32), ref)
+
+
+def test_rope_is_relative():
+    shape = micro()
+    om = OracleModel(shape, make_weights(shape))
+    rng = np.random.default_rng(1)
+    q = rng.normal(size=(1, shape.n_heads, shape.head_dim))
+    k = rng.normal(size=(1, shape.n_heads, shape.head_dim))
+    s1 = np.einsum("nhk,nhk->nh", om.rope(q, [9]), om.rope(k, [4]))
+    s2 = np.einsum("nhk,nhk->nh", om.rope(q, [105]), om.rope(k, [100]))
+    np.testing.assert_allclose(s1, s2, atol=1e-9)
+    np.testing.assert_allclose(np.linalg.norm(om.rope(q, [77])), np.linalg.norm(q), atol=1e-12)
+
+
+@pytest.mark.parametrize("variant", ["looped", "huginn_like"])
+def test_decode_flops_match_closed_form(variant):
+    if variant == "looped":
+        shape = micro(r_max=4)
+    else:
+        shape = micro(r_max=4, n_prelude=1, n_core=1, n_coda=1, has_adapter=True)
+    wts = make_weights(shape)
+    prompt = prompt_for(shape, 5)
+    gen = 4
+    depths = np.array([2, 4, 3], dtype=np.int8)
+    om = OracleModel(shape, wts)
+    # prefill alone
+    decode_sequence(om, prompt, 1)
+    pre = dataclasses.asdict(om.flops)
+    om2 = OracleModel(shape, wts)
+    decode_sequence(om2, prompt, gen, force_exit=depths)
+    got = {k: v - pre[k] for k, v in dataclasses.asdict(om2.flops).items()}
+    d, f, V = shape.d_model, shape.ffn, shape.vocab
+    layer = 2 * (4 * d * d + 3 * d * f)           # qkv, o, gate/up, down
+    adapter = 2 * (2 * d * d) if shape.has_adapter else 0
+    P = len(prompt)
+    ctx = [P + t for t in range(1, gen)]           # keys seen by decode forward t
+    assert got["core"] == sum(int(e) * (shape.n_core * layer + adapter) for e in depths)
+    assert got["prelude"] == (gen - 1) * shape.n_prelude * layer
+    assert got["coda"] == (gen - 1) * (shape.n_coda * layer + 2 * V * d)
+    n_attn = shape.n_prelude + shape.n_coda
+    assert got["attention"] == sum(4 * d * L * (int(e) * shape.n_core + n_attn)
+                                   for e, L in zip(depths, ctx))
+
+
+def test_exit_gaps_never_written():
+    shape = micro(r_max=4)
+    wts = make_weights(shape)
+    prompt = prompt_for(shape, 5)
+    depths = np.array([2, 3, 4, 2], dtype=np.int8)
+    tr = decode_sequence(OracleModel(shape, wts), prompt, 5, force_exit=depths, keep_kv=True)
+    K = tr.kv.K
+    om = OracleModel(shape, wts)
+    P = len(prompt)
+    for l in range(shape.n_core):
+        for dpt in range(1, shape.r_max + 1):
+            sl = om.slot_core(l, dpt)
+            assert np.all(np.isfinite(K[sl, :P]))
+            for t, e in enumerate(depths, start=1):
+                written = np.all(np.isfinite(K[sl, P + t - 1]))
+                assert written == (dpt <= e)
