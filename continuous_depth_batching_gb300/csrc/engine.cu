@@ -1,0 +1,773 @@
+// CDB engine: the C ABI of cdb.h, the arena layout and the GPU executor that
+// carries out the scheduler's stages with the kernels of kernels.cuh.
+//
+// Stage sequencing follows "Depth-adaptive Inference of Looped Language
+// Models via Continuous Depth Batching": prefill at full depth with chunking
+// (Appendix A.1), prelude after prefill or coda, one recurrent-core step over
+// the recurrent queue, coda on exited tokens (§4.1, Algorithms 1-2).  The
+// lookahead flags of each core step are copied to the host on a second stream
+// (§4.3, "asynchronous batch preparation") while the next stages run.
+#include <chrono>
+#include <cmath>
+#include <cstring>
+#include <deque>
+#include <memory>
+#include <string>
+#include <thread>
+#include <vector>
+
+#include "../../include/cdb.h"
+#include "kernels.cuh"
+#include "sched.h"
+
+namespace cdb {
+
+static constexpr int kRing = 8;           // lookahead flag ring (core steps)
+static constexpr size_t kAlign = 256;
+static constexpr size_t kStageSeg = 1 << 20;  // pinned upload segment
+static constexpr int kStageSegs = 8;
+
+static size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
+
+struct Layout {
+  size_t total = 0;
+  size_t pool, etab, bt, out_tok, ftok, fexit, out_depth, gtrace, ltrace, htrace, estore, rope;
+  size_t rows[5], meta[5];  // X, Xc, Pb, Cb, Tp
+  size_t pend_new, ring, status;
+  size_t Xp, Ep, rslot, rpos, rtok, done_idx, Cp, Cp_meta;
+  size_t lslot, lt, lpos;
+  size_t A, QKV, Q, O, Mid, logits, part_o, part_ml;
+  // dims
+  int es, nsl, max_blocks, max_splits, split, R, S, cap;
+};
+
+static bool plan_layout(const cdb_model_desc* m, const cdb_sched_cfg* c, Layout* L) {
+  const int es = m->dtype == CDB_BF16 ? 2 : 4;
+  const size_t d = m->d_model, H = m->n_heads, hd = m->head_dim, f = m->ffn, V = m->vocab;
+  const size_t W = c->W, M = c->M;
+  L->es = es;
+  L->nsl = m->n_prelude + m->n_core * m->r_max + m->n_coda;
+  L->max_blocks = (c->max_ctx + 15) / 16;
+  L->split = c->attn_split > 0 ? c->attn_split : 256;
+  L->max_splits = (c->max_ctx + L->split - 1) / L->split;
+  L->R = (int)(M > W ? M : W);
+  L->cap = c->max_new_cap;
+  L->S = c->S > 0 ? c->S : (c->W / 8 > 1 ? c->W / 8 : 1);
+  const size_t R = L->R, cap = c->max_new_cap, T = c->trace_tokens;
+  size_t o = 0;
+  auto take = [&](size_t bytes) {
+    size_t at = o;
+    o = align_up(o + bytes);
+    return at;
+  };
+  L->pool = take((size_t)c->kv_blocks * L->nsl * 2 * 16 * d * es);
+  L->etab = take((size_t)c->kv_blocks * 16);
+  L->bt = take(W * L->max_blocks * 4);
+  L->out_tok = take(W * cap * 4);
+  L->ftok = take(W * cap * 4);
+  L->fexit = take(W * cap);
+  L->out_depth = take(W * cap);
+  L->gtrace = take(c->trace_gate ? W * cap * m->r_max * 4 : 0);
+  L->ltrace = take(W * T * V * 4);
+  L->htrace = take(W * T * d * 4);
+  L->estore = take(m->has_adapter ? W * d * 4 : 0);
+  L->rope = take((size_t)c->max_ctx * (hd / 2) * 8);
+  for (int i = 0; i < 5; ++i) {
+    L->rows[i] = take(W * d * 4);
+    L->meta[i] = take(W * 5 * 4);
+  }
+  L->pend_new = take(W * 4);
+  L->ring = take(kRing * W);
+  L->status = take(16);
+  L->Xp = take(M * d * 4);
+  L->Ep = take(m->has_adapter ? M * d * 4 : 0);
+  L->rslot = take(M * 4);
+  L->rpos = take(M * 4);
+  L->rtok = take(M * 4);
+  L->done_idx = take(W * 4);
+  L->Cp = take(W * d * 4);
+  L->Cp_meta = take(W * 5 * 4);
+  L->lslot = take(W * 4);
+  L->lt = take(W * 4);
+  L->lpos = take(W * 4);
+  L->A = take(R * 2 * d * es);
+  L->QKV = take(R * 3 * d * 4);
+  L->Q = take(R * d * es);
+  L->O = take(R * d * es);
+  L->Mid = take(R * f * es);
+  L->logits = take(W * V * 4);
+  L->part_o = take(W * H * L->max_splits * hd * 4);
+  L->part_ml = take(W * H * L->max_splits * 2 * 4);
+  L->total = o;
+  return true;
+}
+
+struct LayerW {
+  const void *attn_norm, *wqkv, *wo, *mlp_norm, *wg, *wu, *wd;
+};
+
+struct PendingResult {
+  int64_t id;
+  int slot, n_tokens, active;
+  cudaEvent_t ev;
+};
+
+struct HostResult {
+  int64_t id;
+  int n_tokens;
+  std::vector<int32_t> tokens;
+  std::vector<int8_t> depths;
+  std::vector<float> gate, logits, hidden;
+};
+
+class GpuExecutor;
+
+}  // namespace cdb
+
+struct cdb_ctx {
+  cdb_model_desc m;
+  cdb_sched_cfg c;
+  cdb::Layout L;
+  char* base = nullptr;
+  std::vector<cdb::LayerW> pre, core, coda;
+  const void *embed, *lm_head, *final_norm, *gate_w, *adapter;
+  cudaStream_t cs = nullptr, ps = nullptr;
+  bool own_cs = false, own_ps = false;
+  // pinned host memory
+  char* stage = nullptr;  // kStageSegs * kStageSeg
+  int seg = 0;
+  size_t seg_off = 0;
+  cudaEvent_t seg_ev[cdb::kStageSegs];
+  uint8_t* pend_host = nullptr;  // kRing * W
+  cudaEvent_t ev_core[cdb::kRing], ev_flags[cdb::kRing];
+  char* res_host = nullptr;      // per slot result staging
+  size_t res_stride = 0;
+  std::vector<cdb::PendingResult> pending;  // per slot
+  std::deque<cdb::HostResult> ready;
+  std::unique_ptr<cdb::GpuExecutor> exec;
+  std::unique_ptr<cdb::Scheduler> sched;
+  std::string err;
+  bool dead = false;
+};
+
+namespace cdb {
+
+template <typename P>
+static P* at(cdb_ctx* x, size_t off) {
+  return reinterpret_cast<P*>(x->base + off);
+}
+
+static RowMeta meta_at(cdb_ctx* x, size_t off) {
+  int* p = at<int>(x, off);
+  const int W = x->c.W;
+  return RowMeta{p, p + W, p + 2 * W, p + 3 * W, p + 4 * W};
+}
+
+static int cuda_fail(cdb_ctx* x, cudaError_t e, const char* what) {
+  x->err = std::string(what) + ": " + cudaGetErrorString(e);
+  x->dead = true;
+  return CDB_ERR_CUDA;
+}
+
+#define CK(expr)                                       \
+  do {                                                 \
+    cudaError_t _e = (expr);                           \
+    if (_e != cudaSuccess) return cuda_fail(x, _e, #expr); \
+  } while (0)
+
+// Poll an event with a time limit so a stuck device cannot hang the host.
+static int wait_event(cdb_ctx* x, cudaEvent_t ev, double limit_s) {
+  auto t0 = std::chrono::steady_clock::now();
+  for (;;) {
+    cudaError_t e = cudaEventQuery(ev);
+    if (e == cudaSuccess) return CDB_OK;
+    if (e != cudaErrorNotReady) return cuda_fail(x, e, "cudaEventQuery");
+    double dt = std::chrono::duration<double>(std::chrono::steady_clock::now() - t0).count();
+    if (dt > limit_s) {
+      x->err = "timed out waiting for the device";
+      return CDB_ERR_TIMEOUT;
+    }
+    if (dt > 0.001) std::this_thread::yield();
+  }
+}
+
+// Copy host bytes to a device address through the pinned staging segments.
+static int upload(cdb_ctx* x, void* dst, const void* src, size_t n) {
+  if (n == 0) return CDB_OK;
+  if (n > kStageSeg) {
+    x->err = "upload larger than a staging segment";
+    return CDB_ERR_ARG;
+  }
+  if (x->seg_off + n > kStageSeg) {
+    CK(cudaEventRecord(x->seg_ev[x->seg], x->cs));
+    x->seg = (x->seg + 1) % kStageSegs;
+    int rc = wait_event(x, x->seg_ev[x->seg], 600.0);
+    if (rc < 0) return rc;
+    x->seg_off = 0;
+  }
+  char* h = x->stage + (size_t)x->seg * kStageSeg + x->seg_off;
+  std::memcpy(h, src, n);
+  x->seg_off = (x->seg_off + n + 15) / 16 * 16;
+  CK(cudaMemcpyAsync(dst, h, n, cudaMemcpyHostToDevice, x->cs));
+  return CDB_OK;
+}
+
+class GpuExecutor : public Executor {
+ public:
+  explicit GpuExecutor(cdb_ctx* x) : x_(x) {}
+  const char* error() const override { return x_->err.c_str(); }
+
+  int admit(const Seq& s) override {
+    cdb_ctx* x = x_;
+    const Layout& L = x->L;
+    const int cap = x->c.max_new_cap;
+    std::vector<int32_t> bt(L.max_blocks, -1);
+    for (size_t i = 0; i < s.blocks.size(); ++i) bt[i] = s.blocks[i];
+    int rc = upload(x, at<int>(x, L.bt) + (size_t)s.slot * L.max_blocks, bt.data(), bt.size() * 4);
+    if (rc < 0) return rc;
+    std::vector<int8_t> fe(cap, 0);
+    if (x->c.mode != CDB_MODE_FIXED_DEPTH)
+      for (size_t i = 0; i < s.force_exit.size(); ++i) fe[i] = s.force_exit[i];
+    rc = upload(x, at<int8_t>(x, L.fexit) + (size_t)s.slot * cap, fe.data(), cap);
+    if (rc < 0) return rc;
+    std::vector<int32_t> ft(cap, -1);
+    for (size_t i = 0; i < s.force_tok.size(); ++i) ft[i] = s.force_tok[i];
+    rc = upload(x, at<int>(x, L.ftok) + (size_t)s.slot * cap, ft.data(), cap * 4);
+    if (rc < 0) return rc;
+    if (x->c.trace_gate)
+      CK(cudaMemsetAsync(at<float>(x, L.gtrace) + (size_t)s.slot * cap * x->m.r_max, 0xFF,
+                         (size_t)cap * x->m.r_max * 4, x->cs));
+    return CDB_OK;
+  }
+
+  template <typename T>
+  int block(const LayerW& lw, float* X, int rows, const int* mslot, const int* mpos, const int* mdepth,
+            int depth_uniform, int slot_base, int clamp, bool decode) {
+    cdb_ctx* x = x_;
+    const Layout& L = x->L;
+    const int d = x->m.d_model, f = x->m.ffn, H = x->m.n_heads, hd = x->m.head_dim;
+    cudaStream_t s = x->cs;
+    T* A = at<T>(x, L.A);
+    float* QKV = at<float>(x, L.QKV);
+    T* Q = at<T>(x, L.Q);
+    T* O = at<T>(x, L.O);
+    T* Mid = at<T>(x, L.Mid);
+    int* st = at<int>(x, L.status);
+    KvGeom kv = geom();
+    launch_rmsnorm<T>(s, X, (const T*)lw.attn_norm, A, rows, d, x->m.rms_eps, d);
+    launch_gemm<T>(s, kEpiStore, A, d, (const T*)lw.wqkv, nullptr, 3 * d, d, rows, QKV, nullptr, 3 * d);
+    launch_rope_kv<T>(s, QKV, rows, mslot, mpos, mdepth, depth_uniform, slot_base, clamp, Q, kv, H, hd,
+                      at<float2>(x, L.rope), st);
+    const int split = decode ? L.split : (1 << 30);
+    const int msp = decode ? L.max_splits : 1;
+    launch_attention<T>(s, Q, rows, mslot, mpos, mdepth, depth_uniform, kv, slot_base, clamp, H, hd, split, msp,
+                        O, at<float>(x, L.part_o), at<float>(x, L.part_ml), st);
+    launch_gemm<T>(s, kEpiResid, O, d, (const T*)lw.wo, nullptr, d, d, rows, X, nullptr, d);
+    launch_rmsnorm<T>(s, X, (const T*)lw.mlp_norm, A, rows, d, x->m.rms_eps, d);
+    launch_gemm<T>(s, kEpiSwiglu, A, d, (const T*)lw.wg, (const T*)lw.wu, f, d, rows, nullptr, Mid, f);
+    launch_gemm<T>(s, kEpiResid, Mid, f, (const T*)lw.wd, nullptr, d, f, rows, X, nullptr, d);
+    return CDB_OK;
+  }
+
+  template <typename T>
+  int adapter_step(float* X, int rows, const float* E, int e_per_slot, const int* mslot) {
+    cdb_ctx* x = x_;
+    const int d = x->m.d_model;
+    T* A = at<T>(x, x->L.A);
+    launch_concat<T>(x->cs, E, e_per_slot, mslot, X, A, rows, d);
+    launch_gemm<T>(x->cs, kEpiStore, A, 2 * d, (const T*)x->adapter, nullptr, d, 2 * d, rows, X, nullptr, d);
+    return CDB_OK;
+  }
+
+  // Final RMSNorm + LM head + argmax over rows of H (the coda output).
+  template <typename T>
+  int head(const float* Hrows, int n, RowMeta m) {
+    cdb_ctx* x = x_;
+    const Layout& L = x->L;
+    const int d = x->m.d_model, V = x->m.vocab, cap = x->c.max_new_cap;
+    T* A = at<T>(x, L.A);
+    float* lg = at<float>(x, L.logits);
+    launch_rmsnorm<T>(x->cs, Hrows, (const T*)x->final_norm, A, n, d, x->m.rms_eps, d);
+    launch_gemm<T>(x->cs, kEpiStore, A, d, (const T*)x->lm_head, nullptr, V, d, n, lg, nullptr, V);
+    const bool tr = x->c.trace_tokens > 0;
+    launch_argmax(x->cs, lg, n, V, m, at<int>(x, L.ftok), cap, at<int>(x, L.out_tok), tr ? at<float>(x, L.ltrace) : nullptr,
+                  x->c.trace_tokens, Hrows, tr ? at<float>(x, L.htrace) : nullptr, d, at<int>(x, L.status));
+    return CDB_OK;
+  }
+
+  int prefill(const PrefillPlan& p, const std::vector<Seq>&) override {
+    return x_->m.dtype == CDB_BF16 ? prefill_t<__nv_bfloat16>(p) : prefill_t<float>(p);
+  }
+  template <typename T>
+  int prefill_t(const PrefillPlan& p) {
+    cdb_ctx* x = x_;
+    const Layout& L = x->L;
+    const int n = (int)p.rows.size(), d = x->m.d_model;
+    std::vector<int32_t> a(n), b(n), c(n);
+    for (int i = 0; i < n; ++i) {
+      a[i] = p.rows[i].slot;
+      b[i] = p.rows[i].pos;
+      c[i] = p.rows[i].tok;
+    }
+    int* rslot = at<int>(x, L.rslot);
+    int* rpos = at<int>(x, L.rpos);
+    int* rtok = at<int>(x, L.rtok);
+    int rc;
+    if ((rc = upload(x, rslot, a.data(), n * 4)) < 0) return rc;
+    if ((rc = upload(x, rpos, b.data(), n * 4)) < 0) return rc;
+    if ((rc = upload(x, rtok, c.data(), n * 4)) < 0) return rc;
+    float* Xp = at<float>(x, L.Xp);
+    launch_embed_prefill<T>(x->cs, (const T*)x->embed, d, x->m.vocab, rslot, rpos, rtok, n, Xp, geom(), x->m.r_max,
+                            at<int>(x, L.status));
+    for (int i = 0; i < x->m.n_prelude; ++i) block<T>(x->pre[i], Xp, n, rslot, rpos, nullptr, 1, i, 0, false);
+    float* Ep = at<float>(x, L.Ep);
+    if (x->m.has_adapter) {
+      launch_copy_rows(x->cs, Xp, Ep, n, d);
+      CK(cudaMemsetAsync(Xp, 0, (size_t)n * d * 4, x->cs));
+    }
+    for (int r = 1; r <= x->m.r_max; ++r) {
+      if (x->m.has_adapter) adapter_step<T>(Xp, n, Ep, 0, rslot);
+      for (int l = 0; l < x->m.n_core; ++l)
+        block<T>(x->core[l], Xp, n, rslot, rpos, nullptr, r, x->m.n_prelude + l * x->m.r_max, 1, false);
+    }
+    const int cbase = x->m.n_prelude + x->m.n_core * x->m.r_max;
+    for (int j = 0; j < x->m.n_coda; ++j) block<T>(x->coda[j], Xp, n, rslot, rpos, nullptr, 1, cbase + j, 0, false);
+    const int nd = (int)p.done_rows.size();
+    if (nd > 0) {
+      if ((rc = upload(x, at<int>(x, L.done_idx), p.done_rows.data(), nd * 4)) < 0) return rc;
+      RowMeta cm = meta_at(x, L.Cp_meta);
+      float* Cp = at<float>(x, L.Cp);
+      launch_gather_rows(x->cs, Xp, at<int>(x, L.done_idx), rslot, rpos, nd, Cp, cm, d);
+      head<T>(Cp, nd, cm);
+    }
+    CK(cudaGetLastError());
+    return CDB_OK;
+  }
+
+  int prelude(const PreludePlan& p) override {
+    return x_->m.dtype == CDB_BF16 ? prelude_t<__nv_bfloat16>(p) : prelude_t<float>(p);
+  }
+  template <typename T>
+  int prelude_t(const PreludePlan& p) {
+    cdb_ctx* x = x_;
+    const Layout& L = x->L;
+    const int n = (int)p.rows.size(), d = x->m.d_model;
+    std::vector<int32_t> a(n), b(n), c(n);
+    for (int i = 0; i < n; ++i) {
+      a[i] = p.rows[i].slot;
+      b[i] = p.rows[i].t;
+      c[i] = p.rows[i].pos;
+    }
+    int rc;
+    int *ls = at<int>(x, L.lslot), *lt = at<int>(x, L.lt), *lp = at<int>(x, L.lpos);
+    if ((rc = upload(x, ls, a.data(), n * 4)) < 0) return rc;
+    if ((rc = upload(x, lt, b.data(), n * 4)) < 0) return rc;
+    if ((rc = upload(x, lp, c.data(), n * 4)) < 0) return rc;
+    float* Tp = at<float>(x, L.rows[4]);
+    RowMeta tm = meta_at(x, L.meta[4]);
+    launch_embed_prelude<T>(x->cs, (const T*)x->embed, d, x->m.vocab, ls, lt, lp, n, at<int>(x, L.out_tok),
+                            x->c.max_new_cap, Tp, tm, geom(), x->m.r_max, at<int>(x, L.status));
+    for (int i = 0; i < x->m.n_prelude; ++i) block<T>(x->pre[i], Tp, n, tm.slot, tm.pos, nullptr, 1, i, 0, true);
+    launch_prelude_finish(x->cs, Tp, tm, n, at<float>(x, L.rows[2]), meta_at(x, L.meta[2]), p.dst_off,
+                          x->m.has_adapter ? at<float>(x, L.estore) : nullptr, d, x->m.has_adapter);
+    CK(cudaGetLastError());
+    return CDB_OK;
+  }
+
+  int core(const CorePlan& p) override {
+    return x_->m.dtype == CDB_BF16 ? core_t<__nv_bfloat16>(p) : core_t<float>(p);
+  }
+  template <typename T>
+  int core_t(const CorePlan& p) {
+    cdb_ctx* x = x_;
+    const Layout& L = x->L;
+    const int d = x->m.d_model, B = p.B;
+    float* X = at<float>(x, L.rows[0]);
+    RowMeta mx = meta_at(x, L.meta[0]);
+    launch_gather_core(x->cs, at<float>(x, L.rows[1]), meta_at(x, L.meta[1]), p.B_cont, at<float>(x, L.rows[2]),
+                       meta_at(x, L.meta[2]), p.n_ref, X, mx, d);
+    if (x->m.has_adapter) adapter_step<T>(X, B, at<float>(x, L.estore), 1, mx.slot);
+    for (int l = 0; l < x->m.n_core; ++l)
+      block<T>(x->core[l], X, B, mx.slot, mx.pos, mx.depth, 0, x->m.n_prelude + l * x->m.r_max, 1, true);
+    const int ri = (int)(p.step % kRing);
+    uint8_t* ring = at<uint8_t>(x, L.ring) + (size_t)ri * x->c.W;
+    launch_gate<T>(x->cs, X, (const T*)x->gate_w, x->m.gate_bias, x->m.gate_threshold, x->m.rms_eps, B, d, mx,
+                   x->c.mode, x->m.r_min, x->m.r_max, at<int8_t>(x, L.fexit), x->c.max_new_cap,
+                   at<int>(x, L.pend_new), ring, x->c.trace_gate ? at<float>(x, L.gtrace) : nullptr);
+    launch_compact(x->cs, X, mx, at<int>(x, L.pend_new), B, d, x->m.r_max, p.qc_off, at<float>(x, L.rows[1]),
+                   meta_at(x, L.meta[1]), at<float>(x, L.rows[3]), meta_at(x, L.meta[3]), geom(),
+                   at<int8_t>(x, L.out_depth), x->c.max_new_cap, at<int>(x, L.status));
+    CK(cudaGetLastError());
+    // Lookahead flags to the host on the prep stream.
+    CK(cudaEventRecord(x->ev_core[ri], x->cs));
+    CK(cudaStreamWaitEvent(x->ps, x->ev_core[ri], 0));
+    CK(cudaMemcpyAsync(x->pend_host + (size_t)ri * x->c.W, ring, x->c.W, cudaMemcpyDeviceToHost, x->ps));
+    CK(cudaEventRecord(x->ev_flags[ri], x->ps));
+    return CDB_OK;
+  }
+
+  int core_flags(int64_t step, std::vector<uint8_t>& pend) override {
+    cdb_ctx* x = x_;
+    const int ri = (int)(step % kRing);
+    int rc = wait_event(x, x->ev_flags[ri], 600.0);
+    if (rc < 0) return rc;
+    pend.assign(x->pend_host + (size_t)ri * x->c.W, x->pend_host + (size_t)(ri + 1) * x->c.W);
+    return CDB_OK;
+  }
+
+  int coda(const std::vector<Tok>& rows) override {
+    return x_->m.dtype == CDB_BF16 ? coda_t<__nv_bfloat16>(rows) : coda_t<float>(rows);
+  }
+  template <typename T>
+  int coda_t(const std::vector<Tok>& rows) {
+    cdb_ctx* x = x_;
+    const Layout& L = x->L;
+    const int n = (int)rows.size(), d = x->m.d_model;
+    float* Cb = at<float>(x, L.rows[3]);
+    RowMeta mb = meta_at(x, L.meta[3]);
+    const float* Hrows = Cb;
+    if (x->m.n_coda > 0) {
+      float* Tc = at<float>(x, L.rows[4]);
+      launch_copy_rows(x->cs, Cb, Tc, n, d);
+      const int cbase = x->m.n_prelude + x->m.n_core * x->m.r_max;
+      for (int j = 0; j < x->m.n_coda; ++j) block<T>(x->coda[j], Tc, n, mb.slot, mb.pos, nullptr, 1, cbase + j, 0, true);
+      Hrows = Tc;
+    }
+    head<T>(Hrows, n, mb);
+    CK(cudaGetLastError());
+    return CDB_OK;
+  }
+
+  int finish(const Seq& s) override {
+    cdb_ctx* x = x_;
+    const Layout& L = x->L;
+    int rc = harvest_slot(s.slot, true);
+    if (rc < 0) return rc;
+    const int cap = x->c.max_new_cap, slot = s.slot;
+    char* h = x->res_host + (size_t)slot * x->res_stride;
+    size_t o = 0;
+    CK(cudaMemcpyAsync(h + o, at<int>(x, L.out_tok) + (size_t)slot * cap, cap * 4, cudaMemcpyDeviceToHost, x->cs));
+    o += cap * 4;
+    CK(cudaMemcpyAsync(h + o, at<int8_t>(x, L.out_depth) + (size_t)slot * cap, cap, cudaMemcpyDeviceToHost, x->cs));
+    o += (cap + 15) / 16 * 16;
+    if (x->c.trace_gate) {
+      size_t n = (size_t)cap * x->m.r_max * 4;
+      CK(cudaMemcpyAsync(h + o, at<float>(x, L.gtrace) + (size_t)slot * cap * x->m.r_max, n, cudaMemcpyDeviceToHost,
+                         x->cs));
+      o += n;
+    }
+    if (x->c.trace_tokens > 0) {
+      size_t n = (size_t)x->c.trace_tokens * x->m.vocab * 4;
+      CK(cudaMemcpyAsync(h + o, at<float>(x, L.ltrace) + (size_t)slot * x->c.trace_tokens * x->m.vocab, n,
+                         cudaMemcpyDeviceToHost, x->cs));
+      o += n;
+      n = (size_t)x->c.trace_tokens * x->m.d_model * 4;
+      CK(cudaMemcpyAsync(h + o, at<float>(x, L.htrace) + (size_t)slot * x->c.trace_tokens * x->m.d_model, n,
+                         cudaMemcpyDeviceToHost, x->cs));
+    }
+    PendingResult& pr = x->pending[slot];
+    CK(cudaEventRecord(pr.ev, x->cs));
+    pr.id = s.id;
+    pr.slot = slot;
+    pr.n_tokens = s.max_new;
+    pr.active = 1;
+    return CDB_OK;
+  }
+
+  // Move a finished sequence's results from pinned staging to the host list.
+  int harvest_slot(int slot, bool block_) {
+    cdb_ctx* x = x_;
+    PendingResult& pr = x->pending[slot];
+    if (!pr.active) return CDB_OK;
+    if (!block_ && cudaEventQuery(pr.ev) != cudaSuccess) return CDB_OK;
+    int rc = wait_event(x, pr.ev, 600.0);
+    if (rc < 0) return rc;
+    const int cap = x->c.max_new_cap;
+    const char* h = x->res_host + (size_t)slot * x->res_stride;
+    HostResult r;
+    r.id = pr.id;
+    r.n_tokens = pr.n_tokens;
+    r.tokens.assign((const int32_t*)h, (const int32_t*)h + pr.n_tokens);
+    size_t o = cap * 4;
+    r.depths.assign((const int8_t*)(h + o), (const int8_t*)(h + o) + (pr.n_tokens > 0 ? pr.n_tokens - 1 : 0));
+    o += (cap + 15) / 16 * 16;
+    if (x->c.trace_gate) {
+      const float* g = (const float*)(h + o);
+      r.gate.assign(g, g + (size_t)(pr.n_tokens - 1) * x->m.r_max);
+      o += (size_t)cap * x->m.r_max * 4;
+    }
+    if (x->c.trace_tokens > 0) {
+      const float* g = (const float*)(h + o);
+      r.logits.assign(g, g + (size_t)x->c.trace_tokens * x->m.vocab);
+      o += (size_t)x->c.trace_tokens * x->m.vocab * 4;
+      g = (const float*)(h + o);
+      r.hidden.assign(g, g + (size_t)x->c.trace_tokens * x->m.d_model);
+    }
+    x->ready.push_back(std::move(r));
+    pr.active = 0;
+    return CDB_OK;
+  }
+
+  KvGeom geom() {
+    cdb_ctx* x = x_;
+    KvGeom g;
+    g.pool = x->base + x->L.pool;
+    g.bt = at<int>(x, x->L.bt);
+    g.etab = at<uint8_t>(x, x->L.etab);
+    g.max_blocks = x->L.max_blocks;
+    g.kv_blocks = x->c.kv_blocks;
+    g.nsl = x->L.nsl;
+    g.d = x->m.d_model;
+    return g;
+  }
+
+ private:
+  cdb_ctx* x_;
+};
+
+static int check_status(cdb_ctx* x) {
+  int st = 0;
+  cudaError_t e = cudaMemcpyAsync(&st, at<int>(x, x->L.status), 4, cudaMemcpyDeviceToHost, x->cs);
+  if (e != cudaSuccess) return cuda_fail(x, e, "status copy");
+  e = cudaStreamSynchronize(x->cs);
+  if (e != cudaSuccess) return cuda_fail(x, e, "cudaStreamSynchronize");
+  if (st != 0) {
+    x->err = "device bounds check failed (status " + std::to_string(st) + ")";
+    x->dead = true;
+    return CDB_ERR_DEVICE_BOUNDS;
+  }
+  return CDB_OK;
+}
+
+static bool valid_hd(int hd) { return hd == 8 || hd == 16 || hd == 32 || hd == 64 || hd == 96 || hd == 128; }
+
+}  // namespace cdb
+
+using namespace cdb;
+
+extern "C" {
+
+size_t cdb_arena_bytes(const cdb_model_desc* m, const cdb_sched_cfg* c) {
+  if (!m || !c) return 0;
+  Layout L;
+  plan_layout(m, c, &L);
+  return L.total;
+}
+
+size_t cdb_kv_bytes_per_token(const cdb_model_desc* m) {
+  if (!m) return 0;
+  const size_t es = m->dtype == CDB_BF16 ? 2 : 4;
+  const size_t slots = (size_t)m->n_prelude + m->n_coda + (size_t)m->n_core * m->r_max;
+  return slots * 2 * (size_t)m->d_model * es;
+}
+
+int cdb_init(const cdb_model_desc* m, const cdb_weights* w, const cdb_sched_cfg* c, cdb_ctx** out) {
+  if (!m || !w || !c || !out) return CDB_ERR_ARG;
+  *out = nullptr;
+  if (m->vocab < 2 || m->d_model < 4 || m->n_heads < 1 || m->d_model != m->n_heads * m->head_dim ||
+      m->d_model % 4 != 0 || !valid_hd(m->head_dim) || m->ffn < 1 || m->n_core < 1 || m->n_prelude < 0 ||
+      m->n_coda < 0 || m->r_min < 2 || m->r_max < m->r_min || m->r_max > CDB_MAX_DEPTH ||
+      (m->dtype != CDB_FP32 && m->dtype != CDB_BF16) || (m->has_adapter && !w->adapter))
+    return CDB_ERR_ARG;
+  if (c->W < 1 || c->M < 1 || c->K < 1 || c->kv_blocks < 1 || c->max_ctx < 1 || c->max_new_cap < 1 ||
+      c->mode < 0 || c->mode > 2 || c->trace_tokens < 0 || !c->arena || ((uintptr_t)c->arena % kAlign) != 0 ||
+      c->attn_split < 0 || (c->S > c->W))
+    return CDB_ERR_ARG;
+  if (!w->embed || !w->lm_head || !w->final_norm || !w->gate_w || (m->n_core > 0 && !w->core) ||
+      (m->n_prelude > 0 && !w->prelude) || (m->n_coda > 0 && !w->coda))
+    return CDB_ERR_ARG;
+  std::unique_ptr<cdb_ctx> x(new cdb_ctx);
+  x->m = *m;
+  x->c = *c;
+  plan_layout(m, c, &x->L);
+  if (c->arena_bytes < x->L.total) return CDB_ERR_ARENA;
+  if (x->c.S <= 0) x->c.S = x->L.S;
+  x->base = (char*)c->arena;
+  auto cp = [](const cdb_layer_weights* a, int n, std::vector<LayerW>& v) {
+    for (int i = 0; i < n; ++i)
+      v.push_back({a[i].attn_norm, a[i].wqkv, a[i].wo, a[i].mlp_norm, a[i].wg, a[i].wu, a[i].wd});
+  };
+  cp(w->prelude, m->n_prelude, x->pre);
+  cp(w->core, m->n_core, x->core);
+  cp(w->coda, m->n_coda, x->coda);
+  for (auto* v : {&x->pre, &x->core, &x->coda})
+    for (auto& lw : *v)
+      if (!lw.attn_norm || !lw.wqkv || !lw.wo || !lw.mlp_norm || !lw.wg || !lw.wu || !lw.wd) return CDB_ERR_ARG;
+  x->embed = w->embed;
+  x->lm_head = w->lm_head;
+  x->final_norm = w->final_norm;
+  x->gate_w = w->gate_w;
+  x->adapter = w->adapter;
+  cdb_ctx* xp = x.get();
+  cudaError_t e;
+#define CKI(expr)                                   \
+  do {                                              \
+    e = (expr);                                     \
+    if (e != cudaSuccess) {                         \
+      cuda_fail(xp, e, #expr);                      \
+      return CDB_ERR_CUDA;                          \
+    }                                               \
+  } while (0)
+  x->cs = (cudaStream_t)c->compute_stream;
+  x->ps = (cudaStream_t)c->prep_stream;
+  if (!x->ps) {
+    CKI(cudaStreamCreateWithFlags(&x->ps, cudaStreamNonBlocking));
+    x->own_ps = true;
+  }
+  CKI(cudaMallocHost((void**)&x->stage, (size_t)kStageSegs * kStageSeg));
+  for (int i = 0; i < kStageSegs; ++i) CKI(cudaEventCreateWithFlags(&x->seg_ev[i], cudaEventDisableTiming));
+  for (int i = 0; i < kStageSegs; ++i) CKI(cudaEventRecord(x->seg_ev[i], x->cs));
+  CKI(cudaMallocHost((void**)&x->pend_host, (size_t)kRing * c->W));
+  for (int i = 0; i < kRing; ++i) {
+    CKI(cudaEventCreateWithFlags(&x->ev_core[i], cudaEventDisableTiming));
+    CKI(cudaEventCreateWithFlags(&x->ev_flags[i], cudaEventDisableTiming));
+  }
+  const size_t cap = c->max_new_cap;
+  x->res_stride = cap * 4 + (cap + 15) / 16 * 16 + (c->trace_gate ? cap * m->r_max * 4 : 0) +
+                  (size_t)c->trace_tokens * (m->vocab + m->d_model) * 4;
+  x->res_stride = (x->res_stride + 255) / 256 * 256;
+  CKI(cudaMallocHost((void**)&x->res_host, x->res_stride * c->W));
+  x->pending.resize(c->W);
+  for (auto& p : x->pending) {
+    p.active = 0;
+    CKI(cudaEventCreateWithFlags(&p.ev, cudaEventDisableTiming));
+  }
+  // KV pool to NaN: reading an unwritten exit gap would poison the output.
+  const Layout& L = x->L;
+  CKI(cudaMemsetAsync(x->base + L.pool, 0xFF, L.etab - L.pool, x->cs));
+  CKI(cudaMemsetAsync(x->base + L.etab, 0, L.total - L.etab, x->cs));
+  CKI(cudaMemsetAsync(x->base + L.bt, 0xFF, (size_t)c->W * L.max_blocks * 4, x->cs));
+  launch_rope_table(x->cs, at<float2>(xp, L.rope), c->max_ctx, m->head_dim, m->rope_theta);
+  CKI(cudaGetLastError());
+  CKI(cudaStreamSynchronize(x->cs));
+#undef CKI
+  SchedCfg sc;
+  sc.mode = c->mode;
+  sc.W = c->W;
+  sc.M = c->M;
+  sc.S = x->c.S;
+  sc.K = c->K;
+  sc.r_max = m->r_max;
+  sc.r_min = m->r_min;
+  sc.kv_blocks = c->kv_blocks;
+  sc.kv_headroom = c->kv_headroom;
+  sc.max_ctx = c->max_ctx;
+  sc.max_new_cap = c->max_new_cap;
+  x->exec.reset(new GpuExecutor(xp));
+  x->sched.reset(new Scheduler(sc, x->exec.get()));
+  *out = x.release();
+  return CDB_OK;
+}
+
+int cdb_admit(cdb_ctx* x, int64_t seq_id, const int32_t* prompt, int prompt_len, int max_new_tokens,
+              const int8_t* force_exit, const int32_t* force_token) {
+  if (!x) return CDB_ERR_ARG;
+  if (x->dead) return CDB_ERR_STATE;
+  if (!prompt) {
+    x->err = "prompt is NULL";
+    return CDB_ERR_ARG;
+  }
+  for (int i = 0; i < prompt_len; ++i)
+    if (prompt[i] < 0 || prompt[i] >= x->m.vocab) {
+      x->err = "prompt token out of range";
+      return CDB_ERR_ARG;
+    }
+  if (force_token)
+    for (int i = 0; i < max_new_tokens; ++i)
+      if (force_token[i] < -1 || force_token[i] >= x->m.vocab) {
+        x->err = "force_token out of range";
+        return CDB_ERR_ARG;
+      }
+  int rc = x->sched->admit(seq_id, prompt, prompt_len, max_new_tokens, force_exit, force_token);
+  if (rc < 0) x->err = x->sched->err;
+  return rc;
+}
+
+int cdb_step_boundary(cdb_ctx* x, cdb_step_info* info) {
+  if (!x) return CDB_ERR_ARG;
+  if (x->dead) return CDB_ERR_STATE;
+  int rc = x->sched->step_boundary(info);
+  if (rc < 0) x->err = x->sched->err.empty() ? x->err : x->sched->err;
+  return rc;
+}
+
+int cdb_step_core(cdb_ctx* x, cdb_step_info* info) {
+  if (!x) return CDB_ERR_ARG;
+  if (x->dead) return CDB_ERR_STATE;
+  int rc = x->sched->step_core(info);
+  if (rc < 0) x->err = x->sched->err.empty() ? x->err : x->sched->err;
+  return rc;
+}
+
+int cdb_sync(cdb_ctx* x) {
+  if (!x) return CDB_ERR_ARG;
+  if (x->dead) return CDB_ERR_STATE;
+  cudaError_t e = cudaStreamSynchronize(x->ps);
+  if (e != cudaSuccess) return cuda_fail(x, e, "cudaStreamSynchronize(prep)");
+  return check_status(x);
+}
+
+int cdb_drain(cdb_ctx* x, cdb_result* buf, int cap, int* n_out) {
+  if (!x || !n_out || (cap > 0 && !buf)) return CDB_ERR_ARG;
+  *n_out = 0;
+  if (x->dead) return CDB_ERR_STATE;
+  int rc = check_status(x);
+  if (rc < 0) return rc;
+  for (int s = 0; s < x->c.W; ++s) {
+    rc = x->exec->harvest_slot(s, true);
+    if (rc < 0) return rc;
+  }
+  int n = 0;
+  while (n < cap && !x->ready.empty()) {
+    HostResult& r = x->ready.front();
+    cdb_result& o = buf[n];
+    o.seq_id = r.id;
+    o.n_tokens = r.n_tokens;
+    if (o.tokens) std::memcpy(o.tokens, r.tokens.data(), r.tokens.size() * 4);
+    if (o.exit_depths) std::memcpy(o.exit_depths, r.depths.data(), r.depths.size());
+    if (o.gate_logits && !r.gate.empty()) std::memcpy(o.gate_logits, r.gate.data(), r.gate.size() * 4);
+    if (o.logits && !r.logits.empty()) std::memcpy(o.logits, r.logits.data(), r.logits.size() * 4);
+    if (o.hidden && !r.hidden.empty()) std::memcpy(o.hidden, r.hidden.data(), r.hidden.size() * 4);
+    x->ready.pop_front();
+    ++n;
+  }
+  *n_out = n;
+  return CDB_OK;
+}
+
+void cdb_free(cdb_ctx* x) {
+  if (!x) return;
+  if (x->cs || true) cudaStreamSynchronize(x->cs);
+  if (x->ps) cudaStreamSynchronize(x->ps);
+  for (int i = 0; i < kStageSegs; ++i) cudaEventDestroy(x->seg_ev[i]);
+  for (int i = 0; i < kRing; ++i) {
+    cudaEventDestroy(x->ev_core[i]);
+    cudaEventDestroy(x->ev_flags[i]);
+  }
+  for (auto& p : x->pending) cudaEventDestroy(p.ev);
+  if (x->stage) cudaFreeHost(x->stage);
+  if (x->pend_host) cudaFreeHost(x->pend_host);
+  if (x->res_host) cudaFreeHost(x->res_host);
+  if (x->own_ps) cudaStreamDestroy(x->ps);
+  delete x;
+}
+
+const char* cdb_last_error(const cdb_ctx* x) { return x ? x->err.c_str() : "null context"; }
+
+int cdb_trace_enable(cdb_ctx* x, int on) {
+  if (!x) return CDB_ERR_ARG;
+  x->sched->trace_on = on != 0;
+  if (!on) x->sched->trace().clear();
+  return CDB_OK;
+}
+
+int cdb_trace_read(cdb_ctx* x, cdb_trace_row* rows, int cap, int* n_out) {
+  if (!x || !n_out) return CDB_ERR_ARG;
+  auto& tr = x->sched->trace();
+  int n = (int)tr.size() < cap ? (int)tr.size() : cap;
+  if (rows && n > 0) std::memcpy(rows, tr.data(), sizeof(cdb_trace_row) * n);
+  *n_out = n;
+  return CDB_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,461 @@
+// Bookkeeping and elementwise kernels of one CDB step: embedding (prelude),
+// RMSNorm, RoPE + KV write into the depth-indexed cache, the lookahead exit
+// gate, prefix-sum compaction of the recurrent batch, batch re-formation,
+// greedy argmax (coda) and the RoPE table.
+//
+// Source: "Depth-adaptive Inference of Looped Language Models via Continuous
+// Depth Batching", §2 (prelude / core / coda), §4.2 (depth-indexed KV cache),
+// §4.3 (lookahead gate), Algorithm 2 (exits to the coda queue, the rest back to
+// the recurrent queue), Appendix A.4 (refill mixes loop depths in one batch).
+#include "common.cuh"
+#include "kernels.cuh"
+
+namespace cdb {
+
+// ---------------------------------------------------------------------------
+// prelude: embedding gather
+// ---------------------------------------------------------------------------
+
+// Prefill rows: X[i] = E[tok_i]; the position's exit depth is r_max (prompt
+// tokens run at full depth, Appendix A.1).
+template <typename T>
+__global__ void k_embed_prefill(const T* __restrict__ E, int d, int V, const int* __restrict__ rslot,
+                                const int* __restrict__ rpos, const int* __restrict__ rtok, int rows,
+                                float* __restrict__ X, KvGeom kv, int r_max, int* status) {
+  const int i = blockIdx.x;
+  if (i >= rows) return;
+  int tok = rtok[i];
+  if (tok < 0 || tok >= V) {
+    if (threadIdx.x == 0) atomicOr(status, kStatusBadToken);
+    tok = 0;
+  }
+  const T* e = E + (size_t)tok * d;
+  for (int c = threadIdx.x; c < d; c += blockDim.x) X[(size_t)i * d + c] = to_f(e[c]);
+  if (threadIdx.x == 0) {
+    const int pos = rpos[i];
+    const int blk = kv.bt[rslot[i] * kv.max_blocks + pos / 16];
+    if (blk < 0 || blk >= kv.kv_blocks) atomicOr(status, kStatusBadBlock);
+    else kv.etab[blk * 16 + (pos & 15)] = (uint8_t)r_max;
+  }
+}
+
+// Decode prelude: the input of forward t is generated token t-1 of the slot.
+template <typename T>
+__global__ void k_embed_prelude(const T* __restrict__ E, int d, int V, const int* __restrict__ lslot,
+                                const int* __restrict__ lt, const int* __restrict__ lpos, int rows,
+                                const int* __restrict__ out_tok, int cap, float* __restrict__ X,
+                                RowMeta m, KvGeom kv, int r_max, int* status) {
+  const int i = blockIdx.x;
+  if (i >= rows) return;
+  const int slot = lslot[i], t = lt[i], pos = lpos[i];
+  int tok = out_tok[slot * cap + t - 1];
+  if (tok < 0 || tok >= V) {
+    if (threadIdx.x == 0) atomicOr(status, kStatusBadToken);
+    tok = 0;
+  }
+  const T* e = E + (size_t)tok * d;
+  for (int c = threadIdx.x; c < d; c += blockDim.x) X[(size_t)i * d + c] = to_f(e[c]);
+  if (threadIdx.x == 0) {
+    m.slot[i] = slot;
+    m.pos[i] = pos;
+    m.t[i] = t;
+    m.depth[i] = 0;
+    m.pend[i] = 0;
+    const int blk = kv.bt[slot * kv.max_blocks + pos / 16];
+    if (blk < 0 || blk >= kv.kv_blocks) atomicOr(status, kStatusBadBlock);
+    else kv.etab[blk * 16 + (pos & 15)] = (uint8_t)r_max;  // in flight
+  }
+}
+
+// Move prelude outputs into the refill rows.  With an adapter the loop starts
+// from s_0 = 0 and the prelude output e is kept per slot.
+__global__ void k_prelude_finish(const float* __restrict__ Tp, RowMeta tm, int rows,
+                                 float* __restrict__ Pb, RowMeta pm, int dst_off,
+                                 float* __restrict__ estore, int d, int adapter) {
+  const int i = blockIdx.x;
+  if (i >= rows) return;
+  const int o = dst_off + i, slot = tm.slot[i];
+  for (int c = threadIdx.x; c < d; c += blockDim.x) {
+    const float v = Tp[(size_t)i * d + c];
+    if (adapter) {
+      estore[(size_t)slot * d + c] = v;
+      Pb[(size_t)o * d + c] = 0.f;
+    } else {
+      Pb[(size_t)o * d + c] = v;
+    }
+  }
+  if (threadIdx.x == 0) {
+    pm.slot[o] = slot;
+    pm.pos[o] = tm.pos[i];
+    pm.t[o] = tm.t[i];
+    pm.depth[o] = 0;
+    pm.pend[o] = 0;
+  }
+}
+
+// ---------------------------------------------------------------------------
+// RMSNorm -> GEMM operand; adapter concat
+// ---------------------------------------------------------------------------
+
+template <typename T>
+__global__ void k_rmsnorm(const float* __restrict__ X, const T* __restrict__ g, T* __restrict__ A,
+                          int rows, int d, float eps, int lda) {
+  __shared__ float sh[33];
+  const int i = blockIdx.x;
+  if (i >= rows) return;
+  const float* x = X + (size_t)i * d;
+  float ss = 0.f;
+  for (int c = threadIdx.x; c < d; c += blockDim.x) ss = fmaf(x[c], x[c], ss);
+  ss = block_sum(ss, sh);
+  const float inv = 1.0f / sqrtf(ss / (float)d + eps);
+  for (int c = threadIdx.x; c < d; c += blockDim.x)
+    A[(size_t)i * lda + c] = from_f<T>(x[c] * inv * to_f(g[c]));
+}
+
+// A[i] = [e ; s] rounded to the operand type (x = adapter . [e; s_{d-1}]).
+template <typename T>
+__global__ void k_concat(const float* __restrict__ E, int e_per_slot, const int* __restrict__ mslot,
+                         const float* __restrict__ X, T* __restrict__ A, int rows, int d) {
+  const int i = blockIdx.x;
+  if (i >= rows) return;
+  const float* e = E + (size_t)(e_per_slot ? mslot[i] : i) * d;
+  const float* s = X + (size_t)i * d;
+  T* a = A + (size_t)i * 2 * d;
+  for (int c = threadIdx.x; c < d; c += blockDim.x) {
+    a[c] = from_f<T>(e[c]);
+    a[d + c] = from_f<T>(s[c]);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// RoPE (rotate-half) + KV write into the depth-indexed cache
+// ---------------------------------------------------------------------------
+
+// Row i at position p and loop step r writes K,V into slot slot_base + r-1
+// (core layers, clamp=1) or slot_base (prelude / coda layers).
+template <typename T>
+__global__ void k_rope_kv(const float* __restrict__ QKV, int rows, const int* __restrict__ mslot,
+                          const int* __restrict__ mpos, const int* __restrict__ mdepth,
+                          int depth_uniform, int slot_base, int clamp, T* __restrict__ Q, KvGeom kv,
+                          int H, int hd, const float2* __restrict__ rope, int* status) {
+  const int i = blockIdx.x;
+  if (i >= rows) return;
+  const int d = kv.d, half = hd / 2;
+  const int pos = mpos[i];
+  const int r = depth_uniform > 0 ? depth_uniform : mdepth[i] + 1;
+  const int blk = kv.bt[mslot[i] * kv.max_blocks + pos / 16];
+  const int sl = slot_base + (clamp ? r - 1 : 0);
+  if (blk < 0 || blk >= kv.kv_blocks || sl < 0 || sl >= kv.nsl) {
+    if (threadIdx.x == 0) atomicOr(status, kStatusBadBlock);
+    return;
+  }
+  T* pool = reinterpret_cast<T*>(kv.pool);
+  T* kdst = pool + (((size_t)blk * kv.nsl + sl) * 2 + 0) * 16 * d + (size_t)(pos & 15) * d;
+  T* vdst = pool + (((size_t)blk * kv.nsl + sl) * 2 + 1) * 16 * d + (size_t)(pos & 15) * d;
+  const float* q = QKV + (size_t)i * 3 * d;
+  const float* k = q + d;
+  const float* v = q + 2 * d;
+  const float2* cs = rope + (size_t)pos * half;
+  for (int u = threadIdx.x; u < H * half; u += blockDim.x) {
+    const int h = u / half, j = u % half;
+    const int a = h * hd + j, b = a + half;
+    const float c = cs[j].x, s = cs[j].y;
+    Q[(size_t)i * d + a] = from_f<T>(q[a] * c - q[b] * s);
+    Q[(size_t)i * d + b] = from_f<T>(q[b] * c + q[a] * s);
+    kdst[a] = from_f<T>(k[a] * c - k[b] * s);
+    kdst[b] = from_f<T>(k[b] * c + k[a] * s);
+    vdst[a] = from_f<T>(v[a]);
+    vdst[b] = from_f<T>(v[b]);
+  }
+}
+
+// cos/sin of pos * theta^(-2j/hd), evaluated in double and rounded once.
+__global__ void k_rope_table(float2* tab, int max_ctx, int hd, float theta) {
+  const int half = hd / 2;
+  const int n = max_ctx * half;
+  for (int u = blockIdx.x * blockDim.x + threadIdx.x; u < n; u += gridDim.x * blockDim.x) {
+    const int p = u / half, j = u % half;
+    const double inv = pow((double)theta, -2.0 * (double)j / (double)hd);
+    const double a = (double)p * inv;
+    tab[u] = make_float2((float)cos(a), (float)sin(a));
+  }
+}
+
+// ---------------------------------------------------------------------------
+// lookahead exit gate (§4.3)
+// ---------------------------------------------------------------------------
+
+// z = w . rmsnorm(h) + b.  The flag set after step r makes the token exit
+// after step r+1: live gate -> z > thr and r >= r_min-1; a forced exit depth
+// e -> r + 1 == e; fixed-depth mode never sets it.
+template <typename T>
+__global__ void k_gate(const float* __restrict__ X, const T* __restrict__ w, float bias, float thr,
+                       float eps, int rows, int d, RowMeta m, int mode, int r_min, int r_max,
+                       const int8_t* __restrict__ fexit, int cap, int* __restrict__ pend_new,
+                       uint8_t* __restrict__ ring, float* __restrict__ gtrace) {
+  __shared__ float sh[33];
+  const int i = blockIdx.x;
+  if (i >= rows) return;
+  const float* x = X + (size_t)i * d;
+  float ss = 0.f, dot = 0.f;
+  for (int c = threadIdx.x; c < d; c += blockDim.x) {
+    ss = fmaf(x[c], x[c], ss);
+    dot = fmaf(x[c], to_f(w[c]), dot);
+  }
+  ss = block_sum(ss, sh);
+  dot = block_sum(dot, sh);
+  if (threadIdx.x != 0) return;
+  const float z = dot / sqrtf(ss / (float)d + eps) + bias;
+  const int slot = m.slot[i], t = m.t[i];
+  const int r = m.depth[i] + 1;
+  int p = 0;
+  if (mode != 2) {
+    const int fe = fexit[slot * cap + t - 1];
+    if (fe > 0) p = (r + 1 == fe);
+    else p = (z > thr) && (r >= r_min - 1);
+  }
+  if (r + 1 >= r_max) p = 0;
+  pend_new[i] = p;
+  ring[slot] = (uint8_t)p;
+  if (gtrace) gtrace[((size_t)slot * cap + (t - 1)) * r_max + (r - 1)] = z;
+}
+
+// ---------------------------------------------------------------------------
+// compaction of the recurrent batch (Algorithm 2, lines 15-17)
+// ---------------------------------------------------------------------------
+
+// Row i exits after this step if its previous-step flag was set or it reached
+// r_max.  Exits keep slot order and go to the coda rows after qc_off; the
+// rest keep slot order at the front of the continuing rows.  One block per
+// row; each block ranks its row with a block-wide count over the earlier rows.
+__global__ void k_compact(const float* __restrict__ X, RowMeta m, const int* __restrict__ pend_new,
+                          int B, int d, int r_max, int qc_off, float* __restrict__ Xc, RowMeta mc,
+                          float* __restrict__ Cb, RowMeta mb, KvGeom kv, int8_t* __restrict__ out_depth,
+                          int cap, int* status) {
+  __shared__ float sh[33];
+  const int i = blockIdx.x;
+  if (i >= B) return;
+  auto exits = [&](int j) { return (m.depth[j] >= 1 && m.pend[j]) || (m.depth[j] + 1 >= r_max); };
+  float before = 0.f;
+  for (int j = threadIdx.x; j < i; j += blockDim.x) before += exits(j) ? 1.f : 0.f;
+  const int n_exit_before = (int)(block_sum(before, sh) + 0.5f);
+  const bool ex = exits(i);
+  const int r = m.depth[i] + 1;
+  const int dst = ex ? qc_off + n_exit_before : i - n_exit_before;
+  float* out = ex ? Cb : Xc;
+  for (int c = threadIdx.x; c < d; c += blockDim.x) out[(size_t)dst * d + c] = X[(size_t)i * d + c];
+  if (threadIdx.x == 0) {
+    RowMeta o = ex ? mb : mc;
+    const int slot = m.slot[i], pos = m.pos[i], t = m.t[i];
+    o.slot[dst] = slot;
+    o.pos[dst] = pos;
+    o.t[dst] = t;
+    o.depth[dst] = r;
+    o.pend[dst] = ex ? 0 : pend_new[i];
+    if (ex) {
+      const int blk = kv.bt[slot * kv.max_blocks + pos / 16];
+      if (blk < 0 || blk >= kv.kv_blocks) atomicOr(status, kStatusBadBlock);
+      else kv.etab[blk * 16 + (pos & 15)] = (uint8_t)r;
+      out_depth[slot * cap + t - 1] = (int8_t)r;
+    }
+  }
+}
+
+// Batch re-formation: continuing rows first, then refill rows (slot order).
+__global__ void k_gather_core(const float* __restrict__ Xc, RowMeta mc, int B_cont,
+                              const float* __restrict__ Pb, RowMeta mp, int n_ref,
+                              float* __restrict__ X, RowMeta mx, int d) {
+  const int i = blockIdx.x;
+  if (i >= B_cont + n_ref) return;
+  const bool c = i < B_cont;
+  const int j = c ? i : i - B_cont;
+  const float* src = (c ? Xc : Pb) + (size_t)j * d;
+  const float4* s4 = reinterpret_cast<const float4*>(src);
+  float4* d4 = reinterpret_cast<float4*>(X + (size_t)i * d);
+  for (int u = threadIdx.x; u < d / 4; u += blockDim.x) d4[u] = s4[u];
+  if (threadIdx.x == 0) {
+    const RowMeta& s = c ? mc : mp;
+    mx.slot[i] = s.slot[j];
+    mx.pos[i] = s.pos[j];
+    mx.t[i] = s.t[j];
+    mx.depth[i] = s.depth[j];
+    mx.pend[i] = s.pend[j];
+  }
+}
+
+// dst[k] = src[idx[k]] with metadata (prefill rows that finish a prompt).
+__global__ void k_gather_rows(const float* __restrict__ src, const int* __restrict__ idx,
+                              const int* __restrict__ rslot, const int* __restrict__ rpos, int n,
+                              float* __restrict__ dst, RowMeta md, int d) {
+  const int k = blockIdx.x;
+  if (k >= n) return;
+  const int j = idx[k];
+  for (int c = threadIdx.x; c < d; c += blockDim.x) dst[(size_t)k * d + c] = src[(size_t)j * d + c];
+  if (threadIdx.x == 0) {
+    md.slot[k] = rslot[j];
+    md.pos[k] = rpos[j];
+    md.t[k] = 0;
+    md.depth[k] = 0;
+    md.pend[k] = 0;
+  }
+}
+
+__global__ void k_copy_rows(const float* __restrict__ src, float* __restrict__ dst, size_t n) {
+  for (size_t u = blockIdx.x * (size_t)blockDim.x + threadIdx.x; u < n;
+       u += (size_t)gridDim.x * blockDim.x)
+    dst[u] = src[u];
+}
+
+// ---------------------------------------------------------------------------
+// coda: greedy argmax (ties -> lowest index), forced tokens, traces
+// ---------------------------------------------------------------------------
+
+__global__ void k_argmax(const float* __restrict__ logits, int rows, int V, RowMeta m,
+                         const int* __restrict__ ftok, int cap, int* __restrict__ out_tok,
+                         float* __restrict__ ltrace, int trace_T, const float* __restrict__ Hin,
+                         float* __restrict__ htrace, int d, int* status) {
+  __shared__ float sv[32];
+  __shared__ int si[32];
+  const int i = blockIdx.x;
+  if (i >= rows) return;
+  const float* lg = logits + (size_t)i * V;
+  float best = -INFINITY;
+  int bi = V;
+  bool nan = false;
+  for (int j = threadIdx.x; j < V; j += blockDim.x) {
+    const float v = lg[j];
+    if (v != v) nan = true;
+    if (v > best) {
+      best = v;
+      bi = j;
+    }
+  }
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const float ov = __shfl_xor_sync(0xffffffffu, best, o);
+    const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+    if (ov > best || (ov == best && oi < bi)) {
+      best = ov;
+      bi = oi;
+    }
+  }
+  if (lane == 0) {
+    sv[w] = best;
+    si[w] = bi;
+  }
+  if (nan) atomicOr(status, kStatusNaN);
+  __syncthreads();
+  const int slot = m.slot[i], t = m.t[i];
+  if (threadIdx.x == 0) {
+    for (int u = 1; u < (int)(blockDim.x >> 5); ++u)
+      if (sv[u] > sv[0] || (sv[u] == sv[0] && si[u] < si[0])) {
+        sv[0] = sv[u];
+        si[0] = si[u];
+      }
+    int tok = si[0] >= V ? 0 : si[0];
+    const int f = ftok[slot * cap + t];
+    if (f >= 0) tok = f;
+    out_tok[slot * cap + t] = tok;
+  }
+  if (ltrace && t < trace_T) {
+    float* dst = ltrace + ((size_t)slot * trace_T + t) * V;
+    for (int j = threadIdx.x; j < V; j += blockDim.x) dst[j] = lg[j];
+    float* hd = htrace + ((size_t)slot * trace_T + t) * d;
+    for (int j = threadIdx.x; j < d; j += blockDim.x) hd[j] = Hin[(size_t)i * d + j];
+  }
+}
+
+// ---------------------------------------------------------------------------
+// launchers
+// ---------------------------------------------------------------------------
+
+template <typename T>
+void launch_embed_prefill(cudaStream_t s, const T* E, int d, int V, const int* rslot, const int* rpos,
+                          const int* rtok, int rows, float* X, KvGeom kv, int r_max, int* status) {
+  if (rows > 0) k_embed_prefill<T><<<rows, 256, 0, s>>>(E, d, V, rslot, rpos, rtok, rows, X, kv, r_max, status);
+}
+template <typename T>
+void launch_embed_prelude(cudaStream_t s, const T* E, int d, int V, const int* lslot, const int* lt,
+                          const int* lpos, int rows, const int* out_tok, int cap, float* X,
+                          RowMeta meta, KvGeom kv, int r_max, int* status) {
+  if (rows > 0)
+    k_embed_prelude<T><<<rows, 256, 0, s>>>(E, d, V, lslot, lt, lpos, rows, out_tok, cap, X, meta, kv,
+                                            r_max, status);
+}
+void launch_prelude_finish(cudaStream_t s, const float* Tp, RowMeta tm, int rows, float* Pb, RowMeta pm,
+                           int dst_off, float* estore, int d, int adapter) {
+  if (rows > 0) k_prelude_finish<<<rows, 256, 0, s>>>(Tp, tm, rows, Pb, pm, dst_off, estore, d, adapter);
+}
+template <typename T>
+void launch_rmsnorm(cudaStream_t s, const float* X, const T* g, T* A, int rows, int d, float eps, int lda) {
+  if (rows > 0) k_rmsnorm<T><<<rows, 256, 0, s>>>(X, g, A, rows, d, eps, lda);
+}
+template <typename T>
+void launch_concat(cudaStream_t s, const float* E, int e_per_slot, const int* mslot, const float* X, T* A,
+                   int rows, int d) {
+  if (rows > 0) k_concat<T><<<rows, 256, 0, s>>>(E, e_per_slot, mslot, X, A, rows, d);
+}
+template <typename T>
+void launch_rope_kv(cudaStream_t s, const float* QKV, int rows, const int* mslot, const int* mpos,
+                    const int* mdepth, int depth_uniform, int slot_base, int clamp, T* Q, KvGeom kv, int H,
+                    int hd, const float2* rope, int* status) {
+  if (rows > 0)
+    k_rope_kv<T><<<rows, 256, 0, s>>>(QKV, rows, mslot, mpos, mdepth, depth_uniform, slot_base, clamp, Q,
+                                      kv, H, hd, rope, status);
+}
+template <typename T>
+void launch_gate(cudaStream_t s, const float* X, const T* w, float bias, float thr, float eps, int rows,
+                 int d, RowMeta meta, int mode, int r_min, int r_max, const int8_t* fexit, int cap,
+                 int* pend_new, uint8_t* ring, float* gtrace) {
+  if (rows > 0)
+    k_gate<T><<<rows, 256, 0, s>>>(X, w, bias, thr, eps, rows, d, meta, mode, r_min, r_max, fexit, cap,
+                                   pend_new, ring, gtrace);
+}
+void launch_compact(cudaStream_t s, const float* X, RowMeta m, const int* pend_new, int B, int d, int r_max,
+                    int qc_off, float* Xc, RowMeta mc, float* Cb, RowMeta mb, KvGeom kv, int8_t* out_depth,
+                    int cap, int* status) {
+  if (B > 0)
+    k_compact<<<B, 256, 0, s>>>(X, m, pend_new, B, d, r_max, qc_off, Xc, mc, Cb, mb, kv, out_depth, cap,
+                                status);
+}
+void launch_gather_core(cudaStream_t s, const float* Xc, RowMeta mc, int B_cont, const float* Pb, RowMeta mp,
+                        int n_ref, float* X, RowMeta mx, int d) {
+  if (B_cont + n_ref > 0)
+    k_gather_core<<<B_cont + n_ref, 256, 0, s>>>(Xc, mc, B_cont, Pb, mp, n_ref, X, mx, d);
+}
+void launch_gather_rows(cudaStream_t s, const float* src, const int* idx, const int* rslot, const int* rpos,
+                        int n, float* dst, RowMeta md, int d) {
+  if (n > 0) k_gather_rows<<<n, 256, 0, s>>>(src, idx, rslot, rpos, n, dst, md, d);
+}
+void launch_argmax(cudaStream_t s, const float* logits, int rows, int V, RowMeta m, const int* ftok, int cap,
+                   int* out_tok, float* ltrace, int trace_T, const float* H, float* htrace, int d,
+                   int* status) {
+  if (rows > 0)
+    k_argmax<<<rows, 512, 0, s>>>(logits, rows, V, m, ftok, cap, out_tok, ltrace, trace_T, H, htrace, d,
+                                  status);
+}
+void launch_rope_table(cudaStream_t s, float2* tab, int max_ctx, int hd, float theta) {
+  k_rope_table<<<1024, 256, 0, s>>>(tab, max_ctx, hd, theta);
+}
+void launch_copy_rows(cudaStream_t s, const float* src, float* dst, int rows, int d) {
+  if (rows > 0) k_copy_rows<<<1024, 256, 0, s>>>(src, dst, (size_t)rows * d);
+}
+
+#define CDB_INST(T)                                                                                          \
+  template void launch_embed_prefill<T>(cudaStream_t, const T*, int, int, const int*, const int*,          \
+                                        const int*, int, float*, KvGeom, int, int*);                          \
+  template void launch_embed_prelude<T>(cudaStream_t, const T*, int, int, const int*, const int*,          \
+                                        const int*, int, const int*, int, float*, RowMeta, KvGeom, int,       \
+                                        int*);                                                                \
+  template void launch_rmsnorm<T>(cudaStream_t, const float*, const T*, T*, int, int, float, int);          \
+  template void launch_concat<T>(cudaStream_t, const float*, int, const int*, const float*, T*, int, int);  \
+  template void launch_rope_kv<T>(cudaStream_t, const float*, int, const int*, const int*, const int*, int, \
+                                  int, int, T*, KvGeom, int, int, const float2*, int*);                       \
+  template void launch_gate<T>(cudaStream_t, const float*, const T*, float, float, float, int, int,        \
+                               RowMeta, int, int, int, const int8_t*, int, int*, uint8_t*, float*);
+CDB_INST(float)
+CDB_INST(__nv_bfloat16)
+#undef CDB_INST
+
+}  // namespace cdb

@@ -1,0 +1,105 @@
+// Device kernels of the CDB hot path and their host launchers.
+//
+// Layouts (all device memory, carved from the caller's arena):
+//   row buffers   fp32 [rows][d]      residual / core state of each row
+//   row metadata  int32 per row       slot (sequence slot), pos, t (decode
+//                                     forward index), depth (loop steps
+//                                     completed before this step), pend
+//                                     (lookahead flag from the previous step)
+//   KV pool       T [kv_blocks][NSL][2][16][d]   NSL = n_prelude + n_core*r_max
+//                 + n_coda slots per token; core layer l, loop step r lives in
+//                 slot n_prelude + l*r_max + r-1 (depth-indexed cache, §4.2 of
+//                 "Depth-adaptive Inference of Looped Language Models via
+//                 Continuous Depth Batching")
+//   exit table    uint8 [kv_blocks][16]  exit depth of each cached position
+//                 (r_max for prompt positions and tokens still in flight)
+//   block table   int32 [W][max_blocks]  logical block -> physical block
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace cdb {
+
+struct RowMeta {
+  int* slot;
+  int* pos;
+  int* t;
+  int* depth;
+  int* pend;
+};
+
+// Device status word bits (set by bounds checks instead of trapping).
+enum : int {
+  kStatusBadBlock = 1,
+  kStatusBadDepth = 2,
+  kStatusBadToken = 4,
+  kStatusBadRow = 8,
+  kStatusNaN = 16,
+};
+
+struct KvGeom {
+  void* pool;            // T elements
+  const int* bt;         // [W][max_blocks]
+  uint8_t* etab;         // [kv_blocks][16]
+  int max_blocks, kv_blocks, nsl, d;
+};
+
+// ---- elementwise / bookkeeping (kernels.cu) ----
+template <typename T>
+void launch_embed_prefill(cudaStream_t s, const T* E, int d, int V, const int* rslot,
+                          const int* rpos, const int* rtok, int rows, float* X, KvGeom kv,
+                          int r_max, int* status);
+template <typename T>
+void launch_embed_prelude(cudaStream_t s, const T* E, int d, int V, const int* lslot,
+                          const int* lt, const int* lpos, int rows, const int* out_tok,
+                          int max_new_cap, float* X, RowMeta meta, KvGeom kv, int r_max,
+                          int* status);
+void launch_prelude_finish(cudaStream_t s, const float* Tp, RowMeta tmeta, int rows, float* Pb,
+                           RowMeta pmeta, int dst_off, float* estore, int d, int adapter);
+template <typename T>
+void launch_rmsnorm(cudaStream_t s, const float* X, const T* g, T* A, int rows, int d,
+                    float eps, int lda);
+template <typename T>
+void launch_concat(cudaStream_t s, const float* E, int e_per_slot, const int* mslot,
+                   const float* X, T* A, int rows, int d);
+template <typename T>
+void launch_rope_kv(cudaStream_t s, const float* QKV, int rows, const int* mslot,
+                    const int* mpos, const int* mdepth, int depth_uniform, int slot_base,
+                    int clamp, T* Q, KvGeom kv, int H, int hd, const float2* rope,
+                    int* status);
+template <typename T>
+void launch_gate(cudaStream_t s, const float* X, const T* w, float bias, float thr, float eps,
+                 int rows, int d, RowMeta meta, int mode, int r_min, int r_max,
+                 const int8_t* fexit, int max_new_cap, int* pend_new, uint8_t* ring,
+                 float* gtrace);
+void launch_compact(cudaStream_t s, const float* X, RowMeta m, const int* pend_new, int B,
+                    int d, int r_max, int qc_off, float* Xc, RowMeta mc, float* Cb,
+                    RowMeta mb, KvGeom kv, int8_t* out_depth, int max_new_cap, int* status);
+void launch_gather_core(cudaStream_t s, const float* Xc, RowMeta mc, int B_cont, const float* Pb,
+                        RowMeta mp, int n_ref, float* X, RowMeta mx, int d);
+void launch_gather_rows(cudaStream_t s, const float* src, const int* idx, const int* rslot,
+                        const int* rpos, int n, float* dst, RowMeta md, int d);
+void launch_argmax(cudaStream_t s, const float* logits, int rows, int V, RowMeta m,
+                   const int* ftok, int max_new_cap, int* out_tok, float* ltrace,
+                   int trace_T, const float* H, float* htrace, int d, int* status);
+void launch_rope_table(cudaStream_t s, float2* tab, int max_ctx, int hd, float theta);
+void launch_copy_rows(cudaStream_t s, const float* src, float* dst, int rows, int d);
+
+// ---- attention (attention.cu) ----
+template <typename T>
+void launch_attention(cudaStream_t s, const T* Q, int rows, const int* mslot, const int* mpos,
+                      const int* mdepth, int depth_uniform, KvGeom kv, int slot_base,
+                      int clamp, int H, int hd, int split, int max_splits, T* O,
+                      float* part_o, float* part_ml, int* status);
+
+// ---- GEMM (gemm_simt.cu) ----
+enum GemmEpi { kEpiStore = 0, kEpiResid = 1, kEpiSwiglu = 2 };
+// C = A[rows, K] . W[N, K]^T with fp32 accumulation.  kEpiStore: Cf[r][c] = acc;
+// kEpiResid: Cf[r][c] += acc; kEpiSwiglu: Ct[r][c] = silu(A.W^T) * (A.W2^T).
+template <typename T>
+void launch_gemm(cudaStream_t s, int epi, const T* A, int lda, const T* W, const T* W2, int N,
+                 int K, int rows, float* Cf, T* Ct, int ldc);
+
+}  // namespace cdb

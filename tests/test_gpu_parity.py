@@ -1,0 +1,133 @@
+"""GPU parity: the CUDA library against the CPU oracle, through the C ABI.
+
+Bar (from the method's invariance: batching does not change predictions or
+exit decisions): generated tokens and exit depths identical, with gate logits
+within 1e-3 of the threshold and near-tied argmaxes forced to the oracle's
+decision; logits, coda inputs and gate logits within 1e-4 (fp32 models) or
+2e-2 (bf16 models).
+"""
+
+import dataclasses
+
+import numpy as np
+import pytest
+
+from synth import make_requests, make_weights, model_shape, workload
+from tests.gpu_util import compare, gpu_run, oracle_traces
+
+pytestmark = pytest.mark.gpu
+
+FP32_TOL = 1e-4
+BF16_TOL = 2e-2
+
+
+@pytest.fixture(scope="module")
+def tiny():
+    from continuous_depth_batching_gb300 import binding
+    from continuous_depth_batching_gb300.build import build
+    build()
+    shape = model_shape("tiny")
+    wts = make_weights(shape)
+    reqs = make_requests(workload("tiny"), shape.vocab)
+    return shape, wts, binding.device_weights(shape, wts), reqs
+
+
+@pytest.fixture(scope="module")
+def tiny_ref(tiny):
+    shape, wts, _, reqs = tiny
+    return oracle_traces(shape, wts, reqs, "adaptive", keep_logits=16)
+
+
+def test_tiny_refill_matches_oracle(tiny, tiny_ref):
+    shape, _, dw, reqs = tiny
+    out, trace = gpu_run(shape, dw, reqs, tiny_ref, mode="refill", W=4, K=1, trace_tokens=16,
+                         trace_gate=True, attn_split=16)
+    err = compare(out, tiny_ref, FP32_TOL, check_gate=True)
+    depths = np.concatenate([o["exit_depths"] for o in out.values()])
+    assert set(depths.tolist()) >= {2, 3, 4, 8}, "exit depths should spread"
+    assert any(len(r["hist"]) > 1 for r in trace if r["stage"] == "loop"), "refill mixes depths"
+    print("tiny refill max err", err)
+
+
+def test_tiny_no_refill_matches_oracle(tiny, tiny_ref):
+    shape, _, dw, reqs = tiny
+    out, _ = gpu_run(shape, dw, reqs, tiny_ref, mode="no_refill", W=4, trace_tokens=16, attn_split=16)
+    compare(out, tiny_ref, FP32_TOL)
+
+
+def test_tiny_fixed_depth_matches_oracle(tiny):
+    shape, wts, dw, reqs = tiny
+    ref = oracle_traces(shape, wts, reqs[:4], "fixed", keep_logits=16)
+    out, trace = gpu_run(shape, dw, reqs[:4], ref, mode="fixed_depth", W=4, trace_tokens=16, attn_split=16)
+    compare(out, ref, FP32_TOL)
+    assert all(len(r["hist"]) == 1 for r in trace if r["stage"] == "loop"), "fixed depth runs cohorts"
+    assert all(list(o["exit_depths"]) == [shape.r_max] * 15 for o in out.values())
+
+
+def test_modes_and_batch_sizes_agree_bit_exactly(tiny, tiny_ref):
+    """Refill, no-refill and one-slot sequential runs produce identical bits."""
+    shape, _, dw, reqs = tiny
+    runs = [gpu_run(shape, dw, reqs, tiny_ref, mode=m, W=w, trace_tokens=16, attn_split=16)[0]
+            for m, w in [("refill", 4), ("no_refill", 4), ("refill", 1), ("refill", 8)]]
+    for other in runs[1:]:
+        for sid in runs[0]:
+            np.testing.assert_array_equal(runs[0][sid]["tokens"], other[sid]["tokens"])
+            np.testing.assert_array_equal(runs[0][sid]["exit_depths"], other[sid]["exit_depths"])
+            np.testing.assert_array_equal(runs[0][sid]["logits"], other[sid]["logits"])
+
+
+def test_chunked_prefill_matches_oracle(tiny, tiny_ref):
+    """Prompts split across prefill batches of M=20 tokens give the same result."""
+    shape, _, dw, reqs = tiny
+    out, trace = gpu_run(shape, dw, reqs, tiny_ref, mode="refill", W=4, M=20, trace_tokens=16, attn_split=16)
+    compare(out, tiny_ref, FP32_TOL)
+    assert any(r["stage"] == "prefill" and r["prefill_tokens"] == 20 for r in trace)
+
+
+def test_single_split_attention_matches(tiny, tiny_ref):
+    shape, _, dw, reqs = tiny
+    out, _ = gpu_run(shape, dw, reqs[:3], {k: tiny_ref[k] for k in range(3)}, mode="refill", W=4,
+                     trace_tokens=16, attn_split=0)
+    compare(out, {k: tiny_ref[k] for k in range(3)}, FP32_TOL)
+
+
+def _mini(dtype, **kw):
+    base = dict(name="mini", vocab=1024, d_model=256, n_heads=2, head_dim=128, ffn=512, n_prelude=0,
+                n_core=2, n_coda=0, r_max=5, r_min=2, has_adapter=False, dtype=dtype, gate_bias=0.12)
+    base.update(kw)
+    return dataclasses.replace(model_shape("tiny"), **base)
+
+
+def _reqs(shape, n, plo, phi, gen, seed=5):
+    rng = np.random.default_rng(seed)
+    return [dict(seq_id=i, prompt=rng.integers(0, shape.vocab, int(rng.integers(plo, phi + 1))).astype(np.int32),
+                 gen_len=gen, replay=None) for i in range(n)]
+
+
+def test_bf16_model_matches_oracle():
+    from continuous_depth_batching_gb300 import binding
+    shape = _mini("bf16")
+    wts = make_weights(shape)
+    reqs = _reqs(shape, 6, 20, 70, 10)
+    ref = oracle_traces(shape, wts, reqs, "adaptive", keep_logits=10)
+    out, _ = gpu_run(shape, binding.device_weights(shape, wts), reqs, ref, mode="refill", W=3, K=1,
+                     trace_tokens=10, trace_gate=True, attn_split=32)
+    err = compare(out, ref, BF16_TOL, check_gate=True)
+    print("bf16 mini max err", err)
+
+
+@pytest.mark.parametrize("dtype,tol", [("fp32", FP32_TOL), ("bf16", BF16_TOL)])
+def test_huginn_like_model_matches_oracle(dtype, tol):
+    """Prelude and coda transformer layers, adapter before every loop step, hd 96."""
+    from continuous_depth_batching_gb300 import binding
+    shape = _mini(dtype, d_model=192, n_heads=2, head_dim=96, ffn=384, n_prelude=1, n_core=2, n_coda=1,
+                  has_adapter=True, r_max=6, gate_bias=0.05)
+    wts = make_weights(shape)
+    reqs = _reqs(shape, 5, 10, 40, 8, seed=9)
+    rng = np.random.default_rng(1)
+    for r in reqs[:2]:  # two sequences replay recorded depths, the rest use the live gate
+        r["replay"] = rng.integers(2, shape.r_max + 1, r["gen_len"] - 1).astype(np.int8)
+    ref = oracle_traces(shape, wts, reqs, "adaptive", keep_logits=8)
+    out, _ = gpu_run(shape, binding.device_weights(shape, wts), reqs, ref, mode="refill", W=3, K=2,
+                     trace_tokens=8, trace_gate=True, attn_split=16)
+    compare(out, ref, tol, check_gate=True)
