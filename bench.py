@@ -1,0 +1,330 @@
+#!/usr/bin/env python3
+"""Decoded tokens/s of continuous depth batching on one GB300.
+
+Workload: the Ouro-1.4B-shaped fully looped model (d 2048, 16x128 heads,
+SwiGLU 5632, 24-layer core looped up to 4 times, bf16, seeded random weights)
+decoding 256 synthetic requests (prompt lengths uniform 128..1024, 256
+generated tokens each) in refill mode with W = 64 active sequences, M = 8192
+prefill tokens, K = 1, 16-token KV blocks.
+
+A step is one recurrent-core loop step of the engine (batch re-formation,
+24 shared blocks at each token's own depth, exit gate, compaction) together
+with the coda / prelude / prefill stages the scheduler interleaves before it.
+`value` counts the tokens generated during K timed steps after W warm-up
+steps, with the model and all requests resident (device-timed with CUDA events
+on the library's compute stream).  `e2e` runs the whole offline job through
+the public API (admit host prompts ... drain host results), wall-clocked.
+
+--impl reference times the CPU oracle (the plain per-sequence decoder) on the
+host cores, one generated token per step.
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "decoded tokens/sec at 1 GB300 (refill vs fixed-depth); core-step % of roofline"
+UNIT = "tokens/s"
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=300)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="ouro")
+    ap.add_argument("--mode", default="refill", choices=["refill", "no_refill", "fixed_depth"])
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=20.0)
+    return ap.parse_args()
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d["hbm_gbs"], d["bf16_tflops_sustained"], "measured"
+    return 6800.0, 1700.0, "fallback"
+
+
+class Clocks:
+    """nvidia-smi samples during the timed region."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index=0):
+        self.f = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+        self.index = index
+        self.p = None
+
+    def start(self):
+        try:
+            self.p = subprocess.Popen(["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.Q}",
+                                       "--format=csv,noheader,nounits", "-lms", "100"],
+                                      stdout=self.f, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.p = None
+
+    def stop(self):
+        if self.p is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.p.terminate()
+        try:
+            self.p.wait(5)
+        except subprocess.TimeoutExpired:
+            self.p.kill()
+        self.f.flush()
+        self.f.seek(0)
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.f.read().splitlines():
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        os.unlink(self.f.name)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def dist_setup():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def cpu_baseline(shape, wts, reqs, seconds):
+    """The oracle as it stands, on a bounded sample: shortest prompts, prefill + leading tokens."""
+    import numpy as np  # noqa: F401
+    from oracle.model import OracleModel, iter_decode
+    om = OracleModel(shape, wts)
+    order = sorted(reqs, key=lambda r: len(r["prompt"]))
+    t0 = time.perf_counter()
+    tokens, done = 0, []
+    for r in order:
+        n = 0
+        for _ in iter_decode(om, r["prompt"], r["gen_len"]):
+            n += 1
+            tokens += 1
+            if time.perf_counter() - t0 > seconds:
+                break
+        done.append((r["seq_id"], len(r["prompt"]), n))
+        if time.perf_counter() - t0 > seconds:
+            break
+    dt = time.perf_counter() - t0
+    desc = "; ".join(f"seq {s} (prompt {p}): prefill + {n} generated tokens" for s, p, n in done)
+    return {"value": tokens / dt, "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
+            "sample": desc + f", {dt:.1f} s, fp64 numpy oracle"}
+
+
+def run_reference(args):
+    rank, world, _ = dist_setup()
+    if rank != 0:
+        return
+    from oracle.model import OracleModel, iter_decode
+    from synth import make_requests, make_weights, model_shape, workload
+    wl = workload(args.workload)
+    shape = model_shape(wl.model)
+    wts = make_weights(shape)
+    reqs = sorted(make_requests(wl, shape.vocab, shape.r_max, shape.r_min), key=lambda r: len(r["prompt"]))
+    om = OracleModel(shape, wts)
+
+    def stream():
+        for r in reqs:
+            for _ in iter_decode(om, r["prompt"], r["gen_len"]):
+                yield r["seq_id"]
+
+    g = stream()
+    for _ in range(args.warmup):
+        next(g)
+    t0 = time.perf_counter()
+    used = set()
+    for _ in range(args.steps):
+        used.add(next(g))
+    dt = time.perf_counter() - t0
+    v = args.steps / dt
+    line = {"impl": "reference", "metric": METRIC, "value": v, "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3 / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": _config(wl, shape, args.mode, "oracle, one generated token per step"),
+            "cpu_baseline": {"value": v, "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
+                             "sample": f"sequences {sorted(used)} in prompt-length order, one token per step"},
+            "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def _config(wl, shape, mode, flush):
+    return {"workload": f"{wl.name}-shaped offline decode: {wl.n_seqs} seqs, prompts U[{wl.prompt_lo},"
+                        f"{wl.prompt_hi}], {wl.gen_hi} generated, W={wl.W}, M={wl.M}, K={wl.K}",
+            "model": f"{shape.name}: d{shape.d_model} {shape.n_heads}x{shape.head_dim} ffn{shape.ffn} "
+                     f"{shape.n_prelude}-{shape.n_core}-{shape.n_coda} r_max{shape.r_max} {shape.dtype}",
+            "mode": mode, "global_batch": wl.W, "seq_len": wl.prompt_hi + wl.gen_hi,
+            "parallelism": "replicas", "l2": flush}
+
+
+def run_ours(args):
+    import numpy as np
+    import torch
+
+    from continuous_depth_batching_gb300 import binding
+    from continuous_depth_batching_gb300.build import build
+    from synth import make_requests, make_weights, model_shape, workload
+
+    rank, world, local = dist_setup()
+    torch.cuda.set_device(local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    build()
+    wl = workload(args.workload)
+    shape = model_shape(wl.model)
+    wts = make_weights(shape)
+    dw = binding.device_weights(shape, wts)
+    reqs = make_requests(wl, shape.vocab, shape.r_max, shape.r_min)
+    max_ctx = (wl.prompt_hi + wl.gen_hi - 1 + 15) // 16 * 16
+    kw = dict(mode=args.mode, W=wl.W, M=wl.M, K=wl.K, max_ctx=max_ctx, max_new_cap=wl.gen_hi)
+
+    def admit_all(eng):
+        for r in reqs:
+            eng.admit(r["seq_id"], r["prompt"], r["gen_len"], r["replay"])
+
+    def advance(eng, n_core):
+        toks = cores = 0
+        while cores < n_core:
+            rc, info = eng.step_boundary()
+            toks += info.new_tokens
+            if rc == binding.DONE:
+                break
+            if rc == binding.IDLE:
+                rc, info = eng.step_core()
+                cores += 1
+        return toks, cores
+
+    eng = binding.Engine(shape, dw, **kw)
+    admit_all(eng)
+    advance(eng, args.warmup)
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    stream = torch.cuda.current_stream()
+    eng.profile_enable(True)
+    l0 = binding.kernel_launches()
+    clk = Clocks(local)
+    clk.start()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    e0.record(stream)
+    toks, cores = advance(eng, args.steps)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    clocks = clk.stop()
+    if world > 1:
+        torch.distributed.barrier()
+    ms = e0.elapsed_time(e1)
+    launches = binding.kernel_launches() - l0
+    prof = eng.profile_read()
+    eng.profile_enable(False)
+    eng.close()
+    tot_toks = toks
+    if world > 1:
+        t = torch.tensor([ms, toks], dtype=torch.float64, device="cuda")
+        mx = t.clone()
+        torch.distributed.all_reduce(mx, op=torch.distributed.ReduceOp.MAX)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.SUM)
+        ms, tot_toks = float(mx[0]), float(t[1])
+    value = tot_toks / (ms / 1e3)
+
+    # Roofline of the dominant kernel class (largest device time in the window).
+    hbm, tf, src = peaks()
+    dom = max((k for k in prof if prof[k]["launches"] > 0), key=lambda k: prof[k]["ms"])
+    st = prof[dom]
+    per_launch_ms = st["ms"] / st["launches"]
+    inten = st["flops"] / max(st["bytes"], 1.0)
+    if inten < tf * 1e12 / (hbm * 1e9):
+        achieved = st["bytes"] / st["launches"] / (per_launch_ms / 1e3) / 1e9
+        roof = {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm}
+    else:
+        achieved = st["flops"] / st["launches"] / (per_launch_ms / 1e3) / 1e12
+        roof = {"bound": "tensor", "achieved": achieved, "peak": tf, "unit": "TFLOP/s", "frac": achieved / tf}
+    roof.update({"kernel": dom, "traffic": None, "peak_source": src,
+                 "share_of_step": st["ms"] / ms,
+                 "classes": {k: {"launches": v["launches"], "ms": round(v["ms"], 3),
+                                 "GBps": (v["bytes"] / (v["ms"] / 1e3) / 1e9) if v["ms"] else None,
+                                 "TFps": (v["flops"] / (v["ms"] / 1e3) / 1e12) if v["ms"] else None}
+                             for k, v in prof.items()}})
+
+    e2e = None
+    if not args.no_e2e:
+        eng2 = binding.Engine(shape, dw, **kw)
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        admit_all(eng2)
+        n_core = 0
+        while True:
+            rc, _ = eng2.step_boundary()
+            if rc == binding.DONE:
+                break
+            if rc == binding.IDLE:
+                eng2.step_core()
+                n_core += 1
+        res = eng2.drain(cap=len(reqs))
+        torch.cuda.synchronize()
+        dt = time.perf_counter() - t0
+        gen = sum(len(r["tokens"]) for r in res)
+        h2d, d2h = eng2.io_bytes()
+        eng2.close()
+        e2e = {"value": gen / dt, "unit": UNIT, "h2d_bytes_per_step": h2d / max(n_core, 1),
+               "d2h_bytes_per_step": d2h / max(n_core, 1), "core_steps": n_core, "seconds": dt,
+               "tokens": gen, "finished_sequences": len(res)}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(shape, wts, reqs, args.cpu_seconds)
+
+    if rank == 0:
+        line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+                "warmup": args.warmup, "ms_per_step": ms / max(cores, 1), "higher_is_better": True,
+                "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+                "config": _config(wl, shape, args.mode, "inputs larger than L2 (2.5 GB of weights per step)"),
+                "roofline": roof, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches,
+                "clocks": clocks, "tokens_in_window": tot_toks, "core_steps": cores}
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -52,7 +52,8 @@ class SchedCfg(C.Structure):
 class StepInfo(C.Structure):
     _fields_ = [("stage", C.c_int), ("batch", C.c_int), ("prefill_tokens", C.c_int), ("stage2", C.c_int),
                 ("batch2", C.c_int), ("exits", C.c_int), ("q_r", C.c_int), ("q_c", C.c_int), ("q_p", C.c_int),
-                ("q_d", C.c_int), ("depth_hist", C.c_int * MAX_DEPTH), ("step_index", C.c_int64)]
+                ("q_d", C.c_int), ("depth_hist", C.c_int * MAX_DEPTH), ("step_index", C.c_int64),
+                ("new_tokens", C.c_int)]
 
     def as_dict(self):
         d = {f: getattr(self, f) for f, _ in self._fields_ if f != "depth_hist"}
@@ -64,6 +65,11 @@ class Result(C.Structure):
     _fields_ = [("seq_id", C.c_int64), ("n_tokens", C.c_int), ("tokens", C.POINTER(C.c_int32)),
                 ("exit_depths", C.POINTER(C.c_int8)), ("gate_logits", C.POINTER(C.c_float)),
                 ("logits", C.POINTER(C.c_float)), ("hidden", C.POINTER(C.c_float))]
+
+
+class KernelStat(C.Structure):
+    _fields_ = [("name", C.c_char * 32), ("launches", C.c_int64), ("ms", C.c_double), ("bytes", C.c_double),
+                ("flops", C.c_double)]
 
 
 class TraceRow(C.Structure):
@@ -105,6 +111,11 @@ def lib(path: str | None = None) -> C.CDLL:
     L.cdb_last_error.argtypes = [C.c_void_p]
     L.cdb_last_error.restype = C.c_char_p
     L.cdb_trace_enable.argtypes = [C.c_void_p, C.c_int]
+    L.cdb_profile_enable.argtypes = [C.c_void_p, C.c_int]
+    L.cdb_profile_read.argtypes = [C.c_void_p, C.POINTER(KernelStat), C.c_int, C.POINTER(C.c_int)]
+    L.cdb_kernel_launches.restype = C.c_int64
+    L.cdb_kernel_launches.argtypes = []
+    L.cdb_io_bytes.argtypes = [C.c_void_p, C.POINTER(C.c_int64), C.POINTER(C.c_int64)]
     L.cdb_trace_read.argtypes = [C.c_void_p, C.POINTER(TraceRow), C.c_int, C.POINTER(C.c_int)]
     L.cdb_sim_create.argtypes = [C.c_int] * 8 + [C.c_float, C.c_int, C.c_int, C.POINTER(C.c_void_p)]
     L.cdb_sim_admit.argtypes = [C.c_void_p, C.c_int64, C.c_int, C.c_int, C.POINTER(C.c_int8)]
@@ -116,6 +127,10 @@ def lib(path: str | None = None) -> C.CDLL:
     L.cdb_sim_free.restype = None
     _lib = L
     return L
+
+
+def kernel_launches() -> int:
+    return int(lib().cdb_kernel_launches())
 
 
 class CdbError(RuntimeError):
@@ -264,6 +279,21 @@ class Engine:
                 r["hidden"] = b["hidden"].reshape(self.trace_tokens, s.d_model).copy()
             out.append(r)
         return out
+
+    def profile_enable(self, on=True):
+        self._check(self.L.cdb_profile_enable(self.ctx, int(on)))
+
+    def profile_read(self):
+        st = (KernelStat * 8)()
+        n = C.c_int()
+        self._check(self.L.cdb_profile_read(self.ctx, st, 8, C.byref(n)))
+        return {st[i].name.decode(): dict(launches=st[i].launches, ms=st[i].ms, bytes=st[i].bytes,
+                                          flops=st[i].flops) for i in range(n.value)}
+
+    def io_bytes(self):
+        a, b = C.c_int64(), C.c_int64()
+        self._check(self.L.cdb_io_bytes(self.ctx, C.byref(a), C.byref(b)))
+        return a.value, b.value
 
     def trace_enable(self, on=True):
         self._check(self.L.cdb_trace_enable(self.ctx, int(on)))

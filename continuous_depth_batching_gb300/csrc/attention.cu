@@ -173,10 +173,11 @@ static void attn_hd(cudaStream_t s, const T* Q, int rows, const int* mslot, cons
                     int depth_uniform, KvGeom kv, int slot_base, int clamp, int H, int split, int max_splits,
                     T* O, float* part_o, float* part_ml, int* status) {
   dim3 grid(max_splits, (H + 3) / 4, rows);
+  count_launch();
   k_attn<T, HD><<<grid, 128, 0, s>>>(Q, rows, mslot, mpos, mdepth, depth_uniform, kv, slot_base, clamp, H,
                                      split, max_splits, O, part_o, part_ml, status);
   if (max_splits > 1)
-    k_attn_combine<T><<<rows * H, 128, 0, s>>>(rows, mpos, H, HD, kv.d, split, max_splits, part_o, part_ml, O);
+    count_launch(), k_attn_combine<T><<<rows * H, 128, 0, s>>>(rows, mpos, H, HD, kv.d, split, max_splits, part_o, part_ml, O);
 }
 
 template <typename T>

@@ -148,6 +148,20 @@ struct cdb_ctx {
   std::unique_ptr<cdb::Scheduler> sched;
   std::string err;
   bool dead = false;
+  int64_t io_h2d = 0, io_d2h = 0;
+  // kernel timing (cdb_profile_enable)
+  bool prof_on = false;
+  struct ProfEv {
+    int cls;
+    cudaEvent_t a, b;
+    double bytes, flops;
+  };
+  std::vector<ProfEv> prof_live;
+  std::vector<cudaEvent_t> ev_pool;
+  struct Stat {
+    int64_t launches = 0;
+    double ms = 0, bytes = 0, flops = 0;
+  } stats[3];
 };
 
 namespace cdb {
@@ -209,7 +223,55 @@ static int upload(cdb_ctx* x, void* dst, const void* src, size_t n) {
   std::memcpy(h, src, n);
   x->seg_off = (x->seg_off + n + 15) / 16 * 16;
   CK(cudaMemcpyAsync(dst, h, n, cudaMemcpyHostToDevice, x->cs));
+  x->io_h2d += (int64_t)n;
   return CDB_OK;
+}
+
+static const char* kProfNames[3] = {"attention", "gemm", "prefill_attention"};
+
+static cudaEvent_t pool_event(cdb_ctx* x) {
+  if (!x->ev_pool.empty()) {
+    cudaEvent_t e = x->ev_pool.back();
+    x->ev_pool.pop_back();
+    return e;
+  }
+  cudaEvent_t e = nullptr;
+  cudaEventCreate(&e);
+  return e;
+}
+
+// Bracket one launch with events when timing is on; returns a handle or -1.
+static int prof_begin(cdb_ctx* x, int cls) {
+  if (!x->prof_on) return -1;
+  cdb_ctx::ProfEv ev{cls, pool_event(x), pool_event(x), 0, 0};
+  cudaEventRecord(ev.a, x->cs);
+  x->prof_live.push_back(ev);
+  return (int)x->prof_live.size() - 1;
+}
+
+static void prof_end(cdb_ctx* x, int h, double bytes, double flops) {
+  if (h < 0) return;
+  auto& ev = x->prof_live[h];
+  cudaEventRecord(ev.b, x->cs);
+  ev.bytes = bytes;
+  ev.flops = flops;
+}
+
+// Fold finished event pairs into the per-class totals (after a sync).
+static void prof_collect(cdb_ctx* x) {
+  for (auto& ev : x->prof_live) {
+    float ms = 0.f;
+    if (cudaEventElapsedTime(&ms, ev.a, ev.b) == cudaSuccess) {
+      auto& st = x->stats[ev.cls];
+      st.launches += 1;
+      st.ms += ms;
+      st.bytes += ev.bytes;
+      st.flops += ev.flops;
+    }
+    x->ev_pool.push_back(ev.a);
+    x->ev_pool.push_back(ev.b);
+  }
+  x->prof_live.clear();
 }
 
 class GpuExecutor : public Executor {
@@ -241,8 +303,20 @@ class GpuExecutor : public Executor {
   }
 
   template <typename T>
+  void gemm(int epi, const T* A, int lda, const void* W, const void* W2, int N, int K, int rows, float* Cf, T* Ct,
+            int ldc) {
+    cdb_ctx* x = x_;
+    const double es = sizeof(T), nw = W2 ? 2.0 : 1.0;
+    const int h = prof_begin(x, 1);
+    launch_gemm<T>(x->cs, epi, A, lda, (const T*)W, (const T*)W2, N, K, rows, Cf, Ct, ldc);
+    const double out_b = epi == kEpiSwiglu ? es : (epi == kEpiResid ? 8.0 : 4.0);
+    prof_end(x, h, nw * N * (double)K * es + (double)rows * K * es + (double)rows * N * out_b,
+             2.0 * nw * rows * (double)N * K);
+  }
+
+  template <typename T>
   int block(const LayerW& lw, float* X, int rows, const int* mslot, const int* mpos, const int* mdepth,
-            int depth_uniform, int slot_base, int clamp, bool decode) {
+            int depth_uniform, int slot_base, int clamp, bool decode, double sumL) {
     cdb_ctx* x = x_;
     const Layout& L = x->L;
     const int d = x->m.d_model, f = x->m.ffn, H = x->m.n_heads, hd = x->m.head_dim;
@@ -254,18 +328,22 @@ class GpuExecutor : public Executor {
     T* Mid = at<T>(x, L.Mid);
     int* st = at<int>(x, L.status);
     KvGeom kv = geom();
+    const double es = sizeof(T);
     launch_rmsnorm<T>(s, X, (const T*)lw.attn_norm, A, rows, d, x->m.rms_eps, d);
-    launch_gemm<T>(s, kEpiStore, A, d, (const T*)lw.wqkv, nullptr, 3 * d, d, rows, QKV, nullptr, 3 * d);
+    gemm<T>(kEpiStore, A, d, lw.wqkv, nullptr, 3 * d, d, rows, QKV, nullptr, 3 * d);
     launch_rope_kv<T>(s, QKV, rows, mslot, mpos, mdepth, depth_uniform, slot_base, clamp, Q, kv, H, hd,
                       at<float2>(x, L.rope), st);
     const int split = decode ? L.split : (1 << 30);
     const int msp = decode ? L.max_splits : 1;
+    const int ha = prof_begin(x, decode ? 0 : 2);
     launch_attention<T>(s, Q, rows, mslot, mpos, mdepth, depth_uniform, kv, slot_base, clamp, H, hd, split, msp,
                         O, at<float>(x, L.part_o), at<float>(x, L.part_ml), st);
-    launch_gemm<T>(s, kEpiResid, O, d, (const T*)lw.wo, nullptr, d, d, rows, X, nullptr, d);
+    // Each key row (K and V, d elements each) is read once; q in, o out.
+    prof_end(x, ha, sumL * 2.0 * d * es + 2.0 * rows * d * es, 4.0 * d * sumL);
+    gemm<T>(kEpiResid, O, d, lw.wo, nullptr, d, d, rows, X, nullptr, d);
     launch_rmsnorm<T>(s, X, (const T*)lw.mlp_norm, A, rows, d, x->m.rms_eps, d);
-    launch_gemm<T>(s, kEpiSwiglu, A, d, (const T*)lw.wg, (const T*)lw.wu, f, d, rows, nullptr, Mid, f);
-    launch_gemm<T>(s, kEpiResid, Mid, f, (const T*)lw.wd, nullptr, d, f, rows, X, nullptr, d);
+    gemm<T>(kEpiSwiglu, A, d, lw.wg, lw.wu, f, d, rows, nullptr, Mid, f);
+    gemm<T>(kEpiResid, Mid, f, lw.wd, nullptr, d, f, rows, X, nullptr, d);
     return CDB_OK;
   }
 
@@ -275,7 +353,7 @@ class GpuExecutor : public Executor {
     const int d = x->m.d_model;
     T* A = at<T>(x, x->L.A);
     launch_concat<T>(x->cs, E, e_per_slot, mslot, X, A, rows, d);
-    launch_gemm<T>(x->cs, kEpiStore, A, 2 * d, (const T*)x->adapter, nullptr, d, 2 * d, rows, X, nullptr, d);
+    gemm<T>(kEpiStore, A, 2 * d, x->adapter, nullptr, d, 2 * d, rows, X, nullptr, d);
     return CDB_OK;
   }
 
@@ -288,7 +366,7 @@ class GpuExecutor : public Executor {
     T* A = at<T>(x, L.A);
     float* lg = at<float>(x, L.logits);
     launch_rmsnorm<T>(x->cs, Hrows, (const T*)x->final_norm, A, n, d, x->m.rms_eps, d);
-    launch_gemm<T>(x->cs, kEpiStore, A, d, (const T*)x->lm_head, nullptr, V, d, n, lg, nullptr, V);
+    gemm<T>(kEpiStore, A, d, x->lm_head, nullptr, V, d, n, lg, nullptr, V);
     const bool tr = x->c.trace_tokens > 0;
     launch_argmax(x->cs, lg, n, V, m, at<int>(x, L.ftok), cap, at<int>(x, L.out_tok), tr ? at<float>(x, L.ltrace) : nullptr,
                   x->c.trace_tokens, Hrows, tr ? at<float>(x, L.htrace) : nullptr, d, at<int>(x, L.status));
@@ -319,7 +397,9 @@ class GpuExecutor : public Executor {
     float* Xp = at<float>(x, L.Xp);
     launch_embed_prefill<T>(x->cs, (const T*)x->embed, d, x->m.vocab, rslot, rpos, rtok, n, Xp, geom(), x->m.r_max,
                             at<int>(x, L.status));
-    for (int i = 0; i < x->m.n_prelude; ++i) block<T>(x->pre[i], Xp, n, rslot, rpos, nullptr, 1, i, 0, false);
+    double sumL = 0;
+    for (int i = 0; i < n; ++i) sumL += b[i] + 1;
+    for (int i = 0; i < x->m.n_prelude; ++i) block<T>(x->pre[i], Xp, n, rslot, rpos, nullptr, 1, i, 0, false, sumL);
     float* Ep = at<float>(x, L.Ep);
     if (x->m.has_adapter) {
       launch_copy_rows(x->cs, Xp, Ep, n, d);
@@ -328,10 +408,11 @@ class GpuExecutor : public Executor {
     for (int r = 1; r <= x->m.r_max; ++r) {
       if (x->m.has_adapter) adapter_step<T>(Xp, n, Ep, 0, rslot);
       for (int l = 0; l < x->m.n_core; ++l)
-        block<T>(x->core[l], Xp, n, rslot, rpos, nullptr, r, x->m.n_prelude + l * x->m.r_max, 1, false);
+        block<T>(x->core[l], Xp, n, rslot, rpos, nullptr, r, x->m.n_prelude + l * x->m.r_max, 1, false, sumL);
     }
     const int cbase = x->m.n_prelude + x->m.n_core * x->m.r_max;
-    for (int j = 0; j < x->m.n_coda; ++j) block<T>(x->coda[j], Xp, n, rslot, rpos, nullptr, 1, cbase + j, 0, false);
+    for (int j = 0; j < x->m.n_coda; ++j)
+      block<T>(x->coda[j], Xp, n, rslot, rpos, nullptr, 1, cbase + j, 0, false, sumL);
     const int nd = (int)p.done_rows.size();
     if (nd > 0) {
       if ((rc = upload(x, at<int>(x, L.done_idx), p.done_rows.data(), nd * 4)) < 0) return rc;
@@ -367,7 +448,9 @@ class GpuExecutor : public Executor {
     RowMeta tm = meta_at(x, L.meta[4]);
     launch_embed_prelude<T>(x->cs, (const T*)x->embed, d, x->m.vocab, ls, lt, lp, n, at<int>(x, L.out_tok),
                             x->c.max_new_cap, Tp, tm, geom(), x->m.r_max, at<int>(x, L.status));
-    for (int i = 0; i < x->m.n_prelude; ++i) block<T>(x->pre[i], Tp, n, tm.slot, tm.pos, nullptr, 1, i, 0, true);
+    double sumL = 0;
+    for (int i = 0; i < n; ++i) sumL += c[i] + 1;
+    for (int i = 0; i < x->m.n_prelude; ++i) block<T>(x->pre[i], Tp, n, tm.slot, tm.pos, nullptr, 1, i, 0, true, sumL);
     launch_prelude_finish(x->cs, Tp, tm, n, at<float>(x, L.rows[2]), meta_at(x, L.meta[2]), p.dst_off,
                           x->m.has_adapter ? at<float>(x, L.estore) : nullptr, d, x->m.has_adapter);
     CK(cudaGetLastError());
@@ -387,8 +470,10 @@ class GpuExecutor : public Executor {
     launch_gather_core(x->cs, at<float>(x, L.rows[1]), meta_at(x, L.meta[1]), p.B_cont, at<float>(x, L.rows[2]),
                        meta_at(x, L.meta[2]), p.n_ref, X, mx, d);
     if (x->m.has_adapter) adapter_step<T>(X, B, at<float>(x, L.estore), 1, mx.slot);
+    double sumL = 0;
+    for (const Tok& t : *p.rows) sumL += t.pos + 1;
     for (int l = 0; l < x->m.n_core; ++l)
-      block<T>(x->core[l], X, B, mx.slot, mx.pos, mx.depth, 0, x->m.n_prelude + l * x->m.r_max, 1, true);
+      block<T>(x->core[l], X, B, mx.slot, mx.pos, mx.depth, 0, x->m.n_prelude + l * x->m.r_max, 1, true, sumL);
     const int ri = (int)(p.step % kRing);
     uint8_t* ring = at<uint8_t>(x, L.ring) + (size_t)ri * x->c.W;
     launch_gate<T>(x->cs, X, (const T*)x->gate_w, x->m.gate_bias, x->m.gate_threshold, x->m.rms_eps, B, d, mx,
@@ -402,6 +487,7 @@ class GpuExecutor : public Executor {
     CK(cudaEventRecord(x->ev_core[ri], x->cs));
     CK(cudaStreamWaitEvent(x->ps, x->ev_core[ri], 0));
     CK(cudaMemcpyAsync(x->pend_host + (size_t)ri * x->c.W, ring, x->c.W, cudaMemcpyDeviceToHost, x->ps));
+    x->io_d2h += x->c.W;
     CK(cudaEventRecord(x->ev_flags[ri], x->ps));
     return CDB_OK;
   }
@@ -430,7 +516,10 @@ class GpuExecutor : public Executor {
       float* Tc = at<float>(x, L.rows[4]);
       launch_copy_rows(x->cs, Cb, Tc, n, d);
       const int cbase = x->m.n_prelude + x->m.n_core * x->m.r_max;
-      for (int j = 0; j < x->m.n_coda; ++j) block<T>(x->coda[j], Tc, n, mb.slot, mb.pos, nullptr, 1, cbase + j, 0, true);
+      double sumL = 0;
+      for (const Tok& t : rows) sumL += t.pos + 1;
+      for (int j = 0; j < x->m.n_coda; ++j)
+        block<T>(x->coda[j], Tc, n, mb.slot, mb.pos, nullptr, 1, cbase + j, 0, true, sumL);
       Hrows = Tc;
     }
     head<T>(Hrows, n, mb);
@@ -465,6 +554,7 @@ class GpuExecutor : public Executor {
       CK(cudaMemcpyAsync(h + o, at<float>(x, L.htrace) + (size_t)slot * x->c.trace_tokens * x->m.d_model, n,
                          cudaMemcpyDeviceToHost, x->cs));
     }
+    x->io_d2h += (int64_t)o + (x->c.trace_tokens > 0 ? (int64_t)x->c.trace_tokens * x->m.d_model * 4 : 0);
     PendingResult& pr = x->pending[slot];
     CK(cudaEventRecord(pr.ev, x->cs));
     pr.id = s.id;
@@ -529,6 +619,7 @@ static int check_status(cdb_ctx* x) {
   int st = 0;
   cudaError_t e = cudaMemcpyAsync(&st, at<int>(x, x->L.status), 4, cudaMemcpyDeviceToHost, x->cs);
   if (e != cudaSuccess) return cuda_fail(x, e, "status copy");
+  x->io_d2h += 4;
   e = cudaStreamSynchronize(x->cs);
   if (e != cudaSuccess) return cuda_fail(x, e, "cudaStreamSynchronize");
   if (st != 0) {
@@ -737,7 +828,7 @@ int cdb_drain(cdb_ctx* x, cdb_result* buf, int cap, int* n_out) {
 
 void cdb_free(cdb_ctx* x) {
   if (!x) return;
-  if (x->cs || true) cudaStreamSynchronize(x->cs);
+  cudaStreamSynchronize(x->cs);
   if (x->ps) cudaStreamSynchronize(x->ps);
   for (int i = 0; i < kStageSegs; ++i) cudaEventDestroy(x->seg_ev[i]);
   for (int i = 0; i < kRing; ++i) {
@@ -745,6 +836,11 @@ void cdb_free(cdb_ctx* x) {
     cudaEventDestroy(x->ev_flags[i]);
   }
   for (auto& p : x->pending) cudaEventDestroy(p.ev);
+  for (auto& ev : x->prof_live) {
+    cudaEventDestroy(ev.a);
+    cudaEventDestroy(ev.b);
+  }
+  for (auto e : x->ev_pool) cudaEventDestroy(e);
   if (x->stage) cudaFreeHost(x->stage);
   if (x->pend_host) cudaFreeHost(x->pend_host);
   if (x->res_host) cudaFreeHost(x->res_host);
@@ -753,6 +849,41 @@ void cdb_free(cdb_ctx* x) {
 }
 
 const char* cdb_last_error(const cdb_ctx* x) { return x ? x->err.c_str() : "null context"; }
+
+int64_t cdb_kernel_launches(void) { return (int64_t)launch_count(); }
+
+int cdb_io_bytes(const cdb_ctx* x, int64_t* h2d, int64_t* d2h) {
+  if (!x || !h2d || !d2h) return CDB_ERR_ARG;
+  *h2d = x->io_h2d;
+  *d2h = x->io_d2h;
+  return CDB_OK;
+}
+
+int cdb_profile_enable(cdb_ctx* x, int on) {
+  if (!x) return CDB_ERR_ARG;
+  x->prof_on = on != 0;
+  return CDB_OK;
+}
+
+int cdb_profile_read(cdb_ctx* x, cdb_kernel_stat* out, int cap, int* n_out) {
+  if (!x || !n_out || (cap > 0 && !out)) return CDB_ERR_ARG;
+  cudaError_t e = cudaStreamSynchronize(x->cs);
+  if (e != cudaSuccess) return cuda_fail(x, e, "cudaStreamSynchronize");
+  prof_collect(x);
+  int n = 0;
+  for (int c = 0; c < 3 && n < cap; ++c) {
+    std::memset(&out[n], 0, sizeof(out[n]));
+    std::strncpy(out[n].name, kProfNames[c], sizeof(out[n].name) - 1);
+    out[n].launches = x->stats[c].launches;
+    out[n].ms = x->stats[c].ms;
+    out[n].bytes = x->stats[c].bytes;
+    out[n].flops = x->stats[c].flops;
+    x->stats[c] = cdb_ctx::Stat();
+    ++n;
+  }
+  *n_out = n;
+  return CDB_OK;
+}
 
 int cdb_trace_enable(cdb_ctx* x, int on) {
   if (!x) return CDB_ERR_ARG;

@@ -83,6 +83,7 @@ void launch_gemm(cudaStream_t s, int epi, const T* A, int lda, const T* W, const
                  float* Cf, T* Ct, int ldc) {
   if (rows <= 0) return;
   dim3 grid((N + BN - 1) / BN, (rows + BM - 1) / BM);
+  count_launch();
   if (epi == kEpiStore) k_gemm_simt<T, kEpiStore><<<grid, 256, 0, s>>>(A, lda, W, W2, N, K, rows, Cf, Ct, ldc);
   else if (epi == kEpiResid)
     k_gemm_simt<T, kEpiResid><<<grid, 256, 0, s>>>(A, lda, W, W2, N, K, rows, Cf, Ct, ldc);

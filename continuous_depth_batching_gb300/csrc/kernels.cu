@@ -10,7 +10,13 @@
 #include "common.cuh"
 #include "kernels.cuh"
 
+#include <atomic>
+
 namespace cdb {
+
+static std::atomic<long long> g_launches{0};
+void count_launch(int n) { g_launches.fetch_add(n, std::memory_order_relaxed); }
+long long launch_count() { return g_launches.load(std::memory_order_relaxed); }
 
 // ---------------------------------------------------------------------------
 // prelude: embedding gather
@@ -373,35 +379,35 @@ __global__ void k_argmax(const float* __restrict__ logits, int rows, int V, RowM
 template <typename T>
 void launch_embed_prefill(cudaStream_t s, const T* E, int d, int V, const int* rslot, const int* rpos,
                           const int* rtok, int rows, float* X, KvGeom kv, int r_max, int* status) {
-  if (rows > 0) k_embed_prefill<T><<<rows, 256, 0, s>>>(E, d, V, rslot, rpos, rtok, rows, X, kv, r_max, status);
+  if (rows > 0) count_launch(), k_embed_prefill<T><<<rows, 256, 0, s>>>(E, d, V, rslot, rpos, rtok, rows, X, kv, r_max, status);
 }
 template <typename T>
 void launch_embed_prelude(cudaStream_t s, const T* E, int d, int V, const int* lslot, const int* lt,
                           const int* lpos, int rows, const int* out_tok, int cap, float* X,
                           RowMeta meta, KvGeom kv, int r_max, int* status) {
   if (rows > 0)
-    k_embed_prelude<T><<<rows, 256, 0, s>>>(E, d, V, lslot, lt, lpos, rows, out_tok, cap, X, meta, kv,
+    count_launch(), k_embed_prelude<T><<<rows, 256, 0, s>>>(E, d, V, lslot, lt, lpos, rows, out_tok, cap, X, meta, kv,
                                             r_max, status);
 }
 void launch_prelude_finish(cudaStream_t s, const float* Tp, RowMeta tm, int rows, float* Pb, RowMeta pm,
                            int dst_off, float* estore, int d, int adapter) {
-  if (rows > 0) k_prelude_finish<<<rows, 256, 0, s>>>(Tp, tm, rows, Pb, pm, dst_off, estore, d, adapter);
+  if (rows > 0) count_launch(), k_prelude_finish<<<rows, 256, 0, s>>>(Tp, tm, rows, Pb, pm, dst_off, estore, d, adapter);
 }
 template <typename T>
 void launch_rmsnorm(cudaStream_t s, const float* X, const T* g, T* A, int rows, int d, float eps, int lda) {
-  if (rows > 0) k_rmsnorm<T><<<rows, 256, 0, s>>>(X, g, A, rows, d, eps, lda);
+  if (rows > 0) count_launch(), k_rmsnorm<T><<<rows, 256, 0, s>>>(X, g, A, rows, d, eps, lda);
 }
 template <typename T>
 void launch_concat(cudaStream_t s, const float* E, int e_per_slot, const int* mslot, const float* X, T* A,
                    int rows, int d) {
-  if (rows > 0) k_concat<T><<<rows, 256, 0, s>>>(E, e_per_slot, mslot, X, A, rows, d);
+  if (rows > 0) count_launch(), k_concat<T><<<rows, 256, 0, s>>>(E, e_per_slot, mslot, X, A, rows, d);
 }
 template <typename T>
 void launch_rope_kv(cudaStream_t s, const float* QKV, int rows, const int* mslot, const int* mpos,
                     const int* mdepth, int depth_uniform, int slot_base, int clamp, T* Q, KvGeom kv, int H,
                     int hd, const float2* rope, int* status) {
   if (rows > 0)
-    k_rope_kv<T><<<rows, 256, 0, s>>>(QKV, rows, mslot, mpos, mdepth, depth_uniform, slot_base, clamp, Q,
+    count_launch(), k_rope_kv<T><<<rows, 256, 0, s>>>(QKV, rows, mslot, mpos, mdepth, depth_uniform, slot_base, clamp, Q,
                                       kv, H, hd, rope, status);
 }
 template <typename T>
@@ -409,37 +415,37 @@ void launch_gate(cudaStream_t s, const float* X, const T* w, float bias, float t
                  int d, RowMeta meta, int mode, int r_min, int r_max, const int8_t* fexit, int cap,
                  int* pend_new, uint8_t* ring, float* gtrace) {
   if (rows > 0)
-    k_gate<T><<<rows, 256, 0, s>>>(X, w, bias, thr, eps, rows, d, meta, mode, r_min, r_max, fexit, cap,
+    count_launch(), k_gate<T><<<rows, 256, 0, s>>>(X, w, bias, thr, eps, rows, d, meta, mode, r_min, r_max, fexit, cap,
                                    pend_new, ring, gtrace);
 }
 void launch_compact(cudaStream_t s, const float* X, RowMeta m, const int* pend_new, int B, int d, int r_max,
                     int qc_off, float* Xc, RowMeta mc, float* Cb, RowMeta mb, KvGeom kv, int8_t* out_depth,
                     int cap, int* status) {
   if (B > 0)
-    k_compact<<<B, 256, 0, s>>>(X, m, pend_new, B, d, r_max, qc_off, Xc, mc, Cb, mb, kv, out_depth, cap,
+    count_launch(), k_compact<<<B, 256, 0, s>>>(X, m, pend_new, B, d, r_max, qc_off, Xc, mc, Cb, mb, kv, out_depth, cap,
                                 status);
 }
 void launch_gather_core(cudaStream_t s, const float* Xc, RowMeta mc, int B_cont, const float* Pb, RowMeta mp,
                         int n_ref, float* X, RowMeta mx, int d) {
   if (B_cont + n_ref > 0)
-    k_gather_core<<<B_cont + n_ref, 256, 0, s>>>(Xc, mc, B_cont, Pb, mp, n_ref, X, mx, d);
+    count_launch(), k_gather_core<<<B_cont + n_ref, 256, 0, s>>>(Xc, mc, B_cont, Pb, mp, n_ref, X, mx, d);
 }
 void launch_gather_rows(cudaStream_t s, const float* src, const int* idx, const int* rslot, const int* rpos,
                         int n, float* dst, RowMeta md, int d) {
-  if (n > 0) k_gather_rows<<<n, 256, 0, s>>>(src, idx, rslot, rpos, n, dst, md, d);
+  if (n > 0) count_launch(), k_gather_rows<<<n, 256, 0, s>>>(src, idx, rslot, rpos, n, dst, md, d);
 }
 void launch_argmax(cudaStream_t s, const float* logits, int rows, int V, RowMeta m, const int* ftok, int cap,
                    int* out_tok, float* ltrace, int trace_T, const float* H, float* htrace, int d,
                    int* status) {
   if (rows > 0)
-    k_argmax<<<rows, 512, 0, s>>>(logits, rows, V, m, ftok, cap, out_tok, ltrace, trace_T, H, htrace, d,
+    count_launch(), k_argmax<<<rows, 512, 0, s>>>(logits, rows, V, m, ftok, cap, out_tok, ltrace, trace_T, H, htrace, d,
                                   status);
 }
 void launch_rope_table(cudaStream_t s, float2* tab, int max_ctx, int hd, float theta) {
-  k_rope_table<<<1024, 256, 0, s>>>(tab, max_ctx, hd, theta);
+  count_launch(), k_rope_table<<<1024, 256, 0, s>>>(tab, max_ctx, hd, theta);
 }
 void launch_copy_rows(cudaStream_t s, const float* src, float* dst, int rows, int d) {
-  if (rows > 0) k_copy_rows<<<1024, 256, 0, s>>>(src, dst, (size_t)rows * d);
+  if (rows > 0) count_launch(), k_copy_rows<<<1024, 256, 0, s>>>(src, dst, (size_t)rows * d);
 }
 
 #define CDB_INST(T)                                                                                          \

@@ -22,6 +22,10 @@
 
 namespace cdb {
 
+// Kernel launches issued by the launchers below (process-wide).
+void count_launch(int n = 1);
+long long launch_count();
+
 struct RowMeta {
   int* slot;
   int* pos;

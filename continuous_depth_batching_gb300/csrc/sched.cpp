@@ -178,6 +178,7 @@ int Scheduler::run_prefill(cdb_step_info* info) {
     info->stage = CDB_STAGE_PREFILL;
     info->batch = plan.n_seqs;
     info->prefill_tokens = (int)plan.rows.size();
+    info->new_tokens = (int)plan.done_seqs.size();
   }
   std::vector<Tok> next;
   for (int si : plan.done_seqs) {
@@ -216,6 +217,7 @@ int Scheduler::run_coda(cdb_step_info* info) {
   if (info) {
     info->stage = CDB_STAGE_CODA;
     info->batch = (int)rows.size();
+    info->new_tokens = (int)rows.size();
   }
   std::vector<Tok> next;
   for (auto& t : rows) {

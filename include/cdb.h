@@ -127,6 +127,7 @@ typedef struct {
   int q_r, q_c, q_p, q_d;        /* queue sizes after the call */
   int depth_hist[CDB_MAX_DEPTH]; /* loop: depth_hist[i] tokens ran loop step i+1 */
   int64_t step_index;            /* loop steps issued so far, this one included */
+  int new_tokens;                /* tokens generated by this call (coda rows + prompts completed) */
 } cdb_step_info;
 
 /* One finished sequence.  The caller sets the pointers before cdb_drain; the
@@ -187,6 +188,28 @@ int cdb_sync(cdb_ctx *ctx);
 
 void cdb_free(cdb_ctx *ctx);
 const char *cdb_last_error(const cdb_ctx *ctx);
+
+/* Kernel timing.  When enabled, every launch of the timed kernel classes is
+ * bracketed by CUDA events on the compute stream; cdb_profile_read
+ * synchronizes, returns per class the launch count, summed device time and
+ * the algorithmic bytes and FLOPs of those launches (bytes each launch must
+ * move at least once: weights, KV rows read, activations in and out), and
+ * resets the counters.  Classes: "attention" (split-KV decode attention plus
+ * its combine), "gemm" (all projections), "prefill_attention". */
+typedef struct {
+  char name[32];
+  int64_t launches;
+  double ms, bytes, flops;
+} cdb_kernel_stat;
+int cdb_profile_enable(cdb_ctx *ctx, int on);
+int cdb_profile_read(cdb_ctx *ctx, cdb_kernel_stat *out, int cap, int *n_out);
+
+/* Kernel launches issued by the library in this process, all contexts. */
+int64_t cdb_kernel_launches(void);
+
+/* Host<->device bytes this context has copied so far: prompts, scheduling
+ * tables and lists (h2d); lookahead flags, results and status words (d2h). */
+int cdb_io_bytes(const cdb_ctx *ctx, int64_t *h2d, int64_t *d2h);
 
 /* Scheduling trace: one row per executed stage (the columns of Tables 2-3).
  * Rows are kept only while trace recording is on. */

@@ -10,5 +10,6 @@ from .model import (  # noqa: F401
     OracleModel,
     SeqTrace,
     decode_sequence,
+    iter_decode,
     decode_workload,
 )

@@ -222,7 +222,18 @@ class SeqTrace:
 def decode_sequence(model: OracleModel, prompt, gen_len: int, mode: str = "adaptive",
                     force_exit=None, force_token=None, keep_logits: int = 0,
                     keep_kv: bool = False, near_tol: float = 1e-3) -> SeqTrace:
-    """Decode one sequence alone.
+    """Decode one sequence alone (see iter_decode); returns the full trace."""
+    tr = None
+    for tr in iter_decode(model, prompt, gen_len, mode, force_exit, force_token, keep_logits,
+                          keep_kv, near_tol):
+        pass
+    return tr
+
+
+def iter_decode(model: OracleModel, prompt, gen_len: int, mode: str = "adaptive",
+                force_exit=None, force_token=None, keep_logits: int = 0,
+                keep_kv: bool = False, near_tol: float = 1e-3):
+    """Decode one sequence alone, yielding the trace after each generated token.
 
     mode "adaptive" uses the lookahead gate (or force_exit); "fixed" runs every
     token at r_max loops (token-level continuous batching, §6.1).
@@ -272,6 +283,9 @@ def decode_sequence(model: OracleModel, prompt, gen_len: int, mode: str = "adapt
         y = model.block(f"coda.{j}.", y, pos, kv, sl, np.full(P, sl), "coda")
     last = y[-1:]
     tok = emit(model.logits(last)[0], 0, last[0])
+    if keep_kv:
+        tr.kv = kv
+    yield tr
 
     # ---- decode: one token at a time, one loop step at a time ----
     for t in range(1, gen_len):
@@ -318,9 +332,7 @@ def decode_sequence(model: OracleModel, prompt, gen_len: int, mode: str = "adapt
             sl = model.slot_coda(j)
             y = model.block(f"coda.{j}.", y, ppos, kv, sl, np.full(p + 1, sl), "coda")
         tok = emit(model.logits(y)[0], t, y[0])
-    if keep_kv:
-        tr.kv = kv
-    return tr
+        yield tr
 
 
 def _decode_one(args):
