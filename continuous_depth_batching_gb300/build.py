@@ -29,6 +29,7 @@ SOURCES = [
     "kernels.cu",
     "attention.cu",
     "gemm_simt.cu",
+    "gemm_tc.cu",
 ]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

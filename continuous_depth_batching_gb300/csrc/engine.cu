@@ -7,6 +7,7 @@
 // the recurrent queue, coda on exited tokens (§4.1, Algorithms 1-2).  The
 // lookahead flags of each core step are copied to the host on a second stream
 // (§4.3, "asynchronous batch preparation") while the next stages run.
+#include <algorithm>
 #include <chrono>
 #include <cmath>
 #include <cstring>
@@ -37,6 +38,7 @@ struct Layout {
   size_t Xp, Ep, rslot, rpos, rtok, done_idx, Cp, Cp_meta;
   size_t lslot, lt, lpos;
   size_t A, QKV, Q, O, Mid, logits, part_o, part_ml;
+  size_t gws, gtickets;  // tensor-core GEMM split-K partials and tile tickets
   // dims
   int es, nsl, max_blocks, max_splits, split, R, S, cap;
 };
@@ -98,6 +100,21 @@ static bool plan_layout(const cdb_model_desc* m, const cdb_sched_cfg* c, Layout*
   L->logits = take(W * V * 4);
   L->part_o = take(W * H * L->max_splits * hd * 4);
   L->part_ml = take(W * H * L->max_splits * 2 * 4);
+  {
+    // Split-K workspace of the decode-tiled GEMMs (rows <= W), and one ticket
+    // per output tile of any GEMM.
+    struct G { int N, K; bool sw; };
+    const int dd = (int)d, ff = (int)f, VV = (int)V;
+    const G gs[] = {{3 * dd, dd, false}, {dd, dd, false}, {ff, dd, true}, {dd, ff, false},
+                    {VV, dd, false}, {dd, 2 * dd, false}};
+    size_t ws = 0, tk = 0;
+    for (const G& g : gs) {
+      ws = std::max(ws, gemm_tc_ws_floats(g.N, g.K, (int)W, true, g.sw));
+      tk = std::max(tk, (size_t)((g.N + 127) / 128) * ((W + 63) / 64));
+    }
+    L->gws = take(es == 2 ? ws * 4 : 0);
+    L->gtickets = take(es == 2 ? tk * 4 : 0);
+  }
   L->total = o;
   return true;
 }
@@ -308,7 +325,12 @@ class GpuExecutor : public Executor {
     cdb_ctx* x = x_;
     const double es = sizeof(T), nw = W2 ? 2.0 : 1.0;
     const int h = prof_begin(x, 1);
-    launch_gemm<T>(x->cs, epi, A, lda, (const T*)W, (const T*)W2, N, K, rows, Cf, Ct, ldc);
+    bool done = false;
+    if (sizeof(T) == 2)
+      done = launch_gemm_tc(x->cs, epi, (const __nv_bfloat16*)A, lda, x->L.R, (const __nv_bfloat16*)W,
+                            (const __nv_bfloat16*)W2, N, K, rows, Cf, (__nv_bfloat16*)Ct, ldc, decode_tiles_,
+                            at<float>(x, x->L.gws), at<int>(x, x->L.gtickets), at<int>(x, x->L.status));
+    if (!done) launch_gemm<T>(x->cs, epi, A, lda, (const T*)W, (const T*)W2, N, K, rows, Cf, Ct, ldc);
     const double out_b = epi == kEpiSwiglu ? es : (epi == kEpiResid ? 8.0 : 4.0);
     prof_end(x, h, nw * N * (double)K * es + (double)rows * K * es + (double)rows * N * out_b,
              2.0 * nw * rows * (double)N * K);
@@ -329,6 +351,7 @@ class GpuExecutor : public Executor {
     int* st = at<int>(x, L.status);
     KvGeom kv = geom();
     const double es = sizeof(T);
+    decode_tiles_ = decode;
     launch_rmsnorm<T>(s, X, (const T*)lw.attn_norm, A, rows, d, x->m.rms_eps, d);
     gemm<T>(kEpiStore, A, d, lw.wqkv, nullptr, 3 * d, d, rows, QKV, nullptr, 3 * d);
     launch_rope_kv<T>(s, QKV, rows, mslot, mpos, mdepth, depth_uniform, slot_base, clamp, Q, kv, H, hd,
@@ -352,6 +375,7 @@ class GpuExecutor : public Executor {
     cdb_ctx* x = x_;
     const int d = x->m.d_model;
     T* A = at<T>(x, x->L.A);
+    decode_tiles_ = e_per_slot != 0;
     launch_concat<T>(x->cs, E, e_per_slot, mslot, X, A, rows, d);
     gemm<T>(kEpiStore, A, 2 * d, x->adapter, nullptr, d, 2 * d, rows, X, nullptr, d);
     return CDB_OK;
@@ -365,6 +389,7 @@ class GpuExecutor : public Executor {
     const int d = x->m.d_model, V = x->m.vocab, cap = x->c.max_new_cap;
     T* A = at<T>(x, L.A);
     float* lg = at<float>(x, L.logits);
+    decode_tiles_ = true;
     launch_rmsnorm<T>(x->cs, Hrows, (const T*)x->final_norm, A, n, d, x->m.rms_eps, d);
     gemm<T>(kEpiStore, A, d, x->lm_head, nullptr, V, d, n, lg, nullptr, V);
     const bool tr = x->c.trace_tokens > 0;
@@ -613,6 +638,7 @@ class GpuExecutor : public Executor {
 
  private:
   cdb_ctx* x_;
+  bool decode_tiles_ = true;  // GEMM tiling for the rows being processed
 };
 
 static int check_status(cdb_ctx* x) {
@@ -899,6 +925,45 @@ int cdb_trace_read(cdb_ctx* x, cdb_trace_row* rows, int cap, int* n_out) {
   if (rows && n > 0) std::memcpy(rows, tr.data(), sizeof(cdb_trace_row) * n);
   *n_out = n;
   return CDB_OK;
+}
+
+}  // extern "C"
+
+// ---------------------------------------------------------------------------
+// cdb_testing.h
+// ---------------------------------------------------------------------------
+#include "../../include/cdb_testing.h"
+
+extern "C" {
+
+size_t cdb_test_gemm_ws_bytes(int N, int K, int rows, int tiling, int epi) {
+  const size_t tiles = (size_t)((N + 127) / 128) * ((rows + 63) / 64);
+  return 256 + tiles * 4 + gemm_tc_ws_floats(N, K, rows, tiling == 0, epi == kEpiSwiglu) * 4 + 256;
+}
+
+int cdb_test_gemm(int epi, int tiling, const void* A, int lda, int a_rows, const void* W, const void* W2, int N,
+                  int K, int rows, float* Cf, void* Ct, int ldc, void* ws, size_t ws_bytes, void* stream) {
+  if (epi < 0 || epi > 2 || tiling < 0 || tiling > 2 || !A || !W || (epi == 2 && (!W2 || !Ct)) ||
+      (epi != 2 && !Cf) || !ws || ws_bytes < cdb_test_gemm_ws_bytes(N, K, rows, tiling, epi))
+    return CDB_ERR_ARG;
+  cudaStream_t s = (cudaStream_t)stream;
+  char* w = (char*)ws;
+  int* status = (int*)w;
+  const size_t tiles = (size_t)((N + 127) / 128) * ((rows + 63) / 64);
+  int* tickets = (int*)(w + 256);
+  float* part = (float*)(w + 256 + (tiles * 4 + 255) / 256 * 256);
+  if (tiling == 2) {
+    launch_gemm<__nv_bfloat16>(s, epi, (const __nv_bfloat16*)A, lda, (const __nv_bfloat16*)W,
+                               (const __nv_bfloat16*)W2, N, K, rows, Cf, (__nv_bfloat16*)Ct, ldc);
+  } else if (!launch_gemm_tc(s, epi, (const __nv_bfloat16*)A, lda, a_rows, (const __nv_bfloat16*)W,
+                             (const __nv_bfloat16*)W2, N, K, rows, Cf, (__nv_bfloat16*)Ct, ldc, tiling == 0, part,
+                             tickets, status)) {
+    return CDB_ERR_ARG;
+  }
+  if (cudaGetLastError() != cudaSuccess || cudaStreamSynchronize(s) != cudaSuccess) return CDB_ERR_CUDA;
+  int st = 0;
+  if (cudaMemcpy(&st, status, 4, cudaMemcpyDeviceToHost) != cudaSuccess) return CDB_ERR_CUDA;
+  return st ? CDB_ERR_DEVICE_BOUNDS : CDB_OK;
 }
 
 }  // extern "C"

@@ -1,0 +1,416 @@
+// Tensor-core GEMM for bf16 models: C = A[rows, K] . W[N, K]^T, fp32 accumulate.
+//
+// sm_103a, 5th-generation tensor cores.  One CTA computes a 128 (output
+// features) x BN (activation rows) tile: the weight tile is the 128-row MMA
+// operand and the activation rows form the N side, so a decode batch of a few
+// dozen rows still fills the tensor core's M=128 (swap-AB).  Operands arrive
+// in shared memory through TMA (128-byte swizzle, 64-element K slabs, a ring
+// of STAGES buffers tracked by mbarriers); one thread issues tcgen05.mma into a
+// TMEM accumulator; all four warps then read TMEM with tcgen05.ld and apply
+// the epilogue (store, residual add, or SwiGLU of two accumulators).
+//
+// Split-K: the K range is cut into `splits` pieces whose count depends only on
+// the weight shape, never on the number of rows, so a row's result is the same
+// in every batch.  Each split writes its fp32 partial tile; the last CTA of a
+// tile (atomic ticket) sums the partials in split order and runs the epilogue.
+//
+// Every mbarrier wait is bounded by the global timer; on expiry the kernel
+// records kStatusTimeout, skips the epilogue, releases TMEM and returns.
+#include <cuda.h>
+
+#include <unordered_map>
+
+#include "common.cuh"
+#include "kernels.cuh"
+
+namespace cdb {
+namespace tc {
+
+constexpr int BM = 128;  // output features per tile (MMA M)
+constexpr int BK = 64;   // K per stage: 128 bytes of bf16 = one swizzle row
+constexpr int UK = 16;   // K per tcgen05.mma, kind::f16
+
+__device__ __forceinline__ uint32_t su32(const void* p) {
+  return (uint32_t)__cvta_generic_to_shared(p);
+}
+
+__device__ __forceinline__ uint64_t gtimer() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
+  return t;
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(su32(bar)), "r"(count));
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(su32(bar)), "r"(bytes)
+               : "memory");
+}
+
+// Wait for the phase with the given parity; false after ~2 s.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
+  const uint32_t a = su32(bar);
+  uint64_t t0 = 0;
+  for (uint32_t it = 0;; ++it) {
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+        " selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(ok)
+        : "r"(a), "r"(parity)
+        : "memory");
+    if (ok) return true;
+    if ((it & 255) == 0) {
+      const uint64_t t = gtimer();
+      if (t0 == 0) t0 = t;
+      else if (t - t0 > 2000000000ull) return false;
+    }
+  }
+}
+
+__device__ __forceinline__ void tma_load(void* dst, const CUtensorMap* map, uint64_t* bar, int x, int y) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4}], [%2];" ::"r"(
+          su32(dst)),
+      "l"(map), "r"(su32(bar)), "r"(x), "r"(y)
+      : "memory");
+}
+
+// Shared-memory matrix descriptor: K-major, 128-byte swizzle, 8-row groups
+// 1024 bytes apart (tcgen05 descriptor version 1).
+__device__ __forceinline__ uint64_t sdesc(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);
+  d |= (uint64_t)1 << 16;
+  d |= (uint64_t)(1024 >> 4) << 32;
+  d |= (uint64_t)1 << 46;
+  d |= (uint64_t)2 << 61;
+  return d;
+}
+
+// Instruction descriptor, kind::f16: fp32 accumulator, bf16 A and B, both K-major.
+__host__ __device__ constexpr uint32_t idesc(int M, int N) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+__device__ __forceinline__ void mma(uint32_t d, uint64_t a, uint64_t b, uint32_t id, uint32_t acc) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d),
+      "l"(a), "l"(b), "r"(id), "r"(acc));
+}
+
+__device__ __forceinline__ void mma_commit(uint64_t* bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(su32(bar))
+               : "memory");
+}
+
+__device__ __forceinline__ void fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float* v) {
+  uint32_t r[16];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+template <int BN, bool SW>
+struct Cfg {
+  static constexpr int A_BYTES = BM * BK * 2;
+  static constexpr int B_BYTES = BN * BK * 2;
+  static constexpr int STAGE = A_BYTES * (SW ? 2 : 1) + B_BYTES;
+  static constexpr int STAGES = (200 * 1024) / STAGE > 8 ? 8 : (200 * 1024) / STAGE;
+  static constexpr int ACC = BN * (SW ? 2 : 1);
+  static constexpr int TMEM_COLS = ACC <= 32 ? 32 : ACC <= 64 ? 64 : ACC <= 128 ? 128 : ACC <= 256 ? 256 : 512;
+  static constexpr int SMEM = STAGES * STAGE + 1024 + 256;
+};
+
+template <int BN, int EPI>
+__global__ void __launch_bounds__(128, 1)
+    k_gemm_tc(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmW2,
+              const __grid_constant__ CUtensorMap tmA, int N, int K, int rows, int splits,
+              float* __restrict__ Cf, __nv_bfloat16* __restrict__ Ct, int ldc, float* __restrict__ ws,
+              int* __restrict__ tickets, int* status) {
+  constexpr bool SW = EPI == kEpiSwiglu;
+  using C = Cfg<BN, SW>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::STAGES * C::STAGE);
+  uint64_t* empty = full + C::STAGES;
+  uint64_t* done = empty + C::STAGES;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done + 1);
+  __shared__ int s_last, s_fail;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int n0 = blockIdx.x * BM;
+  const int m0 = blockIdx.y * BN;
+  const int split = blockIdx.z;
+  const int KT = (K + BK - 1) / BK;
+  const int kt0 = (int)((long long)KT * split / splits);
+  const int kt1 = (int)((long long)KT * (split + 1) / splits);
+  const int nkt = kt1 - kt0;
+
+  if (threadIdx.x == 0) {
+    s_fail = 0;
+    for (int s = 0; s < C::STAGES; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    mbar_init(done, 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  }
+  if (warp == 0) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(su32(tmem_slot)),
+                 "r"(C::TMEM_COLS));
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+  }
+  fence_before();
+  __syncthreads();
+  fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0 && lane == 0) {
+    // TMA producer
+    for (int i = 0; i < nkt; ++i) {
+      const int s = i % C::STAGES;
+      if (i >= C::STAGES && !mbar_wait(&empty[s], ((i / C::STAGES) - 1) & 1)) {
+        s_fail = 1;
+        atomicOr(status, kStatusTimeout);
+        break;
+      }
+      uint8_t* st = smem + s * C::STAGE;
+      mbar_expect_tx(&full[s], C::STAGE);
+      const int kx = (kt0 + i) * BK;
+      tma_load(st, &tmW, &full[s], kx, n0);
+      if (SW) tma_load(st + C::A_BYTES, &tmW2, &full[s], kx, n0);
+      tma_load(st + C::A_BYTES * (SW ? 2 : 1), &tmA, &full[s], kx, m0);
+    }
+  } else if (warp == 1 && lane == 0) {
+    // MMA issuer
+    constexpr uint32_t id = idesc(BM, BN);
+    for (int i = 0; i < nkt; ++i) {
+      const int s = i % C::STAGES;
+      if (!mbar_wait(&full[s], (i / C::STAGES) & 1)) {
+        s_fail = 1;
+        atomicOr(status, kStatusTimeout);
+        break;
+      }
+      fence_after();
+      const uint32_t a = su32(smem + s * C::STAGE);
+      const uint32_t a2 = a + C::A_BYTES;
+      const uint32_t b = a + C::A_BYTES * (SW ? 2 : 1);
+#pragma unroll
+      for (int kk = 0; kk < BK / UK; ++kk) {
+        const uint32_t acc = (i > 0 || kk > 0) ? 1u : 0u;
+        mma(tmem, sdesc(a + kk * 32), sdesc(b + kk * 32), id, acc);
+        if (SW) mma(tmem + BN, sdesc(a2 + kk * 32), sdesc(b + kk * 32), id, acc);
+      }
+      mma_commit(&empty[s]);
+    }
+    mma_commit(done);
+  }
+  __syncwarp();
+  const bool ok = mbar_wait(done, 0) && !s_fail;
+  fence_after();
+  if (!ok) {
+    if (threadIdx.x == 0) atomicOr(status, kStatusTimeout);
+  } else {
+    const int f = n0 + warp * 32 + lane;  // output feature of this thread's TMEM lane
+    const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
+    if (splits == 1) {
+#pragma unroll 1
+      for (int c0 = 0; c0 < BN; c0 += 16) {
+        float v[16], u[16];
+        tmem_ld16(lane_base + c0, v);
+        if (SW) tmem_ld16(lane_base + BN + c0, u);
+        if (f < N) {
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            const int r = m0 + c0 + j;
+            if (r >= rows) break;
+            const size_t o = (size_t)r * ldc + f;
+            if (EPI == kEpiStore) Cf[o] = v[j];
+            else if (EPI == kEpiResid) Cf[o] += v[j];
+            else Ct[o] = __float2bfloat16_rn(v[j] / (1.0f + expf(-v[j])) * u[j]);
+          }
+        }
+      }
+    } else {
+      // Write this split's partial [BN][BM(xSW)] tile, then take a ticket.
+      const int tile = blockIdx.y * gridDim.x + blockIdx.x;
+      const int W = BM * (SW ? 2 : 1);
+      float* part = ws + ((size_t)tile * splits + split) * BN * W;
+#pragma unroll 1
+      for (int c0 = 0; c0 < BN; c0 += 16) {
+        float v[16], u[16];
+        tmem_ld16(lane_base + c0, v);
+        if (SW) tmem_ld16(lane_base + BN + c0, u);
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          part[(size_t)(c0 + j) * W + warp * 32 + lane] = v[j];
+          if (SW) part[(size_t)(c0 + j) * W + BM + warp * 32 + lane] = u[j];
+        }
+      }
+      __threadfence();
+      __syncthreads();
+      if (threadIdx.x == 0) s_last = (atomicAdd(&tickets[tile], 1) == splits - 1);
+      __syncthreads();
+      if (s_last) {
+        __threadfence();
+        const float* base = ws + (size_t)tile * splits * BN * W;
+        if (f < N) {
+#pragma unroll 1
+          for (int j = 0; j < BN; ++j) {
+            const int r = m0 + j;
+            if (r >= rows) break;
+            float g = 0.f, up = 0.f;
+            for (int s = 0; s < splits; ++s) {
+              const float* p = base + ((size_t)s * BN + j) * W;
+              g += __ldcg(p + warp * 32 + lane);
+              if (SW) up += __ldcg(p + BM + warp * 32 + lane);
+            }
+            const size_t o = (size_t)r * ldc + f;
+            if (EPI == kEpiStore) Cf[o] = g;
+            else if (EPI == kEpiResid) Cf[o] += g;
+            else Ct[o] = __float2bfloat16_rn(g / (1.0f + expf(-g)) * up);
+          }
+        }
+        if (threadIdx.x == 0) tickets[tile] = 0;
+      }
+    }
+  }
+  fence_before();
+  __syncthreads();
+  if (warp == 0)
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(C::TMEM_COLS));
+}
+
+// ---------------------------------------------------------------------------
+// host side: tensor maps (cached), launch
+// ---------------------------------------------------------------------------
+
+typedef CUresult (*EncodeFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                             const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                             CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static EncodeFn encoder() {
+  static EncodeFn fn = nullptr;
+  static bool tried = false;
+  if (!tried) {
+    tried = true;
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeFn>(p);
+  }
+  return fn;
+}
+
+struct MapKey {
+  const void* p;
+  uint64_t inner, outer, stride;
+  uint32_t box;
+  bool operator==(const MapKey& o) const {
+    return p == o.p && inner == o.inner && outer == o.outer && stride == o.stride && box == o.box;
+  }
+};
+struct MapHash {
+  size_t operator()(const MapKey& k) const {
+    return std::hash<const void*>()(k.p) ^ (k.inner * 1315423911ull) ^ (k.outer << 20) ^ (k.stride << 7) ^ k.box;
+  }
+};
+
+// bf16 [outer][inner] with row stride `stride` bytes, box 64 x box, 128-byte swizzle.
+static const CUtensorMap* get_map(const void* p, uint64_t inner, uint64_t outer, uint64_t stride, uint32_t box) {
+  static std::unordered_map<MapKey, CUtensorMap, MapHash> cache;
+  MapKey k{p, inner, outer, stride, box};
+  auto it = cache.find(k);
+  if (it != cache.end()) return &it->second;
+  EncodeFn enc = encoder();
+  if (!enc) return nullptr;
+  CUtensorMap m;
+  cuuint64_t dims[2] = {inner, outer};
+  cuuint64_t strides[1] = {stride};
+  cuuint32_t boxd[2] = {(cuuint32_t)BK, box};
+  cuuint32_t es[2] = {1, 1};
+  if (enc(&m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(p), dims, strides, boxd, es,
+          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return nullptr;
+  return &cache.emplace(k, m).first->second;
+}
+
+template <int BN, int EPI>
+static bool launch_bn(cudaStream_t s, const __nv_bfloat16* A, int lda, int a_rows, const __nv_bfloat16* W,
+                      const __nv_bfloat16* W2, int N, int K, int rows, int splits, float* Cf,
+                      __nv_bfloat16* Ct, int ldc, float* ws, int* tickets, int* status) {
+  using C = Cfg<BN, EPI == kEpiSwiglu>;
+  const CUtensorMap* mw = get_map(W, K, N, (uint64_t)K * 2, BM);
+  const CUtensorMap* mw2 = EPI == kEpiSwiglu ? get_map(W2, K, N, (uint64_t)K * 2, BM) : mw;
+  const CUtensorMap* ma = get_map(A, K, a_rows, (uint64_t)lda * 2, BN);
+  if (!mw || !mw2 || !ma) return false;
+  static bool attr = false;
+  if (!attr) {
+    if (cudaFuncSetAttribute(k_gemm_tc<BN, EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) !=
+        cudaSuccess)
+      return false;
+    attr = true;
+  }
+  dim3 grid((N + BM - 1) / BM, (rows + BN - 1) / BN, splits);
+  count_launch();
+  k_gemm_tc<BN, EPI><<<grid, 128, C::SMEM, s>>>(*mw, *mw2, *ma, N, K, rows, splits, Cf, Ct, ldc, ws, tickets,
+                                                status);
+  return true;
+}
+
+}  // namespace tc
+
+int gemm_tc_splits(int N, int K, bool decode) {
+  if (!decode) return 1;
+  const int tiles = (N + tc::BM - 1) / tc::BM;
+  const int KT = (K + tc::BK - 1) / tc::BK;
+  int s = (int)((152.0 / tiles) + 0.5);
+  if (s > KT / 4) s = KT / 4;
+  return s < 1 ? 1 : s;
+}
+
+size_t gemm_tc_ws_floats(int N, int K, int rows, bool decode, bool swiglu) {
+  const int s = gemm_tc_splits(N, K, decode);
+  if (s <= 1) return 0;
+  const int bn = decode ? 64 : 128;
+  const size_t tiles = (size_t)((N + tc::BM - 1) / tc::BM) * ((rows + bn - 1) / bn);
+  return tiles * s * bn * tc::BM * (swiglu ? 2 : 1);
+}
+
+bool launch_gemm_tc(cudaStream_t s, int epi, const __nv_bfloat16* A, int lda, int a_rows, const __nv_bfloat16* W,
+                    const __nv_bfloat16* W2, int N, int K, int rows, float* Cf, __nv_bfloat16* Ct, int ldc,
+                    bool decode, float* ws, int* tickets, int* status) {
+  if (rows <= 0) return true;
+  if ((K * 2) % 16 != 0 || (lda * 2) % 16 != 0 || rows > a_rows) return false;
+  const int splits = gemm_tc_splits(N, K, decode);
+  if (decode) {
+    switch (epi) {
+      case kEpiStore: return tc::launch_bn<64, kEpiStore>(s, A, lda, a_rows, W, W2, N, K, rows, splits, Cf, Ct, ldc, ws, tickets, status);
+      case kEpiResid: return tc::launch_bn<64, kEpiResid>(s, A, lda, a_rows, W, W2, N, K, rows, splits, Cf, Ct, ldc, ws, tickets, status);
+      default: return tc::launch_bn<64, kEpiSwiglu>(s, A, lda, a_rows, W, W2, N, K, rows, splits, Cf, Ct, ldc, ws, tickets, status);
+    }
+  }
+  switch (epi) {
+    case kEpiStore: return tc::launch_bn<128, kEpiStore>(s, A, lda, a_rows, W, W2, N, K, rows, splits, Cf, Ct, ldc, ws, tickets, status);
+    case kEpiResid: return tc::launch_bn<128, kEpiResid>(s, A, lda, a_rows, W, W2, N, K, rows, splits, Cf, Ct, ldc, ws, tickets, status);
+    default: return tc::launch_bn<128, kEpiSwiglu>(s, A, lda, a_rows, W, W2, N, K, rows, splits, Cf, Ct, ldc, ws, tickets, status);
+  }
+}
+
+}  // namespace cdb

@@ -1,0 +1,105 @@
+"""Tensor-core projection GEMM (include/cdb_testing.h) against a float64 product.
+
+Checks every epilogue (store, residual add, SwiGLU), both tilings (decode:
+64-row tiles with split-K fixed by the weight shape; prefill: 128-row tiles),
+ragged N and K tails, the split-K shapes of the Ouro-shaped core, agreement
+with the CUDA-core kernel, and that a row's result does not depend on how
+many other rows are in the batch (bit-exact).
+"""
+
+import ctypes as C
+
+import numpy as np
+import pytest
+
+pytestmark = pytest.mark.gpu
+
+TOL = 1e-4  # fp32 accumulation of bf16 products vs a float64 reference, outputs O(1)
+
+
+@pytest.fixture(scope="module")
+def L():
+    from continuous_depth_batching_gb300 import binding
+    from continuous_depth_batching_gb300.build import build
+    build()
+    lib = binding.lib()
+    lib.cdb_test_gemm.argtypes = [C.c_int, C.c_int, C.c_void_p, C.c_int, C.c_int, C.c_void_p, C.c_void_p,
+                                  C.c_int, C.c_int, C.c_int, C.c_void_p, C.c_void_p, C.c_int, C.c_void_p,
+                                  C.c_size_t, C.c_void_p]
+    lib.cdb_test_gemm_ws_bytes.restype = C.c_size_t
+    lib.cdb_test_gemm_ws_bytes.argtypes = [C.c_int] * 5
+    return lib
+
+
+def run(L, epi, tiling, A, W, W2=None, C0=None, a_rows=None):
+    import torch
+    rows, K = A.shape
+    N = W.shape[0]
+    a_rows = a_rows or rows
+    Abuf = torch.zeros(a_rows, K, dtype=torch.bfloat16, device="cuda")
+    Abuf[:rows] = A
+    ws_bytes = L.cdb_test_gemm_ws_bytes(N, K, rows, tiling, epi)
+    ws = torch.zeros(ws_bytes, dtype=torch.uint8, device="cuda")
+    Cf = (C0.clone() if C0 is not None else torch.zeros(rows, N, dtype=torch.float32, device="cuda"))
+    Ct = torch.zeros(rows, N, dtype=torch.bfloat16, device="cuda")
+    rc = L.cdb_test_gemm(epi, tiling, Abuf.data_ptr(), K, a_rows, W.data_ptr(),
+                         W2.data_ptr() if W2 is not None else None, N, K, rows,
+                         Cf.data_ptr(), Ct.data_ptr(), N, ws.data_ptr(), ws_bytes, None)
+    assert rc == 0, rc
+    return Cf, Ct
+
+
+def rnd(*shape, std=1.0, seed=0):
+    import torch
+    g = torch.Generator(device="cpu").manual_seed(seed)
+    return (torch.randn(*shape, generator=g) * std).to(torch.bfloat16).cuda()
+
+
+SHAPES = [(5, 256, 192), (7, 200, 200), (64, 6144, 2048), (64, 2048, 5632), (33, 384, 1000), (300, 384, 256)]
+
+
+@pytest.mark.parametrize("rows,N,K", SHAPES)
+@pytest.mark.parametrize("tiling", [0, 1])
+def test_store_and_residual(L, rows, N, K, tiling):
+    import torch
+    A = rnd(rows, K, seed=1)
+    W = rnd(N, K, std=1.0 / np.sqrt(K), seed=2)
+    ref = A.double() @ W.double().T
+    Cf, _ = run(L, 0, tiling, A, W)
+    assert (Cf.double() - ref).abs().max().item() <= TOL
+    C0 = torch.randn(rows, N, device="cuda")
+    Cr, _ = run(L, 1, tiling, A, W, C0=C0)
+    assert (Cr.double() - (ref + C0.double())).abs().max().item() <= TOL
+
+
+@pytest.mark.parametrize("rows,N,K", [(5, 256, 192), (64, 5632, 2048), (200, 300, 128)])
+@pytest.mark.parametrize("tiling", [0, 1])
+def test_swiglu(L, rows, N, K, tiling):
+    import torch
+    A = rnd(rows, K, seed=3)
+    W = rnd(N, K, std=1.0 / np.sqrt(K), seed=4)
+    W2 = rnd(N, K, std=1.0 / np.sqrt(K), seed=5)
+    g = A.double() @ W.double().T
+    u = A.double() @ W2.double().T
+    ref = g / (1 + torch.exp(-g)) * u
+    _, Ct = run(L, 2, tiling, A, W, W2)
+    # bf16 output: one round-to-nearest (half an ulp, 2^-8 relative) plus fp32 error
+    assert ((Ct.double() - ref).abs() <= ref.abs() * 2.0 ** -8 + 1e-4).all().item()
+
+
+def test_matches_cuda_core_kernel(L):
+    A = rnd(48, 1024, seed=6)
+    W = rnd(640, 1024, std=0.03, seed=7)
+    a, _ = run(L, 0, 0, A, W)
+    b, _ = run(L, 0, 2, A, W)
+    assert (a - b).abs().max().item() <= TOL
+
+
+@pytest.mark.parametrize("N,K", [(6144, 2048), (2048, 5632), (49152, 2048)])
+def test_row_result_independent_of_batch(L, N, K):
+    A = rnd(64, K, seed=8)
+    W = rnd(N, K, std=1.0 / np.sqrt(K), seed=9)
+    full, _ = run(L, 0, 0, A, W, a_rows=64)
+    for r in (1, 17):
+        part, _ = run(L, 0, 0, A[:r].contiguous(), W, a_rows=64)
+        assert (part == full[:r]).all().item(), "row results must not depend on batch size"
