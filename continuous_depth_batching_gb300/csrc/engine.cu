@@ -38,7 +38,6 @@ struct Layout {
   size_t Xp, Ep, rslot, rpos, rtok, done_idx, Cp, Cp_meta;
   size_t lslot, lt, lpos;
   size_t A, QKV, Q, O, Mid, logits, part_o, part_ml;
-  size_t gws, gtickets;  // tensor-core GEMM split-K partials and tile tickets
   // dims
   int es, nsl, max_blocks, max_splits, split, R, S, cap;
 };
@@ -100,21 +99,6 @@ static bool plan_layout(const cdb_model_desc* m, const cdb_sched_cfg* c, Layout*
   L->logits = take(W * V * 4);
   L->part_o = take(W * H * L->max_splits * hd * 4);
   L->part_ml = take(W * H * L->max_splits * 2 * 4);
-  {
-    // Split-K workspace of the decode-tiled GEMMs (rows <= W), and one ticket
-    // per output tile of any GEMM.
-    struct G { int N, K; bool sw; };
-    const int dd = (int)d, ff = (int)f, VV = (int)V;
-    const G gs[] = {{3 * dd, dd, false}, {dd, dd, false}, {ff, dd, true}, {dd, ff, false},
-                    {VV, dd, false}, {dd, 2 * dd, false}};
-    size_t ws = 0, tk = 0;
-    for (const G& g : gs) {
-      ws = std::max(ws, gemm_tc_ws_floats(g.N, g.K, (int)W, true, g.sw));
-      tk = std::max(tk, (size_t)((g.N + 127) / 128) * ((W + 63) / 64));
-    }
-    L->gws = take(es == 2 ? ws * 4 : 0);
-    L->gtickets = take(es == 2 ? tk * 4 : 0);
-  }
   L->total = o;
   return true;
 }
@@ -329,7 +313,7 @@ class GpuExecutor : public Executor {
     if (sizeof(T) == 2)
       done = launch_gemm_tc(x->cs, epi, (const __nv_bfloat16*)A, lda, x->L.R, (const __nv_bfloat16*)W,
                             (const __nv_bfloat16*)W2, N, K, rows, Cf, (__nv_bfloat16*)Ct, ldc, decode_tiles_,
-                            at<float>(x, x->L.gws), at<int>(x, x->L.gtickets), at<int>(x, x->L.status));
+                            at<int>(x, x->L.status));
     if (!done) launch_gemm<T>(x->cs, epi, A, lda, (const T*)W, (const T*)W2, N, K, rows, Cf, Ct, ldc);
     const double out_b = epi == kEpiSwiglu ? es : (epi == kEpiResid ? 8.0 : 4.0);
     prof_end(x, h, nw * N * (double)K * es + (double)rows * K * es + (double)rows * N * out_b,
@@ -936,10 +920,7 @@ int cdb_trace_read(cdb_ctx* x, cdb_trace_row* rows, int cap, int* n_out) {
 
 extern "C" {
 
-size_t cdb_test_gemm_ws_bytes(int N, int K, int rows, int tiling, int epi) {
-  const size_t tiles = (size_t)((N + 127) / 128) * ((rows + 63) / 64);
-  return 256 + tiles * 4 + gemm_tc_ws_floats(N, K, rows, tiling == 0, epi == kEpiSwiglu) * 4 + 256;
-}
+size_t cdb_test_gemm_ws_bytes(int, int, int, int, int) { return 256; }
 
 int cdb_test_gemm(int epi, int tiling, const void* A, int lda, int a_rows, const void* W, const void* W2, int N,
                   int K, int rows, float* Cf, void* Ct, int ldc, void* ws, size_t ws_bytes, void* stream) {
@@ -947,17 +928,13 @@ int cdb_test_gemm(int epi, int tiling, const void* A, int lda, int a_rows, const
       (epi != 2 && !Cf) || !ws || ws_bytes < cdb_test_gemm_ws_bytes(N, K, rows, tiling, epi))
     return CDB_ERR_ARG;
   cudaStream_t s = (cudaStream_t)stream;
-  char* w = (char*)ws;
-  int* status = (int*)w;
-  const size_t tiles = (size_t)((N + 127) / 128) * ((rows + 63) / 64);
-  int* tickets = (int*)(w + 256);
-  float* part = (float*)(w + 256 + (tiles * 4 + 255) / 256 * 256);
+  int* status = (int*)ws;
   if (tiling == 2) {
     launch_gemm<__nv_bfloat16>(s, epi, (const __nv_bfloat16*)A, lda, (const __nv_bfloat16*)W,
                                (const __nv_bfloat16*)W2, N, K, rows, Cf, (__nv_bfloat16*)Ct, ldc);
   } else if (!launch_gemm_tc(s, epi, (const __nv_bfloat16*)A, lda, a_rows, (const __nv_bfloat16*)W,
-                             (const __nv_bfloat16*)W2, N, K, rows, Cf, (__nv_bfloat16*)Ct, ldc, tiling == 0, part,
-                             tickets, status)) {
+                             (const __nv_bfloat16*)W2, N, K, rows, Cf, (__nv_bfloat16*)Ct, ldc, tiling == 0,
+                             status)) {
     return CDB_ERR_ARG;
   }
   if (cudaGetLastError() != cudaSuccess || cudaStreamSynchronize(s) != cudaSuccess) return CDB_ERR_CUDA;

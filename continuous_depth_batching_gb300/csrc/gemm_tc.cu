@@ -11,11 +11,14 @@
 //
 // Split-K: the K range is cut into `splits` pieces whose count depends only on
 // the weight shape, never on the number of rows, so a row's result is the same
-// in every batch.  Each split writes its fp32 partial tile; the last CTA of a
-// tile (atomic ticket) sums the partials in split order and runs the epilogue.
+// in every batch.  The split CTAs of one tile form a thread-block cluster; each
+// parks its fp32 partial tile in its own shared memory, and after a cluster
+// barrier CTA r sums a slice of the tile's rows over all peers' shared memory
+// (distributed shared memory) in split order and runs the epilogue for them.
 //
 // Every mbarrier wait is bounded by the global timer; on expiry the kernel
 // records kStatusTimeout, skips the epilogue, releases TMEM and returns.
+#include <cooperative_groups.h>
 #include <cuda.h>
 
 #include <unordered_map>
@@ -137,8 +140,7 @@ template <int BN, int EPI>
 __global__ void __launch_bounds__(128, 1)
     k_gemm_tc(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmW2,
               const __grid_constant__ CUtensorMap tmA, int N, int K, int rows, int splits,
-              float* __restrict__ Cf, __nv_bfloat16* __restrict__ Ct, int ldc, float* __restrict__ ws,
-              int* __restrict__ tickets, int* status) {
+              float* __restrict__ Cf, __nv_bfloat16* __restrict__ Ct, int ldc, int* status) {
   constexpr bool SW = EPI == kEpiSwiglu;
   using C = Cfg<BN, SW>;
   extern __shared__ uint8_t smem_raw[];
@@ -147,7 +149,7 @@ __global__ void __launch_bounds__(128, 1)
   uint64_t* empty = full + C::STAGES;
   uint64_t* done = empty + C::STAGES;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done + 1);
-  __shared__ int s_last, s_fail;
+  __shared__ int s_fail;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int n0 = blockIdx.x * BM;
@@ -245,10 +247,10 @@ __global__ void __launch_bounds__(128, 1)
         }
       }
     } else {
-      // Write this split's partial [BN][BM(xSW)] tile, then take a ticket.
-      const int tile = blockIdx.y * gridDim.x + blockIdx.x;
-      const int W = BM * (SW ? 2 : 1);
-      float* part = ws + ((size_t)tile * splits + split) * BN * W;
+      // Park this split's partial tile red[j][0..BM) (and [BM..2BM) for the
+      // second accumulator) in shared memory; the pipeline buffers are idle.
+      constexpr int RW = BM * (SW ? 2 : 1);
+      float* red = reinterpret_cast<float*>(smem);
 #pragma unroll 1
       for (int c0 = 0; c0 < BN; c0 += 16) {
         float v[16], u[16];
@@ -256,37 +258,52 @@ __global__ void __launch_bounds__(128, 1)
         if (SW) tmem_ld16(lane_base + BN + c0, u);
 #pragma unroll
         for (int j = 0; j < 16; ++j) {
-          part[(size_t)(c0 + j) * W + warp * 32 + lane] = v[j];
-          if (SW) part[(size_t)(c0 + j) * W + BM + warp * 32 + lane] = u[j];
+          red[(c0 + j) * RW + warp * 32 + lane] = v[j];
+          if (SW) red[(c0 + j) * RW + BM + warp * 32 + lane] = u[j];
         }
-      }
-      __threadfence();
-      __syncthreads();
-      if (threadIdx.x == 0) s_last = (atomicAdd(&tickets[tile], 1) == splits - 1);
-      __syncthreads();
-      if (s_last) {
-        __threadfence();
-        const float* base = ws + (size_t)tile * splits * BN * W;
-        if (f < N) {
-#pragma unroll 1
-          for (int j = 0; j < BN; ++j) {
-            const int r = m0 + j;
-            if (r >= rows) break;
-            float g = 0.f, up = 0.f;
-            for (int s = 0; s < splits; ++s) {
-              const float* p = base + ((size_t)s * BN + j) * W;
-              g += __ldcg(p + warp * 32 + lane);
-              if (SW) up += __ldcg(p + BM + warp * 32 + lane);
-            }
-            const size_t o = (size_t)r * ldc + f;
-            if (EPI == kEpiStore) Cf[o] = g;
-            else if (EPI == kEpiResid) Cf[o] += g;
-            else Ct[o] = __float2bfloat16_rn(g / (1.0f + expf(-g)) * up);
-          }
-        }
-        if (threadIdx.x == 0) tickets[tile] = 0;
       }
     }
+  }
+  if (splits > 1) {
+    // Every CTA of the cluster reaches both barriers, failed or not.
+    namespace cg = cooperative_groups;
+    cg::cluster_group cl = cg::this_cluster();
+    cl.sync();
+    if (ok) {
+      constexpr int RW = BM * (SW ? 2 : 1);
+      float* red = reinterpret_cast<float*>(smem);
+      const int rank = (int)cl.block_rank();
+      const int j0 = BN * rank / splits, j1 = BN * (rank + 1) / splits;
+      const int f = n0 + threadIdx.x;  // one output feature per thread
+      const float* peer[8];
+#pragma unroll
+      for (int q = 0; q < 8; ++q) peer[q] = q < splits ? cl.map_shared_rank(red, q) : red;
+      for (int j = j0; j < j1; ++j) {
+        const int r = m0 + j;
+        if (r >= rows) break;
+        float gv[8], uv[8];
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          gv[q] = q < splits ? peer[q][j * RW + threadIdx.x] : 0.f;
+          if (SW) uv[q] = q < splits ? peer[q][j * RW + BM + threadIdx.x] : 0.f;
+        }
+        float g = 0.f, up = 0.f;
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          if (q < splits) {
+            g += gv[q];
+            if (SW) up += uv[q];
+          }
+        }
+        if (f < N) {
+          const size_t o = (size_t)r * ldc + f;
+          if (EPI == kEpiStore) Cf[o] = g;
+          else if (EPI == kEpiResid) Cf[o] += g;
+          else Ct[o] = __float2bfloat16_rn(g / (1.0f + expf(-g)) * up);
+        }
+      }
+    }
+    cl.sync();
   }
   fence_before();
   __syncthreads();
@@ -354,7 +371,7 @@ static const CUtensorMap* get_map(const void* p, uint64_t inner, uint64_t outer,
 template <int BN, int EPI>
 static bool launch_bn(cudaStream_t s, const __nv_bfloat16* A, int lda, int a_rows, const __nv_bfloat16* W,
                       const __nv_bfloat16* W2, int N, int K, int rows, int splits, float* Cf,
-                      __nv_bfloat16* Ct, int ldc, float* ws, int* tickets, int* status) {
+                      __nv_bfloat16* Ct, int ldc, int* status) {
   using C = Cfg<BN, EPI == kEpiSwiglu>;
   const CUtensorMap* mw = get_map(W, K, N, (uint64_t)K * 2, BM);
   const CUtensorMap* mw2 = EPI == kEpiSwiglu ? get_map(W2, K, N, (uint64_t)K * 2, BM) : mw;
@@ -367,11 +384,21 @@ static bool launch_bn(cudaStream_t s, const __nv_bfloat16* A, int lda, int a_row
       return false;
     attr = true;
   }
-  dim3 grid((N + BM - 1) / BM, (rows + BN - 1) / BN, splits);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((N + BM - 1) / BM, (rows + BN - 1) / BN, splits);
+  cfg.blockDim = dim3(128, 1, 1);
+  cfg.dynamicSmemBytes = C::SMEM;
+  cfg.stream = s;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeClusterDimension;
+  at[0].val.clusterDim.x = 1;
+  at[0].val.clusterDim.y = 1;
+  at[0].val.clusterDim.z = splits;
+  cfg.attrs = at;
+  cfg.numAttrs = splits > 1 ? 1 : 0;
   count_launch();
-  k_gemm_tc<BN, EPI><<<grid, 128, C::SMEM, s>>>(*mw, *mw2, *ma, N, K, rows, splits, Cf, Ct, ldc, ws, tickets,
-                                                status);
-  return true;
+  return cudaLaunchKernelEx(&cfg, k_gemm_tc<BN, EPI>, *mw, *mw2, *ma, N, K, rows, splits, Cf, Ct, ldc, status) ==
+         cudaSuccess;
 }
 
 }  // namespace tc
@@ -382,34 +409,27 @@ int gemm_tc_splits(int N, int K, bool decode) {
   const int KT = (K + tc::BK - 1) / tc::BK;
   int s = (int)((152.0 / tiles) + 0.5);
   if (s > KT / 4) s = KT / 4;
+  if (s > 8) s = 8;  // one portable cluster per tile
   return s < 1 ? 1 : s;
-}
-
-size_t gemm_tc_ws_floats(int N, int K, int rows, bool decode, bool swiglu) {
-  const int s = gemm_tc_splits(N, K, decode);
-  if (s <= 1) return 0;
-  const int bn = decode ? 64 : 128;
-  const size_t tiles = (size_t)((N + tc::BM - 1) / tc::BM) * ((rows + bn - 1) / bn);
-  return tiles * s * bn * tc::BM * (swiglu ? 2 : 1);
 }
 
 bool launch_gemm_tc(cudaStream_t s, int epi, const __nv_bfloat16* A, int lda, int a_rows, const __nv_bfloat16* W,
                     const __nv_bfloat16* W2, int N, int K, int rows, float* Cf, __nv_bfloat16* Ct, int ldc,
-                    bool decode, float* ws, int* tickets, int* status) {
+                    bool decode, int* status) {
   if (rows <= 0) return true;
   if ((K * 2) % 16 != 0 || (lda * 2) % 16 != 0 || rows > a_rows) return false;
   const int splits = gemm_tc_splits(N, K, decode);
   if (decode) {
     switch (epi) {
-      case kEpiStore: return tc::launch_bn<64, kEpiStore>(s, A, lda, a_rows, W, W2, N, K, rows, splits, Cf, Ct, ldc, ws, tickets, status);
-      case kEpiResid: return tc::launch_bn<64, kEpiResid>(s, A, lda, a_rows, W, W2, N, K, rows, splits, Cf, Ct, ldc, ws, tickets, status);
-      default: return tc::launch_bn<64, kEpiSwiglu>(s, A, lda, a_rows, W, W2, N, K, rows, splits, Cf, Ct, ldc, ws, tickets, status);
+      case kEpiStore: return tc::launch_bn<64, kEpiStore>(s, A, lda, a_rows, W, W2, N, K, rows, splits, Cf, Ct, ldc, status);
+      case kEpiResid: return tc::launch_bn<64, kEpiResid>(s, A, lda, a_rows, W, W2, N, K, rows, splits, Cf, Ct, ldc, status);
+      default: return tc::launch_bn<64, kEpiSwiglu>(s, A, lda, a_rows, W, W2, N, K, rows, splits, Cf, Ct, ldc, status);
     }
   }
   switch (epi) {
-    case kEpiStore: return tc::launch_bn<128, kEpiStore>(s, A, lda, a_rows, W, W2, N, K, rows, splits, Cf, Ct, ldc, ws, tickets, status);
-    case kEpiResid: return tc::launch_bn<128, kEpiResid>(s, A, lda, a_rows, W, W2, N, K, rows, splits, Cf, Ct, ldc, ws, tickets, status);
-    default: return tc::launch_bn<128, kEpiSwiglu>(s, A, lda, a_rows, W, W2, N, K, rows, splits, Cf, Ct, ldc, ws, tickets, status);
+    case kEpiStore: return tc::launch_bn<128, kEpiStore>(s, A, lda, a_rows, W, W2, N, K, rows, splits, Cf, Ct, ldc, status);
+    case kEpiResid: return tc::launch_bn<128, kEpiResid>(s, A, lda, a_rows, W, W2, N, K, rows, splits, Cf, Ct, ldc, status);
+    default: return tc::launch_bn<128, kEpiSwiglu>(s, A, lda, a_rows, W, W2, N, K, rows, splits, Cf, Ct, ldc, status);
   }
 }
 

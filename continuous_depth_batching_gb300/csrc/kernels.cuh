@@ -108,14 +108,13 @@ void launch_gemm(cudaStream_t s, int epi, const T* A, int lda, const T* W, const
                  int K, int rows, float* Cf, T* Ct, int ldc);
 
 // ---- tensor-core GEMM (gemm_tc.cu), bf16 only ----
-// decode = true: 64-row tiles and a split-K count fixed by (N, K); false:
-// 128-row tiles, no split.  a_rows: rows allocated in A (TMA bounds).  ws and
-// tickets: split-K partials and per-tile counters (zero-initialised, left
-// zero).  Returns false when the shape is not supported.
+// decode = true: 64-row tiles and a split-K count fixed by (N, K), split CTAs
+// reduce through distributed shared memory; false: 128-row tiles, no split.
+// a_rows: rows allocated in A (TMA bounds).  Returns false when the shape is
+// not supported.
 int gemm_tc_splits(int N, int K, bool decode);
-size_t gemm_tc_ws_floats(int N, int K, int rows, bool decode, bool swiglu);
 bool launch_gemm_tc(cudaStream_t s, int epi, const __nv_bfloat16* A, int lda, int a_rows,
                     const __nv_bfloat16* W, const __nv_bfloat16* W2, int N, int K, int rows, float* Cf,
-                    __nv_bfloat16* Ct, int ldc, bool decode, float* ws, int* tickets, int* status);
+                    __nv_bfloat16* Ct, int ldc, bool decode, int* status);
 
 }  // namespace cdb

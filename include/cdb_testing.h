@@ -19,9 +19,9 @@ extern "C" {
  *   tiling 0: tensor cores, decode tiles (64 rows, split-K fixed by N and K)
  *   tiling 1: tensor cores, prefill tiles (128 rows, no split)
  *   tiling 2: the CUDA-core kernel (fp32 FMA), for comparison
- * a_rows: rows allocated in A (>= rows).  ws: device scratch of at least
- * cdb_test_gemm_ws_bytes() bytes, zero-filled by the caller before the first
- * call (the kernel leaves it reusable).  stream: cudaStream_t or NULL.
+ * a_rows: rows allocated in A (>= rows).  ws: zero-filled device memory of at
+ * least cdb_test_gemm_ws_bytes() bytes that receives the kernel's status
+ * word.  stream: cudaStream_t or NULL.
  * Synchronizes the stream; returns CDB_OK (0), CDB_ERR_ARG (-1) for an
  * unsupported shape, CDB_ERR_CUDA (-4), or CDB_ERR_DEVICE_BOUNDS (-5) when a
  * bounded wait inside the kernel expired. */
