@@ -233,6 +233,7 @@ def run_ours(args):
     stream = torch.cuda.current_stream()
     eng.profile_enable(True)
     l0 = binding.kernel_launches()
+    print(f"launches_before_timed={l0}", file=sys.stderr, flush=True)
     clk = Clocks(local)
     clk.start()
     e0 = torch.cuda.Event(enable_timing=True)

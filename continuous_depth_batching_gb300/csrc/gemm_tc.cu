@@ -125,6 +125,30 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float* v) {
   for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
 }
 
+// Apply the epilogue to n (<= 16) consecutive rows of one output column:
+// v = first accumulator, u = second (SwiGLU up); o = offset of the first row.
+// All residual loads are issued before any store.
+template <int EPI>
+__device__ __forceinline__ void epilogue16(const float* v, const float* u, int n, float* __restrict__ Cf,
+                                           __nv_bfloat16* __restrict__ Ct, size_t o, int ldc) {
+  if (EPI == kEpiStore) {
+#pragma unroll
+    for (int j = 0; j < 16; ++j)
+      if (j < n) Cf[o + (size_t)j * ldc] = v[j];
+  } else if (EPI == kEpiResid) {
+    float old[16];
+#pragma unroll
+    for (int j = 0; j < 16; ++j) old[j] = j < n ? Cf[o + (size_t)j * ldc] : 0.f;
+#pragma unroll
+    for (int j = 0; j < 16; ++j)
+      if (j < n) Cf[o + (size_t)j * ldc] = old[j] + v[j];
+  } else {
+#pragma unroll
+    for (int j = 0; j < 16; ++j)
+      if (j < n) Ct[o + (size_t)j * ldc] = __float2bfloat16_rn(v[j] / (1.0f + expf(-v[j])) * u[j]);
+  }
+}
+
 template <int BN, bool SW>
 struct Cfg {
   static constexpr int A_BYTES = BM * BK * 2;
@@ -234,17 +258,8 @@ __global__ void __launch_bounds__(128, 1)
         float v[16], u[16];
         tmem_ld16(lane_base + c0, v);
         if (SW) tmem_ld16(lane_base + BN + c0, u);
-        if (f < N) {
-#pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            const int r = m0 + c0 + j;
-            if (r >= rows) break;
-            const size_t o = (size_t)r * ldc + f;
-            if (EPI == kEpiStore) Cf[o] = v[j];
-            else if (EPI == kEpiResid) Cf[o] += v[j];
-            else Ct[o] = __float2bfloat16_rn(v[j] / (1.0f + expf(-v[j])) * u[j]);
-          }
-        }
+        const int jn = min(16, rows - (m0 + c0));
+        if (f < N && jn > 0) epilogue16<EPI>(v, u, jn, Cf, Ct, (size_t)(m0 + c0) * ldc + f, ldc);
       }
     } else {
       // Park this split's partial tile red[j][0..BM) (and [BM..2BM) for the
@@ -278,29 +293,32 @@ __global__ void __launch_bounds__(128, 1)
       const float* peer[8];
 #pragma unroll
       for (int q = 0; q < 8; ++q) peer[q] = q < splits ? cl.map_shared_rank(red, q) : red;
-      for (int j = j0; j < j1; ++j) {
-        const int r = m0 + j;
-        if (r >= rows) break;
-        float gv[8], uv[8];
+      const int jend = min(j1, rows - m0);
+      for (int jb = j0; jb < jend; jb += 4) {
+        const int jn = min(4, jend - jb);
+        float gv[4][8], uv[4][8];
 #pragma unroll
-        for (int q = 0; q < 8; ++q) {
-          gv[q] = q < splits ? peer[q][j * RW + threadIdx.x] : 0.f;
-          if (SW) uv[q] = q < splits ? peer[q][j * RW + BM + threadIdx.x] : 0.f;
-        }
-        float g = 0.f, up = 0.f;
+        for (int i = 0; i < 4; ++i)
 #pragma unroll
-        for (int q = 0; q < 8; ++q) {
-          if (q < splits) {
-            g += gv[q];
-            if (SW) up += uv[q];
+          for (int q = 0; q < 8; ++q) {
+            const bool on = i < jn && q < splits;
+            gv[i][q] = on ? peer[q][(jb + i) * RW + threadIdx.x] : 0.f;
+            if (SW) uv[i][q] = on ? peer[q][(jb + i) * RW + BM + threadIdx.x] : 0.f;
           }
+        float gs[16], us[16];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          float g = 0.f, up = 0.f;
+#pragma unroll
+          for (int q = 0; q < 8; ++q)
+            if (q < splits) {  // split order, whatever CTA reduces
+              g += gv[i][q];
+              if (SW) up += uv[i][q];
+            }
+          gs[i] = g;
+          us[i] = up;
         }
-        if (f < N) {
-          const size_t o = (size_t)r * ldc + f;
-          if (EPI == kEpiStore) Cf[o] = g;
-          else if (EPI == kEpiResid) Cf[o] += g;
-          else Ct[o] = __float2bfloat16_rn(g / (1.0f + expf(-g)) * up);
-        }
+        if (f < N) epilogue16<EPI>(gs, us, jn, Cf, Ct, (size_t)(m0 + jb) * ldc + f, ldc);
       }
     }
     cl.sync();
@@ -403,14 +421,49 @@ static bool launch_bn(cudaStream_t s, const __nv_bfloat16* A, int lda, int a_row
 
 }  // namespace tc
 
-int gemm_tc_splits(int N, int K, bool decode) {
-  if (!decode) return 1;
+// Clusters of `size` CTAs of this kernel that can be resident at once.
+template <int BN, int EPI>
+static int max_clusters(int size) {
+  static int cache[9] = {0};
+  if (size < 1 || size > 8) return 0;
+  if (cache[size]) return cache[size];
+  using C = tc::Cfg<BN, EPI == kEpiSwiglu>;
+  cudaFuncSetAttribute(tc::k_gemm_tc<BN, EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+  cudaFuncSetAttribute(tc::k_gemm_tc<BN, EPI>, cudaFuncAttributeNonPortableClusterSizeAllowed, 0);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(1, 1, size);
+  cfg.blockDim = dim3(128, 1, 1);
+  cfg.dynamicSmemBytes = C::SMEM;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeClusterDimension;
+  at[0].val.clusterDim.x = 1;
+  at[0].val.clusterDim.y = 1;
+  at[0].val.clusterDim.z = size;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, tc::k_gemm_tc<BN, EPI>, &cfg) != cudaSuccess) n = 0;
+  cache[size] = n > 0 ? n : 1;
+  return cache[size];
+}
+
+// Split count for a decode GEMM: about one CTA per SM, at least 4 K slabs per
+// split, and every tile's cluster resident in one wave.  Depends only on the
+// weight shape (and the device), never on the number of rows.
+template <int BN, int EPI>
+static int splits_for(int N, int K) {
   const int tiles = (N + tc::BM - 1) / tc::BM;
   const int KT = (K + tc::BK - 1) / tc::BK;
   int s = (int)((152.0 / tiles) + 0.5);
   if (s > KT / 4) s = KT / 4;
-  if (s > 8) s = 8;  // one portable cluster per tile
+  if (s > 8) s = 8;
+  while (s > 1 && tiles > max_clusters<BN, EPI>(s)) --s;
   return s < 1 ? 1 : s;
+}
+
+int gemm_tc_splits(int N, int K, bool decode) {
+  if (!decode) return 1;
+  return splits_for<64, kEpiStore>(N, K);
 }
 
 bool launch_gemm_tc(cudaStream_t s, int epi, const __nv_bfloat16* A, int lda, int a_rows, const __nv_bfloat16* W,
@@ -418,14 +471,21 @@ bool launch_gemm_tc(cudaStream_t s, int epi, const __nv_bfloat16* A, int lda, in
                     bool decode, int* status) {
   if (rows <= 0) return true;
   if ((K * 2) % 16 != 0 || (lda * 2) % 16 != 0 || rows > a_rows) return false;
-  const int splits = gemm_tc_splits(N, K, decode);
   if (decode) {
+    int splits;
     switch (epi) {
-      case kEpiStore: return tc::launch_bn<64, kEpiStore>(s, A, lda, a_rows, W, W2, N, K, rows, splits, Cf, Ct, ldc, status);
-      case kEpiResid: return tc::launch_bn<64, kEpiResid>(s, A, lda, a_rows, W, W2, N, K, rows, splits, Cf, Ct, ldc, status);
-      default: return tc::launch_bn<64, kEpiSwiglu>(s, A, lda, a_rows, W, W2, N, K, rows, splits, Cf, Ct, ldc, status);
+      case kEpiStore:
+        splits = splits_for<64, kEpiStore>(N, K);
+        return tc::launch_bn<64, kEpiStore>(s, A, lda, a_rows, W, W2, N, K, rows, splits, Cf, Ct, ldc, status);
+      case kEpiResid:
+        splits = splits_for<64, kEpiResid>(N, K);
+        return tc::launch_bn<64, kEpiResid>(s, A, lda, a_rows, W, W2, N, K, rows, splits, Cf, Ct, ldc, status);
+      default:
+        splits = splits_for<64, kEpiSwiglu>(N, K);
+        return tc::launch_bn<64, kEpiSwiglu>(s, A, lda, a_rows, W, W2, N, K, rows, splits, Cf, Ct, ldc, status);
     }
   }
+  const int splits = 1;
   switch (epi) {
     case kEpiStore: return tc::launch_bn<128, kEpiStore>(s, A, lda, a_rows, W, W2, N, K, rows, splits, Cf, Ct, ldc, status);
     case kEpiResid: return tc::launch_bn<128, kEpiResid>(s, A, lda, a_rows, W, W2, N, K, rows, splits, Cf, Ct, ldc, status);

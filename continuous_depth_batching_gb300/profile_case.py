@@ -1,0 +1,71 @@
+"""A small decode case for kernel profiling (ncu), with the bench's per-launch shapes.
+
+Runs the Ouro-shaped model and workload of bench.py (d 2048, 16x128 heads,
+SwiGLU 5632, W = 64, prompts 128..1024) but with --layers core layers instead
+of 24, so every attention and projection launch has exactly the bench's
+shape while the depth-indexed KV pool stays a few GB.  Prints the kernel-class
+timing of the decode steps.  Not a benchmark: bench.py is.
+
+    python -m continuous_depth_batching_gb300.profile_case --layers 1 --steps 4
+"""
+
+from __future__ import annotations
+
+import argparse
+import dataclasses
+import json
+import os
+import sys
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--layers", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=4)
+    ap.add_argument("--warmup", type=int, default=2)
+    ap.add_argument("--workload", default="ouro")
+    args = ap.parse_args()
+
+    import torch
+
+    from continuous_depth_batching_gb300 import binding
+    from continuous_depth_batching_gb300.build import build
+    from synth import make_requests, make_weights, model_shape, workload
+
+    build()
+    wl = workload(args.workload)
+    shape = dataclasses.replace(model_shape(wl.model), n_core=args.layers)
+    dw = binding.device_weights(shape, make_weights(shape))
+    reqs = make_requests(wl, shape.vocab, shape.r_max, shape.r_min)
+    max_ctx = (wl.prompt_hi + wl.gen_hi - 1 + 15) // 16 * 16
+    eng = binding.Engine(shape, dw, mode="refill", W=wl.W, M=wl.M, K=wl.K, max_ctx=max_ctx,
+                         max_new_cap=wl.gen_hi)
+    for r in reqs:
+        eng.admit(r["seq_id"], r["prompt"], r["gen_len"], r["replay"])
+
+    def advance(n):
+        done = 0
+        while done < n:
+            rc, _ = eng.step_boundary()
+            if rc == binding.DONE:
+                break
+            if rc == binding.IDLE:
+                eng.step_core()
+                done += 1
+
+    advance(args.warmup)
+    torch.cuda.synchronize()
+    eng.profile_enable(True)
+    advance(args.steps)
+    prof = eng.profile_read()
+    eng.close()
+    print(json.dumps({k: dict(v, GBps=(v["bytes"] / v["ms"] / 1e6) if v["ms"] else None)
+                      for k, v in prof.items()}))
+
+
+if __name__ == "__main__":
+    main()
