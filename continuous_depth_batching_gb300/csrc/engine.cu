@@ -672,7 +672,7 @@ int cdb_init(const cdb_model_desc* m, const cdb_weights* w, const cdb_sched_cfg*
     return CDB_ERR_ARG;
   if (c->W < 1 || c->M < 1 || c->K < 1 || c->kv_blocks < 1 || c->max_ctx < 1 || c->max_new_cap < 1 ||
       c->mode < 0 || c->mode > 2 || c->trace_tokens < 0 || !c->arena || ((uintptr_t)c->arena % kAlign) != 0 ||
-      c->attn_split < 0 || (c->S > c->W))
+      c->attn_split < 0 || c->attn_split % 16 != 0 || (c->S > c->W))
     return CDB_ERR_ARG;
   if (!w->embed || !w->lm_head || !w->final_norm || !w->gate_w || (m->n_core > 0 && !w->core) ||
       (m->n_prelude > 0 && !w->prelude) || (m->n_coda > 0 && !w->coda))
@@ -937,6 +937,49 @@ int cdb_test_gemm(int epi, int tiling, const void* A, int lda, int a_rows, const
                              status)) {
     return CDB_ERR_ARG;
   }
+  if (cudaGetLastError() != cudaSuccess || cudaStreamSynchronize(s) != cudaSuccess) return CDB_ERR_CUDA;
+  int st = 0;
+  if (cudaMemcpy(&st, status, 4, cudaMemcpyDeviceToHost) != cudaSuccess) return CDB_ERR_CUDA;
+  return st ? CDB_ERR_DEVICE_BOUNDS : CDB_OK;
+}
+
+size_t cdb_test_attention_scratch_bytes(int rows, int n_heads, int head_dim, int split, int max_ctx) {
+  if (rows < 0 || n_heads < 1 || head_dim < 1 || split < 1 || max_ctx < 1) return 0;
+  const size_t ms = (size_t)(max_ctx + split - 1) / split;
+  const size_t po = (size_t)rows * n_heads * ms * head_dim * 4;
+  return 256 + (po + 255) / 256 * 256 + (size_t)rows * n_heads * ms * 2 * 4;
+}
+
+int cdb_test_attention(const void* q, int rows, const int32_t* slot, const int32_t* pos, const int32_t* depth,
+                       const void* kv_pool, const int32_t* block_table, int max_blocks, const uint8_t* exit_table,
+                       int kv_blocks, int n_kv_slots, int slot_base, int n_heads, int head_dim, int dtype, int split,
+                       int max_ctx, void* out, void* scratch, size_t scratch_bytes, void* stream) {
+  if (!q || rows < 1 || !slot || !pos || !depth || !kv_pool || !block_table || max_blocks < 1 || !exit_table ||
+      kv_blocks < 1 || n_kv_slots < 1 || slot_base < 0 || n_heads < 1 || !valid_hd(head_dim) ||
+      (dtype != CDB_FP32 && dtype != CDB_BF16) || split < 16 || split % 16 != 0 || max_ctx < 1 || !out ||
+      !scratch || scratch_bytes < cdb_test_attention_scratch_bytes(rows, n_heads, head_dim, split, max_ctx))
+    return CDB_ERR_ARG;
+  cudaStream_t s = (cudaStream_t)stream;
+  char* w = (char*)scratch;
+  int* status = (int*)w;
+  const size_t ms = (size_t)(max_ctx + split - 1) / split;
+  float* part_o = (float*)(w + 256);
+  float* part_ml = (float*)(w + 256 + ((size_t)rows * n_heads * ms * head_dim * 4 + 255) / 256 * 256);
+  if (cudaMemsetAsync(status, 0, 4, s) != cudaSuccess) return CDB_ERR_CUDA;
+  KvGeom g;
+  g.pool = const_cast<void*>(kv_pool);
+  g.bt = block_table;
+  g.etab = const_cast<uint8_t*>(exit_table);
+  g.max_blocks = max_blocks;
+  g.kv_blocks = kv_blocks;
+  g.nsl = n_kv_slots;
+  g.d = n_heads * head_dim;
+  if (dtype == CDB_BF16)
+    launch_attention<__nv_bfloat16>(s, (const __nv_bfloat16*)q, rows, slot, pos, depth, 0, g, slot_base, 1, n_heads,
+                                    head_dim, split, (int)ms, (__nv_bfloat16*)out, part_o, part_ml, status);
+  else
+    launch_attention<float>(s, (const float*)q, rows, slot, pos, depth, 0, g, slot_base, 1, n_heads, head_dim,
+                            split, (int)ms, (float*)out, part_o, part_ml, status);
   if (cudaGetLastError() != cudaSuccess || cudaStreamSynchronize(s) != cudaSuccess) return CDB_ERR_CUDA;
   int st = 0;
   if (cudaMemcpy(&st, status, 4, cudaMemcpyDeviceToHost) != cudaSuccess) return CDB_ERR_CUDA;

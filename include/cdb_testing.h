@@ -30,6 +30,31 @@ int cdb_test_gemm(int epi, int tiling, const void *A, int lda, int a_rows, const
                   void *stream);
 size_t cdb_test_gemm_ws_bytes(int N, int K, int rows, int tiling, int epi);
 
+/* Decode attention over the depth-indexed paged KV cache, as in the core step
+ * ("Depth-adaptive Inference of Looped Language Models via Continuous Depth
+ * Batching", §4.2: row i at loop step r reads cached position j from step
+ * min(r, e_j); Appendix A.1: 16-token pages through a block table).
+ *   q        [rows][n_heads*head_dim], dtype elements (0 fp32, 1 bf16)
+ *   slot, pos, depth  int32 [rows]: sequence slot, own position (keys
+ *            0..pos are read), loop steps completed (this step is depth+1)
+ *   kv_pool  [kv_blocks][n_kv_slots][2][16][n_heads*head_dim] (K then V)
+ *   block_table int32 [*][max_blocks]; exit_table uint8 [kv_blocks][16]
+ *   slot_base: cache slot of loop step 1 of this core layer
+ *   split:   keys per split-KV partial (fixed, so results do not depend on
+ *            the batch); out [rows][n_heads*head_dim], dtype elements
+ *   scratch: device memory of cdb_test_attention_scratch_bytes() bytes for
+ *            the split partials (any contents; every value read is written
+ *            by the same call)
+ * All pointers are device pointers owned by the caller.  Synchronizes the
+ * stream.  Returns CDB_OK, CDB_ERR_ARG (bad shape or scratch too small),
+ * CDB_ERR_CUDA, or CDB_ERR_DEVICE_BOUNDS (a page or depth out of range). */
+int cdb_test_attention(const void *q, int rows, const int32_t *slot, const int32_t *pos,
+                       const int32_t *depth, const void *kv_pool, const int32_t *block_table,
+                       int max_blocks, const uint8_t *exit_table, int kv_blocks, int n_kv_slots,
+                       int slot_base, int n_heads, int head_dim, int dtype, int split, int max_ctx,
+                       void *out, void *scratch, size_t scratch_bytes, void *stream);
+size_t cdb_test_attention_scratch_bytes(int rows, int n_heads, int head_dim, int split, int max_ctx);
+
 #ifdef __cplusplus
 }
 #endif

@@ -1,0 +1,125 @@
+"""Decode attention over the depth-indexed paged cache (include/cdb_testing.h).
+
+Reference: a float64 torch restatement of the read rule of §4.2 ("Depth-
+adaptive Inference of Looped Language Models via Continuous Depth Batching"):
+row i at loop step r reads position j from loop step min(r, e_j) through the
+sequence's 16-token pages.  Exit gaps (steps above e_j) hold NaN, so a gap read
+would poison the output.  Also: split sizes agree, and each row's bits do not
+depend on the other rows in the call.
+"""
+
+import ctypes as C
+
+import numpy as np
+import pytest
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def L():
+    from continuous_depth_batching_gb300 import binding
+    from continuous_depth_batching_gb300.build import build
+    build()
+    lib = binding.lib()
+    lib.cdb_test_attention.argtypes = ([C.c_void_p, C.c_int] + [C.c_void_p] * 5 + [C.c_int, C.c_void_p] +
+                                       [C.c_int] * 8 + [C.c_void_p, C.c_void_p, C.c_size_t, C.c_void_p])
+    lib.cdb_test_attention_scratch_bytes.restype = C.c_size_t
+    lib.cdb_test_attention_scratch_bytes.argtypes = [C.c_int] * 5
+    return lib
+
+
+def make_case(dtype, H, hd, rows=6, r_max=4, n_core=2, layer=1, max_ctx=700, seed=0):
+    import torch
+    rng = np.random.default_rng(seed)
+    d = H * hd
+    nsl = n_core * r_max
+    max_blocks = (max_ctx + 15) // 16
+    kv_blocks = rows * max_blocks + 7
+    tdt = torch.bfloat16 if dtype == 1 else torch.float32
+    pool = torch.randn(kv_blocks, nsl, 2, 16, d, dtype=torch.float64)
+    perm = rng.permutation(kv_blocks)[: rows * max_blocks].reshape(rows, max_blocks)
+    bt = torch.from_numpy(perm.astype(np.int32))
+    etab = torch.from_numpy(rng.integers(1, r_max + 1, (kv_blocks, 16)).astype(np.uint8))
+    pos = rng.integers(0, max_ctx, rows).astype(np.int32)
+    pos[0], pos[1] = 0, max_ctx - 1
+    depth = rng.integers(0, r_max, rows).astype(np.int32)
+    slot = np.arange(rows, dtype=np.int32)
+    base = layer * r_max
+    for i in range(rows):  # own position is in flight: read at the current step
+        b = perm[i, pos[i] // 16]
+        etab[b, pos[i] % 16] = r_max
+    # exit gaps -> NaN
+    for b in range(kv_blocks):
+        for o in range(16):
+            e = int(etab[b, o])
+            pool[b, base + e:base + r_max, :, o, :] = float("nan")
+    q = torch.randn(rows, d, dtype=torch.float64)
+    return dict(pool=pool.to(tdt), bt=bt, etab=etab, pos=pos, depth=depth, slot=slot, q=q.to(tdt), H=H, hd=hd,
+                nsl=nsl, base=base, max_blocks=max_blocks, kv_blocks=kv_blocks, max_ctx=max_ctx, r_max=r_max,
+                dtype=dtype)
+
+
+def reference(cs):
+    import torch
+    pool = cs["pool"].double()
+    q = cs["q"].double()
+    H, hd = cs["H"], cs["hd"]
+    out = torch.zeros_like(q)
+    for i in range(len(cs["pos"])):
+        r = int(cs["depth"][i]) + 1
+        P = int(cs["pos"][i]) + 1
+        j = torch.arange(P)
+        blk = cs["bt"][int(cs["slot"][i])][j // 16].long()
+        off = j % 16
+        e = cs["etab"][blk, off].long()
+        sl = cs["base"] + torch.clamp(e, max=r) - 1
+        K = pool[blk, sl, 0, off]
+        V = pool[blk, sl, 1, off]
+        for h in range(H):
+            s = K[:, h * hd:(h + 1) * hd] @ q[i, h * hd:(h + 1) * hd] / np.sqrt(hd)
+            p = torch.softmax(s, 0)
+            out[i, h * hd:(h + 1) * hd] = p @ V[:, h * hd:(h + 1) * hd]
+    return out
+
+
+def run(L, cs, split, rows=None):
+    import torch
+    n = rows or len(cs["pos"])
+    dev = {k: cs[k].cuda() for k in ("pool", "bt", "etab", "q")}
+    slot = torch.from_numpy(cs["slot"][:n]).cuda()
+    pos = torch.from_numpy(cs["pos"][:n]).cuda()
+    depth = torch.from_numpy(cs["depth"][:n]).cuda()
+    out = torch.zeros(n, cs["H"] * cs["hd"], dtype=cs["q"].dtype, device="cuda")
+    nb = L.cdb_test_attention_scratch_bytes(n, cs["H"], cs["hd"], split, cs["max_ctx"])
+    scratch = torch.empty(nb, dtype=torch.uint8, device="cuda")
+    rc = L.cdb_test_attention(dev["q"].data_ptr(), n, slot.data_ptr(), pos.data_ptr(), depth.data_ptr(),
+                              dev["pool"].data_ptr(), dev["bt"].data_ptr(), cs["max_blocks"], dev["etab"].data_ptr(),
+                              cs["kv_blocks"], cs["nsl"], cs["base"], cs["H"], cs["hd"], cs["dtype"], split,
+                              cs["max_ctx"], out.data_ptr(), scratch.data_ptr(), nb, None)
+    assert rc == 0, rc
+    return out
+
+
+@pytest.mark.parametrize("dtype,H,hd", [(0, 4, 64), (1, 16, 128), (1, 5, 96), (0, 2, 8)])
+@pytest.mark.parametrize("split", [16, 256])
+def test_matches_reference(L, dtype, H, hd, split):
+    cs = make_case(dtype, H, hd)
+    out = run(L, cs, split).double().cpu()
+    ref = reference(cs)
+    assert torch_finite(out)
+    tol = 2e-5 if dtype == 0 else 1e-2
+    err = (out - ref).abs()
+    assert (err <= tol * (1 + ref.abs())).all().item(), err.max().item()
+
+
+def torch_finite(t):
+    import torch
+    return bool(torch.isfinite(t).all().item())
+
+
+def test_row_bits_independent_of_batch(L):
+    cs = make_case(1, 16, 128, rows=8, seed=3)
+    full = run(L, cs, 256)
+    part = run(L, cs, 256, rows=3)
+    assert (full[:3] == part).all().item()
