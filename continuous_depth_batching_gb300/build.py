@@ -30,6 +30,7 @@ SOURCES = [
     "attention.cu",
     "gemm_simt.cu",
     "gemm_tc.cu",
+    "attention_noalloc.cu",
 ]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

@@ -55,6 +55,29 @@ int cdb_test_attention(const void *q, int rows, const int32_t *slot, const int32
                        void *out, void *scratch, size_t scratch_bytes, void *stream);
 size_t cdb_test_attention_scratch_bytes(int rows, int n_heads, int head_dim, int split, int max_ctx);
 
+/* The same decode attention for callers that must not allocate device memory
+ * (for example a plugin whose host program's memory manager owns all device
+ * memory, or a latency-critical path that cannot take an allocation's implicit
+ * synchronisation).  The paper has no counterpart to this entry point; it is a
+ * deployment convenience of this library.
+ * Arguments and results are those of cdb_test_attention without the scratch
+ * arguments: the split partials and the status word live in a 16 MiB array
+ * built into the library, which every GPU that loads the library keeps
+ * reserved until the process exits.  A call whose partials
+ * (rows * n_heads * ceil(max_ctx / split) * (head_dim + 2) floats, plus 256
+ * bytes) exceed 16 MiB is rejected with CDB_ERR_ARG before any GPU work.
+ * Nothing is allocated: no cudaMalloc, cudaFree or allocating library call.
+ * The first call on a device looks up the array's device address (once per
+ * device, with that device current); make that first call before any stream
+ * capture.  All calls share the one array and it keeps the previous call's
+ * contents, so calls that overlap on the GPU (other streams, other host
+ * threads) race; issue them one after another.  Synchronizes the stream. */
+int cdb_attention_noalloc(const void *q, int rows, const int32_t *slot, const int32_t *pos,
+                          const int32_t *depth, const void *kv_pool, const int32_t *block_table,
+                          int max_blocks, const uint8_t *exit_table, int kv_blocks, int n_kv_slots,
+                          int slot_base, int n_heads, int head_dim, int dtype, int split, int max_ctx,
+                          void *out, void *stream);
+
 #ifdef __cplusplus
 }
 #endif
