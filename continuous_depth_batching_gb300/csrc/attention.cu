@@ -78,6 +78,8 @@ __global__ void __launch_bounds__(128)
            const int* __restrict__ mdepth, int depth_uniform, KvGeom kv, int slot_base, int clamp, int H,
            int split, int max_splits, T* __restrict__ O, float* __restrict__ part_o,
            float* __restrict__ part_ml, int* status) {
+  pdl_wait();
+  pdl_trigger();
   using S = AttnShape<T, HD>;
   constexpr int CPE = S::CPE, LPK = S::LPK, CPL = S::CPL, KPW = S::KPW, UNR = S::UNR, NCH = S::NCH;
   constexpr int EPL = CPL * CPE;  // elements per lane
@@ -248,6 +250,8 @@ template <typename T>
 __global__ void k_attn_combine(int rows, const int* __restrict__ mpos, int H, int HDv, int d, int split,
                                int max_splits, const float* __restrict__ part_o,
                                const float* __restrict__ part_ml, T* __restrict__ O) {
+  pdl_wait();
+  pdl_trigger();
   const int row = blockIdx.x / H, h = blockIdx.x % H;
   if (row >= rows) return;
   const int L = mpos[row] + 1;
@@ -272,10 +276,10 @@ static void attn_hd(cudaStream_t s, const T* Q, int rows, const int* mslot, cons
                     T* O, float* part_o, float* part_ml, int* status) {
   dim3 grid(max_splits, (H + 3) / 4, rows);
   count_launch();
-  k_attn<T, HD><<<grid, 128, 0, s>>>(Q, rows, mslot, mpos, mdepth, depth_uniform, kv, slot_base, clamp, H,
+  launch_pdl(k_attn<T, HD>, dim3(grid), dim3(128), 0, s, Q, rows, mslot, mpos, mdepth, depth_uniform, kv, slot_base, clamp, H,
                                      split, max_splits, O, part_o, part_ml, status);
   if (max_splits > 1)
-    count_launch(), k_attn_combine<T><<<rows * H, 128, 0, s>>>(rows, mpos, H, HD, kv.d, split, max_splits, part_o, part_ml, O);
+    count_launch(), launch_pdl(k_attn_combine<T>, dim3(rows * H), dim3(128), 0, s, rows, mpos, H, HD, kv.d, split, max_splits, part_o, part_ml, O);
 }
 
 template <typename T>

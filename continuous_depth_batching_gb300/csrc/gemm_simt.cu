@@ -17,6 +17,8 @@ template <typename T, int EPI>
 __global__ void __launch_bounds__(256)
     k_gemm_simt(const T* __restrict__ A, int lda, const T* __restrict__ W, const T* __restrict__ W2, int N,
                 int K, int rows, float* __restrict__ Cf, T* __restrict__ Ct, int ldc) {
+  pdl_wait();
+  pdl_trigger();
   constexpr bool SW = EPI == kEpiSwiglu;
   __shared__ float As[BK][BM + 4];
   __shared__ float Bs[BK][BN + 4];
@@ -84,10 +86,10 @@ void launch_gemm(cudaStream_t s, int epi, const T* A, int lda, const T* W, const
   if (rows <= 0) return;
   dim3 grid((N + BN - 1) / BN, (rows + BM - 1) / BM);
   count_launch();
-  if (epi == kEpiStore) k_gemm_simt<T, kEpiStore><<<grid, 256, 0, s>>>(A, lda, W, W2, N, K, rows, Cf, Ct, ldc);
+  if (epi == kEpiStore) launch_pdl(k_gemm_simt<T, kEpiStore>, dim3(grid), dim3(256), 0, s, A, lda, W, W2, N, K, rows, Cf, Ct, ldc);
   else if (epi == kEpiResid)
-    k_gemm_simt<T, kEpiResid><<<grid, 256, 0, s>>>(A, lda, W, W2, N, K, rows, Cf, Ct, ldc);
-  else k_gemm_simt<T, kEpiSwiglu><<<grid, 256, 0, s>>>(A, lda, W, W2, N, K, rows, Cf, Ct, ldc);
+    launch_pdl(k_gemm_simt<T, kEpiResid>, dim3(grid), dim3(256), 0, s, A, lda, W, W2, N, K, rows, Cf, Ct, ldc);
+  else launch_pdl(k_gemm_simt<T, kEpiSwiglu>, dim3(grid), dim3(256), 0, s, A, lda, W, W2, N, K, rows, Cf, Ct, ldc);
 }
 
 template void launch_gemm<float>(cudaStream_t, int, const float*, int, const float*, const float*, int, int, int,

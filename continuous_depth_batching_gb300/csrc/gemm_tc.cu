@@ -205,10 +205,24 @@ __global__ void __launch_bounds__(128, 1)
   const uint32_t tmem = *tmem_slot;
 
   if (warp == 0 && lane == 0) {
-    // TMA producer
-    for (int i = 0; i < nkt; ++i) {
+    // TMA producer.  Weights never change, so the first ring of weight tiles
+    // is requested before waiting for the previous kernel; activation tiles
+    // only after it has completed.
+    const int pre = nkt < C::STAGES ? nkt : C::STAGES;
+    for (int i = 0; i < pre; ++i) {
+      uint8_t* st = smem + i * C::STAGE;
+      mbar_expect_tx(&full[i], C::STAGE);
+      const int kx = (kt0 + i) * BK;
+      tma_load(st, &tmW, &full[i], kx, n0);
+      if (SW) tma_load(st + C::A_BYTES, &tmW2, &full[i], kx, n0);
+    }
+    pdl_wait();
+    pdl_trigger();
+    for (int i = 0; i < pre; ++i)
+      tma_load(smem + i * C::STAGE + C::A_BYTES * (SW ? 2 : 1), &tmA, &full[i], (kt0 + i) * BK, m0);
+    for (int i = pre; i < nkt; ++i) {
       const int s = i % C::STAGES;
-      if (i >= C::STAGES && !mbar_wait(&empty[s], ((i / C::STAGES) - 1) & 1)) {
+      if (!mbar_wait(&empty[s], ((i / C::STAGES) - 1) & 1)) {
         s_fail = 1;
         atomicOr(status, kStatusTimeout);
         break;
@@ -245,6 +259,7 @@ __global__ void __launch_bounds__(128, 1)
     mma_commit(done);
   }
   __syncwarp();
+  pdl_wait();  // outputs (and residual inputs) belong to earlier kernels
   const bool ok = mbar_wait(done, 0) && !s_fail;
   fence_after();
   if (!ok) {
@@ -407,13 +422,15 @@ static bool launch_bn(cudaStream_t s, const __nv_bfloat16* A, int lda, int a_row
   cfg.blockDim = dim3(128, 1, 1);
   cfg.dynamicSmemBytes = C::SMEM;
   cfg.stream = s;
-  cudaLaunchAttribute at[1];
-  at[0].id = cudaLaunchAttributeClusterDimension;
-  at[0].val.clusterDim.x = 1;
-  at[0].val.clusterDim.y = 1;
-  at[0].val.clusterDim.z = splits;
+  cudaLaunchAttribute at[2];
+  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[0].val.programmaticStreamSerializationAllowed = 1;
+  at[1].id = cudaLaunchAttributeClusterDimension;
+  at[1].val.clusterDim.x = 1;
+  at[1].val.clusterDim.y = 1;
+  at[1].val.clusterDim.z = splits;
   cfg.attrs = at;
-  cfg.numAttrs = splits > 1 ? 1 : 0;
+  cfg.numAttrs = splits > 1 ? 2 : 1;
   count_launch();
   return cudaLaunchKernelEx(&cfg, k_gemm_tc<BN, EPI>, *mw, *mw2, *ma, N, K, rows, splits, Cf, Ct, ldc, status) ==
          cudaSuccess;

@@ -28,6 +28,8 @@ template <typename T>
 __global__ void k_embed_prefill(const T* __restrict__ E, int d, int V, const int* __restrict__ rslot,
                                 const int* __restrict__ rpos, const int* __restrict__ rtok, int rows,
                                 float* __restrict__ X, KvGeom kv, int r_max, int* status) {
+  pdl_wait();
+  pdl_trigger();
   const int i = blockIdx.x;
   if (i >= rows) return;
   int tok = rtok[i];
@@ -51,6 +53,8 @@ __global__ void k_embed_prelude(const T* __restrict__ E, int d, int V, const int
                                 const int* __restrict__ lt, const int* __restrict__ lpos, int rows,
                                 const int* __restrict__ out_tok, int cap, float* __restrict__ X,
                                 RowMeta m, KvGeom kv, int r_max, int* status) {
+  pdl_wait();
+  pdl_trigger();
   const int i = blockIdx.x;
   if (i >= rows) return;
   const int slot = lslot[i], t = lt[i], pos = lpos[i];
@@ -78,6 +82,8 @@ __global__ void k_embed_prelude(const T* __restrict__ E, int d, int V, const int
 __global__ void k_prelude_finish(const float* __restrict__ Tp, RowMeta tm, int rows,
                                  float* __restrict__ Pb, RowMeta pm, int dst_off,
                                  float* __restrict__ estore, int d, int adapter) {
+  pdl_wait();
+  pdl_trigger();
   const int i = blockIdx.x;
   if (i >= rows) return;
   const int o = dst_off + i, slot = tm.slot[i];
@@ -106,6 +112,8 @@ __global__ void k_prelude_finish(const float* __restrict__ Tp, RowMeta tm, int r
 template <typename T>
 __global__ void k_rmsnorm(const float* __restrict__ X, const T* __restrict__ g, T* __restrict__ A,
                           int rows, int d, float eps, int lda) {
+  pdl_wait();
+  pdl_trigger();
   __shared__ float sh[33];
   const int i = blockIdx.x;
   if (i >= rows) return;
@@ -122,6 +130,8 @@ __global__ void k_rmsnorm(const float* __restrict__ X, const T* __restrict__ g, 
 template <typename T>
 __global__ void k_concat(const float* __restrict__ E, int e_per_slot, const int* __restrict__ mslot,
                          const float* __restrict__ X, T* __restrict__ A, int rows, int d) {
+  pdl_wait();
+  pdl_trigger();
   const int i = blockIdx.x;
   if (i >= rows) return;
   const float* e = E + (size_t)(e_per_slot ? mslot[i] : i) * d;
@@ -144,6 +154,8 @@ __global__ void k_rope_kv(const float* __restrict__ QKV, int rows, const int* __
                           const int* __restrict__ mpos, const int* __restrict__ mdepth,
                           int depth_uniform, int slot_base, int clamp, T* __restrict__ Q, KvGeom kv,
                           int H, int hd, const float2* __restrict__ rope, int* status) {
+  pdl_wait();
+  pdl_trigger();
   const int i = blockIdx.x;
   if (i >= rows) return;
   const int d = kv.d, half = hd / 2;
@@ -177,6 +189,8 @@ __global__ void k_rope_kv(const float* __restrict__ QKV, int rows, const int* __
 
 // cos/sin of pos * theta^(-2j/hd), evaluated in double and rounded once.
 __global__ void k_rope_table(float2* tab, int max_ctx, int hd, float theta) {
+  pdl_wait();
+  pdl_trigger();
   const int half = hd / 2;
   const int n = max_ctx * half;
   for (int u = blockIdx.x * blockDim.x + threadIdx.x; u < n; u += gridDim.x * blockDim.x) {
@@ -199,6 +213,8 @@ __global__ void k_gate(const float* __restrict__ X, const T* __restrict__ w, flo
                        float eps, int rows, int d, RowMeta m, int mode, int r_min, int r_max,
                        const int8_t* __restrict__ fexit, int cap, int* __restrict__ pend_new,
                        uint8_t* __restrict__ ring, float* __restrict__ gtrace) {
+  pdl_wait();
+  pdl_trigger();
   __shared__ float sh[33];
   const int i = blockIdx.x;
   if (i >= rows) return;
@@ -238,6 +254,8 @@ __global__ void k_compact(const float* __restrict__ X, RowMeta m, const int* __r
                           int B, int d, int r_max, int qc_off, float* __restrict__ Xc, RowMeta mc,
                           float* __restrict__ Cb, RowMeta mb, KvGeom kv, int8_t* __restrict__ out_depth,
                           int cap, int* status) {
+  pdl_wait();
+  pdl_trigger();
   __shared__ float sh[33];
   const int i = blockIdx.x;
   if (i >= B) return;
@@ -271,6 +289,8 @@ __global__ void k_compact(const float* __restrict__ X, RowMeta m, const int* __r
 __global__ void k_gather_core(const float* __restrict__ Xc, RowMeta mc, int B_cont,
                               const float* __restrict__ Pb, RowMeta mp, int n_ref,
                               float* __restrict__ X, RowMeta mx, int d) {
+  pdl_wait();
+  pdl_trigger();
   const int i = blockIdx.x;
   if (i >= B_cont + n_ref) return;
   const bool c = i < B_cont;
@@ -293,6 +313,8 @@ __global__ void k_gather_core(const float* __restrict__ Xc, RowMeta mc, int B_co
 __global__ void k_gather_rows(const float* __restrict__ src, const int* __restrict__ idx,
                               const int* __restrict__ rslot, const int* __restrict__ rpos, int n,
                               float* __restrict__ dst, RowMeta md, int d) {
+  pdl_wait();
+  pdl_trigger();
   const int k = blockIdx.x;
   if (k >= n) return;
   const int j = idx[k];
@@ -307,6 +329,8 @@ __global__ void k_gather_rows(const float* __restrict__ src, const int* __restri
 }
 
 __global__ void k_copy_rows(const float* __restrict__ src, float* __restrict__ dst, size_t n) {
+  pdl_wait();
+  pdl_trigger();
   for (size_t u = blockIdx.x * (size_t)blockDim.x + threadIdx.x; u < n;
        u += (size_t)gridDim.x * blockDim.x)
     dst[u] = src[u];
@@ -320,6 +344,8 @@ __global__ void k_argmax(const float* __restrict__ logits, int rows, int V, RowM
                          const int* __restrict__ ftok, int cap, int* __restrict__ out_tok,
                          float* __restrict__ ltrace, int trace_T, const float* __restrict__ Hin,
                          float* __restrict__ htrace, int d, int* status) {
+  pdl_wait();
+  pdl_trigger();
   __shared__ float sv[32];
   __shared__ int si[32];
   const int i = blockIdx.x;
@@ -379,35 +405,35 @@ __global__ void k_argmax(const float* __restrict__ logits, int rows, int V, RowM
 template <typename T>
 void launch_embed_prefill(cudaStream_t s, const T* E, int d, int V, const int* rslot, const int* rpos,
                           const int* rtok, int rows, float* X, KvGeom kv, int r_max, int* status) {
-  if (rows > 0) count_launch(), k_embed_prefill<T><<<rows, 256, 0, s>>>(E, d, V, rslot, rpos, rtok, rows, X, kv, r_max, status);
+  if (rows > 0) count_launch(), launch_pdl(k_embed_prefill<T>, dim3(rows), dim3(256), 0, s, E, d, V, rslot, rpos, rtok, rows, X, kv, r_max, status);
 }
 template <typename T>
 void launch_embed_prelude(cudaStream_t s, const T* E, int d, int V, const int* lslot, const int* lt,
                           const int* lpos, int rows, const int* out_tok, int cap, float* X,
                           RowMeta meta, KvGeom kv, int r_max, int* status) {
   if (rows > 0)
-    count_launch(), k_embed_prelude<T><<<rows, 256, 0, s>>>(E, d, V, lslot, lt, lpos, rows, out_tok, cap, X, meta, kv,
+    count_launch(), launch_pdl(k_embed_prelude<T>, dim3(rows), dim3(256), 0, s, E, d, V, lslot, lt, lpos, rows, out_tok, cap, X, meta, kv,
                                             r_max, status);
 }
 void launch_prelude_finish(cudaStream_t s, const float* Tp, RowMeta tm, int rows, float* Pb, RowMeta pm,
                            int dst_off, float* estore, int d, int adapter) {
-  if (rows > 0) count_launch(), k_prelude_finish<<<rows, 256, 0, s>>>(Tp, tm, rows, Pb, pm, dst_off, estore, d, adapter);
+  if (rows > 0) count_launch(), launch_pdl(k_prelude_finish, dim3(rows), dim3(256), 0, s, Tp, tm, rows, Pb, pm, dst_off, estore, d, adapter);
 }
 template <typename T>
 void launch_rmsnorm(cudaStream_t s, const float* X, const T* g, T* A, int rows, int d, float eps, int lda) {
-  if (rows > 0) count_launch(), k_rmsnorm<T><<<rows, 256, 0, s>>>(X, g, A, rows, d, eps, lda);
+  if (rows > 0) count_launch(), launch_pdl(k_rmsnorm<T>, dim3(rows), dim3(256), 0, s, X, g, A, rows, d, eps, lda);
 }
 template <typename T>
 void launch_concat(cudaStream_t s, const float* E, int e_per_slot, const int* mslot, const float* X, T* A,
                    int rows, int d) {
-  if (rows > 0) count_launch(), k_concat<T><<<rows, 256, 0, s>>>(E, e_per_slot, mslot, X, A, rows, d);
+  if (rows > 0) count_launch(), launch_pdl(k_concat<T>, dim3(rows), dim3(256), 0, s, E, e_per_slot, mslot, X, A, rows, d);
 }
 template <typename T>
 void launch_rope_kv(cudaStream_t s, const float* QKV, int rows, const int* mslot, const int* mpos,
                     const int* mdepth, int depth_uniform, int slot_base, int clamp, T* Q, KvGeom kv, int H,
                     int hd, const float2* rope, int* status) {
   if (rows > 0)
-    count_launch(), k_rope_kv<T><<<rows, 256, 0, s>>>(QKV, rows, mslot, mpos, mdepth, depth_uniform, slot_base, clamp, Q,
+    count_launch(), launch_pdl(k_rope_kv<T>, dim3(rows), dim3(256), 0, s, QKV, rows, mslot, mpos, mdepth, depth_uniform, slot_base, clamp, Q,
                                       kv, H, hd, rope, status);
 }
 template <typename T>
@@ -415,37 +441,37 @@ void launch_gate(cudaStream_t s, const float* X, const T* w, float bias, float t
                  int d, RowMeta meta, int mode, int r_min, int r_max, const int8_t* fexit, int cap,
                  int* pend_new, uint8_t* ring, float* gtrace) {
   if (rows > 0)
-    count_launch(), k_gate<T><<<rows, 256, 0, s>>>(X, w, bias, thr, eps, rows, d, meta, mode, r_min, r_max, fexit, cap,
+    count_launch(), launch_pdl(k_gate<T>, dim3(rows), dim3(256), 0, s, X, w, bias, thr, eps, rows, d, meta, mode, r_min, r_max, fexit, cap,
                                    pend_new, ring, gtrace);
 }
 void launch_compact(cudaStream_t s, const float* X, RowMeta m, const int* pend_new, int B, int d, int r_max,
                     int qc_off, float* Xc, RowMeta mc, float* Cb, RowMeta mb, KvGeom kv, int8_t* out_depth,
                     int cap, int* status) {
   if (B > 0)
-    count_launch(), k_compact<<<B, 256, 0, s>>>(X, m, pend_new, B, d, r_max, qc_off, Xc, mc, Cb, mb, kv, out_depth, cap,
+    count_launch(), launch_pdl(k_compact, dim3(B), dim3(256), 0, s, X, m, pend_new, B, d, r_max, qc_off, Xc, mc, Cb, mb, kv, out_depth, cap,
                                 status);
 }
 void launch_gather_core(cudaStream_t s, const float* Xc, RowMeta mc, int B_cont, const float* Pb, RowMeta mp,
                         int n_ref, float* X, RowMeta mx, int d) {
   if (B_cont + n_ref > 0)
-    count_launch(), k_gather_core<<<B_cont + n_ref, 256, 0, s>>>(Xc, mc, B_cont, Pb, mp, n_ref, X, mx, d);
+    count_launch(), launch_pdl(k_gather_core, dim3(B_cont + n_ref), dim3(256), 0, s, Xc, mc, B_cont, Pb, mp, n_ref, X, mx, d);
 }
 void launch_gather_rows(cudaStream_t s, const float* src, const int* idx, const int* rslot, const int* rpos,
                         int n, float* dst, RowMeta md, int d) {
-  if (n > 0) count_launch(), k_gather_rows<<<n, 256, 0, s>>>(src, idx, rslot, rpos, n, dst, md, d);
+  if (n > 0) count_launch(), launch_pdl(k_gather_rows, dim3(n), dim3(256), 0, s, src, idx, rslot, rpos, n, dst, md, d);
 }
 void launch_argmax(cudaStream_t s, const float* logits, int rows, int V, RowMeta m, const int* ftok, int cap,
                    int* out_tok, float* ltrace, int trace_T, const float* H, float* htrace, int d,
                    int* status) {
   if (rows > 0)
-    count_launch(), k_argmax<<<rows, 512, 0, s>>>(logits, rows, V, m, ftok, cap, out_tok, ltrace, trace_T, H, htrace, d,
+    count_launch(), launch_pdl(k_argmax, dim3(rows), dim3(512), 0, s, logits, rows, V, m, ftok, cap, out_tok, ltrace, trace_T, H, htrace, d,
                                   status);
 }
 void launch_rope_table(cudaStream_t s, float2* tab, int max_ctx, int hd, float theta) {
-  count_launch(), k_rope_table<<<1024, 256, 0, s>>>(tab, max_ctx, hd, theta);
+  count_launch(), launch_pdl(k_rope_table, dim3(1024), dim3(256), 0, s, tab, max_ctx, hd, theta);
 }
 void launch_copy_rows(cudaStream_t s, const float* src, float* dst, int rows, int d) {
-  if (rows > 0) count_launch(), k_copy_rows<<<1024, 256, 0, s>>>(src, dst, (size_t)rows * d);
+  if (rows > 0) count_launch(), launch_pdl(k_copy_rows, dim3(1024), dim3(256), 0, s, src, dst, (size_t)rows * d);
 }
 
 #define CDB_INST(T)                                                                                          \

@@ -1,0 +1,82 @@
+"""Parity at full size, in the launch configuration bench.py times.
+
+The Ouro-shaped model (1.4 G parameters, bf16) decodes the whole 256-request
+workload in refill mode with W = 64, M = 8192, K = 1.  The CPU oracle decodes
+the two shortest-prompt sequences alone for their first 8 generated tokens;
+those must match exactly (tokens, exit depths; gate logits near the threshold
+and near-tied argmaxes forced to the oracle's decision), with logits, coda
+inputs and gate logits within 2e-2.  Every sequence must finish with 256
+tokens and exit depths in [r_min, r_max].
+"""
+
+import numpy as np
+import pytest
+
+from synth import make_requests, make_weights, model_shape, workload
+from tests.gpu_util import force_tables
+
+pytestmark = pytest.mark.gpu
+
+T = 8
+TOL = 2e-2
+
+
+def test_ouro_full_workload_matches_oracle_sample():
+    from continuous_depth_batching_gb300 import binding
+    from continuous_depth_batching_gb300.build import build
+    from oracle.model import OracleModel, decode_sequence
+
+    build()
+    wl = workload("ouro")
+    shape = model_shape(wl.model)
+    wts = make_weights(shape)
+    reqs = make_requests(wl, shape.vocab, shape.r_max, shape.r_min)
+    sample = sorted(reqs, key=lambda r: len(r["prompt"]))[:2]
+    om = OracleModel(shape, wts)
+    ref = {r["seq_id"]: decode_sequence(om, r["prompt"], T, keep_logits=T) for r in sample}
+    del om
+
+    max_ctx = (wl.prompt_hi + wl.gen_hi - 1 + 15) // 16 * 16
+    eng = binding.Engine(shape, binding.device_weights(shape, wts), mode="refill", W=wl.W, M=wl.M, K=wl.K,
+                         max_ctx=max_ctx, max_new_cap=wl.gen_hi, trace_tokens=T, trace_gate=True)
+    for r in reqs:
+        fe = ft = None
+        if r["seq_id"] in ref:
+            fe8, ft8 = force_tables(ref[r["seq_id"]])
+            fe = np.zeros(r["gen_len"] - 1, np.int8)
+            fe[: len(fe8)] = fe8
+            ft = np.full(r["gen_len"], -1, np.int32)
+            ft[: len(ft8)] = ft8
+        eng.admit(r["seq_id"], r["prompt"], r["gen_len"], fe, ft)
+    eng.run()
+    out = {o["seq_id"]: o for o in eng.drain(cap=len(reqs))}
+    eng.close()
+
+    assert sorted(out) == [r["seq_id"] for r in reqs]
+    for r in reqs:
+        o = out[r["seq_id"]]
+        assert len(o["tokens"]) == r["gen_len"]
+        assert o["exit_depths"].min() >= shape.r_min and o["exit_depths"].max() <= shape.r_max
+    depths = np.concatenate([o["exit_depths"] for o in out.values()])
+    assert 2.5 < depths.mean() < 3.5, depths.mean()
+
+    worst = 0.0
+    for sid, tr in ref.items():
+        o = out[sid]
+        assert list(o["tokens"][:T]) == tr.tokens
+        assert list(o["exit_depths"][: T - 1]) == tr.exit_depths
+        lg, hd = np.array(tr.logits), np.array(tr.hidden)
+        e_l = np.abs(o["logits"] - lg)
+        e_h = np.abs(o["hidden"] - hd)
+        z_ref = np.concatenate([np.array(z) for z in tr.gate_logits if z])
+        z_got = np.concatenate([o["gate_logits"][t, : len(z)] for t, z in enumerate(tr.gate_logits) if z])
+        e_z = np.abs(z_got - z_ref)
+        print(f"seq {sid}: logits |ref| max {np.abs(lg).max():.3f} rms {np.sqrt((lg**2).mean()):.3f} "
+              f"err max {e_l.max():.4f}; hidden |ref| max {np.abs(hd).max():.3f} rms "
+              f"{np.sqrt((hd**2).mean()):.3f} err max {e_h.max():.4f} p99 {np.quantile(e_h, 0.99):.4f}; "
+              f"gate |z| max {np.abs(z_ref).max():.3f} err max {e_z.max():.5f}")
+        per_t = [float(np.abs(o['hidden'][t] - hd[t]).max() / np.sqrt((hd[t]**2).mean())) for t in range(T)]
+        print("  hidden err / rms per token", [round(x, 5) for x in per_t])
+        worst = max(worst, float(e_l.max()), float(e_z.max()))
+    print("full-size max abs error (logits, gate)", worst)
+    assert worst <= TOL, worst
