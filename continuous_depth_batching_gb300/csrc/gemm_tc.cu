@@ -154,14 +154,17 @@ struct Cfg {
   static constexpr int A_BYTES = BM * BK * 2;
   static constexpr int B_BYTES = BN * BK * 2;
   static constexpr int STAGE = A_BYTES * (SW ? 2 : 1) + B_BYTES;
-  static constexpr int STAGES = (200 * 1024) / STAGE > 8 ? 8 : (200 * 1024) / STAGE;
+  // 64-row (decode) tiles keep two CTAs per SM, so one CTA's prologue and
+  // epilogue overlap the other's weight stream; 128-row tiles use one.
+  static constexpr int BUDGET = BN == 64 ? 104 * 1024 : 200 * 1024;
+  static constexpr int STAGES = BUDGET / STAGE > 8 ? 8 : BUDGET / STAGE;
   static constexpr int ACC = BN * (SW ? 2 : 1);
   static constexpr int TMEM_COLS = ACC <= 32 ? 32 : ACC <= 64 ? 64 : ACC <= 128 ? 128 : ACC <= 256 ? 256 : 512;
   static constexpr int SMEM = STAGES * STAGE + 1024 + 256;
 };
 
 template <int BN, int EPI>
-__global__ void __launch_bounds__(128, 1)
+__global__ void __launch_bounds__(128, BN == 64 ? 2 : 1)
     k_gemm_tc(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmW2,
               const __grid_constant__ CUtensorMap tmA, int N, int K, int rows, int splits,
               float* __restrict__ Cf, __nv_bfloat16* __restrict__ Ct, int ldc, int* status) {
@@ -185,6 +188,9 @@ __global__ void __launch_bounds__(128, 1)
   const int nkt = kt1 - kt0;
 
   if (threadIdx.x == 0) {
+    asm volatile("prefetch.tensormap [%0];" ::"l"(&tmW) : "memory");
+    asm volatile("prefetch.tensormap [%0];" ::"l"(&tmA) : "memory");
+    if (SW) asm volatile("prefetch.tensormap [%0];" ::"l"(&tmW2) : "memory");
     s_fail = 0;
     for (int s = 0; s < C::STAGES; ++s) {
       mbar_init(&full[s], 1);
@@ -471,7 +477,7 @@ template <int BN, int EPI>
 static int splits_for(int N, int K) {
   const int tiles = (N + tc::BM - 1) / tc::BM;
   const int KT = (K + tc::BK - 1) / tc::BK;
-  int s = (int)((152.0 / tiles) + 0.5);
+  int s = (int)((304.0 / tiles) + 0.5);  // about two CTAs per SM
   if (s > KT / 4) s = KT / 4;
   if (s > 8) s = 8;
   while (s > 1 && tiles > max_clusters<BN, EPI>(s)) --s;
