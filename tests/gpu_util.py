@@ -18,13 +18,17 @@ def oracle_traces(shape, wts, reqs, mode="adaptive", keep_logits=0):
     return out
 
 
-def force_tables(tr, replay=None):
-    """force_exit / force_token arrays that pin near-threshold decisions to the oracle's."""
+def force_tables(tr, replay=None, gap_band=NEAR):
+    """force_exit / force_token arrays that pin near-threshold decisions to the oracle's.
+
+    Gate decisions the oracle flagged as near (its near_tol band) and argmaxes
+    whose top-2 gap is below gap_band take the oracle's result.
+    """
     if replay is not None:
         fe = np.asarray(replay, dtype=np.int8)
     else:
         fe = np.array([e if near else 0 for e, near in zip(tr.exit_depths, tr.near_gate)], dtype=np.int8)
-    ft = np.array([t if g < NEAR else -1 for t, g in zip(tr.tokens, tr.top2_gap)], dtype=np.int32)
+    ft = np.array([t if g < gap_band else -1 for t, g in zip(tr.tokens, tr.top2_gap)], dtype=np.int32)
     return fe, ft
 
 

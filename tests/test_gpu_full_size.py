@@ -3,10 +3,16 @@
 The Ouro-shaped model (1.4 G parameters, bf16) decodes the whole 256-request
 workload in refill mode with W = 64, M = 8192, K = 1.  The CPU oracle decodes
 the two shortest-prompt sequences alone for their first 8 generated tokens;
-those must match exactly (tokens, exit depths; gate logits near the threshold
-and near-tied argmaxes forced to the oracle's decision), with logits, coda
-inputs and gate logits within 2e-2.  Every sequence must finish with 256
-tokens and exit depths in [r_min, r_max].
+tokens and exit depths must match exactly.  Every sequence must finish with
+256 tokens and exit depths in [r_min, r_max].
+
+Tolerances: after 96 layer applications in bf16, two correct oracles (float64
+vs float32 reductions, same bf16 rounding points; oracle/noise_floor.py)
+already differ by 0.050 in logits, 0.69 in hidden states (RMS 9.7, about 4%)
+and 0.013 in gate logits.  The bounds below are about twice that floor, and
+gate logits within 0.05 of the threshold and top-2 logit gaps below 0.1 are
+forced to the oracle's decision (about 3x and 2x the floor), since a
+narrower band would leave decisions to rounding noise.
 """
 
 import numpy as np
@@ -18,7 +24,11 @@ from tests.gpu_util import force_tables
 pytestmark = pytest.mark.gpu
 
 T = 8
-TOL = 2e-2
+LOGIT_TOL = 0.1        # absolute
+HIDDEN_TOL = 0.1       # relative to the token's hidden-state RMS
+GATE_TOL = 0.04        # absolute
+GATE_BAND = 0.05       # forcing band around the threshold
+GAP_BAND = 0.1         # forcing band for near-tied argmaxes
 
 
 def test_ouro_full_workload_matches_oracle_sample():
@@ -33,7 +43,7 @@ def test_ouro_full_workload_matches_oracle_sample():
     reqs = make_requests(wl, shape.vocab, shape.r_max, shape.r_min)
     sample = sorted(reqs, key=lambda r: len(r["prompt"]))[:2]
     om = OracleModel(shape, wts)
-    ref = {r["seq_id"]: decode_sequence(om, r["prompt"], T, keep_logits=T) for r in sample}
+    ref = {r["seq_id"]: decode_sequence(om, r["prompt"], T, keep_logits=T, near_tol=GATE_BAND) for r in sample}
     del om
 
     max_ctx = (wl.prompt_hi + wl.gen_hi - 1 + 15) // 16 * 16
@@ -42,7 +52,7 @@ def test_ouro_full_workload_matches_oracle_sample():
     for r in reqs:
         fe = ft = None
         if r["seq_id"] in ref:
-            fe8, ft8 = force_tables(ref[r["seq_id"]])
+            fe8, ft8 = force_tables(ref[r["seq_id"]], gap_band=GAP_BAND)
             fe = np.zeros(r["gen_len"] - 1, np.int8)
             fe[: len(fe8)] = fe8
             ft = np.full(r["gen_len"], -1, np.int32)
@@ -60,7 +70,6 @@ def test_ouro_full_workload_matches_oracle_sample():
     depths = np.concatenate([o["exit_depths"] for o in out.values()])
     assert 2.5 < depths.mean() < 3.5, depths.mean()
 
-    worst = 0.0
     for sid, tr in ref.items():
         o = out[sid]
         assert list(o["tokens"][:T]) == tr.tokens
@@ -77,6 +86,6 @@ def test_ouro_full_workload_matches_oracle_sample():
               f"gate |z| max {np.abs(z_ref).max():.3f} err max {e_z.max():.5f}")
         per_t = [float(np.abs(o['hidden'][t] - hd[t]).max() / np.sqrt((hd[t]**2).mean())) for t in range(T)]
         print("  hidden err / rms per token", [round(x, 5) for x in per_t])
-        worst = max(worst, float(e_l.max()), float(e_z.max()))
-    print("full-size max abs error (logits, gate)", worst)
-    assert worst <= TOL, worst
+        assert e_l.max() <= LOGIT_TOL, e_l.max()
+        assert max(per_t) <= HIDDEN_TOL, per_t
+        assert e_z.max() <= GATE_TOL, e_z.max()
