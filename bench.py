@@ -47,6 +47,7 @@ def parse():
     ap.add_argument("--workload", default="ouro")
     ap.add_argument("--mode", default="refill", choices=["refill", "no_refill", "fixed_depth"])
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-modes", action="store_true", help="skip the no-refill and fixed-depth full jobs")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=20.0)
     return ap.parse_args()
@@ -190,7 +191,7 @@ def run_ours(args):
     import numpy as np
     import torch
 
-    from continuous_depth_batching_gb300 import binding
+    from continuous_depth_batching_gb300 import binding, metrics
     from continuous_depth_batching_gb300.build import build
     from synth import make_requests, make_weights, model_shape, workload
 
@@ -290,29 +291,68 @@ def run_ours(args):
                                  "TFps": (v["flops"] / (v["ms"] / 1e3) / 1e12) if v["ms"] else None}
                              for k, v in prof.items()}})
 
-    e2e = None
-    if not args.no_e2e:
-        eng2 = binding.Engine(shape, dw, **kw)
+    def full_job(mode):
+        """The whole offline job through the public API: admit host prompts ... drain host results.
+
+        Also returns the prefill share of GPU time (alpha of eq. 2), from CUDA
+        events around every boundary call that ran a prefill stage.
+        """
+        eng2 = binding.Engine(shape, dw, **dict(kw, mode=mode))
         torch.cuda.synchronize()
+        g0 = torch.cuda.Event(enable_timing=True)
+        g1 = torch.cuda.Event(enable_timing=True)
+        pairs = []
         t0 = time.perf_counter()
+        g0.record(stream)
         admit_all(eng2)
         n_core = 0
         while True:
-            rc, _ = eng2.step_boundary()
+            a = torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            rc, info = eng2.step_boundary()
+            if info.stage == binding_stage_prefill:
+                b = torch.cuda.Event(enable_timing=True)
+                b.record(stream)
+                pairs.append((a, b))
             if rc == binding.DONE:
                 break
             if rc == binding.IDLE:
                 eng2.step_core()
                 n_core += 1
         res = eng2.drain(cap=len(reqs))
+        g1.record(stream)
         torch.cuda.synchronize()
         dt = time.perf_counter() - t0
+        gpu_ms = g0.elapsed_time(g1)
+        pre_ms = sum(a.elapsed_time(b) for a, b in pairs)
         gen = sum(len(r["tokens"]) for r in res)
+        depth = float(np.mean(np.concatenate([r["exit_depths"] for r in res if len(r["exit_depths"])])))
         h2d, d2h = eng2.io_bytes()
         eng2.close()
-        e2e = {"value": gen / dt, "unit": UNIT, "h2d_bytes_per_step": h2d / max(n_core, 1),
-               "d2h_bytes_per_step": d2h / max(n_core, 1), "core_steps": n_core, "seconds": dt,
-               "tokens": gen, "finished_sequences": len(res)}
+        return {"value": gen / dt, "unit": UNIT, "h2d_bytes_per_step": h2d / max(n_core, 1),
+                "d2h_bytes_per_step": d2h / max(n_core, 1), "core_steps": n_core, "seconds": dt,
+                "tokens": gen, "finished_sequences": len(res), "alpha": pre_ms / gpu_ms,
+                "mean_exit_depth": depth}
+
+    binding_stage_prefill = 1
+    e2e = None
+    modes = None
+    if not args.no_e2e:
+        e2e = full_job(args.mode)
+        if not args.no_modes and args.mode == "refill":
+            fixed = full_job("fixed_depth")
+            norefill = full_job("no_refill")
+            F0, Fr = metrics.token_flops(shape)
+            sdec = metrics.s_dec(F0, Fr, shape.r_max, e2e["mean_exit_depth"])
+            se2e = metrics.s_e2e(fixed["alpha"], sdec)
+            speed = e2e["value"] / fixed["value"]
+            modes = {"refill": e2e["value"], "no_refill": norefill["value"], "fixed_depth": fixed["value"],
+                     "unit": UNIT, "refill_vs_fixed": speed, "no_refill_vs_fixed": norefill["value"] / fixed["value"],
+                     "mean_exit_depth": e2e["mean_exit_depth"], "S_dec": sdec,
+                     "alpha_fixed_depth": fixed["alpha"], "alpha_refill": e2e["alpha"], "S_e2e": se2e,
+                     "realised_fraction_of_S_e2e": speed / se2e,
+                     "note": "whole 256-sequence jobs through the public API, wall clock; S_dec eq. (1) "
+                             "with parameter FLOPs, S_e2e eq. (2) with alpha from the fixed-depth job"}
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -323,7 +363,7 @@ def run_ours(args):
                 "warmup": args.warmup, "ms_per_step": ms / max(cores, 1), "higher_is_better": True,
                 "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
                 "config": _config(wl, shape, args.mode, "inputs larger than L2 (2.5 GB of weights per step)"),
-                "roofline": roof, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches,
+                "roofline": roof, "cpu_baseline": cpu, "e2e": e2e, "modes": modes, "gpu_launches": launches,
                 "clocks": clocks, "tokens_in_window": tot_toks, "core_steps": cores}
         print(json.dumps(line), flush=True)
     if world > 1:
