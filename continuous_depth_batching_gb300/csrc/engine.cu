@@ -49,7 +49,7 @@ static bool plan_layout(const cdb_model_desc* m, const cdb_sched_cfg* c, Layout*
   L->es = es;
   L->nsl = m->n_prelude + m->n_core * m->r_max + m->n_coda;
   L->max_blocks = (c->max_ctx + 15) / 16;
-  L->split = c->attn_split > 0 ? c->attn_split : 256;
+  L->split = c->attn_split > 0 ? c->attn_split : 128;
   L->max_splits = (c->max_ctx + L->split - 1) / L->split;
   L->R = (int)(M > W ? M : W);
   L->cap = c->max_new_cap;

@@ -28,6 +28,7 @@ def main():
     ap.add_argument("--steps", type=int, default=4)
     ap.add_argument("--warmup", type=int, default=2)
     ap.add_argument("--workload", default="ouro")
+    ap.add_argument("--split", type=int, default=0, help="keys per split-KV partial (0: library default)")
     args = ap.parse_args()
 
     import torch
@@ -43,7 +44,7 @@ def main():
     reqs = make_requests(wl, shape.vocab, shape.r_max, shape.r_min)
     max_ctx = (wl.prompt_hi + wl.gen_hi - 1 + 15) // 16 * 16
     eng = binding.Engine(shape, dw, mode="refill", W=wl.W, M=wl.M, K=wl.K, max_ctx=max_ctx,
-                         max_new_cap=wl.gen_hi)
+                         max_new_cap=wl.gen_hi, attn_split=args.split)
     for r in reqs:
         eng.admit(r["seq_id"], r["prompt"], r["gen_len"], r["replay"])
 

@@ -115,7 +115,7 @@ typedef struct {
   size_t arena_bytes;
   void *compute_stream; /* cudaStream_t (NULL: legacy default stream) */
   void *prep_stream;    /* cudaStream_t for host<->device copies of scheduling data */
-  int attn_split;    /* keys per split-KV partial in decode attention, a multiple of 16 (0: 256) */
+  int attn_split;    /* keys per split-KV partial in decode attention, a multiple of 16 (0: 128) */
 } cdb_sched_cfg;
 
 /* Per-call report.  For a boundary call that ran two stages (coda or prefill,
