@@ -118,6 +118,19 @@ def dist_setup():
     return rank, world, local
 
 
+def aggregate(ms: float, tokens: float, world: int, device: str = "cuda"):
+    """Whole-job figures over replicas: max of the ranks' times, sum of their tokens."""
+    if world <= 1:
+        return ms, tokens
+    import torch
+    import torch.distributed as dist
+    mx = torch.tensor([ms], dtype=torch.float64, device=device)
+    sm = torch.tensor([tokens], dtype=torch.float64, device=device)
+    dist.all_reduce(mx, op=dist.ReduceOp.MAX)
+    dist.all_reduce(sm, op=dist.ReduceOp.SUM)
+    return float(mx[0]), float(sm[0])
+
+
 def cpu_baseline(shape, wts, reqs, seconds):
     """The oracle as it stands, on a bounded sample: shortest prompts, prefill + leading tokens."""
     import numpy as np  # noqa: F401
@@ -262,13 +275,7 @@ def run_ours(args):
     eng.profile_enable(False)
     prof_ms = p0.elapsed_time(p1)
     eng.close()
-    tot_toks = toks
-    if world > 1:
-        t = torch.tensor([ms, toks], dtype=torch.float64, device="cuda")
-        mx = t.clone()
-        torch.distributed.all_reduce(mx, op=torch.distributed.ReduceOp.MAX)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.SUM)
-        ms, tot_toks = float(mx[0]), float(t[1])
+    ms, tot_toks = aggregate(ms, toks, world)
     value = tot_toks / (ms / 1e3)
 
     # Roofline of the dominant kernel class (largest device time in the window).
