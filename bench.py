@@ -53,6 +53,25 @@ def parse():
     return ap.parse_args()
 
 
+def attention_traffic_ratio():
+    """DRAM traffic / algorithmic bytes of the decode-attention kernel from the
+    committed ncu summary, if it was captured from the current source."""
+    import hashlib
+    prof = os.path.join(ROOT, "profiles", "k_attn_ouro_decode.md")
+    src = os.path.join(ROOT, "continuous_depth_batching_gb300", "csrc", "attention.cu")
+    if not (os.path.exists(prof) and os.path.exists(src)):
+        return None
+    kv = {}
+    for line in open(prof):
+        if ":" in line and not line.startswith(("|", " ", "#")):
+            k, _, v = line.partition(":")
+            kv[k.strip()] = v.strip()
+    sha = hashlib.sha256(open(src, "rb").read()).hexdigest()
+    if kv.get("source_sha256") != sha or "traffic_ratio_dram_over_algorithmic" not in kv:
+        return None
+    return float(kv["traffic_ratio_dram_over_algorithmic"])
+
+
 def peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -290,7 +309,12 @@ def run_ours(args):
     else:
         achieved = st["flops"] / st["launches"] / (per_launch_ms / 1e3) / 1e12
         roof = {"bound": "tensor", "achieved": achieved, "peak": tf, "unit": "TFLOP/s", "frac": achieved / tf}
-    roof.update({"kernel": dom, "traffic": None, "peak_source": src,
+    ratio = attention_traffic_ratio() if dom == "attention" else None
+    traffic = ratio * st["bytes"] / st["launches"] if ratio is not None else None
+    roof.update({"kernel": dom, "traffic": traffic, "peak_source": src,
+                 "traffic_source": ("ncu dram__bytes_read+write of one captured launch over its algorithmic "
+                                    "bytes (profiles/k_attn_ouro_decode.md), times this window's algorithmic "
+                                    "bytes per launch") if traffic is not None else None,
                  "window": f"{pcores} core steps right after the timed ones, CUDA events on the compute stream",
                  "share_of_step": st["ms"] / prof_ms,
                  "classes": {k: {"launches": v["launches"], "ms": round(v["ms"], 3),

@@ -58,14 +58,31 @@ def main():
                 eng.step_core()
                 done += 1
 
-    advance(args.warmup)
-    torch.cuda.synchronize()
+    # Per decode step (one decode-attention launch per step with one layer):
+    # the attention launch's index among all attention launches and its
+    # algorithmic bytes, so an ncu capture (-k k_attn -s INDEX) can be matched.
     eng.profile_enable(True)
-    advance(args.steps)
-    prof = eng.profile_read()
+    n_attn = 0
+    per_step = []
+    total = {}
+    for i in range(args.warmup + args.steps):
+        advance(1)
+        st = eng.profile_read()
+        n_attn += st["prefill_attention"]["launches"]
+        if st["attention"]["launches"]:
+            per_step.append({"step": i, "attn_index": n_attn, "attn_launches": st["attention"]["launches"],
+                             "attn_bytes": st["attention"]["bytes"], "attn_ms": st["attention"]["ms"]})
+        n_attn += st["attention"]["launches"]
+        if i >= args.warmup:
+            for k, v in st.items():
+                t = total.setdefault(k, dict(launches=0, ms=0.0, bytes=0.0, flops=0.0))
+                for f in t:
+                    t[f] += v[f]
     eng.close()
+    for r in per_step:
+        print(json.dumps(r))
     print(json.dumps({k: dict(v, GBps=(v["bytes"] / v["ms"] / 1e6) if v["ms"] else None)
-                      for k, v in prof.items()}))
+                      for k, v in total.items()}))
 
 
 if __name__ == "__main__":
