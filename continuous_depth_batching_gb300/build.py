@@ -31,6 +31,7 @@ SOURCES = [
     "gemm_simt.cu",
     "gemm_tc.cu",
     "attention_noalloc.cu",
+    "tmap.cu",
 ]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

@@ -8,17 +8,31 @@
 // never read.  Appendix A.1: keys live in 16-token blocks found through the
 // sequence's block table.
 //
-// One warp handles one (row, head, key split).  Keys are split in fixed-size
-// ranges (split), independent of the batch, so a row's result does not depend
-// on what else is in the batch.  Inside a warp, groups of LPK (<= 4) lanes
-// each own one key at a time; each lane loads CPL 16-byte chunks of the key
-// row and of the value row, the group reduces q.k with shuffles and keeps its
-// own online-softmax state, rescaled once per block of UNR keys (scores in the
-// log2 domain, exp2).  The groups are merged in a fixed order at the end.
-// With one split the warp writes the normalised output; otherwise it writes
-// (m, l, acc) partials that k_attn_combine merges in split order.
+// Pool layout [block][slot][K|V][head][16 keys][head_dim]: one head's page of
+// one slot is a contiguous run of 16 * head_dim elements.
+//
+// Keys are split in fixed-size ranges (split), independent of the batch, so a
+// row's result does not depend on what else is in the batch.  A work item is
+// (key split, group of kWarps heads, row); items are numbered split-major
+// (every row has split 0) and handed out by a device counter to a grid of
+// resident CTAs, so which CTA computes an item never changes its result.
+// In a CTA a producer warp streams the item's pages (16 keys, each key from
+// its own depth slot) through a ring of shared-memory stages with 16-byte
+// async copies whose completion lands on the stage's mbarrier; rows are
+// padded by 16 bytes so matrix loads of 8 keys hit 8 different banks.  One
+// consumer warp per head computes:
+//  - bf16, head_dim % 16 == 0: per page, scores s^T = K_page . q and
+//    o^T += V_page^T . p on the warp-level bf16 MMA (m16n8k16, fp32
+//    accumulate), q and p in column 0 of the B operand, p fed as a bf16 pair
+//    p_hi + p_lo (about 16 significant bits); online softmax once per page;
+//  - otherwise: LPK lanes per key, q.k reduced with shuffles, online softmax
+//    per lane group, groups merged in a fixed order at the end.
+// Scores are kept in the log2 domain (exp2).  With one split the warp writes
+// the normalised output; otherwise (m, l, acc) partials that k_attn_combine
+// merges in split order.
 #include "common.cuh"
 #include "kernels.cuh"
+#include "tmap.h"
 
 namespace cdb {
 
@@ -49,198 +63,762 @@ struct Unpack<__nv_bfloat16> {
   }
 };
 
-// 16-byte load of streamed KV data: read-only path, no L1 allocation, so the
-// block-table and exit-depth lines stay cached.
-template <typename T>
-__device__ __forceinline__ uint4 ld_stream(const T* p) {
-  uint4 v;
-  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
-               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-               : "l"(p));
-  return v;
+namespace attn {
+
+constexpr int kWarps = 4;   // consumer warps per CTA, one head each
+constexpr int kStages = 3;  // ring depth (pages)
+
+// Per-stage record: item, flags (bit 0 first page of the item, bit 1 last,
+// bit 2 end of work), valid-key mask, the row's split count.
+struct StageMeta {
+  int item, flags, mask, nsp;
+};
+enum : int { kFirst = 1, kLast = 2, kEnd = 4 };
+
+// Stage layout: rows (K|V, head, key) of RS bytes, then kWarps q rows.
+template <typename T, int HD>
+struct Geo {
+  static constexpr int ES = sizeof(T);
+  static constexpr int RB = HD * ES;             // bytes of one head row
+  static constexpr int RS = RB + 16;             // padded shared-memory row
+  static constexpr int CR = RB / 16;             // 16-byte chunks per row
+  static constexpr int NR = 2 * kWarps * 16;     // K and V rows of one page
+  static constexpr int STAGE = (NR + kWarps) * RS;
+  static constexpr size_t SMEM = (size_t)kStages * STAGE + kStages * (2 * 8 + sizeof(StageMeta));
+  static_assert(RB % 16 == 0, "head row must be a multiple of 16 bytes");
+  static_assert((NR * CR) % 32 == 0, "chunks per page");
+};
+
+__device__ __forceinline__ uint32_t su32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(su32(bar)), "r"(count));
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(su32(bar)) : "memory");
+}
+// Wait for the phase of the given parity; false after ~2 s of global time.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
+  const uint32_t a = su32(bar);
+  uint64_t t0 = 0;
+  for (uint32_t it = 0;; ++it) {
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(ok)
+        : "r"(a), "r"(parity)
+        : "memory");
+    if (ok) return true;
+    if ((it & 63) == 0) {
+      uint64_t t;
+      asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
+      if (t0 == 0) t0 = t;
+      else if (t - t0 > 2000000000ull) return false;
+    }
+  }
 }
 
-// Lanes per key and 16-byte chunks per lane for a head row of HD elements.
+__device__ __forceinline__ void cp16(uint32_t dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+// Arrive on the mbarrier once every earlier cp.async of this thread has
+// landed (counted against the barrier's initial count).
+__device__ __forceinline__ void cp_arrive(uint64_t* bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(su32(bar)) : "memory");
+}
+
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t* r) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t* r) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr));
+}
+// D[16x8] += A[16x16] . B[16x8], bf16 operands, fp32 accumulate.
+__device__ __forceinline__ void mma_bf16(float* d, const uint32_t* a, uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+  const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&v);
+}
+
+}  // namespace attn
+
+// Lanes sharing one key in the CUDA-core path: each lane owns one 16-byte
+// chunk of the head row.
 template <typename T, int HD>
 struct AttnShape {
-  static constexpr int CPE = Unpack<T>::N;       // elements per chunk
-  static constexpr int NCH = HD / CPE;           // chunks per head row
-  static constexpr int LPK = NCH >= 4 ? 4 : 2;  // lanes sharing one key
-  static constexpr int CPL = NCH >= LPK ? NCH / LPK : 1;  // chunks per lane
-  static constexpr int KPW = 32 / LPK;           // keys per warp per pass
-  static constexpr int UNR = 16 / KPW;           // passes per 16-key page
-  static_assert(HD % CPE == 0 && (NCH < LPK || NCH % LPK == 0), "head dim");
+  static constexpr int CPE = Unpack<T>::N;  // elements per chunk
+  static constexpr int NCH = HD / CPE;      // chunks per head row
+  static constexpr int LPK = NCH <= 1 ? 1 : NCH <= 2 ? 2 : NCH <= 4 ? 4 : NCH <= 8 ? 8 : NCH <= 16 ? 16 : 32;
+  static constexpr int KPW = 32 / LPK;      // keys per warp per pass
+  static_assert(HD % CPE == 0 && NCH <= 32, "head dim");
+};
+
+// Online-softmax state of one compute warp (one head) for the current item.
+template <typename T, int HD, bool MMA>
+struct Acc;
+
+// MMA path: lane 4i holds head dims 16t + i (acc[t][0]) and 16t + i + 8
+// (acc[t][2]); the other lanes' accumulators hold zero columns.
+template <typename T, int HD>
+struct Acc<T, HD, true> {
+  static constexpr int NT = HD / 16;
+  uint32_t qb[NT][2];
+  float acc[NT][4];
+  float m, l;
+
+  __device__ __forceinline__ void start(const uint8_t* qrow, int lane) {
+    const uint32_t* qs = reinterpret_cast<const uint32_t*>(qrow);
+#pragma unroll
+    for (int t = 0; t < NT; ++t) {
+      qb[t][0] = lane < 4 ? qs[t * 8 + lane] : 0u;
+      qb[t][1] = lane < 4 ? qs[t * 8 + 4 + lane] : 0u;
+      acc[t][0] = acc[t][1] = acc[t][2] = acc[t][3] = 0.f;
+    }
+    m = -INFINITY;
+    l = 0.f;
+  }
+
+  // sk / sv: shared addresses of this head's first K / V row in the stage.
+  __device__ __forceinline__ void page(uint32_t sk, uint32_t sv, uint32_t mask, int lane) {
+    using Gm = attn::Geo<T, HD>;
+    const float scale = 1.4426950408889634f / sqrtf((float)HD);  // log2(e) / sqrt(HD)
+    const bool real = (lane & 3) == 0;
+    const uint32_t koff = sk + ((lane & 7) + 8 * ((lane >> 3) & 1)) * Gm::RS + 16 * (lane >> 4);
+    const uint32_t voff = sv + ((lane & 7) + 8 * (lane >> 4)) * Gm::RS + 16 * ((lane >> 3) & 1);
+    float sc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int t = 0; t < NT; ++t) {
+      uint32_t a[4];
+      attn::ldsm_x4(koff + t * 32, a);
+      attn::mma_bf16(sc, a, qb[t][0], qb[t][1]);
+    }
+    // sc[0]: key lane/4, sc[2]: key lane/4 + 8 (column 0 on real lanes).
+    const int k0 = lane >> 2;
+    const float s0 = (real && ((mask >> k0) & 1u)) ? sc[0] * scale : -INFINITY;
+    const float s1 = (real && ((mask >> (k0 + 8)) & 1u)) ? sc[2] * scale : -INFINITY;
+    float mx = fmaxf(s0, s1);
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+    const float mn = fmaxf(m, __shfl_sync(0xffffffffu, mx, 0));
+    if (mn == -INFINITY) return;
+    const float corr = exp2f(m - mn);
+    const float p0 = exp2f(s0 - mn), p1 = exp2f(s1 - mn);
+    // p as the B operand: lane t < 4 needs keys 2t, 2t+1 (rows 0..7 of B)
+    // and 2t+8, 2t+9; key k sits on lane 4(k & 7), in p0 for k < 8.
+    const int t4 = lane & 3;
+    const float x0 = __shfl_sync(0xffffffffu, p0, 8 * t4);
+    const float x1 = __shfl_sync(0xffffffffu, p0, 8 * t4 + 4);
+    const float x2 = __shfl_sync(0xffffffffu, p1, 8 * t4);
+    const float x3 = __shfl_sync(0xffffffffu, p1, 8 * t4 + 4);
+    uint32_t bh0 = 0, bh1 = 0, bl0 = 0, bl1 = 0;
+    if (lane < 4) {
+      const float h0 = __bfloat162float(__float2bfloat16_rn(x0)), h1 = __bfloat162float(__float2bfloat16_rn(x1));
+      const float h2 = __bfloat162float(__float2bfloat16_rn(x2)), h3 = __bfloat162float(__float2bfloat16_rn(x3));
+      bh0 = attn::pack_bf16(h0, h1);
+      bh1 = attn::pack_bf16(h2, h3);
+      bl0 = attn::pack_bf16(x0 - h0, x1 - h1);
+      bl1 = attn::pack_bf16(x2 - h2, x3 - h3);
+    }
+    l = fmaf(l, corr, p0 + p1);
+#pragma unroll
+    for (int t = 0; t < NT; ++t) {
+      acc[t][0] *= corr;
+      acc[t][2] *= corr;
+      uint32_t a[4];
+      attn::ldsm_x4_t(voff + t * 32, a);
+      attn::mma_bf16(acc[t], a, bh0, bh1);
+      attn::mma_bf16(acc[t], a, bl0, bl1);
+    }
+    m = mn;
+  }
+
+  __device__ __forceinline__ void finish(int lane, bool write, bool single, T* out, float* po, float* pml) {
+    float lt = l;
+    lt += __shfl_xor_sync(0xffffffffu, lt, 4);
+    lt += __shfl_xor_sync(0xffffffffu, lt, 8);
+    lt += __shfl_xor_sync(0xffffffffu, lt, 16);
+    if (!write || (lane & 3) != 0) return;
+    const int i = lane >> 2;
+    if (single) {
+      const float inv = 1.f / lt;
+#pragma unroll
+      for (int t = 0; t < NT; ++t) {
+        out[16 * t + i] = from_f<T>(acc[t][0] * inv);
+        out[16 * t + i + 8] = from_f<T>(acc[t][2] * inv);
+      }
+    } else {
+#pragma unroll
+      for (int t = 0; t < NT; ++t) {
+        po[16 * t + i] = acc[t][0];
+        po[16 * t + i + 8] = acc[t][2];
+      }
+      if (lane == 0) {
+        pml[0] = m;  // log2 domain
+        pml[1] = lt;
+      }
+    }
+  }
+};
+
+// CUDA-core path (fp32 models and head rows too narrow for the MMA tiles).
+template <typename T, int HD>
+struct Acc<T, HD, false> {
+  using S = AttnShape<T, HD>;
+  static constexpr int CPE = S::CPE, NCH = S::NCH, LPK = S::LPK, KPW = S::KPW;
+  float q[CPE], acc[CPE];
+  float m, l;
+
+  __device__ __forceinline__ void start(const uint8_t* qrow, int lane) {
+    const int c = lane % LPK;
+    uint4 raw = make_uint4(0, 0, 0, 0);
+    if (c < NCH) raw = *reinterpret_cast<const uint4*>(qrow + c * 16);
+    Unpack<T>::run(raw, q);
+    const float scale = 1.4426950408889634f / sqrtf((float)HD);
+#pragma unroll
+    for (int e = 0; e < CPE; ++e) {
+      q[e] *= scale;
+      acc[e] = 0.f;
+    }
+    m = -INFINITY;
+    l = 0.f;
+  }
+
+  // sk / sv: this head's first K / V row in the stage.
+  __device__ __forceinline__ void page(const uint8_t* sk, const uint8_t* sv, uint32_t mask, int lane) {
+    using Gm = attn::Geo<T, HD>;
+    const int g = lane / LPK, c = lane % LPK;
+    const bool act = c < NCH;
+#pragma unroll 1
+    for (int kb = 0; kb < 16; kb += KPW) {
+      const int k = kb + g;
+      const bool valid = k < 16 && ((mask >> k) & 1u);
+      uint4 kr = make_uint4(0, 0, 0, 0), vr = make_uint4(0, 0, 0, 0);
+      if (valid && act) {
+        kr = *reinterpret_cast<const uint4*>(sk + k * Gm::RS + c * 16);
+        vr = *reinterpret_cast<const uint4*>(sv + k * Gm::RS + c * 16);
+      }
+      float kf[CPE];
+      Unpack<T>::run(kr, kf);
+      float a = 0.f;
+#pragma unroll
+      for (int e = 0; e < CPE; ++e) a = fmaf(q[e], kf[e], a);
+#pragma unroll
+      for (int o = LPK / 2; o > 0; o >>= 1) a += __shfl_xor_sync(0xffffffffu, a, o);
+      const float sc = valid ? a : -INFINITY;
+      const float mn = fmaxf(m, sc);
+      if (mn != -INFINITY) {
+        const float corr = exp2f(m - mn);
+        const float p = exp2f(sc - mn);
+        float vf[CPE];
+        Unpack<T>::run(vr, vf);
+        l = fmaf(l, corr, p);
+#pragma unroll
+        for (int e = 0; e < CPE; ++e) acc[e] = fmaf(acc[e], corr, p * vf[e]);
+        m = mn;
+      }
+    }
+  }
+
+  __device__ __forceinline__ void finish(int lane, bool write, bool single, T* out, float* po, float* pml) {
+    // Merge the KPW key groups of the warp (fixed butterfly order).
+#pragma unroll
+    for (int o = LPK; o < 32; o <<= 1) {
+      const float m2 = __shfl_xor_sync(0xffffffffu, m, o);
+      const float l2 = __shfl_xor_sync(0xffffffffu, l, o);
+      const float mn = fmaxf(m, m2);
+      const float c1 = (m == -INFINITY) ? 0.f : exp2f(m - mn);
+      const float c2 = (m2 == -INFINITY) ? 0.f : exp2f(m2 - mn);
+#pragma unroll
+      for (int e = 0; e < CPE; ++e) {
+        const float a2 = __shfl_xor_sync(0xffffffffu, acc[e], o);
+        acc[e] = acc[e] * c1 + a2 * c2;
+      }
+      l = l * c1 + l2 * c2;
+      m = mn;
+    }
+    const int g = lane / LPK, c = lane % LPK;
+    if (!write || g != 0 || c >= NCH) return;
+    if (single) {
+      const float inv = 1.f / l;
+#pragma unroll
+      for (int e = 0; e < CPE; ++e) out[c * CPE + e] = from_f<T>(acc[e] * inv);
+    } else {
+#pragma unroll
+      for (int e = 0; e < CPE; ++e) po[c * CPE + e] = acc[e];
+      if (c == 0) {
+        pml[0] = m;  // log2 domain
+        pml[1] = l;
+      }
+    }
+  }
 };
 
 template <typename T, int HD>
-__global__ void __launch_bounds__(128)
+__global__ void __launch_bounds__((attn::kWarps + 1) * 32)
     k_attn(const T* __restrict__ Q, int rows, const int* __restrict__ mslot, const int* __restrict__ mpos,
-           const int* __restrict__ mdepth, int depth_uniform, KvGeom kv, int slot_base, int clamp, int H,
-           int split, int max_splits, T* __restrict__ O, float* __restrict__ part_o,
-           float* __restrict__ part_ml, int* status) {
+           const int* __restrict__ mdepth, int depth_uniform, KvGeom kv, int slot_base, int clamp, int H, int split,
+           int max_splits, T* __restrict__ O, float* __restrict__ part_o, float* __restrict__ part_ml,
+           int* status) {
+  using Gm = attn::Geo<T, HD>;
+  constexpr bool MMA = sizeof(T) == 2 && HD % 16 == 0;
+  constexpr int G = attn::kWarps, NS = attn::kStages;
+  extern __shared__ __align__(128) uint8_t smem[];
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + (size_t)NS * Gm::STAGE);
+  uint64_t* empty = full + NS;
+  attn::StageMeta* meta = reinterpret_cast<attn::StageMeta*>(empty + NS);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int ngroups = (H + G - 1) / G;
+  const int per_sp = rows * ngroups;
+  const int n_items = max_splits * per_sp;
+  int* counter = status + kWorkCounter;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < NS; ++i) {
+      attn::mbar_init(&full[i], 33);  // 32 producer lanes' copies + lane 0's record
+      attn::mbar_init(&empty[i], G);
+    }
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  __syncthreads();
   pdl_wait();
   pdl_trigger();
-  using S = AttnShape<T, HD>;
-  constexpr int CPE = S::CPE, LPK = S::LPK, CPL = S::CPL, KPW = S::KPW, UNR = S::UNR, NCH = S::NCH;
-  constexpr int EPL = CPL * CPE;  // elements per lane
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int row = blockIdx.z;
-  const int h = blockIdx.y * 4 + warp;
-  if (row >= rows || h >= H) return;
-  const int pos = mpos[row];
-  const int L = pos + 1;
-  const int nsp = (L + split - 1) / split;
-  const int sp = blockIdx.x;
-  if (sp >= nsp) return;
-  const int k_lo = sp * split;
-  const int k_hi = min(L, k_lo + split);
-  const int r = depth_uniform > 0 ? depth_uniform : mdepth[row] + 1;
-  const int slot = mslot[row];
-  const int d = kv.d;
-  const int g = lane / LPK, c = lane % LPK;
-  const bool act = c < NCH;  // a one-chunk head row leaves the second lane idle
-  // Scores are kept in the log2 domain: s * log2(e) / sqrt(HD).
-  const float scale = 1.4426950408889634f / sqrtf((float)HD);
 
-  // Chunk cc of this lane covers elements (c + LPK*cc)*CPE .. +CPE of the head
-  // row, so for each cc the LPK lanes of a key read 16*LPK contiguous bytes.
-  float q[EPL];
-  {
-    const T* qp = Q + (size_t)row * d + h * HD;
-#pragma unroll
-    for (int cc = 0; cc < CPL; ++cc) {
-      const uint4 raw = act ? *reinterpret_cast<const uint4*>(qp + (c + LPK * cc) * CPE) : make_uint4(0, 0, 0, 0);
-      Unpack<T>::run(raw, q + cc * CPE);
-    }
-#pragma unroll
-    for (int e = 0; e < EPL; ++e) q[e] *= scale;
-  }
-
-  const T* pool = reinterpret_cast<const T*>(kv.pool);
-  const int* bt = kv.bt + slot * kv.max_blocks;
-  const size_t slot_stride = (size_t)2 * 16 * d;  // elements between slots of one block
-  float m = -INFINITY, l = 0.f;
-  float acc[EPL];
-#pragma unroll
-  for (int e = 0; e < EPL; ++e) acc[e] = 0.f;
-
-  // Keys go in blocks of KPW*UNR = 16, one KV page each (split starts are
-  // multiples of 16).  The page's physical block and exit depths are fetched
-  // one block ahead so the address chain overlaps the previous block's loads.
-  static_assert(KPW * UNR == 16, "one 16-key page per pass");
-  int blk_n = bt[k_lo >> 4];
-  uint4 e16_n = make_uint4(0, 0, 0, 0);
-  if (clamp && blk_n >= 0 && blk_n < kv.kv_blocks) e16_n = *reinterpret_cast<const uint4*>(kv.etab + blk_n * 16);
-  for (int j0 = k_lo; j0 < k_hi; j0 += 16) {
-    const int blk = blk_n;
-    const uint4 e16 = e16_n;
-    const bool blk_ok = blk >= 0 && blk < kv.kv_blocks;
-    uint4 kr[UNR][CPL], vr[UNR][CPL];
-    bool valid[UNR];
-#pragma unroll
-    for (int u = 0; u < UNR; ++u) {
-      const int off = u * KPW + g;
-      const int j = j0 + off;
-      valid[u] = j < k_hi;
-#pragma unroll
-      for (int cc = 0; cc < CPL; ++cc) kr[u][cc] = vr[u][cc] = make_uint4(0, 0, 0, 0);
-      if (valid[u]) {
-        int dr = 1;
-        if (clamp) {
-          const uint32_t w = off < 4 ? e16.x : off < 8 ? e16.y : off < 12 ? e16.z : e16.w;
-          dr = min(r, (int)((w >> (8 * (off & 3))) & 0xFFu));
+  if (warp == G) {
+    // ---------------- producer warp ----------------
+    const T* pool = reinterpret_cast<const T*>(kv.pool);
+    const size_t head_elems = (size_t)16 * HD;       // one head's page
+    const size_t kv_elems = (size_t)H * head_elems;  // K (or V) of one block-slot
+    auto fetch = [&]() -> int {  // next active item, or n_items when the queue is empty
+      int it = 0;
+      if (lane == 0) {
+        do {
+          it = atomicAdd(counter, 1);
+          if (it >= n_items) break;
+          const int sp = it / per_sp, row = (it - sp * per_sp) / ngroups;
+          if (sp * split <= __ldg(&mpos[row])) break;  // split sp starts at or before the row's last key
+        } while (true);
+      }
+      return __shfl_sync(0xffffffffu, it, 0);
+    };
+    int st = 0;
+    bool fail = false;
+    auto acquire = [&](int s) -> bool {  // stage s free for writing
+      if (st < NS) return true;
+      const bool ok = attn::mbar_wait(&empty[s], ((st / NS) - 1) & 1);
+      return __all_sync(0xffffffffu, ok) != 0;
+    };
+    int item = fetch();
+    while (true) {
+      const int s = st % NS;
+      if (item >= n_items) {  // end marker
+        if (!acquire(s)) {
+          fail = true;
+          break;
         }
-        const int sl = slot_base + dr - 1;
-        if (!blk_ok || dr < 1 || sl >= kv.nsl) {
-          valid[u] = false;
-          if (c == 0) atomicOr(status, kStatusBadDepth);
-        } else if (act) {
-          const T* kp = pool + ((size_t)blk * kv.nsl + sl) * slot_stride + (size_t)off * d + h * HD;
-          const T* vp = kp + (size_t)16 * d;
-#pragma unroll
-          for (int cc = 0; cc < CPL; ++cc) {
-            kr[u][cc] = ld_stream(kp + (c + LPK * cc) * CPE);
-            vr[u][cc] = ld_stream(vp + (c + LPK * cc) * CPE);
+        if (lane == 0) meta[s].flags = attn::kEnd;
+        __syncwarp();
+        attn::cp_arrive(&full[s]);
+        if (lane == 0) attn::mbar_arrive(&full[s]);
+        break;
+      }
+      const int sp = item / per_sp;
+      const int row = (item - sp * per_sp) / ngroups;
+      const int h0 = (item - sp * per_sp - row * ngroups) * G;
+      const int L = mpos[row] + 1;
+      const int nsp = (L + split - 1) / split;
+      const int k_lo = sp * split, k_hi = min(L, k_lo + split);
+      const int npg = (k_hi - k_lo + 15) >> 4;
+      const int r = depth_uniform > 0 ? depth_uniform : mdepth[row] + 1;
+      const int* bt = kv.bt + mslot[row] * kv.max_blocks;
+      const int next = fetch();  // overlaps this item's pages
+      for (int pg = 0; pg < npg; ++pg) {
+        const int s2 = st % NS;
+        // Block-slot index of this lane's key (lanes 0..15), -1 if not read.
+        const int key = k_lo + pg * 16 + (lane & 15);
+        int kidx = -1;
+        if (key < k_hi) {
+          const int blk = bt[key >> 4];
+          // clamp 0: the layer's single slot; 1: step min(r, e_j) from the
+          // exit-depth table; 2: step r for every key (no table read).
+          int dr = 1;
+          if (clamp == 1 && blk >= 0 && blk < kv.kv_blocks) dr = min(r, (int)kv.etab[(size_t)blk * 16 + (key & 15)]);
+          else if (clamp == 2) dr = r;
+          const int sl = slot_base + dr - 1;
+          if (blk < 0 || blk >= kv.kv_blocks || dr < 1 || sl >= kv.nsl) {
+            if (lane < 16) atomicOr(status, kStatusBadDepth);
+          } else {
+            kidx = blk * kv.nsl + sl;
           }
         }
+        const uint32_t mask = __ballot_sync(0xffffffffu, kidx >= 0) & 0xFFFFu;
+        if (!acquire(s2)) {
+          fail = true;
+          break;
+        }
+        uint8_t* stage = smem + (size_t)s2 * Gm::STAGE;
+        const uint32_t sdst = attn::su32(stage);
+        // Rows (kv, head hh, key k) of CR chunks; chunk c*32 + lane.
+#pragma unroll 4
+        for (int c = 0; c < Gm::NR * Gm::CR / 32; ++c) {
+          const int idx = c * 32 + lane;
+          const int rw = idx / Gm::CR, ch = idx - rw * Gm::CR;
+          const int k = rw & 15, hh = (rw >> 4) % G, kvh = rw / (16 * G);
+          const int ki = __shfl_sync(0xffffffffu, kidx, k);
+          const uint32_t dst = sdst + rw * Gm::RS + ch * 16;
+          if (ki >= 0 && h0 + hh < H) {
+            const T* src = pool + ((size_t)ki * 2 + kvh) * kv_elems + (size_t)(h0 + hh) * head_elems +
+                           (size_t)k * HD + ch * (16 / Gm::ES);
+            attn::cp16(dst, src);
+          } else if (kvh == 1) {  // V rows not read hold zeros: p = 0 must not meet a stale NaN
+            asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(dst), "r"(0) : "memory");
+          }
+        }
+        if (pg == 0) {  // the G heads' q rows
+          for (int idx = lane; idx < G * Gm::CR; idx += 32) {
+            const int hh = idx / Gm::CR, ch = idx - hh * Gm::CR;
+            if (h0 + hh < H)
+              attn::cp16(sdst + (Gm::NR + hh) * Gm::RS + ch * 16,
+                         Q + (size_t)row * kv.d + (size_t)(h0 + hh) * HD + ch * (16 / Gm::ES));
+          }
+        }
+        if (lane == 0) {
+          meta[s2].item = item;
+          meta[s2].flags = (pg == 0 ? attn::kFirst : 0) | (pg == npg - 1 ? attn::kLast : 0);
+          meta[s2].mask = (int)mask;
+          meta[s2].nsp = nsp;
+        }
+        __syncwarp();
+        attn::cp_arrive(&full[s2]);
+        if (lane == 0) attn::mbar_arrive(&full[s2]);
+        ++st;
+      }
+      if (fail) break;
+      item = next;
+    }
+    if (fail) {
+      if (lane == 0) atomicOr(status, kStatusTimeout);
+      // Copies already issued land before the CTA may exit.
+      asm volatile("cp.async.wait_all;" ::: "memory");
+    }
+    // The last CTA to finish with the queue resets it for the next launch.
+    if (lane == 0) {
+      __threadfence();
+      if (atomicAdd(counter + 1, 1) == (int)gridDim.x - 1) {
+        atomicExch(counter, 0);
+        atomicExch(counter + 1, 0);
       }
     }
-    if (j0 + 16 < k_hi) {
-      blk_n = bt[(j0 + 16) >> 4];
-      if (clamp && blk_n >= 0 && blk_n < kv.kv_blocks) e16_n = *reinterpret_cast<const uint4*>(kv.etab + blk_n * 16);
-    }
-    float s[UNR];
-#pragma unroll
-    for (int u = 0; u < UNR; ++u) {
-      float a = 0.f;
-#pragma unroll
-      for (int cc = 0; cc < CPL; ++cc) {
-        float kf[CPE];
-        Unpack<T>::run(kr[u][cc], kf);
-#pragma unroll
-        for (int e = 0; e < CPE; ++e) a = fmaf(q[cc * CPE + e], kf[e], a);
-      }
-#pragma unroll
-      for (int o = LPK / 2; o > 0; o >>= 1) a += __shfl_xor_sync(0xffffffffu, a, o);
-      s[u] = valid[u] ? a : -INFINITY;
-    }
-    // One rescale per block of UNR keys.
-    float mn = m;
-#pragma unroll
-    for (int u = 0; u < UNR; ++u) mn = fmaxf(mn, s[u]);
-    if (mn == -INFINITY) continue;  // no valid key in this block for this group
-    const float corr = exp2f(m - mn);
-    l *= corr;
-#pragma unroll
-    for (int e = 0; e < EPL; ++e) acc[e] *= corr;
-#pragma unroll
-    for (int u = 0; u < UNR; ++u) {
-      const float p = exp2f(s[u] - mn);  // 0 for invalid keys
-      l += p;
-#pragma unroll
-      for (int cc = 0; cc < CPL; ++cc) {
-        float vf[CPE];
-        Unpack<T>::run(vr[u][cc], vf);
-#pragma unroll
-        for (int e = 0; e < CPE; ++e) acc[cc * CPE + e] = fmaf(p, vf[e], acc[cc * CPE + e]);
-      }
-    }
-    m = mn;
+    asm volatile("cp.async.wait_all;" ::: "memory");
+    return;
   }
-  // Merge the KPW key groups of the warp (fixed butterfly order).
-#pragma unroll
-  for (int o = LPK; o < 32; o <<= 1) {
-    const float m2 = __shfl_xor_sync(0xffffffffu, m, o);
-    const float l2 = __shfl_xor_sync(0xffffffffu, l, o);
-    const float mn = fmaxf(m, m2);
-    const float c1 = (m == -INFINITY) ? 0.f : exp2f(m - mn);
-    const float c2 = (m2 == -INFINITY) ? 0.f : exp2f(m2 - mn);
-#pragma unroll
-    for (int e = 0; e < EPL; ++e) {
-      const float a2 = __shfl_xor_sync(0xffffffffu, acc[e], o);
-      acc[e] = acc[e] * c1 + a2 * c2;
+
+  // ---------------- consumer warps: warp w handles head h0 + w ----------------
+  Acc<T, HD, MMA> A;
+  for (int st = 0;; ++st) {
+    const int s = st % NS;
+    const bool ok = attn::mbar_wait(&full[s], (st / NS) & 1);
+    if (!__all_sync(0xffffffffu, ok)) {
+      if (lane == 0) atomicOr(status, kStatusTimeout);
+      return;
     }
-    l = l * c1 + l2 * c2;
-    m = mn;
+    const int flags = meta[s].flags;
+    if (flags & attn::kEnd) return;
+    const int item = meta[s].item;
+    const uint32_t mask = (uint32_t)meta[s].mask;
+    const int nsp = meta[s].nsp;
+    const uint8_t* stage = smem + (size_t)s * Gm::STAGE;
+    if (flags & attn::kFirst) A.start(stage + (Gm::NR + warp) * Gm::RS, lane);
+    const uint8_t* sk = stage + (size_t)warp * 16 * Gm::RS;
+    const uint8_t* sv = stage + (size_t)(G + warp) * 16 * Gm::RS;
+    if constexpr (MMA) A.page(attn::su32(sk), attn::su32(sv), mask, lane);
+    else A.page(sk, sv, mask, lane);
+    __syncwarp();
+    if (lane == 0) attn::mbar_arrive(&empty[s]);
+    if (flags & attn::kLast) {
+      const int sp = item / per_sp;
+      const int row = (item - sp * per_sp) / ngroups;
+      const int h = (item - sp * per_sp - row * ngroups) * G + warp;
+      const size_t pi = ((size_t)row * H + h) * max_splits + sp;
+      A.finish(lane, h < H, nsp == 1, O + (size_t)row * kv.d + (size_t)h * HD, part_o + pi * HD, part_ml + pi * 2);
+    }
   }
-  if (g != 0 || !act) return;
+}
+
+// ---------------------------------------------------------------------------
+// Uniform-slot variant (bf16, head_dim 32, 64, 96 or 128): every key of a row
+// is read from the same slot (slot_base + r - 1 for core layers, slot_base
+// otherwise).  The engine guarantees this by filling exit gaps when a token
+// leaves the loop (k_compact), so the depth-clamped read rule needs no
+// per-key slot here.  A page of the kWarps heads of one slot is then two
+// rectangular tiles of the pool (K and V: 16 keys x kWarps heads rows of
+// head_dim elements) that a producer thread moves with 2D TMA tensor copies,
+// head_dim split into 64- (or 32-) element slices under the 128-byte (or
+// 64-byte) swizzle, so the consumers' matrix loads of 8 keys hit 8 different
+// bank groups.  One CTA per (key split, head group, row); consumers as in the
+// MMA path above.
+// ---------------------------------------------------------------------------
+namespace attn {
+
+template <int HD>
+struct TmaGeo {
+  static constexpr int SWB = HD % 64 == 0 ? 128 : 64;  // swizzle span = bytes of one slice row
+  static constexpr int XW = SWB / 2;                    // elements per slice
+  static constexpr int NX = HD / XW;                    // slices per head row
+  static constexpr int ROWS = 16 * kWarps;              // tile rows: kWarps heads x 16 keys
+  static constexpr int SLICE = ROWS * SWB;              // bytes of one slice tile
+  static constexpr int KREG = NX * SLICE;               // K (or V) of one page
+  static constexpr int QB = kWarps * HD * 2;            // q rows of the item
+  static constexpr int STAGE = (2 * KREG + QB + 1023) / 1024 * 1024;
+  static constexpr int NS = 3;
+  static constexpr size_t SMEM = 1024 + (size_t)NS * STAGE + NS * (2 * 8 + sizeof(StageMeta));
+  static_assert(HD % 32 == 0, "head dim");
+};
+
+__device__ __forceinline__ void tma_2d(uint32_t dst, const CUtensorMap* map, uint64_t* bar, int x, int y,
+                                       uint64_t pol) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(dst),
+      "l"(map), "r"(su32(bar)), "r"(x), "r"(y), "l"(pol)
+      : "memory");
+}
+__device__ __forceinline__ void bulk_1d(uint32_t dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+               "l"(src), "r"(bytes), "r"(su32(bar))
+               : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(su32(bar)), "r"(bytes) : "memory");
+}
+
+// Shared address of 16-byte chunk c (within a slice row) of tile row `row`.
+template <int SWB>
+__device__ __forceinline__ uint32_t swz(uint32_t slice, int row, int c) {
+  const int pc = SWB == 128 ? (c ^ (row & 7)) : (c ^ ((row >> 1) & 3));
+  return slice + (uint32_t)row * SWB + (uint32_t)pc * 16;
+}
+
+}  // namespace attn
+
+template <int HD>
+__global__ void __launch_bounds__((attn::kWarps + 1) * 32)
+    k_attn_tma(const __grid_constant__ CUtensorMap tm, const __nv_bfloat16* __restrict__ Q, int rows,
+               const int* __restrict__ mslot, const int* __restrict__ mpos, const int* __restrict__ mdepth,
+               int depth_uniform, KvGeom kv, int slot_base, int clamp, int H, int split, int max_splits,
+               __nv_bfloat16* __restrict__ O, float* __restrict__ part_o, float* __restrict__ part_ml,
+               int* status) {
+  using Gm = attn::TmaGeo<HD>;
+  constexpr int G = attn::kWarps, NS = Gm::NS, NT = HD / 16;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + (size_t)NS * Gm::STAGE);
+  uint64_t* empty = full + NS;
+  attn::StageMeta* meta = reinterpret_cast<attn::StageMeta*>(empty + NS);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int row = blockIdx.z, h0 = blockIdx.y * G, sp = blockIdx.x;
+
+  if (threadIdx.x == 0) {
+    asm volatile("prefetch.tensormap [%0];" ::"l"(&tm) : "memory");
+    for (int i = 0; i < NS; ++i) {
+      attn::mbar_init(&full[i], 1);
+      attn::mbar_init(&empty[i], G);
+    }
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  __syncthreads();
+  pdl_wait();
+  pdl_trigger();
+  if (row >= rows) return;
+  const int L = mpos[row] + 1;
+  const int nsp = (L + split - 1) / split;
+  if (sp >= nsp) return;
+  const int k_lo = sp * split, k_hi = min(L, k_lo + split);
+  const int npg = (k_hi - k_lo + 15) >> 4;
+  const int Gc = min(G, H - h0);
+
+  if (warp == G) {
+    // ---------------- producer warp ----------------
+    const int r = depth_uniform > 0 ? depth_uniform : mdepth[row] + 1;
+    const int sl = slot_base + (clamp ? r - 1 : 0);
+    const int* bt = kv.bt + mslot[row] * kv.max_blocks;
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+    const bool sl_ok = sl >= 0 && sl < kv.nsl;
+    if (!sl_ok && lane == 0) atomicOr(status, kStatusBadDepth);
+    int blk_l = -1;
+    bool fail = false;
+    for (int pg = 0; pg < npg; ++pg) {
+      const int s = pg % NS;
+      if ((pg & 31) == 0) {
+        const int p = (k_lo >> 4) + pg + lane;
+        blk_l = (pg + lane < npg) ? bt[p] : -1;
+      }
+      const int blk = __shfl_sync(0xffffffffu, blk_l, pg & 31);
+      if (pg >= NS) {
+        const bool ok = attn::mbar_wait(&empty[s], ((pg / NS) - 1) & 1);
+        if (!__all_sync(0xffffffffu, ok)) {
+          fail = true;
+          break;
+        }
+      }
+      if (lane == 0) {
+        const bool ok = sl_ok && blk >= 0 && blk < kv.kv_blocks;
+        if (!ok && sl_ok) atomicOr(status, kStatusBadBlock);
+        const int key0 = k_lo + pg * 16;
+        const int nk = min(16, k_hi - key0);
+        meta[s].flags = (pg == 0 ? attn::kFirst : 0) | (pg == npg - 1 ? attn::kLast : 0);
+        meta[s].mask = ok ? (int)((1u << nk) - 1u) : 0;
+        const uint32_t qb = (uint32_t)Gc * HD * 2;
+        const uint32_t st = attn::su32(smem + (size_t)s * Gm::STAGE);
+        attn::mbar_arrive_tx(&full[s], (ok ? 2u * Gm::KREG : 0u) + (pg == 0 ? qb : 0u));
+        if (ok) {
+          // Tile row 0 = head h0, key 0 of this page at this slot.
+          const int y0 = (int)((((long long)blk * kv.nsl + sl) * 2) * H * 16 + (long long)h0 * 16);
+          for (int kvh = 0; kvh < 2; ++kvh)
+            for (int j = 0; j < Gm::NX; ++j)
+              attn::tma_2d(st + kvh * Gm::KREG + j * Gm::SLICE, &tm, &full[s], j * Gm::XW, y0 + kvh * H * 16, pol);
+        }
+        if (pg == 0) attn::bulk_1d(st + 2 * Gm::KREG, Q + (size_t)row * kv.d + (size_t)h0 * HD, qb, &full[s]);
+      }
+      __syncwarp();
+    }
+    if (fail && lane == 0) atomicOr(status, kStatusTimeout);
+    return;
+  }
+
+  // ---------------- consumer warps: warp w handles head h0 + w ----------------
+  const int h = h0 + warp;
+  const float scale = 1.4426950408889634f / sqrtf((float)HD);
+  const bool real = (lane & 3) == 0;
+  uint32_t qb[NT][2];
+  float acc[NT][4];
+  float m = -INFINITY, l = 0.f;
+  const uint32_t base = attn::su32(smem);
+  // Tile rows of this lane's ldmatrix addresses (K: keys in matrix order 0-7,
+  // 8-15 for lanes 0-15 and again for 16-31; V transposed: 0-7, 0-7, 8-15, 8-15).
+  const int krow = warp * 16 + (lane & 7) + 8 * ((lane >> 3) & 1);
+  const int vrow = warp * 16 + (lane & 7) + 8 * (lane >> 4);
+  for (int pg = 0; pg < npg; ++pg) {
+    const int s = pg % NS;
+    const bool ok = attn::mbar_wait(&full[s], (pg / NS) & 1);
+    if (!__all_sync(0xffffffffu, ok)) {
+      if (lane == 0) atomicOr(status, kStatusTimeout);
+      return;
+    }
+    const uint32_t mask = (uint32_t)meta[s].mask;
+    const int flags = meta[s].flags;
+    const uint32_t st = base + (uint32_t)s * Gm::STAGE;
+    if (flags & attn::kFirst) {
+      const uint32_t* qs = reinterpret_cast<const uint32_t*>(smem + (size_t)s * Gm::STAGE + 2 * Gm::KREG) +
+                           warp * (HD / 2);
+#pragma unroll
+      for (int t = 0; t < NT; ++t) {
+        qb[t][0] = (lane < 4 && warp < Gc) ? qs[t * 8 + lane] : 0u;
+        qb[t][1] = (lane < 4 && warp < Gc) ? qs[t * 8 + 4 + lane] : 0u;
+        acc[t][0] = acc[t][1] = acc[t][2] = acc[t][3] = 0.f;
+      }
+    }
+    if (mask != 0xFFFFu) {
+      // Keys past the row's end (or a bad page): zero their V rows so that
+      // p = 0 never meets stale or NaN values in the MMA.
+      uint8_t* vt = smem + (size_t)s * Gm::STAGE + Gm::KREG;
+      for (int u = lane; u < 16 * Gm::NX * (Gm::SWB / 16); u += 32) {
+        const int k = u / (Gm::NX * (Gm::SWB / 16));
+        if ((mask >> k) & 1u) continue;
+        const int rem = u - k * (Gm::NX * (Gm::SWB / 16));
+        const int j = rem / (Gm::SWB / 16), c = rem % (Gm::SWB / 16);
+        *reinterpret_cast<uint4*>(vt + (size_t)j * Gm::SLICE + (size_t)(warp * 16 + k) * Gm::SWB + c * 16) =
+            make_uint4(0, 0, 0, 0);
+      }
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      __syncwarp();
+    }
+    // Scores s^T = K_page . q.
+    float sc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int t = 0; t < NT; ++t) {
+      const int j = (16 * t) / Gm::XW, c = ((16 * t) % Gm::XW) / 8 + (lane >> 4);
+      uint32_t a[4];
+      attn::ldsm_x4(attn::swz<Gm::SWB>(st + j * Gm::SLICE, krow, c), a);
+      attn::mma_bf16(sc, a, qb[t][0], qb[t][1]);
+    }
+    const int k0 = lane >> 2;
+    const float s0 = (real && ((mask >> k0) & 1u)) ? sc[0] * scale : -INFINITY;
+    const float s1 = (real && ((mask >> (k0 + 8)) & 1u)) ? sc[2] * scale : -INFINITY;
+    float mx = fmaxf(s0, s1);
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+    const float mn = fmaxf(m, __shfl_sync(0xffffffffu, mx, 0));
+    if (mn != -INFINITY) {
+      const float corr = exp2f(m - mn);
+      const float p0 = exp2f(s0 - mn), p1 = exp2f(s1 - mn);
+      const int t4 = lane & 3;
+      const float x0 = __shfl_sync(0xffffffffu, p0, 8 * t4);
+      const float x1 = __shfl_sync(0xffffffffu, p0, 8 * t4 + 4);
+      const float x2 = __shfl_sync(0xffffffffu, p1, 8 * t4);
+      const float x3 = __shfl_sync(0xffffffffu, p1, 8 * t4 + 4);
+      uint32_t bh0 = 0, bh1 = 0, bl0 = 0, bl1 = 0;
+      if (lane < 4) {
+        const float e0 = __bfloat162float(__float2bfloat16_rn(x0)), e1 = __bfloat162float(__float2bfloat16_rn(x1));
+        const float e2 = __bfloat162float(__float2bfloat16_rn(x2)), e3 = __bfloat162float(__float2bfloat16_rn(x3));
+        bh0 = attn::pack_bf16(e0, e1);
+        bh1 = attn::pack_bf16(e2, e3);
+        bl0 = attn::pack_bf16(x0 - e0, x1 - e1);
+        bl1 = attn::pack_bf16(x2 - e2, x3 - e3);
+      }
+      l = fmaf(l, corr, p0 + p1);
+#pragma unroll
+      for (int t = 0; t < NT; ++t) {
+        acc[t][0] *= corr;
+        acc[t][2] *= corr;
+        const int j = (16 * t) / Gm::XW, c = ((16 * t) % Gm::XW) / 8 + ((lane >> 3) & 1);
+        uint32_t a[4];
+        attn::ldsm_x4_t(attn::swz<Gm::SWB>(st + Gm::KREG + j * Gm::SLICE, vrow, c), a);
+        attn::mma_bf16(acc[t], a, bh0, bh1);
+        attn::mma_bf16(acc[t], a, bl0, bl1);
+      }
+      m = mn;
+    }
+    __syncwarp();
+    if (lane == 0) attn::mbar_arrive(&empty[s]);
+  }
+  float lt = l;
+  lt += __shfl_xor_sync(0xffffffffu, lt, 4);
+  lt += __shfl_xor_sync(0xffffffffu, lt, 8);
+  lt += __shfl_xor_sync(0xffffffffu, lt, 16);
+  if (h >= H || !real) return;
+  const int i = lane >> 2;
   if (nsp == 1) {
-    const float inv = 1.f / l;
-    T* out = O + (size_t)row * d + h * HD;
+    const float inv = 1.f / lt;
+    __nv_bfloat16* out = O + (size_t)row * kv.d + (size_t)h * HD;
 #pragma unroll
-    for (int cc = 0; cc < CPL; ++cc)
-#pragma unroll
-      for (int e = 0; e < CPE; ++e) out[(c + LPK * cc) * CPE + e] = from_f<T>(acc[cc * CPE + e] * inv);
+    for (int t = 0; t < NT; ++t) {
+      out[16 * t + i] = __float2bfloat16_rn(acc[t][0] * inv);
+      out[16 * t + i + 8] = __float2bfloat16_rn(acc[t][2] * inv);
+    }
   } else {
     const size_t pi = ((size_t)row * H + h) * max_splits + sp;
     float* po = part_o + pi * HD;
 #pragma unroll
-    for (int cc = 0; cc < CPL; ++cc)
-#pragma unroll
-      for (int e = 0; e < CPE; ++e) po[(c + LPK * cc) * CPE + e] = acc[cc * CPE + e];
-    if (c == 0) {
+    for (int t = 0; t < NT; ++t) {
+      po[16 * t + i] = acc[t][0];
+      po[16 * t + i + 8] = acc[t][2];
+    }
+    if (lane == 0) {
       part_ml[pi * 2] = m;  // log2 domain
-      part_ml[pi * 2 + 1] = l;
+      part_ml[pi * 2 + 1] = lt;
     }
   }
 }
@@ -270,38 +848,84 @@ __global__ void k_attn_combine(int rows, const int* __restrict__ mpos, int H, in
   }
 }
 
+// Uniform-slot TMA path; false when the shape or pool does not fit it.
+template <int HD>
+static bool attn_tma(cudaStream_t s, const __nv_bfloat16* Q, int rows, const int* mslot, const int* mpos,
+                     const int* mdepth, int depth_uniform, KvGeom kv, int slot_base, int clamp, int H, int split,
+                     int max_splits, __nv_bfloat16* O, float* part_o, float* part_ml, int* status) {
+  using Gm = attn::TmaGeo<HD>;
+  const uint64_t pool_rows = (uint64_t)kv.kv_blocks * kv.nsl * 2 * H * 16;
+  if (pool_rows + 16 * attn::kWarps >= (1ull << 31)) return false;  // tile row coordinates are int32
+  const CUtensorMap* tm = tmap_bf16_2d(kv.pool, HD, pool_rows, (uint64_t)HD * 2, Gm::XW, Gm::ROWS, Gm::SWB);
+  if (!tm) return false;
+  static bool set = false;
+  if (!set) {
+    if (cudaFuncSetAttribute(k_attn_tma<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Gm::SMEM) !=
+        cudaSuccess)
+      return false;
+    set = true;
+  }
+  dim3 grid(max_splits, (H + attn::kWarps - 1) / attn::kWarps, rows);
+  count_launch();
+  launch_pdl(k_attn_tma<HD>, grid, dim3((attn::kWarps + 1) * 32), Gm::SMEM, s, *tm, Q, rows, mslot, mpos, mdepth,
+             depth_uniform, kv, slot_base, clamp, H, split, max_splits, O, part_o, part_ml, status);
+  return true;
+}
+
 template <typename T, int HD>
 static void attn_hd(cudaStream_t s, const T* Q, int rows, const int* mslot, const int* mpos, const int* mdepth,
                     int depth_uniform, KvGeom kv, int slot_base, int clamp, int H, int split, int max_splits,
-                    T* O, float* part_o, float* part_ml, int* status) {
-  dim3 grid(max_splits, (H + 3) / 4, rows);
-  count_launch();
-  launch_pdl(k_attn<T, HD>, dim3(grid), dim3(128), 0, s, Q, rows, mslot, mpos, mdepth, depth_uniform, kv, slot_base, clamp, H,
-                                     split, max_splits, O, part_o, part_ml, status);
+                    T* O, float* part_o, float* part_ml, int* status, bool uniform) {
+  bool done = false;
+  if constexpr (sizeof(T) == 2 && HD % 32 == 0) {
+    if (uniform)
+      done = attn_tma<HD>(s, Q, rows, mslot, mpos, mdepth, depth_uniform, kv, slot_base, clamp, H, split, max_splits,
+                          O, part_o, part_ml, status);
+  }
+  if (!done) {
+    using Gm = attn::Geo<T, HD>;
+    static int ctas = 0;
+    if (!ctas) {
+      cudaFuncSetAttribute(k_attn<T, HD>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Gm::SMEM);
+      int dev = 0, sms = 0, per_sm = 0;
+      cudaGetDevice(&dev);
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_attn<T, HD>, (attn::kWarps + 1) * 32, Gm::SMEM);
+      ctas = sms * (per_sm > 0 ? per_sm : 1);
+    }
+    const long long items = (long long)max_splits * rows * ((H + attn::kWarps - 1) / attn::kWarps);
+    const int grid = (int)(items < ctas ? items : ctas);
+    const int mode = (uniform && clamp) ? 2 : clamp;  // uniform reads never touch the exit-depth table
+    count_launch();
+    launch_pdl(k_attn<T, HD>, dim3(grid), dim3((attn::kWarps + 1) * 32), Gm::SMEM, s, Q, rows, mslot, mpos, mdepth,
+               depth_uniform, kv, slot_base, mode, H, split, max_splits, O, part_o, part_ml, status);
+  }
   if (max_splits > 1)
-    count_launch(), launch_pdl(k_attn_combine<T>, dim3(rows * H), dim3(128), 0, s, rows, mpos, H, HD, kv.d, split, max_splits, part_o, part_ml, O);
+    count_launch(), launch_pdl(k_attn_combine<T>, dim3(rows * H), dim3(128), 0, s, rows, mpos, H, HD, kv.d, split,
+                               max_splits, part_o, part_ml, O);
 }
 
 template <typename T>
 void launch_attention(cudaStream_t s, const T* Q, int rows, const int* mslot, const int* mpos,
                       const int* mdepth, int depth_uniform, KvGeom kv, int slot_base, int clamp, int H, int hd,
-                      int split, int max_splits, T* O, float* part_o, float* part_ml, int* status) {
+                      int split, int max_splits, T* O, float* part_o, float* part_ml, int* status,
+                      bool uniform) {
   if (rows <= 0) return;
   switch (hd) {
-    case 8: attn_hd<T, 8>(s, Q, rows, mslot, mpos, mdepth, depth_uniform, kv, slot_base, clamp, H, split, max_splits, O, part_o, part_ml, status); break;
-    case 16: attn_hd<T, 16>(s, Q, rows, mslot, mpos, mdepth, depth_uniform, kv, slot_base, clamp, H, split, max_splits, O, part_o, part_ml, status); break;
-    case 32: attn_hd<T, 32>(s, Q, rows, mslot, mpos, mdepth, depth_uniform, kv, slot_base, clamp, H, split, max_splits, O, part_o, part_ml, status); break;
-    case 64: attn_hd<T, 64>(s, Q, rows, mslot, mpos, mdepth, depth_uniform, kv, slot_base, clamp, H, split, max_splits, O, part_o, part_ml, status); break;
-    case 96: attn_hd<T, 96>(s, Q, rows, mslot, mpos, mdepth, depth_uniform, kv, slot_base, clamp, H, split, max_splits, O, part_o, part_ml, status); break;
-    case 128: attn_hd<T, 128>(s, Q, rows, mslot, mpos, mdepth, depth_uniform, kv, slot_base, clamp, H, split, max_splits, O, part_o, part_ml, status); break;
+    case 8: attn_hd<T, 8>(s, Q, rows, mslot, mpos, mdepth, depth_uniform, kv, slot_base, clamp, H, split, max_splits, O, part_o, part_ml, status, uniform); break;
+    case 16: attn_hd<T, 16>(s, Q, rows, mslot, mpos, mdepth, depth_uniform, kv, slot_base, clamp, H, split, max_splits, O, part_o, part_ml, status, uniform); break;
+    case 32: attn_hd<T, 32>(s, Q, rows, mslot, mpos, mdepth, depth_uniform, kv, slot_base, clamp, H, split, max_splits, O, part_o, part_ml, status, uniform); break;
+    case 64: attn_hd<T, 64>(s, Q, rows, mslot, mpos, mdepth, depth_uniform, kv, slot_base, clamp, H, split, max_splits, O, part_o, part_ml, status, uniform); break;
+    case 96: attn_hd<T, 96>(s, Q, rows, mslot, mpos, mdepth, depth_uniform, kv, slot_base, clamp, H, split, max_splits, O, part_o, part_ml, status, uniform); break;
+    case 128: attn_hd<T, 128>(s, Q, rows, mslot, mpos, mdepth, depth_uniform, kv, slot_base, clamp, H, split, max_splits, O, part_o, part_ml, status, uniform); break;
     default: break;  // rejected at init
   }
 }
 
 template void launch_attention<float>(cudaStream_t, const float*, int, const int*, const int*, const int*, int,
-                                      KvGeom, int, int, int, int, int, int, float*, float*, float*, int*);
+                                      KvGeom, int, int, int, int, int, int, float*, float*, float*, int*, bool);
 template void launch_attention<__nv_bfloat16>(cudaStream_t, const __nv_bfloat16*, int, const int*, const int*,
                                               const int*, int, KvGeom, int, int, int, int, int, int,
-                                              __nv_bfloat16*, float*, float*, int*);
+                                              __nv_bfloat16*, float*, float*, int*, bool);
 
 }  // namespace cdb

@@ -75,9 +75,9 @@ int cdb_attention_noalloc(const void* q, int rows, const int32_t* slot, const in
   float* part_o = reinterpret_cast<float*>(w + 256);
   float* part_ml = reinterpret_cast<float*>(w + 256 + po_bytes);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  // The array keeps the previous call's contents; only the status word must
+  // The array keeps the previous call's contents; only the status area must
   // start at zero (every partial read is written earlier in this call).
-  if (cudaMemsetAsync(status, 0, sizeof(int), s) != cudaSuccess) return CDB_ERR_CUDA;
+  if (cudaMemsetAsync(status, 0, cdb::kStatusBytes, s) != cudaSuccess) return CDB_ERR_CUDA;
   cdb::KvGeom g;
   g.pool = const_cast<void*>(kv_pool);
   g.bt = block_table;
@@ -89,11 +89,11 @@ int cdb_attention_noalloc(const void* q, int rows, const int32_t* slot, const in
   if (dtype == CDB_BF16)
     cdb::launch_attention<__nv_bfloat16>(s, static_cast<const __nv_bfloat16*>(q), rows, slot, pos, depth, 0, g,
                                          slot_base, 1, n_heads, head_dim, split, (int)splits,
-                                         static_cast<__nv_bfloat16*>(out), part_o, part_ml, status);
+                                         static_cast<__nv_bfloat16*>(out), part_o, part_ml, status, false);
   else
     cdb::launch_attention<float>(s, static_cast<const float*>(q), rows, slot, pos, depth, 0, g, slot_base, 1,
                                  n_heads, head_dim, split, (int)splits, static_cast<float*>(out), part_o, part_ml,
-                                 status);
+                                 status, false);
   if (cudaGetLastError() != cudaSuccess || cudaStreamSynchronize(s) != cudaSuccess) return CDB_ERR_CUDA;
   int st = 0;
   if (cudaMemcpy(&st, status, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return CDB_ERR_CUDA;

@@ -79,7 +79,7 @@ static bool plan_layout(const cdb_model_desc* m, const cdb_sched_cfg* c, Layout*
   }
   L->pend_new = take(W * 4);
   L->ring = take(kRing * W);
-  L->status = take(16);
+  L->status = take(kStatusBytes);
   L->Xp = take(M * d * 4);
   L->Ep = take(m->has_adapter ? M * d * 4 : 0);
   L->rslot = take(M * 4);
@@ -343,8 +343,10 @@ class GpuExecutor : public Executor {
     const int split = decode ? L.split : (1 << 30);
     const int msp = decode ? L.max_splits : 1;
     const int ha = prof_begin(x, decode ? 0 : 2);
+    // Exit gaps are filled at compaction, so every key of a row is read from
+    // the row's own slot.
     launch_attention<T>(s, Q, rows, mslot, mpos, mdepth, depth_uniform, kv, slot_base, clamp, H, hd, split, msp,
-                        O, at<float>(x, L.part_o), at<float>(x, L.part_ml), st);
+                        O, at<float>(x, L.part_o), at<float>(x, L.part_ml), st, true);
     // Each key row (K and V, d elements each) is read once; q in, o out.
     prof_end(x, ha, sumL * 2.0 * d * es + 2.0 * rows * d * es, 4.0 * d * sumL);
     gemm<T>(kEpiResid, O, d, lw.wo, nullptr, d, d, rows, X, nullptr, d);
@@ -490,7 +492,8 @@ class GpuExecutor : public Executor {
                    at<int>(x, L.pend_new), ring, x->c.trace_gate ? at<float>(x, L.gtrace) : nullptr);
     launch_compact(x->cs, X, mx, at<int>(x, L.pend_new), B, d, x->m.r_max, p.qc_off, at<float>(x, L.rows[1]),
                    meta_at(x, L.meta[1]), at<float>(x, L.rows[3]), meta_at(x, L.meta[3]), geom(),
-                   at<int8_t>(x, L.out_depth), x->c.max_new_cap, at<int>(x, L.status));
+                   at<int8_t>(x, L.out_depth), x->c.max_new_cap, x->m.n_core, x->m.n_prelude, x->m.head_dim,
+                   (int)sizeof(T), at<int>(x, L.status));
     CK(cudaGetLastError());
     // Lookahead flags to the host on the prep stream.
     CK(cudaEventRecord(x->ev_core[ri], x->cs));
@@ -950,14 +953,15 @@ size_t cdb_test_attention_scratch_bytes(int rows, int n_heads, int head_dim, int
   return 256 + (po + 255) / 256 * 256 + (size_t)rows * n_heads * ms * 2 * 4;
 }
 
-int cdb_test_attention(const void* q, int rows, const int32_t* slot, const int32_t* pos, const int32_t* depth,
-                       const void* kv_pool, const int32_t* block_table, int max_blocks, const uint8_t* exit_table,
-                       int kv_blocks, int n_kv_slots, int slot_base, int n_heads, int head_dim, int dtype, int split,
-                       int max_ctx, void* out, void* scratch, size_t scratch_bytes, void* stream) {
-  if (!q || rows < 1 || !slot || !pos || !depth || !kv_pool || !block_table || max_blocks < 1 || !exit_table ||
-      kv_blocks < 1 || n_kv_slots < 1 || slot_base < 0 || n_heads < 1 || !valid_hd(head_dim) ||
-      (dtype != CDB_FP32 && dtype != CDB_BF16) || split < 16 || split % 16 != 0 || max_ctx < 1 || !out ||
-      !scratch || scratch_bytes < cdb_test_attention_scratch_bytes(rows, n_heads, head_dim, split, max_ctx))
+static int test_attention(const void* q, int rows, const int32_t* slot, const int32_t* pos, const int32_t* depth,
+                          const void* kv_pool, const int32_t* block_table, int max_blocks, const uint8_t* exit_table,
+                          int kv_blocks, int n_kv_slots, int slot_base, int n_heads, int head_dim, int dtype, int split,
+                          int max_ctx, void* out, void* scratch, size_t scratch_bytes, void* stream, bool uniform) {
+  if (!q || rows < 1 || !slot || !pos || !depth || !kv_pool || !block_table || max_blocks < 1 ||
+      (!exit_table && !uniform) || kv_blocks < 1 || n_kv_slots < 1 || slot_base < 0 || n_heads < 1 ||
+      !valid_hd(head_dim) || (dtype != CDB_FP32 && dtype != CDB_BF16) || split < 16 || split % 16 != 0 ||
+      max_ctx < 1 || !out || !scratch ||
+      scratch_bytes < cdb_test_attention_scratch_bytes(rows, n_heads, head_dim, split, max_ctx))
     return CDB_ERR_ARG;
   cudaStream_t s = (cudaStream_t)stream;
   char* w = (char*)scratch;
@@ -965,7 +969,7 @@ int cdb_test_attention(const void* q, int rows, const int32_t* slot, const int32
   const size_t ms = (size_t)(max_ctx + split - 1) / split;
   float* part_o = (float*)(w + 256);
   float* part_ml = (float*)(w + 256 + ((size_t)rows * n_heads * ms * head_dim * 4 + 255) / 256 * 256);
-  if (cudaMemsetAsync(status, 0, 4, s) != cudaSuccess) return CDB_ERR_CUDA;
+  if (cudaMemsetAsync(status, 0, kStatusBytes, s) != cudaSuccess) return CDB_ERR_CUDA;
   KvGeom g;
   g.pool = const_cast<void*>(kv_pool);
   g.bt = block_table;
@@ -976,14 +980,32 @@ int cdb_test_attention(const void* q, int rows, const int32_t* slot, const int32
   g.d = n_heads * head_dim;
   if (dtype == CDB_BF16)
     launch_attention<__nv_bfloat16>(s, (const __nv_bfloat16*)q, rows, slot, pos, depth, 0, g, slot_base, 1, n_heads,
-                                    head_dim, split, (int)ms, (__nv_bfloat16*)out, part_o, part_ml, status);
+                                    head_dim, split, (int)ms, (__nv_bfloat16*)out, part_o, part_ml, status, uniform);
   else
     launch_attention<float>(s, (const float*)q, rows, slot, pos, depth, 0, g, slot_base, 1, n_heads, head_dim,
-                            split, (int)ms, (float*)out, part_o, part_ml, status);
+                            split, (int)ms, (float*)out, part_o, part_ml, status, uniform);
   if (cudaGetLastError() != cudaSuccess || cudaStreamSynchronize(s) != cudaSuccess) return CDB_ERR_CUDA;
   int st = 0;
   if (cudaMemcpy(&st, status, 4, cudaMemcpyDeviceToHost) != cudaSuccess) return CDB_ERR_CUDA;
   return st ? CDB_ERR_DEVICE_BOUNDS : CDB_OK;
+}
+
+int cdb_test_attention(const void* q, int rows, const int32_t* slot, const int32_t* pos, const int32_t* depth,
+                       const void* kv_pool, const int32_t* block_table, int max_blocks, const uint8_t* exit_table,
+                       int kv_blocks, int n_kv_slots, int slot_base, int n_heads, int head_dim, int dtype, int split,
+                       int max_ctx, void* out, void* scratch, size_t scratch_bytes, void* stream) {
+  return test_attention(q, rows, slot, pos, depth, kv_pool, block_table, max_blocks, exit_table, kv_blocks,
+                        n_kv_slots, slot_base, n_heads, head_dim, dtype, split, max_ctx, out, scratch, scratch_bytes,
+                        stream, false);
+}
+
+int cdb_test_attention_uniform(const void* q, int rows, const int32_t* slot, const int32_t* pos, const int32_t* depth,
+                               const void* kv_pool, const int32_t* block_table, int max_blocks, int kv_blocks,
+                               int n_kv_slots, int slot_base, int n_heads, int head_dim, int dtype, int split,
+                               int max_ctx, void* out, void* scratch, size_t scratch_bytes, void* stream) {
+  return test_attention(q, rows, slot, pos, depth, kv_pool, block_table, max_blocks, nullptr, kv_blocks, n_kv_slots,
+                        slot_base, n_heads, head_dim, dtype, split, max_ctx, out, scratch, scratch_bytes, stream,
+                        true);
 }
 
 }  // extern "C"

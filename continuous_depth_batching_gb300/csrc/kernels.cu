@@ -167,9 +167,11 @@ __global__ void k_rope_kv(const float* __restrict__ QKV, int rows, const int* __
     if (threadIdx.x == 0) atomicOr(status, kStatusBadBlock);
     return;
   }
+  // Pool layout [block][slot][K|V][head][16][hd]: head h of this position
+  // starts at (pos & 15) * hd inside its head's page.
   T* pool = reinterpret_cast<T*>(kv.pool);
-  T* kdst = pool + (((size_t)blk * kv.nsl + sl) * 2 + 0) * 16 * d + (size_t)(pos & 15) * d;
-  T* vdst = pool + (((size_t)blk * kv.nsl + sl) * 2 + 1) * 16 * d + (size_t)(pos & 15) * d;
+  T* kdst = pool + (((size_t)blk * kv.nsl + sl) * 2 + 0) * 16 * d + (size_t)(pos & 15) * hd;
+  T* vdst = kdst + (size_t)16 * d;
   const float* q = QKV + (size_t)i * 3 * d;
   const float* k = q + d;
   const float* v = q + 2 * d;
@@ -177,13 +179,14 @@ __global__ void k_rope_kv(const float* __restrict__ QKV, int rows, const int* __
   for (int u = threadIdx.x; u < H * half; u += blockDim.x) {
     const int h = u / half, j = u % half;
     const int a = h * hd + j, b = a + half;
+    const size_t ka = (size_t)h * 16 * hd + j, kb = ka + half;
     const float c = cs[j].x, s = cs[j].y;
     Q[(size_t)i * d + a] = from_f<T>(q[a] * c - q[b] * s);
     Q[(size_t)i * d + b] = from_f<T>(q[b] * c + q[a] * s);
-    kdst[a] = from_f<T>(k[a] * c - k[b] * s);
-    kdst[b] = from_f<T>(k[b] * c + k[a] * s);
-    vdst[a] = from_f<T>(v[a]);
-    vdst[b] = from_f<T>(v[b]);
+    kdst[ka] = from_f<T>(k[a] * c - k[b] * s);
+    kdst[kb] = from_f<T>(k[b] * c + k[a] * s);
+    vdst[ka] = from_f<T>(v[a]);
+    vdst[kb] = from_f<T>(v[b]);
   }
 }
 
@@ -250,16 +253,46 @@ __global__ void k_gate(const float* __restrict__ X, const T* __restrict__ w, flo
 // r_max.  Exits keep slot order and go to the coda rows after qc_off; the
 // rest keep slot order at the front of the continuing rows.  One block per
 // row; each block ranks its row with a block-wide count over the earlier rows.
+// blockIdx.y == 0 compacts row blockIdx.x; blockIdx.y = 1 + l fills the exit
+// gaps of core layer l: a row leaving after loop step r < r_max copies its
+// slot-r K and V into slots r+1 .. r_max of that layer.  A later reader at
+// step r' then finds in slot r' exactly the entry of slot min(r', r), the one
+// the depth-clamped read rule selects, so every key of a page is read from
+// one slot.
 __global__ void k_compact(const float* __restrict__ X, RowMeta m, const int* __restrict__ pend_new,
                           int B, int d, int r_max, int qc_off, float* __restrict__ Xc, RowMeta mc,
                           float* __restrict__ Cb, RowMeta mb, KvGeom kv, int8_t* __restrict__ out_depth,
-                          int cap, int* status) {
+                          int cap, int core_slot0, int hd, int es, int* status) {
   pdl_wait();
   pdl_trigger();
   __shared__ float sh[33];
   const int i = blockIdx.x;
   if (i >= B) return;
   auto exits = [&](int j) { return (m.depth[j] >= 1 && m.pend[j]) || (m.depth[j] + 1 >= r_max); };
+  if (blockIdx.y > 0) {
+    const int r = m.depth[i] + 1;
+    if (!exits(i) || r >= r_max) return;
+    const int pos = m.pos[i];
+    const int blk = kv.bt[m.slot[i] * kv.max_blocks + pos / 16];
+    if (blk < 0 || blk >= kv.kv_blocks) return;  // flagged by the compaction block
+    const int base = core_slot0 + (blockIdx.y - 1) * r_max;
+    // Per (block, slot): [K|V][head][16][hd]; this position's head rows are
+    // hd elements at (pos & 15) * hd inside each head's page.
+    const size_t row_b = (size_t)hd * es, page_b = 16 * row_b, kv_b = (size_t)16 * d * es;
+    const int H = d / hd, cpr = (int)(row_b / 16);  // 16-byte chunks per head row
+    const uint8_t* pool = reinterpret_cast<const uint8_t*>(kv.pool);
+    const uint8_t* src = pool + ((size_t)blk * kv.nsl + base + r - 1) * 2 * kv_b + (size_t)(pos & 15) * row_b;
+    for (int rr = r + 1; rr <= r_max; ++rr) {
+      uint8_t* dst = const_cast<uint8_t*>(pool) + ((size_t)blk * kv.nsl + base + rr - 1) * 2 * kv_b +
+                     (size_t)(pos & 15) * row_b;
+      for (int u = threadIdx.x; u < 2 * H * cpr; u += blockDim.x) {
+        const int kvh = u / (H * cpr), h = (u / cpr) % H, c = u % cpr;
+        const size_t o = kvh * kv_b + h * page_b + (size_t)c * 16;
+        *reinterpret_cast<uint4*>(dst + o) = *reinterpret_cast<const uint4*>(src + o);
+      }
+    }
+    return;
+  }
   float before = 0.f;
   for (int j = threadIdx.x; j < i; j += blockDim.x) before += exits(j) ? 1.f : 0.f;
   const int n_exit_before = (int)(block_sum(before, sh) + 0.5f);
@@ -446,10 +479,10 @@ void launch_gate(cudaStream_t s, const float* X, const T* w, float bias, float t
 }
 void launch_compact(cudaStream_t s, const float* X, RowMeta m, const int* pend_new, int B, int d, int r_max,
                     int qc_off, float* Xc, RowMeta mc, float* Cb, RowMeta mb, KvGeom kv, int8_t* out_depth,
-                    int cap, int* status) {
+                    int cap, int n_core, int core_slot0, int hd, int es, int* status) {
   if (B > 0)
-    count_launch(), launch_pdl(k_compact, dim3(B), dim3(256), 0, s, X, m, pend_new, B, d, r_max, qc_off, Xc, mc, Cb, mb, kv, out_depth, cap,
-                                status);
+    count_launch(), launch_pdl(k_compact, dim3(B, 1 + n_core), dim3(256), 0, s, X, m, pend_new, B, d, r_max, qc_off,
+                               Xc, mc, Cb, mb, kv, out_depth, cap, core_slot0, hd, es, status);
 }
 void launch_gather_core(cudaStream_t s, const float* Xc, RowMeta mc, int B_cont, const float* Pb, RowMeta mp,
                         int n_ref, float* X, RowMeta mx, int d) {

@@ -43,6 +43,11 @@ enum : int {
   kStatusNaN = 16,
   kStatusTimeout = 32,  // a bounded wait inside a kernel expired
 };
+// The status area is kStatusBytes of zeroed device memory: word 0 holds the
+// bits above; words kWorkCounter and kWorkCounter + 1 are the work queue of
+// the persistent attention kernel, which leaves them at zero after each launch.
+constexpr int kStatusBytes = 256;
+constexpr int kWorkCounter = 32;
 
 struct KvGeom {
   void* pool;            // T elements
@@ -79,9 +84,12 @@ void launch_gate(cudaStream_t s, const float* X, const T* w, float bias, float t
                  int rows, int d, RowMeta meta, int mode, int r_min, int r_max,
                  const int8_t* fexit, int max_new_cap, int* pend_new, uint8_t* ring,
                  float* gtrace);
+// Compaction of the core batch after the exit gate, plus the exit-gap fill of
+// the n_core core layers (KV slots core_slot0 + l * r_max + r - 1).
 void launch_compact(cudaStream_t s, const float* X, RowMeta m, const int* pend_new, int B,
                     int d, int r_max, int qc_off, float* Xc, RowMeta mc, float* Cb,
-                    RowMeta mb, KvGeom kv, int8_t* out_depth, int max_new_cap, int* status);
+                    RowMeta mb, KvGeom kv, int8_t* out_depth, int max_new_cap, int n_core,
+                    int core_slot0, int hd, int es, int* status);
 void launch_gather_core(cudaStream_t s, const float* Xc, RowMeta mc, int B_cont, const float* Pb,
                         RowMeta mp, int n_ref, float* X, RowMeta mx, int d);
 void launch_gather_rows(cudaStream_t s, const float* src, const int* idx, const int* rslot,
@@ -93,11 +101,15 @@ void launch_rope_table(cudaStream_t s, float2* tab, int max_ctx, int hd, float t
 void launch_copy_rows(cudaStream_t s, const float* src, float* dst, int rows, int d);
 
 // ---- attention (attention.cu) ----
+// Decode (and prefill) attention.  uniform: every key of a row is read from
+// one slot (slot_base + r - 1 with clamp, slot_base without), which holds
+// whenever exit gaps are filled (k_compact); otherwise key j is read from
+// step min(r, e_j) through the exit-depth table.
 template <typename T>
 void launch_attention(cudaStream_t s, const T* Q, int rows, const int* mslot, const int* mpos,
                       const int* mdepth, int depth_uniform, KvGeom kv, int slot_base,
                       int clamp, int H, int hd, int split, int max_splits, T* O,
-                      float* part_o, float* part_ml, int* status);
+                      float* part_o, float* part_ml, int* status, bool uniform);
 
 // ---- GEMM (gemm_simt.cu) ----
 enum GemmEpi { kEpiStore = 0, kEpiResid = 1, kEpiSwiglu = 2 };

@@ -37,7 +37,8 @@ size_t cdb_test_gemm_ws_bytes(int N, int K, int rows, int tiling, int epi);
  *   q        [rows][n_heads*head_dim], dtype elements (0 fp32, 1 bf16)
  *   slot, pos, depth  int32 [rows]: sequence slot, own position (keys
  *            0..pos are read), loop steps completed (this step is depth+1)
- *   kv_pool  [kv_blocks][n_kv_slots][2][16][n_heads*head_dim] (K then V)
+ *   kv_pool  [kv_blocks][n_kv_slots][2][n_heads][16][head_dim]: per block and
+ *            slot, K then V, each head's 16 keys contiguous
  *   block_table int32 [*][max_blocks]; exit_table uint8 [kv_blocks][16]
  *   slot_base: cache slot of loop step 1 of this core layer
  *   split:   keys per split-KV partial (fixed, so results do not depend on
@@ -54,6 +55,20 @@ int cdb_test_attention(const void *q, int rows, const int32_t *slot, const int32
                        int slot_base, int n_heads, int head_dim, int dtype, int split, int max_ctx,
                        void *out, void *scratch, size_t scratch_bytes, void *stream);
 size_t cdb_test_attention_scratch_bytes(int rows, int n_heads, int head_dim, int split, int max_ctx);
+
+/* The attention the engine runs: the same computation as cdb_test_attention
+ * when every key of row i is read from one slot, slot_base + depth[i] (loop
+ * step depth[i] + 1).  The engine keeps that true by filling exit gaps when a
+ * token leaves the loop (its last computed K and V are copied into the slots
+ * of the deeper steps it skipped), which makes the slot of loop step r hold
+ * the entry of step min(r, e_j) for every cached position j.  Same arguments
+ * as cdb_test_attention without exit_table; the same pool layout; keys past
+ * a row's position are never used even when the pool holds NaN there. */
+int cdb_test_attention_uniform(const void *q, int rows, const int32_t *slot, const int32_t *pos,
+                               const int32_t *depth, const void *kv_pool, const int32_t *block_table,
+                               int max_blocks, int kv_blocks, int n_kv_slots, int slot_base, int n_heads,
+                               int head_dim, int dtype, int split, int max_ctx, void *out, void *scratch,
+                               size_t scratch_bytes, void *stream);
 
 /* The same decode attention for callers that must not allocate device memory
  * (for example a plugin whose host program's memory manager owns all device

@@ -24,6 +24,8 @@ def L():
     lib = binding.lib()
     lib.cdb_test_attention.argtypes = ([C.c_void_p, C.c_int] + [C.c_void_p] * 5 + [C.c_int, C.c_void_p] +
                                        [C.c_int] * 8 + [C.c_void_p, C.c_void_p, C.c_size_t, C.c_void_p])
+    lib.cdb_test_attention_uniform.argtypes = ([C.c_void_p, C.c_int] + [C.c_void_p] * 5 + [C.c_int] * 9 +
+                                               [C.c_void_p, C.c_void_p, C.c_size_t, C.c_void_p])
     lib.cdb_test_attention_scratch_bytes.restype = C.c_size_t
     lib.cdb_test_attention_scratch_bytes.argtypes = [C.c_int] * 5
     return lib
@@ -37,7 +39,7 @@ def make_case(dtype, H, hd, rows=6, r_max=4, n_core=2, layer=1, max_ctx=700, see
     max_blocks = (max_ctx + 15) // 16
     kv_blocks = rows * max_blocks + 7
     tdt = torch.bfloat16 if dtype == 1 else torch.float32
-    pool = torch.randn(kv_blocks, nsl, 2, 16, d, dtype=torch.float64)
+    pool = torch.randn(kv_blocks, nsl, 2, H, 16, hd, dtype=torch.float64)
     perm = rng.permutation(kv_blocks)[: rows * max_blocks].reshape(rows, max_blocks)
     bt = torch.from_numpy(perm.astype(np.int32))
     etab = torch.from_numpy(rng.integers(1, r_max + 1, (kv_blocks, 16)).astype(np.uint8))
@@ -53,7 +55,7 @@ def make_case(dtype, H, hd, rows=6, r_max=4, n_core=2, layer=1, max_ctx=700, see
     for b in range(kv_blocks):
         for o in range(16):
             e = int(etab[b, o])
-            pool[b, base + e:base + r_max, :, o, :] = float("nan")
+            pool[b, base + e:base + r_max, :, :, o, :] = float("nan")
     q = torch.randn(rows, d, dtype=torch.float64)
     return dict(pool=pool.to(tdt), bt=bt, etab=etab, pos=pos, depth=depth, slot=slot, q=q.to(tdt), H=H, hd=hd,
                 nsl=nsl, base=base, max_blocks=max_blocks, kv_blocks=kv_blocks, max_ctx=max_ctx, r_max=r_max,
@@ -74,12 +76,12 @@ def reference(cs):
         off = j % 16
         e = cs["etab"][blk, off].long()
         sl = cs["base"] + torch.clamp(e, max=r) - 1
-        K = pool[blk, sl, 0, off]
-        V = pool[blk, sl, 1, off]
+        K = pool[blk, sl, 0, :, off]  # [P, H, hd]
+        V = pool[blk, sl, 1, :, off]
         for h in range(H):
-            s = K[:, h * hd:(h + 1) * hd] @ q[i, h * hd:(h + 1) * hd] / np.sqrt(hd)
+            s = K[:, h] @ q[i, h * hd:(h + 1) * hd] / np.sqrt(hd)
             p = torch.softmax(s, 0)
-            out[i, h * hd:(h + 1) * hd] = p @ V[:, h * hd:(h + 1) * hd]
+            out[i, h * hd:(h + 1) * hd] = p @ V[:, h]
     return out
 
 
@@ -101,7 +103,8 @@ def run(L, cs, split, rows=None):
     return out
 
 
-@pytest.mark.parametrize("dtype,H,hd", [(0, 4, 64), (1, 16, 128), (1, 5, 96), (0, 2, 8)])
+@pytest.mark.parametrize("dtype,H,hd", [(0, 4, 64), (1, 16, 128), (1, 5, 96), (0, 2, 8), (1, 3, 64), (1, 6, 32),
+                                        (1, 2, 16), (1, 3, 8)])
 @pytest.mark.parametrize("split", [16, 256])
 def test_matches_reference(L, dtype, H, hd, split):
     cs = make_case(dtype, H, hd)
@@ -123,3 +126,78 @@ def test_row_bits_independent_of_batch(L):
     full = run(L, cs, 256)
     part = run(L, cs, 256, rows=3)
     assert (full[:3] == part).all().item()
+
+
+def make_uniform_case(dtype, H, hd, rows=6, seed=0, max_ctx=700):
+    """No exit gaps (every e_j = r_max), so the read rule is slot r for every
+    key; positions past each row's own one hold NaN in every slot."""
+    cs = make_case(dtype, H, hd, rows=rows, max_ctx=max_ctx, seed=seed)
+    pool = cs["pool"].double()
+    cs["etab"][:] = cs["r_max"]
+    rng = np.random.default_rng(seed + 100)
+    pool = torch_randn_like(pool, rng)
+    for i in range(rows):
+        p = int(cs["pos"][i])
+        b = int(cs["bt"][int(cs["slot"][i])][p // 16])
+        if p % 16 != 15:
+            pool[b, :, :, :, p % 16 + 1:, :] = float("nan")
+    cs["pool"] = pool.to(cs["pool"].dtype)
+    return cs
+
+
+def torch_randn_like(t, rng):
+    import torch
+    return torch.from_numpy(rng.standard_normal(tuple(t.shape))).to(t.dtype)
+
+
+def run_uniform(L, cs, split):
+    import torch
+    n = len(cs["pos"])
+    dev = {k: cs[k].cuda() for k in ("pool", "bt", "q")}
+    slot = torch.from_numpy(cs["slot"]).cuda()
+    pos = torch.from_numpy(cs["pos"]).cuda()
+    depth = torch.from_numpy(cs["depth"]).cuda()
+    out = torch.zeros(n, cs["H"] * cs["hd"], dtype=cs["q"].dtype, device="cuda")
+    nb = L.cdb_test_attention_scratch_bytes(n, cs["H"], cs["hd"], split, cs["max_ctx"])
+    scratch = torch.empty(nb, dtype=torch.uint8, device="cuda")
+    rc = L.cdb_test_attention_uniform(dev["q"].data_ptr(), n, slot.data_ptr(), pos.data_ptr(), depth.data_ptr(),
+                                      dev["pool"].data_ptr(), dev["bt"].data_ptr(), cs["max_blocks"],
+                                      cs["kv_blocks"], cs["nsl"], cs["base"], cs["H"], cs["hd"], cs["dtype"],
+                                      split, cs["max_ctx"], out.data_ptr(), scratch.data_ptr(), nb, None)
+    assert rc == 0, rc
+    return out
+
+
+@pytest.mark.parametrize("dtype,H,hd", [(1, 16, 128), (1, 5, 96), (1, 3, 64), (1, 6, 32), (1, 2, 16), (0, 4, 64)])
+@pytest.mark.parametrize("split", [16, 128, 256])
+def test_uniform_matches_reference(L, dtype, H, hd, split):
+    cs = make_uniform_case(dtype, H, hd, seed=5)
+    out = run_uniform(L, cs, split).double().cpu()
+    ref = reference(cs)
+    assert torch_finite(out)
+    tol = 2e-5 if dtype == 0 else 1e-2
+    err = (out - ref).abs()
+    assert (err <= tol * (1 + ref.abs())).all().item(), err.max().item()
+
+
+def test_uniform_equals_clamped_read_after_gap_fill(L):
+    """Filling each position's exit gaps with its deepest entry (what the
+    engine does when a token leaves the loop) makes the uniform read agree
+    with the depth-clamped reference."""
+    import torch
+    cs = make_case(1, 16, 128, rows=5, max_ctx=400, seed=9)
+    ref_clamped = run(L, cs, 128)
+    pool = cs["pool"].clone()
+    base, r_max = cs["base"], cs["r_max"]
+    for b in range(cs["kv_blocks"]):
+        for o in range(16):
+            e = int(cs["etab"][b, o])
+            for rr in range(e + 1, r_max + 1):
+                pool[b, base + rr - 1, :, :, o, :] = pool[b, base + e - 1, :, :, o, :]
+    cs2 = dict(cs, pool=pool)
+    out = run_uniform(L, cs2, 128)
+    ref = reference(cs)
+    err_u = (out.double().cpu() - ref).abs().max().item()
+    err_c = (ref_clamped.double().cpu() - ref).abs().max().item()
+    assert torch_finite(out)
+    assert err_u <= 1e-2 * (1 + ref.abs().max().item()), (err_u, err_c)

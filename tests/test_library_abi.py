@@ -29,7 +29,7 @@ def L():
 
 def declared_functions():
     names = set()
-    for h in ("cdb.h", "cdb_sim.h"):
+    for h in sorted(f for f in os.listdir(os.path.join(ROOT, "include")) if f.endswith(".h")):
         src = open(os.path.join(ROOT, "include", h)).read()
         src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
         for m in re.finditer(r"^\s*(?:const\s+)?[\w]+\s*\*?\s*(cdb_\w+)\s*\(", src, flags=re.M):
