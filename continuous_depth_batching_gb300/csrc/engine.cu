@@ -37,7 +37,8 @@ struct Layout {
   size_t pend_new, ring, status;
   size_t Xp, Ep, rslot, rpos, rtok, done_idx, Cp, Cp_meta;
   size_t lslot, lt, lpos;
-  size_t A, QKV, Q, O, Mid, logits, part_o, part_ml;
+  size_t A, QKV, Q, O, Mid, logits, part_o, part_ml, gpart;
+  size_t gpart_floats;
   // dims
   int es, nsl, max_blocks, max_splits, split, R, S, cap;
 };
@@ -99,6 +100,9 @@ static bool plan_layout(const cdb_model_desc* m, const cdb_sched_cfg* c, Layout*
   L->logits = take(W * V * 4);
   L->part_o = take(W * H * L->max_splits * hd * 4);
   L->part_ml = take(W * H * L->max_splits * 2 * 4);
+  // Split-K partials of one decode GEMM ([split][row][ldp], ldp <= max(3d, 2f)).
+  L->gpart_floats = (size_t)kGemmMaxSplits * W * std::max(3 * d, 2 * f);
+  L->gpart = take(L->gpart_floats * 4);
   L->total = o;
   return true;
 }
@@ -303,21 +307,53 @@ class GpuExecutor : public Executor {
     return CDB_OK;
   }
 
+  // Returns the number of split-K partials left in the gpart workspace for the
+  // consumer to fold (0: the epilogue ran in place).  parts: the caller folds.
   template <typename T>
-  void gemm(int epi, const T* A, int lda, const void* W, const void* W2, int N, int K, int rows, float* Cf, T* Ct,
-            int ldc) {
+  int gemm(int epi, const T* A, int lda, const void* W, const void* W2, int N, int K, int rows, float* Cf, T* Ct,
+           int ldc, bool parts) {
     cdb_ctx* x = x_;
     const double es = sizeof(T), nw = W2 ? 2.0 : 1.0;
     const int h = prof_begin(x, 1);
-    bool done = false;
+    int ns = -1;
     if (sizeof(T) == 2)
-      done = launch_gemm_tc(x->cs, epi, (const __nv_bfloat16*)A, lda, x->L.R, (const __nv_bfloat16*)W,
-                            (const __nv_bfloat16*)W2, N, K, rows, Cf, (__nv_bfloat16*)Ct, ldc, decode_tiles_,
-                            at<int>(x, x->L.status));
-    if (!done) launch_gemm<T>(x->cs, epi, A, lda, (const T*)W, (const T*)W2, N, K, rows, Cf, Ct, ldc);
+      ns = launch_gemm_tc(x->cs, epi, (const __nv_bfloat16*)A, lda, x->L.R, (const __nv_bfloat16*)W,
+                          (const __nv_bfloat16*)W2, N, K, rows, Cf, (__nv_bfloat16*)Ct, ldc, decode_tiles_,
+                          parts ? at<float>(x, x->L.gpart) : nullptr, x->L.gpart_floats, at<int>(x, x->L.status));
+    if (ns < 0) {
+      launch_gemm<T>(x->cs, epi, A, lda, (const T*)W, (const T*)W2, N, K, rows, Cf, Ct, ldc);
+      ns = 0;
+    }
     const double out_b = epi == kEpiSwiglu ? es : (epi == kEpiResid ? 8.0 : 4.0);
     prof_end(x, h, nw * N * (double)K * es + (double)rows * K * es + (double)rows * N * out_b,
              2.0 * nw * rows * (double)N * K);
+    return ns;
+  }
+
+  // Pending split-K partials of a residual (mode 1) or store (mode 2) GEMM
+  // into X, folded by the next RMSNorm of X or by flush().
+  struct Pending {
+    float* X = nullptr;
+    int rows = 0, ns = 0, mode = 0;
+  };
+  Pending pend_;
+
+  template <typename T>
+  void norm(float* X, const void* g, T* A, int rows) {
+    cdb_ctx* x = x_;
+    if (pend_.ns && (pend_.X != X || pend_.rows != rows)) flush<T>();
+    launch_rmsnorm<T>(x->cs, X, (const T*)g, A, rows, x->m.d_model, x->m.rms_eps, x->m.d_model,
+                      at<float>(x, x->L.gpart), pend_.ns, pend_.mode);
+    pend_ = Pending();
+  }
+
+  template <typename T>
+  void flush() {
+    if (!pend_.ns) return;
+    cdb_ctx* x = x_;
+    launch_fold(x->cs, at<float>(x, x->L.gpart), pend_.ns, pend_.rows, x->m.d_model, pend_.X, x->m.d_model,
+                pend_.mode);
+    pend_ = Pending();
   }
 
   template <typename T>
@@ -329,6 +365,7 @@ class GpuExecutor : public Executor {
     cudaStream_t s = x->cs;
     T* A = at<T>(x, L.A);
     float* QKV = at<float>(x, L.QKV);
+    float* GP = at<float>(x, L.gpart);
     T* Q = at<T>(x, L.Q);
     T* O = at<T>(x, L.O);
     T* Mid = at<T>(x, L.Mid);
@@ -336,9 +373,9 @@ class GpuExecutor : public Executor {
     KvGeom kv = geom();
     const double es = sizeof(T);
     decode_tiles_ = decode;
-    launch_rmsnorm<T>(s, X, (const T*)lw.attn_norm, A, rows, d, x->m.rms_eps, d);
-    gemm<T>(kEpiStore, A, d, lw.wqkv, nullptr, 3 * d, d, rows, QKV, nullptr, 3 * d);
-    launch_rope_kv<T>(s, QKV, rows, mslot, mpos, mdepth, depth_uniform, slot_base, clamp, Q, kv, H, hd,
+    norm<T>(X, lw.attn_norm, A, rows);
+    int ns = gemm<T>(kEpiStore, A, d, lw.wqkv, nullptr, 3 * d, d, rows, QKV, nullptr, 3 * d, true);
+    launch_rope_kv<T>(s, ns ? GP : QKV, ns, rows, mslot, mpos, mdepth, depth_uniform, slot_base, clamp, Q, kv, H, hd,
                       at<float2>(x, L.rope), st);
     const int split = decode ? L.split : (1 << 30);
     const int msp = decode ? L.max_splits : 1;
@@ -349,10 +386,13 @@ class GpuExecutor : public Executor {
                         O, at<float>(x, L.part_o), at<float>(x, L.part_ml), st, true);
     // Each key row (K and V, d elements each) is read once; q in, o out.
     prof_end(x, ha, sumL * 2.0 * d * es + 2.0 * rows * d * es, 4.0 * d * sumL);
-    gemm<T>(kEpiResid, O, d, lw.wo, nullptr, d, d, rows, X, nullptr, d);
-    launch_rmsnorm<T>(s, X, (const T*)lw.mlp_norm, A, rows, d, x->m.rms_eps, d);
-    gemm<T>(kEpiSwiglu, A, d, lw.wg, lw.wu, f, d, rows, nullptr, Mid, f);
-    gemm<T>(kEpiResid, Mid, f, lw.wd, nullptr, d, f, rows, X, nullptr, d);
+    ns = gemm<T>(kEpiResid, O, d, lw.wo, nullptr, d, d, rows, X, nullptr, d, true);
+    if (ns) pend_ = Pending{X, rows, ns, 1};
+    norm<T>(X, lw.mlp_norm, A, rows);
+    ns = gemm<T>(kEpiSwiglu, A, d, lw.wg, lw.wu, f, d, rows, nullptr, Mid, f, true);
+    if (ns) launch_swiglu_combine<T>(s, GP, ns, rows, f, Mid);
+    ns = gemm<T>(kEpiResid, Mid, f, lw.wd, nullptr, d, f, rows, X, nullptr, d, true);
+    if (ns) pend_ = Pending{X, rows, ns, 1};
     return CDB_OK;
   }
 
@@ -361,9 +401,11 @@ class GpuExecutor : public Executor {
     cdb_ctx* x = x_;
     const int d = x->m.d_model;
     T* A = at<T>(x, x->L.A);
+    flush<T>();
     decode_tiles_ = e_per_slot != 0;
     launch_concat<T>(x->cs, E, e_per_slot, mslot, X, A, rows, d);
-    gemm<T>(kEpiStore, A, 2 * d, x->adapter, nullptr, d, 2 * d, rows, X, nullptr, d);
+    const int ns = gemm<T>(kEpiStore, A, 2 * d, x->adapter, nullptr, d, 2 * d, rows, X, nullptr, d, true);
+    if (ns) pend_ = Pending{X, rows, ns, 2};
     return CDB_OK;
   }
 
@@ -376,8 +418,10 @@ class GpuExecutor : public Executor {
     T* A = at<T>(x, L.A);
     float* lg = at<float>(x, L.logits);
     decode_tiles_ = true;
-    launch_rmsnorm<T>(x->cs, Hrows, (const T*)x->final_norm, A, n, d, x->m.rms_eps, d);
-    gemm<T>(kEpiStore, A, d, x->lm_head, nullptr, V, d, n, lg, nullptr, V);
+    flush<T>();
+    launch_rmsnorm<T>(x->cs, const_cast<float*>(Hrows), (const T*)x->final_norm, A, n, d, x->m.rms_eps, d, nullptr, 0,
+                      0);
+    gemm<T>(kEpiStore, A, d, x->lm_head, nullptr, V, d, n, lg, nullptr, V, false);
     const bool tr = x->c.trace_tokens > 0;
     launch_argmax(x->cs, lg, n, V, m, at<int>(x, L.ftok), cap, at<int>(x, L.out_tok), tr ? at<float>(x, L.ltrace) : nullptr,
                   x->c.trace_tokens, Hrows, tr ? at<float>(x, L.htrace) : nullptr, d, at<int>(x, L.status));
@@ -411,6 +455,7 @@ class GpuExecutor : public Executor {
     double sumL = 0;
     for (int i = 0; i < n; ++i) sumL += b[i] + 1;
     for (int i = 0; i < x->m.n_prelude; ++i) block<T>(x->pre[i], Xp, n, rslot, rpos, nullptr, 1, i, 0, false, sumL);
+    flush<T>();
     float* Ep = at<float>(x, L.Ep);
     if (x->m.has_adapter) {
       launch_copy_rows(x->cs, Xp, Ep, n, d);
@@ -424,6 +469,7 @@ class GpuExecutor : public Executor {
     const int cbase = x->m.n_prelude + x->m.n_core * x->m.r_max;
     for (int j = 0; j < x->m.n_coda; ++j)
       block<T>(x->coda[j], Xp, n, rslot, rpos, nullptr, 1, cbase + j, 0, false, sumL);
+    flush<T>();
     const int nd = (int)p.done_rows.size();
     if (nd > 0) {
       if ((rc = upload(x, at<int>(x, L.done_idx), p.done_rows.data(), nd * 4)) < 0) return rc;
@@ -462,6 +508,7 @@ class GpuExecutor : public Executor {
     double sumL = 0;
     for (int i = 0; i < n; ++i) sumL += c[i] + 1;
     for (int i = 0; i < x->m.n_prelude; ++i) block<T>(x->pre[i], Tp, n, tm.slot, tm.pos, nullptr, 1, i, 0, true, sumL);
+    flush<T>();
     launch_prelude_finish(x->cs, Tp, tm, n, at<float>(x, L.rows[2]), meta_at(x, L.meta[2]), p.dst_off,
                           x->m.has_adapter ? at<float>(x, L.estore) : nullptr, d, x->m.has_adapter);
     CK(cudaGetLastError());
@@ -485,6 +532,7 @@ class GpuExecutor : public Executor {
     for (const Tok& t : *p.rows) sumL += t.pos + 1;
     for (int l = 0; l < x->m.n_core; ++l)
       block<T>(x->core[l], X, B, mx.slot, mx.pos, mx.depth, 0, x->m.n_prelude + l * x->m.r_max, 1, true, sumL);
+    flush<T>();
     const int ri = (int)(p.step % kRing);
     uint8_t* ring = at<uint8_t>(x, L.ring) + (size_t)ri * x->c.W;
     launch_gate<T>(x->cs, X, (const T*)x->gate_w, x->m.gate_bias, x->m.gate_threshold, x->m.rms_eps, B, d, mx,
@@ -532,6 +580,7 @@ class GpuExecutor : public Executor {
       for (const Tok& t : rows) sumL += t.pos + 1;
       for (int j = 0; j < x->m.n_coda; ++j)
         block<T>(x->coda[j], Tc, n, mb.slot, mb.pos, nullptr, 1, cbase + j, 0, true, sumL);
+      flush<T>();
       Hrows = Tc;
     }
     head<T>(Hrows, n, mb);
@@ -923,7 +972,12 @@ int cdb_trace_read(cdb_ctx* x, cdb_trace_row* rows, int cap, int* n_out) {
 
 extern "C" {
 
-size_t cdb_test_gemm_ws_bytes(int, int, int, int, int) { return 256; }
+size_t cdb_test_gemm_ws_bytes(int N, int K, int rows, int tiling, int epi) {
+  if (N < 1 || K < 1 || rows < 0) return 0;
+  (void)K;
+  const size_t ldp = epi == 2 ? 2 * (size_t)N : (size_t)N;
+  return 256 + (tiling == 0 ? (size_t)kGemmMaxSplits * rows * ldp * 4 : 0);
+}
 
 int cdb_test_gemm(int epi, int tiling, const void* A, int lda, int a_rows, const void* W, const void* W2, int N,
                   int K, int rows, float* Cf, void* Ct, int ldc, void* ws, size_t ws_bytes, void* stream) {
@@ -932,13 +986,22 @@ int cdb_test_gemm(int epi, int tiling, const void* A, int lda, int a_rows, const
     return CDB_ERR_ARG;
   cudaStream_t s = (cudaStream_t)stream;
   int* status = (int*)ws;
+  float* parts = (float*)((char*)ws + 256);
+  if (cudaMemsetAsync(status, 0, 4, s) != cudaSuccess) return CDB_ERR_CUDA;
   if (tiling == 2) {
     launch_gemm<__nv_bfloat16>(s, epi, (const __nv_bfloat16*)A, lda, (const __nv_bfloat16*)W,
                                (const __nv_bfloat16*)W2, N, K, rows, Cf, (__nv_bfloat16*)Ct, ldc);
-  } else if (!launch_gemm_tc(s, epi, (const __nv_bfloat16*)A, lda, a_rows, (const __nv_bfloat16*)W,
-                             (const __nv_bfloat16*)W2, N, K, rows, Cf, (__nv_bfloat16*)Ct, ldc, tiling == 0,
-                             status)) {
-    return CDB_ERR_ARG;
+  } else {
+    // The decode tiling leaves split-K partials for a consumer; fold them here
+    // the way the engine's consumers do (split order, then the epilogue).
+    const int ns = launch_gemm_tc(s, epi, (const __nv_bfloat16*)A, lda, a_rows, (const __nv_bfloat16*)W,
+                                  (const __nv_bfloat16*)W2, N, K, rows, Cf, (__nv_bfloat16*)Ct, ldc, tiling == 0,
+                                  tiling == 0 ? parts : nullptr, (ws_bytes - 256) / 4, status);
+    if (ns < 0) return CDB_ERR_ARG;
+    if (ns > 0) {
+      if (epi == 2) launch_swiglu_combine<__nv_bfloat16>(s, parts, ns, rows, N, (__nv_bfloat16*)Ct);
+      else launch_fold(s, parts, ns, rows, N, Cf, ldc, epi == 1 ? 1 : 2);
+    }
   }
   if (cudaGetLastError() != cudaSuccess || cudaStreamSynchronize(s) != cudaSuccess) return CDB_ERR_CUDA;
   int st = 0;

@@ -9,16 +9,16 @@
 // TMEM accumulator; all four warps then read TMEM with tcgen05.ld and apply
 // the epilogue (store, residual add, or SwiGLU of two accumulators).
 //
-// Split-K: the K range is cut into `splits` pieces whose count depends only on
-// the weight shape, never on the number of rows, so a row's result is the same
-// in every batch.  The split CTAs of one tile form a thread-block cluster; each
-// parks its fp32 partial tile in its own shared memory, and after a cluster
-// barrier CTA r sums a slice of the tile's rows over all peers' shared memory
-// (distributed shared memory) in split order and runs the epilogue for them.
+// Split-K (decode tilings): the K range is cut into `splits` pieces whose
+// count depends only on the weight shape, never on the number of rows, so a
+// row's result is the same in every batch.  Each split CTA stores its fp32
+// partial tile to a workspace P[split][row][ldp]; the kernel that consumes the
+// GEMM's output (RoPE + KV write, residual + RMSNorm, the SwiGLU combine, or
+// the residual fold) sums the partials in split order while it reads them.
+// With one split the epilogue (store, residual add, SwiGLU) runs in place.
 //
 // Every mbarrier wait is bounded by the global timer; on expiry the kernel
 // records kStatusTimeout, skips the epilogue, releases TMEM and returns.
-#include <cooperative_groups.h>
 #include <cuda.h>
 
 #include <unordered_map>
@@ -167,7 +167,8 @@ template <int BN, int EPI>
 __global__ void __launch_bounds__(128, BN == 64 ? 2 : 1)
     k_gemm_tc(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmW2,
               const __grid_constant__ CUtensorMap tmA, int N, int K, int rows, int splits,
-              float* __restrict__ Cf, __nv_bfloat16* __restrict__ Ct, int ldc, int* status) {
+              float* __restrict__ Cf, __nv_bfloat16* __restrict__ Ct, int ldc, float* __restrict__ ws,
+              int* status) {
   constexpr bool SW = EPI == kEpiSwiglu;
   using C = Cfg<BN, SW>;
   extern __shared__ uint8_t smem_raw[];
@@ -273,7 +274,7 @@ __global__ void __launch_bounds__(128, BN == 64 ? 2 : 1)
   } else {
     const int f = n0 + warp * 32 + lane;  // output feature of this thread's TMEM lane
     const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
-    if (splits == 1) {
+    if (ws == nullptr) {
 #pragma unroll 1
       for (int c0 = 0; c0 < BN; c0 += 16) {
         float v[16], u[16];
@@ -283,66 +284,26 @@ __global__ void __launch_bounds__(128, BN == 64 ? 2 : 1)
         if (f < N && jn > 0) epilogue16<EPI>(v, u, jn, Cf, Ct, (size_t)(m0 + c0) * ldc + f, ldc);
       }
     } else {
-      // Park this split's partial tile red[j][0..BM) (and [BM..2BM) for the
-      // second accumulator) in shared memory; the pipeline buffers are idle.
-      constexpr int RW = BM * (SW ? 2 : 1);
-      float* red = reinterpret_cast<float*>(smem);
+      // This split's partial tile: P[split][row][f] (SwiGLU: up at f + N).
+      const size_t ldp = SW ? 2 * (size_t)N : (size_t)N;
+      float* P = ws + (size_t)split * rows * ldp;
 #pragma unroll 1
       for (int c0 = 0; c0 < BN; c0 += 16) {
         float v[16], u[16];
         tmem_ld16(lane_base + c0, v);
         if (SW) tmem_ld16(lane_base + BN + c0, u);
+        const int jn = min(16, rows - (m0 + c0));
+        if (f < N && jn > 0) {
+          float* o = P + (size_t)(m0 + c0) * ldp + f;
 #pragma unroll
-        for (int j = 0; j < 16; ++j) {
-          red[(c0 + j) * RW + warp * 32 + lane] = v[j];
-          if (SW) red[(c0 + j) * RW + BM + warp * 32 + lane] = u[j];
-        }
-      }
-    }
-  }
-  if (splits > 1) {
-    // Every CTA of the cluster reaches both barriers, failed or not.
-    namespace cg = cooperative_groups;
-    cg::cluster_group cl = cg::this_cluster();
-    cl.sync();
-    if (ok) {
-      constexpr int RW = BM * (SW ? 2 : 1);
-      float* red = reinterpret_cast<float*>(smem);
-      const int rank = (int)cl.block_rank();
-      const int j0 = BN * rank / splits, j1 = BN * (rank + 1) / splits;
-      const int f = n0 + threadIdx.x;  // one output feature per thread
-      const float* peer[8];
-#pragma unroll
-      for (int q = 0; q < 8; ++q) peer[q] = q < splits ? cl.map_shared_rank(red, q) : red;
-      const int jend = min(j1, rows - m0);
-      for (int jb = j0; jb < jend; jb += 4) {
-        const int jn = min(4, jend - jb);
-        float gv[4][8], uv[4][8];
-#pragma unroll
-        for (int i = 0; i < 4; ++i)
-#pragma unroll
-          for (int q = 0; q < 8; ++q) {
-            const bool on = i < jn && q < splits;
-            gv[i][q] = on ? peer[q][(jb + i) * RW + threadIdx.x] : 0.f;
-            if (SW) uv[i][q] = on ? peer[q][(jb + i) * RW + BM + threadIdx.x] : 0.f;
-          }
-        float gs[16], us[16];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          float g = 0.f, up = 0.f;
-#pragma unroll
-          for (int q = 0; q < 8; ++q)
-            if (q < splits) {  // split order, whatever CTA reduces
-              g += gv[i][q];
-              if (SW) up += uv[i][q];
+          for (int j = 0; j < 16; ++j)
+            if (j < jn) {
+              o[(size_t)j * ldp] = v[j];
+              if (SW) o[(size_t)j * ldp + N] = u[j];
             }
-          gs[i] = g;
-          us[i] = up;
         }
-        if (f < N) epilogue16<EPI>(gs, us, jn, Cf, Ct, (size_t)(m0 + jb) * ldc + f, ldc);
       }
     }
-    cl.sync();
   }
   fence_before();
   __syncthreads();
@@ -410,7 +371,7 @@ static const CUtensorMap* get_map(const void* p, uint64_t inner, uint64_t outer,
 template <int BN, int EPI>
 static bool launch_bn(cudaStream_t s, const __nv_bfloat16* A, int lda, int a_rows, const __nv_bfloat16* W,
                       const __nv_bfloat16* W2, int N, int K, int rows, int splits, float* Cf,
-                      __nv_bfloat16* Ct, int ldc, int* status) {
+                      __nv_bfloat16* Ct, int ldc, float* ws, int* status) {
   using C = Cfg<BN, EPI == kEpiSwiglu>;
   const CUtensorMap* mw = get_map(W, K, N, (uint64_t)K * 2, BM);
   const CUtensorMap* mw2 = EPI == kEpiSwiglu ? get_map(W2, K, N, (uint64_t)K * 2, BM) : mw;
@@ -423,97 +384,63 @@ static bool launch_bn(cudaStream_t s, const __nv_bfloat16* A, int lda, int a_row
       return false;
     attr = true;
   }
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((N + BM - 1) / BM, (rows + BN - 1) / BN, splits);
-  cfg.blockDim = dim3(128, 1, 1);
-  cfg.dynamicSmemBytes = C::SMEM;
-  cfg.stream = s;
-  cudaLaunchAttribute at[2];
-  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  at[0].val.programmaticStreamSerializationAllowed = 1;
-  at[1].id = cudaLaunchAttributeClusterDimension;
-  at[1].val.clusterDim.x = 1;
-  at[1].val.clusterDim.y = 1;
-  at[1].val.clusterDim.z = splits;
-  cfg.attrs = at;
-  cfg.numAttrs = splits > 1 ? 2 : 1;
   count_launch();
-  return cudaLaunchKernelEx(&cfg, k_gemm_tc<BN, EPI>, *mw, *mw2, *ma, N, K, rows, splits, Cf, Ct, ldc, status) ==
-         cudaSuccess;
+  return launch_pdl(k_gemm_tc<BN, EPI>, dim3((N + BM - 1) / BM, (rows + BN - 1) / BN, splits), dim3(128), C::SMEM, s,
+                    *mw, *mw2, *ma, N, K, rows, splits, Cf, Ct, ldc, ws, status) == cudaSuccess;
 }
 
 }  // namespace tc
 
-// Clusters of `size` CTAs of this kernel that can be resident at once.
-template <int BN, int EPI>
-static int max_clusters(int size) {
-  static int cache[9] = {0};
-  if (size < 1 || size > 8) return 0;
-  if (cache[size]) return cache[size];
-  using C = tc::Cfg<BN, EPI == kEpiSwiglu>;
-  cudaFuncSetAttribute(tc::k_gemm_tc<BN, EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
-  cudaFuncSetAttribute(tc::k_gemm_tc<BN, EPI>, cudaFuncAttributeNonPortableClusterSizeAllowed, 0);
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(1, 1, size);
-  cfg.blockDim = dim3(128, 1, 1);
-  cfg.dynamicSmemBytes = C::SMEM;
-  cudaLaunchAttribute at[1];
-  at[0].id = cudaLaunchAttributeClusterDimension;
-  at[0].val.clusterDim.x = 1;
-  at[0].val.clusterDim.y = 1;
-  at[0].val.clusterDim.z = size;
-  cfg.attrs = at;
-  cfg.numAttrs = 1;
-  int n = 0;
-  if (cudaOccupancyMaxActiveClusters(&n, tc::k_gemm_tc<BN, EPI>, &cfg) != cudaSuccess) n = 0;
-  cache[size] = n > 0 ? n : 1;
-  return cache[size];
+static int sm_count() {
+  static int n = 0;
+  if (!n) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) !=
+                                                  cudaSuccess || n <= 0)
+      n = 1;
+  }
+  return n;
 }
 
-// Split count for a decode GEMM: about one CTA per SM, at least 4 K slabs per
-// split, and every tile's cluster resident in one wave.  Depends only on the
-// weight shape (and the device), never on the number of rows.
-template <int BN, int EPI>
-static int splits_for(int N, int K) {
+// Split count of a decode GEMM: as many CTAs as two per SM hold, at least
+// four 64-element K slabs per split, at most kGemmMaxSplits.  Depends only on
+// the weight shape (and the device), never on the number of rows.
+int gemm_tc_splits(int N, int K, bool decode) {
+  if (!decode) return 1;
   const int tiles = (N + tc::BM - 1) / tc::BM;
   const int KT = (K + tc::BK - 1) / tc::BK;
-  int s = (int)((304.0 / tiles) + 0.5);  // about two CTAs per SM
+  int s = 2 * sm_count() / tiles;
   if (s > KT / 4) s = KT / 4;
-  if (s > 8) s = 8;
-  while (s > 1 && tiles > max_clusters<BN, EPI>(s)) --s;
+  if (s > kGemmMaxSplits) s = kGemmMaxSplits;
   return s < 1 ? 1 : s;
 }
 
-int gemm_tc_splits(int N, int K, bool decode) {
-  if (!decode) return 1;
-  return splits_for<64, kEpiStore>(N, K);
-}
-
-bool launch_gemm_tc(cudaStream_t s, int epi, const __nv_bfloat16* A, int lda, int a_rows, const __nv_bfloat16* W,
-                    const __nv_bfloat16* W2, int N, int K, int rows, float* Cf, __nv_bfloat16* Ct, int ldc,
-                    bool decode, int* status) {
-  if (rows <= 0) return true;
-  if ((K * 2) % 16 != 0 || (lda * 2) % 16 != 0 || rows > a_rows) return false;
+int launch_gemm_tc(cudaStream_t s, int epi, const __nv_bfloat16* A, int lda, int a_rows, const __nv_bfloat16* W,
+                   const __nv_bfloat16* W2, int N, int K, int rows, float* Cf, __nv_bfloat16* Ct, int ldc,
+                   bool decode, float* ws, size_t ws_floats, int* status) {
+  if (rows <= 0) return 0;
+  if ((K * 2) % 16 != 0 || (lda * 2) % 16 != 0 || rows > a_rows) return -1;
+  int splits = ws ? gemm_tc_splits(N, K, decode) : 1;
+  const size_t ldp = epi == kEpiSwiglu ? 2 * (size_t)N : (size_t)N;
+  // Consumers fold partials four columns at a time.
+  if (splits > 1 && ((size_t)splits * rows * ldp > ws_floats || N % 4 != 0)) splits = 1;
+  float* P = splits > 1 ? ws : nullptr;
+  bool ok;
   if (decode) {
-    int splits;
     switch (epi) {
-      case kEpiStore:
-        splits = splits_for<64, kEpiStore>(N, K);
-        return tc::launch_bn<64, kEpiStore>(s, A, lda, a_rows, W, W2, N, K, rows, splits, Cf, Ct, ldc, status);
-      case kEpiResid:
-        splits = splits_for<64, kEpiResid>(N, K);
-        return tc::launch_bn<64, kEpiResid>(s, A, lda, a_rows, W, W2, N, K, rows, splits, Cf, Ct, ldc, status);
-      default:
-        splits = splits_for<64, kEpiSwiglu>(N, K);
-        return tc::launch_bn<64, kEpiSwiglu>(s, A, lda, a_rows, W, W2, N, K, rows, splits, Cf, Ct, ldc, status);
+      case kEpiStore: ok = tc::launch_bn<64, kEpiStore>(s, A, lda, a_rows, W, W2, N, K, rows, splits, Cf, Ct, ldc, P, status); break;
+      case kEpiResid: ok = tc::launch_bn<64, kEpiResid>(s, A, lda, a_rows, W, W2, N, K, rows, splits, Cf, Ct, ldc, P, status); break;
+      default: ok = tc::launch_bn<64, kEpiSwiglu>(s, A, lda, a_rows, W, W2, N, K, rows, splits, Cf, Ct, ldc, P, status); break;
+    }
+  } else {
+    switch (epi) {
+      case kEpiStore: ok = tc::launch_bn<128, kEpiStore>(s, A, lda, a_rows, W, W2, N, K, rows, 1, Cf, Ct, ldc, nullptr, status); break;
+      case kEpiResid: ok = tc::launch_bn<128, kEpiResid>(s, A, lda, a_rows, W, W2, N, K, rows, 1, Cf, Ct, ldc, nullptr, status); break;
+      default: ok = tc::launch_bn<128, kEpiSwiglu>(s, A, lda, a_rows, W, W2, N, K, rows, 1, Cf, Ct, ldc, nullptr, status); break;
     }
   }
-  const int splits = 1;
-  switch (epi) {
-    case kEpiStore: return tc::launch_bn<128, kEpiStore>(s, A, lda, a_rows, W, W2, N, K, rows, splits, Cf, Ct, ldc, status);
-    case kEpiResid: return tc::launch_bn<128, kEpiResid>(s, A, lda, a_rows, W, W2, N, K, rows, splits, Cf, Ct, ldc, status);
-    default: return tc::launch_bn<128, kEpiSwiglu>(s, A, lda, a_rows, W, W2, N, K, rows, splits, Cf, Ct, ldc, status);
-  }
+  if (!ok) return -1;
+  return P ? splits : 0;
 }
 
 }  // namespace cdb

@@ -109,21 +109,106 @@ __global__ void k_prelude_finish(const float* __restrict__ Tp, RowMeta tm, int r
 // RMSNorm -> GEMM operand; adapter concat
 // ---------------------------------------------------------------------------
 
+// Split-K partials of a GEMM output: P[split][row][ld] with split stride ss;
+// their sum in split order (the reduction every consumer uses, so a value is
+// the same whichever kernel folds it).
+struct Parts {
+  const float* P;
+  int ns;     // number of partials (<= kGemmMaxSplits); 0 = nothing to fold
+  size_t ss;  // floats between consecutive splits
+  int ld;     // floats between consecutive rows
+  // Sum of columns c..c+3 of `row` (c and ld multiples of 4): every partial
+  // is loaded before the first add, then added in split order.
+  __device__ __forceinline__ float4 sum4(int row, int c) const {
+    const float4* p = reinterpret_cast<const float4*>(P + (size_t)row * ld + c);
+    const size_t s4 = ss / 4;
+    float4 v[kGemmMaxSplits];
+#pragma unroll
+    for (int q = 0; q < kGemmMaxSplits; ++q) v[q] = q < ns ? p[q * s4] : make_float4(0.f, 0.f, 0.f, 0.f);
+    float4 g = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int q = 0; q < kGemmMaxSplits; ++q)
+      if (q < ns) {
+        g.x += v[q].x;
+        g.y += v[q].y;
+        g.z += v[q].z;
+        g.w += v[q].w;
+      }
+    return g;
+  }
+};
+
+// With pending partials (mode 1: residual, X += sum; mode 2: store, X = sum)
+// X is updated first, then normalised.
 template <typename T>
-__global__ void k_rmsnorm(const float* __restrict__ X, const T* __restrict__ g, T* __restrict__ A,
-                          int rows, int d, float eps, int lda) {
+__global__ void k_rmsnorm(float* __restrict__ X, const T* __restrict__ g, T* __restrict__ A, int rows, int d,
+                          float eps, int lda, Parts pp, int mode) {
   pdl_wait();
   pdl_trigger();
   __shared__ float sh[33];
   const int i = blockIdx.x;
   if (i >= rows) return;
-  const float* x = X + (size_t)i * d;
+  float* x = X + (size_t)i * d;
   float ss = 0.f;
-  for (int c = threadIdx.x; c < d; c += blockDim.x) ss = fmaf(x[c], x[c], ss);
+  if (pp.ns > 0) {  // d is a multiple of 4 whenever partials exist (bf16 models)
+    for (int c = threadIdx.x * 4; c < d; c += blockDim.x * 4) {
+      const float4 v = pp.sum4(i, c);
+      float4 o = *reinterpret_cast<const float4*>(x + c);
+      if (mode == 1) {
+        o.x += v.x;
+        o.y += v.y;
+        o.z += v.z;
+        o.w += v.w;
+      } else {
+        o = v;
+      }
+      *reinterpret_cast<float4*>(x + c) = o;
+      ss = fmaf(o.x, o.x, ss);
+      ss = fmaf(o.y, o.y, ss);
+      ss = fmaf(o.z, o.z, ss);
+      ss = fmaf(o.w, o.w, ss);
+    }
+  } else {
+    for (int c = threadIdx.x; c < d; c += blockDim.x) ss = fmaf(x[c], x[c], ss);
+  }
   ss = block_sum(ss, sh);
   const float inv = 1.0f / sqrtf(ss / (float)d + eps);
+  if (A == nullptr) return;
   for (int c = threadIdx.x; c < d; c += blockDim.x)
     A[(size_t)i * lda + c] = from_f<T>(x[c] * inv * to_f(g[c]));
+}
+
+// C[i][c] (row stride ldc) = sum of the partials (mode 2) or C + sum (mode 1).
+// Grid (rows, column blocks of 4 * blockDim).
+__global__ void k_fold(Parts pp, int rows, int n, float* __restrict__ C, int ldc, int mode) {
+  pdl_wait();
+  pdl_trigger();
+  const int i = blockIdx.x;
+  const int c = (blockIdx.y * blockDim.x + threadIdx.x) * 4;
+  if (i >= rows || c >= n) return;
+  const float4 v = pp.sum4(i, c);
+  float* o = C + (size_t)i * ldc + c;
+  const float w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int e = 0; e < 4; ++e)
+    if (c + e < n) o[e] = mode == 1 ? o[e] + w[e] : w[e];
+}
+
+// Mid[i][c] = silu(sum g) * (sum u), rounded to the operand type, from the
+// partials of the gate/up GEMM (g at column c, u at c + f).  Grid (rows,
+// column blocks of 4 * blockDim).
+template <typename T>
+__global__ void k_swiglu_combine(Parts pp, int rows, int f, T* __restrict__ Mid) {
+  pdl_wait();
+  pdl_trigger();
+  const int i = blockIdx.x;
+  const int c = (blockIdx.y * blockDim.x + threadIdx.x) * 4;
+  if (i >= rows || c >= f) return;
+  const float4 g4 = pp.sum4(i, c), u4 = pp.sum4(i, c + f);
+  const float g[4] = {g4.x, g4.y, g4.z, g4.w}, u[4] = {u4.x, u4.y, u4.z, u4.w};
+#pragma unroll
+  for (int e = 0; e < 4; ++e)
+    if (c + e < f) Mid[(size_t)i * f + c + e] = from_f<T>(g[e] / (1.0f + expf(-g[e])) * u[e]);
 }
 
 // A[i] = [e ; s] rounded to the operand type (x = adapter . [e; s_{d-1}]).
@@ -149,8 +234,10 @@ __global__ void k_concat(const float* __restrict__ E, int e_per_slot, const int*
 
 // Row i at position p and loop step r writes K,V into slot slot_base + r-1
 // (core layers, clamp=1) or slot_base (prelude / coda layers).
+// QKV arrives as split-K partials (qkv.ns >= 1; one partial is the plain
+// GEMM output).
 template <typename T>
-__global__ void k_rope_kv(const float* __restrict__ QKV, int rows, const int* __restrict__ mslot,
+__global__ void k_rope_kv(Parts qkv, int rows, const int* __restrict__ mslot,
                           const int* __restrict__ mpos, const int* __restrict__ mdepth,
                           int depth_uniform, int slot_base, int clamp, T* __restrict__ Q, KvGeom kv,
                           int H, int hd, const float2* __restrict__ rope, int* status) {
@@ -172,21 +259,30 @@ __global__ void k_rope_kv(const float* __restrict__ QKV, int rows, const int* __
   T* pool = reinterpret_cast<T*>(kv.pool);
   T* kdst = pool + (((size_t)blk * kv.nsl + sl) * 2 + 0) * 16 * d + (size_t)(pos & 15) * hd;
   T* vdst = kdst + (size_t)16 * d;
-  const float* q = QKV + (size_t)i * 3 * d;
-  const float* k = q + d;
-  const float* v = q + 2 * d;
   const float2* cs = rope + (size_t)pos * half;
-  for (int u = threadIdx.x; u < H * half; u += blockDim.x) {
-    const int h = u / half, j = u % half;
-    const int a = h * hd + j, b = a + half;
-    const size_t ka = (size_t)h * 16 * hd + j, kb = ka + half;
-    const float c = cs[j].x, s = cs[j].y;
-    Q[(size_t)i * d + a] = from_f<T>(q[a] * c - q[b] * s);
-    Q[(size_t)i * d + b] = from_f<T>(q[b] * c + q[a] * s);
-    kdst[ka] = from_f<T>(k[a] * c - k[b] * s);
-    kdst[kb] = from_f<T>(k[b] * c + k[a] * s);
-    vdst[ka] = from_f<T>(v[a]);
-    vdst[kb] = from_f<T>(v[b]);
+  // Four consecutive rotation pairs (j, j + half) per thread; half is a
+  // multiple of 4 for every supported head dim.
+  const int quads = H * half / 4;
+  for (int u = blockIdx.y * blockDim.x + threadIdx.x; u < quads; u += gridDim.y * blockDim.x) {
+    const int h = u / (half / 4), j0 = (u % (half / 4)) * 4;
+    const int a = h * hd + j0, b = a + half;
+    const float4 qa = qkv.sum4(i, a), qb = qkv.sum4(i, b);
+    const float4 ka = qkv.sum4(i, d + a), kb = qkv.sum4(i, d + b);
+    const float4 va = qkv.sum4(i, 2 * d + a), vb = qkv.sum4(i, 2 * d + b);
+    const float qa_[4] = {qa.x, qa.y, qa.z, qa.w}, qb_[4] = {qb.x, qb.y, qb.z, qb.w};
+    const float ka_[4] = {ka.x, ka.y, ka.z, ka.w}, kb_[4] = {kb.x, kb.y, kb.z, kb.w};
+    const float va_[4] = {va.x, va.y, va.z, va.w}, vb_[4] = {vb.x, vb.y, vb.z, vb.w};
+    const size_t kofs = (size_t)h * 16 * hd + j0;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const float c = cs[j0 + e].x, s = cs[j0 + e].y;
+      Q[(size_t)i * d + a + e] = from_f<T>(qa_[e] * c - qb_[e] * s);
+      Q[(size_t)i * d + b + e] = from_f<T>(qb_[e] * c + qa_[e] * s);
+      kdst[kofs + e] = from_f<T>(ka_[e] * c - kb_[e] * s);
+      kdst[kofs + half + e] = from_f<T>(kb_[e] * c + ka_[e] * s);
+      vdst[kofs + e] = from_f<T>(va_[e]);
+      vdst[kofs + half + e] = from_f<T>(vb_[e]);
+    }
   }
 }
 
@@ -453,8 +549,21 @@ void launch_prelude_finish(cudaStream_t s, const float* Tp, RowMeta tm, int rows
   if (rows > 0) count_launch(), launch_pdl(k_prelude_finish, dim3(rows), dim3(256), 0, s, Tp, tm, rows, Pb, pm, dst_off, estore, d, adapter);
 }
 template <typename T>
-void launch_rmsnorm(cudaStream_t s, const float* X, const T* g, T* A, int rows, int d, float eps, int lda) {
-  if (rows > 0) count_launch(), launch_pdl(k_rmsnorm<T>, dim3(rows), dim3(256), 0, s, X, g, A, rows, d, eps, lda);
+void launch_rmsnorm(cudaStream_t s, float* X, const T* g, T* A, int rows, int d, float eps, int lda,
+                    const float* P, int ns, int mode) {
+  Parts pp{P, ns, (size_t)rows * d, d};
+  if (rows > 0) count_launch(), launch_pdl(k_rmsnorm<T>, dim3(rows), dim3(256), 0, s, X, g, A, rows, d, eps, lda, pp, mode);
+}
+void launch_fold(cudaStream_t s, const float* P, int ns, int rows, int n, float* C, int ldc, int mode) {
+  Parts pp{P, ns, (size_t)rows * n, n};
+  if (rows > 0 && ns > 0)
+    count_launch(), launch_pdl(k_fold, dim3(rows, (n + 511) / 512), dim3(128), 0, s, pp, rows, n, C, ldc, mode);
+}
+template <typename T>
+void launch_swiglu_combine(cudaStream_t s, const float* P, int ns, int rows, int f, T* Mid) {
+  Parts pp{P, ns, (size_t)rows * 2 * f, 2 * f};
+  if (rows > 0)
+    count_launch(), launch_pdl(k_swiglu_combine<T>, dim3(rows, (f + 511) / 512), dim3(128), 0, s, pp, rows, f, Mid);
 }
 template <typename T>
 void launch_concat(cudaStream_t s, const float* E, int e_per_slot, const int* mslot, const float* X, T* A,
@@ -462,11 +571,14 @@ void launch_concat(cudaStream_t s, const float* E, int e_per_slot, const int* ms
   if (rows > 0) count_launch(), launch_pdl(k_concat<T>, dim3(rows), dim3(256), 0, s, E, e_per_slot, mslot, X, A, rows, d);
 }
 template <typename T>
-void launch_rope_kv(cudaStream_t s, const float* QKV, int rows, const int* mslot, const int* mpos,
+void launch_rope_kv(cudaStream_t s, const float* QKV, int ns, int rows, const int* mslot, const int* mpos,
                     const int* mdepth, int depth_uniform, int slot_base, int clamp, T* Q, KvGeom kv, int H,
                     int hd, const float2* rope, int* status) {
+  Parts qkv{QKV, ns < 1 ? 1 : ns, (size_t)rows * 3 * kv.d, 3 * kv.d};
+  const int quads = H * (hd / 2) / 4;
+  const int gy = (quads + 127) / 128;
   if (rows > 0)
-    count_launch(), launch_pdl(k_rope_kv<T>, dim3(rows), dim3(256), 0, s, QKV, rows, mslot, mpos, mdepth, depth_uniform, slot_base, clamp, Q,
+    count_launch(), launch_pdl(k_rope_kv<T>, dim3(rows, gy), dim3(128), 0, s, qkv, rows, mslot, mpos, mdepth, depth_uniform, slot_base, clamp, Q,
                                       kv, H, hd, rope, status);
 }
 template <typename T>
@@ -513,10 +625,12 @@ void launch_copy_rows(cudaStream_t s, const float* src, float* dst, int rows, in
   template void launch_embed_prelude<T>(cudaStream_t, const T*, int, int, const int*, const int*,          \
                                         const int*, int, const int*, int, float*, RowMeta, KvGeom, int,       \
                                         int*);                                                                \
-  template void launch_rmsnorm<T>(cudaStream_t, const float*, const T*, T*, int, int, float, int);          \
+  template void launch_rmsnorm<T>(cudaStream_t, float*, const T*, T*, int, int, float, int, const float*,   \
+                                  int, int);                                                                \
+  template void launch_swiglu_combine<T>(cudaStream_t, const float*, int, int, int, T*);                   \
   template void launch_concat<T>(cudaStream_t, const float*, int, const int*, const float*, T*, int, int);  \
-  template void launch_rope_kv<T>(cudaStream_t, const float*, int, const int*, const int*, const int*, int, \
-                                  int, int, T*, KvGeom, int, int, const float2*, int*);                       \
+  template void launch_rope_kv<T>(cudaStream_t, const float*, int, int, const int*, const int*, const int*,  \
+                                  int, int, int, T*, KvGeom, int, int, const float2*, int*);                  \
   template void launch_gate<T>(cudaStream_t, const float*, const T*, float, float, float, int, int,        \
                                RowMeta, int, int, int, const int8_t*, int, int*, uint8_t*, float*);
 CDB_INST(float)

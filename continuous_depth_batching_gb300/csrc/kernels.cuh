@@ -69,13 +69,23 @@ void launch_embed_prelude(cudaStream_t s, const T* E, int d, int V, const int* l
 void launch_prelude_finish(cudaStream_t s, const float* Tp, RowMeta tmeta, int rows, float* Pb,
                            RowMeta pmeta, int dst_off, float* estore, int d, int adapter);
 template <typename T>
-void launch_rmsnorm(cudaStream_t s, const float* X, const T* g, T* A, int rows, int d,
-                    float eps, int lda);
+// A = RMSNorm(X) * g.  With ns > 0 pending GEMM partials P (split stride
+// rows * d) are folded into X first: mode 1 X += sum, mode 2 X = sum.  A may be
+// null (fold only).
+void launch_rmsnorm(cudaStream_t s, float* X, const T* g, T* A, int rows, int d, float eps,
+                    int lda, const float* P, int ns, int mode);
+// C (row stride ldc) = sum of ns partials [split][row][n] (mode 2) or C + sum (mode 1).
+void launch_fold(cudaStream_t s, const float* P, int ns, int rows, int n, float* C, int ldc, int mode);
+// Mid = silu(sum of gate partials) * (sum of up partials), from the ns split-K
+// partials of the gate/up GEMM ([split][row][2f], up at +f).
+template <typename T>
+void launch_swiglu_combine(cudaStream_t s, const float* P, int ns, int rows, int f, T* Mid);
 template <typename T>
 void launch_concat(cudaStream_t s, const float* E, int e_per_slot, const int* mslot,
                    const float* X, T* A, int rows, int d);
 template <typename T>
-void launch_rope_kv(cudaStream_t s, const float* QKV, int rows, const int* mslot,
+// QKV: ns split-K partials [split][row][3d] (ns <= 1: the plain GEMM output).
+void launch_rope_kv(cudaStream_t s, const float* QKV, int ns, int rows, const int* mslot,
                     const int* mpos, const int* mdepth, int depth_uniform, int slot_base,
                     int clamp, T* Q, KvGeom kv, int H, int hd, const float2* rope,
                     int* status);
@@ -120,13 +130,19 @@ void launch_gemm(cudaStream_t s, int epi, const T* A, int lda, const T* W, const
                  int K, int rows, float* Cf, T* Ct, int ldc);
 
 // ---- tensor-core GEMM (gemm_tc.cu), bf16 only ----
-// decode = true: 64-row tiles and a split-K count fixed by (N, K), split CTAs
-// reduce through distributed shared memory; false: 128-row tiles, no split.
-// a_rows: rows allocated in A (TMA bounds).  Returns false when the shape is
-// not supported.
+// decode: 64-row tiles with
+// split-K; otherwise 128-row tiles, one split.  With ws (room for ws_floats)
+// and more than one split, each split's fp32 partial goes to
+// ws[split][row][ldp] (ldp = N, or 2N for SwiGLU with the up projection at
+// +N) and the epilogue is left to the consumer (sum the partials in split
+// order, then apply it); the return value is then the split count.  Returns 0
+// when the epilogue was applied in place, -1 when the shape is unsupported.
+// a_rows: rows allocated in A (TMA bounds).
+constexpr int kGemmMaxSplits = 16;
 int gemm_tc_splits(int N, int K, bool decode);
-bool launch_gemm_tc(cudaStream_t s, int epi, const __nv_bfloat16* A, int lda, int a_rows,
-                    const __nv_bfloat16* W, const __nv_bfloat16* W2, int N, int K, int rows, float* Cf,
-                    __nv_bfloat16* Ct, int ldc, bool decode, int* status);
+int launch_gemm_tc(cudaStream_t s, int epi, const __nv_bfloat16* A, int lda, int a_rows,
+                   const __nv_bfloat16* W, const __nv_bfloat16* W2, int N, int K, int rows,
+                   float* Cf, __nv_bfloat16* Ct, int ldc, bool decode, float* ws, size_t ws_floats,
+                   int* status);
 
 }  // namespace cdb

@@ -16,12 +16,14 @@ extern "C" {
  * fp32 accumulation, bf16 A and W (row-major, device pointers).
  *   epi 0: Cf[r][c] = acc (fp32 out)      epi 1: Cf[r][c] += acc
  *   epi 2: Ct[r][c] = bf16(silu(A.W^T) * (A.W2^T))   (SwiGLU, bf16 out)
- *   tiling 0: tensor cores, decode tiles (64 rows, split-K fixed by N and K)
+ *   tiling 0: tensor cores, decode tiles (64 rows, split-K fixed by N and K;
+ *             the fp32 partials are summed in split order by a second kernel,
+ *             as the engine's consumer kernels do, then the epilogue applied)
  *   tiling 1: tensor cores, prefill tiles (128 rows, no split)
  *   tiling 2: the CUDA-core kernel (fp32 FMA), for comparison
- * a_rows: rows allocated in A (>= rows).  ws: zero-filled device memory of at
- * least cdb_test_gemm_ws_bytes() bytes that receives the kernel's status
- * word.  stream: cudaStream_t or NULL.
+ * a_rows: rows allocated in A (>= rows).  ws: device memory of at least
+ * cdb_test_gemm_ws_bytes() bytes: the kernel's status word, then the split-K
+ * partials.  stream: cudaStream_t or NULL.
  * Synchronizes the stream; returns CDB_OK (0), CDB_ERR_ARG (-1) for an
  * unsupported shape, CDB_ERR_CUDA (-4), or CDB_ERR_DEVICE_BOUNDS (-5) when a
  * bounded wait inside the kernel expired. */
