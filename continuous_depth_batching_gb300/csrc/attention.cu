@@ -823,6 +823,250 @@ __global__ void __launch_bounds__((attn::kWarps + 1) * 32)
   }
 }
 
+// ---------------------------------------------------------------------------
+// Prefill attention (bf16, head_dim 32, 64, 96 or 128), causal, in the style
+// of FlashAttention-2 on the warp-level MMA.  The rows of a prefill chunk come
+// sequence by sequence with consecutive positions; the host cuts them into
+// query tiles of up to kPfRows rows of one sequence.  One CTA per (tile,
+// head): a producer warp moves the tile's q rows once and then streams the
+// sequence's key pages (16 keys, every key from the same slot) through a ring
+// with 2D TMA tensor copies under the same swizzle as the decode kernel; four
+// consumer warps own 16 query rows each.  Per page: S = Q.K^T (m16n8k16, fp32
+// accumulate), causal mask, online softmax per row, O += P.V with P fed as a
+// bf16 hi/lo pair.  Each page is read once per tile instead of once per row.
+// ---------------------------------------------------------------------------
+namespace attn {
+
+constexpr int kPfRows = 64;   // query rows per tile (4 warps x 16)
+constexpr int kPfStages = 4;  // pages in flight per CTA
+
+template <int HD>
+struct PfGeo {
+  using Tg = TmaGeo<HD>;
+  static constexpr int SWB = Tg::SWB, XW = Tg::XW, NX = Tg::NX;
+  static constexpr int QSLICE = kPfRows * SWB;           // q rows of one slice
+  static constexpr int QBYTES = NX * QSLICE;
+  static constexpr int PSLICE = 16 * SWB;                // one page slice (16 keys)
+  static constexpr int KV = NX * PSLICE;                 // K (or V) of one page
+  static constexpr int STAGE = (2 * KV + 1023) / 1024 * 1024;
+  static constexpr size_t SMEM = 1024 + (size_t)QBYTES + (size_t)kPfStages * STAGE + 2 * kPfStages * 8 + 8;
+};
+
+}  // namespace attn
+
+template <int HD>
+__global__ void __launch_bounds__(5 * 32)
+    k_attn_prefill(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
+                   const int4* __restrict__ tiles, KvGeom kv, int slot, int H, __nv_bfloat16* __restrict__ O,
+                   int* status) {
+  using Pg = attn::PfGeo<HD>;
+  constexpr int NS = attn::kPfStages, NT = HD / 16, NV = HD / 8;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* qs = smem;
+  uint8_t* ring = smem + Pg::QBYTES;
+  uint64_t* full = reinterpret_cast<uint64_t*>(ring + (size_t)NS * Pg::STAGE);
+  uint64_t* empty = full + NS;
+  uint64_t* qbar = empty + NS;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int h = blockIdx.y;
+
+  if (threadIdx.x == 0) {
+    asm volatile("prefetch.tensormap [%0];" ::"l"(&tmq) : "memory");
+    asm volatile("prefetch.tensormap [%0];" ::"l"(&tmk) : "memory");
+    for (int i = 0; i < NS; ++i) {
+      attn::mbar_init(&full[i], 1);
+      attn::mbar_init(&empty[i], 4);
+    }
+    attn::mbar_init(qbar, 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  __syncthreads();
+  pdl_wait();
+  pdl_trigger();
+  const int4 tile = tiles[blockIdx.x];  // (first row, rows, sequence slot, position of the first row)
+  const int row0 = tile.x, nq = tile.y, p0 = tile.w;
+  const int npg = (p0 + nq + 15) >> 4;  // pages up to the tile's last position
+
+  if (warp == 4) {
+    // ---------------- producer warp ----------------
+    if (lane == 0) {
+      uint64_t pol;
+      asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
+      attn::mbar_arrive_tx(qbar, Pg::QBYTES);
+      for (int j = 0; j < Pg::NX; ++j)
+        attn::tma_2d(attn::su32(qs + j * Pg::QSLICE), &tmq, qbar, h * HD + j * Pg::XW, row0, pol);
+      const int* bt = kv.bt + tile.z * kv.max_blocks;
+      const bool sl_ok = slot >= 0 && slot < kv.nsl;
+      if (!sl_ok) atomicOr(status, kStatusBadDepth);
+      for (int pg = 0; pg < npg; ++pg) {
+        const int s = pg % NS;
+        if (pg >= NS && !attn::mbar_wait(&empty[s], ((pg / NS) - 1) & 1)) {
+          atomicOr(status, kStatusTimeout);
+          break;
+        }
+        const int blk = bt[pg];
+        const bool ok = sl_ok && blk >= 0 && blk < kv.kv_blocks;
+        if (!ok && sl_ok) atomicOr(status, kStatusBadBlock);
+        attn::mbar_arrive_tx(&full[s], ok ? 2u * Pg::KV : 0u);
+        if (ok) {
+          // Page rows of head h at this slot: K then V (H * 16 rows later).
+          const int y = (int)((((long long)blk * kv.nsl + slot) * 2 * H + h) * 16);
+          const uint32_t st = attn::su32(ring + (size_t)s * Pg::STAGE);
+          for (int j = 0; j < Pg::NX; ++j) {
+            attn::tma_2d(st + j * Pg::PSLICE, &tmk, &full[s], j * Pg::XW, y, pol);
+            attn::tma_2d(st + Pg::KV + j * Pg::PSLICE, &tmk, &full[s], j * Pg::XW, y + H * 16, pol);
+          }
+        }
+      }
+    }
+    return;
+  }
+
+  // ---------------- consumer warps: query rows 16 * warp .. + 15 ----------------
+  const float scale = 1.4426950408889634f / sqrtf((float)HD);
+  const int g = lane >> 2, q4 = lane & 3;
+  const int qr0 = p0 + warp * 16 + g, qr1 = qr0 + 8;  // positions of this thread's two rows
+  if (!attn::mbar_wait(qbar, 0)) {
+    if (lane == 0) atomicOr(status, kStatusTimeout);
+    return;
+  }
+  uint32_t qa[NT][4];
+  {
+    const uint32_t qb = attn::su32(qs);
+    const int r = warp * 16 + (lane & 15);
+#pragma unroll
+    for (int t = 0; t < NT; ++t) {
+      const int j = (16 * t) / Pg::XW, c = ((16 * t) % Pg::XW) / 8 + (lane >> 4);
+      attn::ldsm_x4(attn::swz<Pg::SWB>(qb + j * Pg::QSLICE, r, c), qa[t]);
+    }
+  }
+  float o[NV][4];
+#pragma unroll
+  for (int v = 0; v < NV; ++v) o[v][0] = o[v][1] = o[v][2] = o[v][3] = 0.f;
+  float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+  const uint32_t rb = attn::su32(ring);
+  for (int pg = 0; pg < npg; ++pg) {
+    const int s = pg % NS;
+    if (!attn::mbar_wait(&full[s], (pg / NS) & 1)) {
+      if (lane == 0) atomicOr(status, kStatusTimeout);
+      return;
+    }
+    const uint32_t st = rb + (uint32_t)s * Pg::STAGE;
+    // S = Q . K^T for keys 16 pg .. + 15 (two n-tiles of 8 keys).
+    float sc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+    {
+      const int key = (lane & 7) + 8 * (lane >> 4);
+#pragma unroll
+      for (int t = 0; t < NT; ++t) {
+        const int j = (16 * t) / Pg::XW, c = ((16 * t) % Pg::XW) / 8 + ((lane >> 3) & 1);
+        uint32_t b[4];
+        attn::ldsm_x4(attn::swz<Pg::SWB>(st + j * Pg::PSLICE, key, c), b);
+        attn::mma_bf16(sc[0], qa[t], b[0], b[1]);
+        attn::mma_bf16(sc[1], qa[t], b[2], b[3]);
+      }
+    }
+    // Causal mask and scale: element (row, key) of the C fragments.
+    const int kb = pg * 16;
+    float sv[2][4];
+#pragma unroll
+    for (int u = 0; u < 2; ++u)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int key = kb + 8 * u + 2 * q4 + (e & 1);
+        const int qp = e < 2 ? qr0 : qr1;
+        sv[u][e] = key <= qp ? sc[u][e] * scale : -INFINITY;
+      }
+    float mx0 = fmaxf(fmaxf(sv[0][0], sv[0][1]), fmaxf(sv[1][0], sv[1][1]));
+    float mx1 = fmaxf(fmaxf(sv[0][2], sv[0][3]), fmaxf(sv[1][2], sv[1][3]));
+    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
+    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
+    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
+    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
+    const float n0 = fmaxf(m0, mx0), n1 = fmaxf(m1, mx1);
+    // Rows with no visible key so far keep zero weights (no -inf - -inf).
+    const float c0 = n0 == -INFINITY ? 1.f : exp2f(m0 - n0), c1 = n1 == -INFINITY ? 1.f : exp2f(m1 - n1);
+    float p[2][4];
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      p[u][0] = n0 == -INFINITY ? 0.f : exp2f(sv[u][0] - n0);
+      p[u][1] = n0 == -INFINITY ? 0.f : exp2f(sv[u][1] - n0);
+      p[u][2] = n1 == -INFINITY ? 0.f : exp2f(sv[u][2] - n1);
+      p[u][3] = n1 == -INFINITY ? 0.f : exp2f(sv[u][3] - n1);
+    }
+    l0 = l0 * c0 + p[0][0] + p[0][1] + p[1][0] + p[1][1];
+    l1 = l1 * c1 + p[0][2] + p[0][3] + p[1][2] + p[1][3];
+    m0 = n0;
+    m1 = n1;
+#pragma unroll
+    for (int v = 0; v < NV; ++v) {
+      o[v][0] *= c0;
+      o[v][1] *= c0;
+      o[v][2] *= c1;
+      o[v][3] *= c1;
+    }
+    // P as the A operand (rows x keys), hi and lo bf16 parts.
+    uint32_t ph[4], pl[4];
+    {
+      const float* f[4] = {&p[0][0], &p[0][2], &p[1][0], &p[1][2]};  // a0a1, a2a3, a4a5, a6a7
+#pragma unroll
+      for (int r = 0; r < 4; ++r) {
+        const float x0 = f[r][0], x1 = f[r][1];
+        const float e0 = __bfloat162float(__float2bfloat16_rn(x0)), e1 = __bfloat162float(__float2bfloat16_rn(x1));
+        ph[r] = attn::pack_bf16(e0, e1);
+        pl[r] = attn::pack_bf16(x0 - e0, x1 - e1);
+      }
+    }
+    // Keys past the tile's last position may hold NaN in the pool: their
+    // weights are 0, and their V values are zeroed in the B fragments.
+    const int kmax = p0 + nq - 1;
+    const bool tail = kb + 15 > kmax;
+    {
+      const int key = (lane & 7) + 8 * ((lane >> 3) & 1);
+#pragma unroll
+      for (int vp = 0; vp < NV / 2; ++vp) {
+        const int j = (16 * vp) / Pg::XW, c = ((16 * vp) % Pg::XW) / 8 + (lane >> 4);
+        uint32_t b[4];
+        attn::ldsm_x4_t(attn::swz<Pg::SWB>(st + Pg::KV + j * Pg::PSLICE, key, c), b);
+        if (tail) {
+          // b[0], b[2]: keys 2q4, 2q4+1; b[1], b[3]: keys 2q4+8, 2q4+9.
+          const int k0 = kb + 2 * q4;
+#pragma unroll
+          for (int r = 0; r < 4; ++r) {
+            const int kk = k0 + ((r & 1) ? 8 : 0);
+            uint32_t mk = 0;
+            if (kk <= kmax) mk |= 0x0000FFFFu;
+            if (kk + 1 <= kmax) mk |= 0xFFFF0000u;
+            b[r] &= mk;
+          }
+        }
+        attn::mma_bf16(o[2 * vp], ph, b[0], b[1]);
+        attn::mma_bf16(o[2 * vp], pl, b[0], b[1]);
+        attn::mma_bf16(o[2 * vp + 1], ph, b[2], b[3]);
+        attn::mma_bf16(o[2 * vp + 1], pl, b[2], b[3]);
+      }
+    }
+    __syncwarp();
+    if (lane == 0) attn::mbar_arrive(&empty[s]);
+  }
+  l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
+  l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
+  l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
+  l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
+  const int r0 = warp * 16 + g, r1 = r0 + 8;
+  const float i0 = 1.f / l0, i1 = 1.f / l1;
+#pragma unroll
+  for (int v = 0; v < NV; ++v) {
+    const int dcol = h * HD + 8 * v + 2 * q4;
+    if (r0 < nq)
+      *reinterpret_cast<__nv_bfloat162*>(O + (size_t)(row0 + r0) * kv.d + dcol) =
+          __floats2bfloat162_rn(o[v][0] * i0, o[v][1] * i0);
+    if (r1 < nq)
+      *reinterpret_cast<__nv_bfloat162*>(O + (size_t)(row0 + r1) * kv.d + dcol) =
+          __floats2bfloat162_rn(o[v][2] * i1, o[v][3] * i1);
+  }
+}
+
 // Merge split partials in split order: o = sum_s e^{m_s - m} acc_s / sum_s e^{m_s - m} l_s.
 template <typename T>
 __global__ void k_attn_combine(int rows, const int* __restrict__ mpos, int H, int HDv, int d, int split,
@@ -903,6 +1147,39 @@ static void attn_hd(cudaStream_t s, const T* Q, int rows, const int* mslot, cons
   if (max_splits > 1)
     count_launch(), launch_pdl(k_attn_combine<T>, dim3(rows * H), dim3(128), 0, s, rows, mpos, H, HD, kv.d, split,
                                max_splits, part_o, part_ml, O);
+}
+
+template <int HD>
+static bool prefill_hd(cudaStream_t s, const __nv_bfloat16* Q, int q_rows, const int4* tiles, int n_tiles, KvGeom kv,
+                       int slot, int H, __nv_bfloat16* O, int* status) {
+  using Pg = attn::PfGeo<HD>;
+  const uint64_t pool_rows = (uint64_t)kv.kv_blocks * kv.nsl * 2 * H * 16;
+  if (pool_rows + 16 >= (1ull << 31) || q_rows + attn::kPfRows >= (1 << 30)) return false;
+  const CUtensorMap* tk = tmap_bf16_2d(kv.pool, HD, pool_rows, (uint64_t)HD * 2, Pg::XW, 16, Pg::SWB);
+  const CUtensorMap* tq = tmap_bf16_2d(Q, (uint64_t)kv.d, q_rows, (uint64_t)kv.d * 2, Pg::XW, attn::kPfRows, Pg::SWB);
+  if (!tk || !tq) return false;
+  static bool set = false;
+  if (!set) {
+    if (cudaFuncSetAttribute(k_attn_prefill<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Pg::SMEM) !=
+        cudaSuccess)
+      return false;
+    set = true;
+  }
+  count_launch();
+  return launch_pdl(k_attn_prefill<HD>, dim3(n_tiles, H), dim3(5 * 32), Pg::SMEM, s, *tq, *tk, tiles, kv, slot, H, O,
+                    status) == cudaSuccess;
+}
+
+bool launch_prefill_attention(cudaStream_t s, const __nv_bfloat16* Q, int q_rows, const int4* tiles, int n_tiles,
+                              KvGeom kv, int slot, int H, int hd, __nv_bfloat16* O, int* status) {
+  if (n_tiles <= 0) return true;
+  switch (hd) {
+    case 32: return prefill_hd<32>(s, Q, q_rows, tiles, n_tiles, kv, slot, H, O, status);
+    case 64: return prefill_hd<64>(s, Q, q_rows, tiles, n_tiles, kv, slot, H, O, status);
+    case 96: return prefill_hd<96>(s, Q, q_rows, tiles, n_tiles, kv, slot, H, O, status);
+    case 128: return prefill_hd<128>(s, Q, q_rows, tiles, n_tiles, kv, slot, H, O, status);
+    default: return false;
+  }
 }
 
 template <typename T>

@@ -35,7 +35,7 @@ struct Layout {
   size_t pool, etab, bt, out_tok, ftok, fexit, out_depth, gtrace, ltrace, htrace, estore, rope;
   size_t rows[5], meta[5];  // X, Xc, Pb, Cb, Tp
   size_t pend_new, ring, status;
-  size_t Xp, Ep, rslot, rpos, rtok, done_idx, Cp, Cp_meta;
+  size_t Xp, Ep, rslot, rpos, rtok, ptiles, done_idx, Cp, Cp_meta;
   size_t lslot, lt, lpos;
   size_t A, QKV, Q, O, Mid, logits, part_o, part_ml, gpart;
   size_t gpart_floats;
@@ -86,6 +86,7 @@ static bool plan_layout(const cdb_model_desc* m, const cdb_sched_cfg* c, Layout*
   L->rslot = take(M * 4);
   L->rpos = take(M * 4);
   L->rtok = take(M * 4);
+  L->ptiles = take(((size_t)M / kPrefillTileRows + W + 2) * 16);
   L->done_idx = take(W * 4);
   L->Cp = take(W * d * 4);
   L->Cp_meta = take(W * 5 * 4);
@@ -166,7 +167,7 @@ struct cdb_ctx {
   struct Stat {
     int64_t launches = 0;
     double ms = 0, bytes = 0, flops = 0;
-  } stats[3];
+  } stats[5];
 };
 
 namespace cdb {
@@ -232,7 +233,7 @@ static int upload(cdb_ctx* x, void* dst, const void* src, size_t n) {
   return CDB_OK;
 }
 
-static const char* kProfNames[3] = {"attention", "gemm", "prefill_attention"};
+static const char* kProfNames[5] = {"attention", "gemm", "prefill_attention", "rowwise", "prefill_gemm"};
 
 static cudaEvent_t pool_event(cdb_ctx* x) {
   if (!x->ev_pool.empty()) {
@@ -314,7 +315,7 @@ class GpuExecutor : public Executor {
            int ldc, bool parts) {
     cdb_ctx* x = x_;
     const double es = sizeof(T), nw = W2 ? 2.0 : 1.0;
-    const int h = prof_begin(x, 1);
+    const int h = prof_begin(x, decode_tiles_ ? 1 : 4);
     int ns = -1;
     if (sizeof(T) == 2)
       ns = launch_gemm_tc(x->cs, epi, (const __nv_bfloat16*)A, lda, x->L.R, (const __nv_bfloat16*)W,
@@ -342,8 +343,10 @@ class GpuExecutor : public Executor {
   void norm(float* X, const void* g, T* A, int rows) {
     cdb_ctx* x = x_;
     if (pend_.ns && (pend_.X != X || pend_.rows != rows)) flush<T>();
+    const int h = prof_begin(x, 3);
     launch_rmsnorm<T>(x->cs, X, (const T*)g, A, rows, x->m.d_model, x->m.rms_eps, x->m.d_model,
                       at<float>(x, x->L.gpart), pend_.ns, pend_.mode);
+    prof_end(x, h, (double)rows * x->m.d_model * ((pend_.ns ? 8.0 : 4.0) + sizeof(T)), 0.0);
     pend_ = Pending();
   }
 
@@ -351,8 +354,10 @@ class GpuExecutor : public Executor {
   void flush() {
     if (!pend_.ns) return;
     cdb_ctx* x = x_;
+    const int h = prof_begin(x, 3);
     launch_fold(x->cs, at<float>(x, x->L.gpart), pend_.ns, pend_.rows, x->m.d_model, pend_.X, x->m.d_model,
                 pend_.mode);
+    prof_end(x, h, (double)pend_.rows * x->m.d_model * 8.0, 0.0);
     pend_ = Pending();
   }
 
@@ -375,22 +380,33 @@ class GpuExecutor : public Executor {
     decode_tiles_ = decode;
     norm<T>(X, lw.attn_norm, A, rows);
     int ns = gemm<T>(kEpiStore, A, d, lw.wqkv, nullptr, 3 * d, d, rows, QKV, nullptr, 3 * d, true);
+    int hr = prof_begin(x, 3);
     launch_rope_kv<T>(s, ns ? GP : QKV, ns, rows, mslot, mpos, mdepth, depth_uniform, slot_base, clamp, Q, kv, H, hd,
                       at<float2>(x, L.rope), st);
+    prof_end(x, hr, (double)rows * d * (12.0 + 3.0 * es), 0.0);  // q, k, v in; q, K, V rows out
     const int split = decode ? L.split : (1 << 30);
     const int msp = decode ? L.max_splits : 1;
     const int ha = prof_begin(x, decode ? 0 : 2);
     // Exit gaps are filled at compaction, so every key of a row is read from
-    // the row's own slot.
-    launch_attention<T>(s, Q, rows, mslot, mpos, mdepth, depth_uniform, kv, slot_base, clamp, H, hd, split, msp,
-                        O, at<float>(x, L.part_o), at<float>(x, L.part_ml), st, true);
+    // the row's own slot.  Prefill chunks go through query tiles.
+    bool done = false;
+    if (!decode && sizeof(T) == 2 && pf_tiles_ > 0 && depth_uniform > 0)
+      done = launch_prefill_attention(s, (const __nv_bfloat16*)Q, L.R, at<int4>(x, L.ptiles), pf_tiles_, kv,
+                                      slot_base + (clamp ? depth_uniform - 1 : 0), H, hd, (__nv_bfloat16*)O, st);
+    if (!done)
+      launch_attention<T>(s, Q, rows, mslot, mpos, mdepth, depth_uniform, kv, slot_base, clamp, H, hd, split, msp,
+                          O, at<float>(x, L.part_o), at<float>(x, L.part_ml), st, true);
     // Each key row (K and V, d elements each) is read once; q in, o out.
     prof_end(x, ha, sumL * 2.0 * d * es + 2.0 * rows * d * es, 4.0 * d * sumL);
     ns = gemm<T>(kEpiResid, O, d, lw.wo, nullptr, d, d, rows, X, nullptr, d, true);
     if (ns) pend_ = Pending{X, rows, ns, 1};
     norm<T>(X, lw.mlp_norm, A, rows);
     ns = gemm<T>(kEpiSwiglu, A, d, lw.wg, lw.wu, f, d, rows, nullptr, Mid, f, true);
-    if (ns) launch_swiglu_combine<T>(s, GP, ns, rows, f, Mid);
+    if (ns) {
+      hr = prof_begin(x, 3);
+      launch_swiglu_combine<T>(s, GP, ns, rows, f, Mid);
+      prof_end(x, hr, (double)rows * f * (8.0 + es), 0.0);
+    }
     ns = gemm<T>(kEpiResid, Mid, f, lw.wd, nullptr, d, f, rows, X, nullptr, d, true);
     if (ns) pend_ = Pending{X, rows, ns, 1};
     return CDB_OK;
@@ -449,6 +465,17 @@ class GpuExecutor : public Executor {
     if ((rc = upload(x, rslot, a.data(), n * 4)) < 0) return rc;
     if ((rc = upload(x, rpos, b.data(), n * 4)) < 0) return rc;
     if ((rc = upload(x, rtok, c.data(), n * 4)) < 0) return rc;
+    // Query tiles for the prefill attention: runs of consecutive positions of
+    // one sequence, at most kPrefillTileRows rows each.
+    std::vector<int4> tiles;
+    for (int i = 0; i < n;) {
+      int j = i + 1;
+      while (j < n && j - i < kPrefillTileRows && a[j] == a[i] && b[j] == b[i] + (j - i)) ++j;
+      tiles.push_back(make_int4(i, j - i, a[i], b[i]));
+      i = j;
+    }
+    if ((rc = upload(x, at<int4>(x, L.ptiles), tiles.data(), tiles.size() * sizeof(int4))) < 0) return rc;
+    pf_tiles_ = (int)tiles.size();
     float* Xp = at<float>(x, L.Xp);
     launch_embed_prefill<T>(x->cs, (const T*)x->embed, d, x->m.vocab, rslot, rpos, rtok, n, Xp, geom(), x->m.r_max,
                             at<int>(x, L.status));
@@ -478,6 +505,7 @@ class GpuExecutor : public Executor {
       launch_gather_rows(x->cs, Xp, at<int>(x, L.done_idx), rslot, rpos, nd, Cp, cm, d);
       head<T>(Cp, nd, cm);
     }
+    pf_tiles_ = 0;
     CK(cudaGetLastError());
     return CDB_OK;
   }
@@ -675,6 +703,7 @@ class GpuExecutor : public Executor {
  private:
   cdb_ctx* x_;
   bool decode_tiles_ = true;  // GEMM tiling for the rows being processed
+  int pf_tiles_ = 0;          // query tiles of the prefill chunk being processed
 };
 
 static int check_status(cdb_ctx* x) {
@@ -933,7 +962,7 @@ int cdb_profile_read(cdb_ctx* x, cdb_kernel_stat* out, int cap, int* n_out) {
   if (e != cudaSuccess) return cuda_fail(x, e, "cudaStreamSynchronize");
   prof_collect(x);
   int n = 0;
-  for (int c = 0; c < 3 && n < cap; ++c) {
+  for (int c = 0; c < 5 && n < cap; ++c) {
     std::memset(&out[n], 0, sizeof(out[n]));
     std::strncpy(out[n].name, kProfNames[c], sizeof(out[n].name) - 1);
     out[n].launches = x->stats[c].launches;
@@ -1047,6 +1076,46 @@ static int test_attention(const void* q, int rows, const int32_t* slot, const in
   else
     launch_attention<float>(s, (const float*)q, rows, slot, pos, depth, 0, g, slot_base, 1, n_heads, head_dim,
                             split, (int)ms, (float*)out, part_o, part_ml, status, uniform);
+  if (cudaGetLastError() != cudaSuccess || cudaStreamSynchronize(s) != cudaSuccess) return CDB_ERR_CUDA;
+  int st = 0;
+  if (cudaMemcpy(&st, status, 4, cudaMemcpyDeviceToHost) != cudaSuccess) return CDB_ERR_CUDA;
+  return st ? CDB_ERR_DEVICE_BOUNDS : CDB_OK;
+}
+
+int cdb_test_attention_prefill(const void* q, int rows, const int32_t* row_slot, const int32_t* row_pos,
+                               const void* kv_pool, const int32_t* block_table, int max_blocks, int kv_blocks,
+                               int n_kv_slots, int slot, int n_heads, int head_dim, void* out, void* scratch,
+                               size_t scratch_bytes, void* stream) {
+  if (!q || rows < 1 || !row_slot || !row_pos || !kv_pool || !block_table || max_blocks < 1 || kv_blocks < 1 ||
+      n_kv_slots < 1 || slot < 0 || slot >= n_kv_slots || n_heads < 1 || !out || !scratch)
+    return CDB_ERR_ARG;
+  std::vector<int4> tiles;
+  for (int i = 0; i < rows;) {
+    if (row_slot[i] < 0 || row_pos[i] < 0 || row_pos[i] >= max_blocks * 16) return CDB_ERR_ARG;
+    int j = i + 1;
+    while (j < rows && j - i < kPrefillTileRows && row_slot[j] == row_slot[i] && row_pos[j] == row_pos[i] + (j - i))
+      ++j;
+    tiles.push_back(make_int4(i, j - i, row_slot[i], row_pos[i]));
+    i = j;
+  }
+  if (scratch_bytes < 256 + tiles.size() * sizeof(int4)) return CDB_ERR_ARG;
+  cudaStream_t s = (cudaStream_t)stream;
+  int* status = (int*)scratch;
+  int4* dt = (int4*)((char*)scratch + 256);
+  if (cudaMemsetAsync(status, 0, kStatusBytes, s) != cudaSuccess ||
+      cudaMemcpyAsync(dt, tiles.data(), tiles.size() * sizeof(int4), cudaMemcpyHostToDevice, s) != cudaSuccess)
+    return CDB_ERR_CUDA;
+  KvGeom g;
+  g.pool = const_cast<void*>(kv_pool);
+  g.bt = block_table;
+  g.etab = nullptr;
+  g.max_blocks = max_blocks;
+  g.kv_blocks = kv_blocks;
+  g.nsl = n_kv_slots;
+  g.d = n_heads * head_dim;
+  if (!launch_prefill_attention(s, (const __nv_bfloat16*)q, rows, dt, (int)tiles.size(), g, slot, n_heads, head_dim,
+                                (__nv_bfloat16*)out, status))
+    return CDB_ERR_ARG;
   if (cudaGetLastError() != cudaSuccess || cudaStreamSynchronize(s) != cudaSuccess) return CDB_ERR_CUDA;
   int st = 0;
   if (cudaMemcpy(&st, status, 4, cudaMemcpyDeviceToHost) != cudaSuccess) return CDB_ERR_CUDA;

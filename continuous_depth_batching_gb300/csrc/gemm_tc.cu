@@ -21,6 +21,7 @@
 // records kStatusTimeout, skips the epilogue, releases TMEM and returns.
 #include <cuda.h>
 
+#include <cstdlib>
 #include <unordered_map>
 
 #include "common.cuh"
@@ -405,13 +406,24 @@ static int sm_count() {
 // Split count of a decode GEMM: as many CTAs as two per SM hold, at least
 // four 64-element K slabs per split, at most kGemmMaxSplits.  Depends only on
 // the weight shape (and the device), never on the number of rows.
+// CDB_GEMM_SPLIT_CAP (1..kGemmMaxSplits) lowers the cap, for tuning.
+static int split_cap() {
+  static int cap = 0;
+  if (!cap) {
+    const char* e = std::getenv("CDB_GEMM_SPLIT_CAP");
+    const int v = e ? std::atoi(e) : 0;
+    cap = v >= 1 && v <= kGemmMaxSplits ? v : kGemmMaxSplits;
+  }
+  return cap;
+}
+
 int gemm_tc_splits(int N, int K, bool decode) {
   if (!decode) return 1;
   const int tiles = (N + tc::BM - 1) / tc::BM;
   const int KT = (K + tc::BK - 1) / tc::BK;
   int s = 2 * sm_count() / tiles;
   if (s > KT / 4) s = KT / 4;
-  if (s > kGemmMaxSplits) s = kGemmMaxSplits;
+  if (s > split_cap()) s = split_cap();
   return s < 1 ? 1 : s;
 }
 

@@ -121,6 +121,15 @@ void launch_attention(cudaStream_t s, const T* Q, int rows, const int* mslot, co
                       int clamp, int H, int hd, int split, int max_splits, T* O,
                       float* part_o, float* part_ml, int* status, bool uniform);
 
+// Causal prefill attention over query tiles (bf16, head_dim 32/64/96/128):
+// tiles[t] = (first row, rows <= 64, sequence slot, position of the first
+// row); rows of a tile are consecutive positions of one sequence, and every
+// key is read from KV slot `slot`.  Q and O are [q_rows][d].  Returns false
+// (nothing launched) for shapes it does not cover.
+constexpr int kPrefillTileRows = 64;
+bool launch_prefill_attention(cudaStream_t s, const __nv_bfloat16* Q, int q_rows, const int4* tiles, int n_tiles,
+                              KvGeom kv, int slot, int H, int hd, __nv_bfloat16* O, int* status);
+
 // ---- GEMM (gemm_simt.cu) ----
 enum GemmEpi { kEpiStore = 0, kEpiResid = 1, kEpiSwiglu = 2 };
 // C = A[rows, K] . W[N, K]^T with fp32 accumulation.  kEpiStore: Cf[r][c] = acc;

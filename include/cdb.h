@@ -195,7 +195,10 @@ const char *cdb_last_error(const cdb_ctx *ctx);
  * the algorithmic bytes and FLOPs of those launches (bytes each launch must
  * move at least once: weights, KV rows read, activations in and out), and
  * resets the counters.  Classes: "attention" (split-KV decode attention plus
- * its combine), "gemm" (all projections), "prefill_attention". */
+ * its combine), "gemm" (projections of decode-sized batches), "prefill_gemm"
+ * (projections of prefill chunks), "prefill_attention", "rowwise"
+ * (RMSNorm with the fold of pending split-K partials, RoPE + KV write, the
+ * SwiGLU combine, the residual fold). */
 typedef struct {
   char name[32];
   int64_t launches;

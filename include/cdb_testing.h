@@ -72,6 +72,20 @@ int cdb_test_attention_uniform(const void *q, int rows, const int32_t *slot, con
                                int head_dim, int dtype, int split, int max_ctx, void *out, void *scratch,
                                size_t scratch_bytes, void *stream);
 
+/* The causal prefill attention of a prompt chunk (bf16 only, head_dim 32, 64,
+ * 96 or 128): row i (query q[i], sequence slot row_slot[i], position
+ * row_pos[i]) attends to positions 0..row_pos[i] of its sequence, every key
+ * read from KV slot `slot`.  Rows of one sequence must come as runs of
+ * consecutive positions (how the scheduler packs a chunk); the library cuts
+ * them into query tiles of up to 64 rows.  row_slot and row_pos are HOST
+ * arrays; q, kv_pool (layout of cdb_test_attention), block_table and out are
+ * device pointers.  scratch: device memory of at least 256 + 16 * (rows + 1)
+ * bytes.  Returns CDB_ERR_ARG for an unsupported shape (nothing launched). */
+int cdb_test_attention_prefill(const void *q, int rows, const int32_t *row_slot, const int32_t *row_pos,
+                               const void *kv_pool, const int32_t *block_table, int max_blocks, int kv_blocks,
+                               int n_kv_slots, int slot, int n_heads, int head_dim, void *out, void *scratch,
+                               size_t scratch_bytes, void *stream);
+
 /* The same decode attention for callers that must not allocate device memory
  * (for example a plugin whose host program's memory manager owns all device
  * memory, or a latency-critical path that cannot take an allocation's implicit

@@ -201,3 +201,54 @@ def test_uniform_equals_clamped_read_after_gap_fill(L):
     err_c = (ref_clamped.double().cpu() - ref).abs().max().item()
     assert torch_finite(out)
     assert err_u <= 1e-2 * (1 + ref.abs().max().item()), (err_u, err_c)
+
+
+@pytest.mark.parametrize("H,hd", [(16, 128), (5, 96), (3, 64), (2, 32)])
+def test_prefill_tiles_match_causal_reference(L, H, hd):
+    """Causal prefill attention over query tiles against a float64 reference.
+    Three sequences: a fresh prompt, a continuing chunk starting mid-page,
+    and one short enough to fit in a single partial tile; positions past each
+    sequence's last row hold NaN in the pool."""
+    import torch
+    L.cdb_test_attention_prefill.argtypes = ([C.c_void_p, C.c_int, C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p] +
+                                             [C.c_int] * 6 + [C.c_void_p, C.c_void_p, C.c_size_t, C.c_void_p])
+    rng = np.random.default_rng(17)
+    d = H * hd
+    nsl, slot = 6, 4
+    runs = [(0, 0, 150), (1, 37, 170), (2, 0, 9)]  # (sequence slot, first position, rows)
+    max_blocks = 16
+    kv_blocks = 3 * max_blocks + 5
+    perm = rng.permutation(kv_blocks)[: 3 * max_blocks].reshape(3, max_blocks)
+    bt = torch.from_numpy(perm.astype(np.int32))
+    pool = torch.from_numpy(rng.standard_normal((kv_blocks, nsl, 2, H, 16, hd)))
+    last = {sq: p0 + n - 1 for sq, p0, n in runs}
+    for sq in range(3):
+        for p in range(last[sq] + 1, max_blocks * 16):
+            pool[perm[sq, p // 16], :, :, :, p % 16, :] = float("nan")
+    row_slot = np.concatenate([np.full(n, sq, np.int32) for sq, p0, n in runs])
+    row_pos = np.concatenate([np.arange(p0, p0 + n, dtype=np.int32) for sq, p0, n in runs])
+    rows = len(row_pos)
+    q = torch.from_numpy(rng.standard_normal((rows, d))).to(torch.bfloat16)
+    poolb = pool.to(torch.bfloat16)
+    ref = torch.zeros(rows, d, dtype=torch.float64)
+    pd, qd = poolb.double(), q.double()
+    for i in range(rows):
+        sq, p = int(row_slot[i]), int(row_pos[i])
+        j = torch.arange(p + 1)
+        blk = bt[sq][j // 16].long()
+        K = pd[blk, slot, 0, :, j % 16]
+        V = pd[blk, slot, 1, :, j % 16]
+        for h in range(H):
+            w = torch.softmax(K[:, h] @ qd[i, h * hd:(h + 1) * hd] / np.sqrt(hd), 0)
+            ref[i, h * hd:(h + 1) * hd] = w @ V[:, h]
+    out = torch.zeros(rows, d, dtype=torch.bfloat16, device="cuda")
+    scratch = torch.zeros(256 + 16 * (rows + 1), dtype=torch.uint8, device="cuda")
+    dq, dp, dbt = q.cuda(), poolb.cuda(), bt.cuda()
+    rc = L.cdb_test_attention_prefill(dq.data_ptr(), rows, row_slot.ctypes.data, row_pos.ctypes.data, dp.data_ptr(),
+                                      dbt.data_ptr(), max_blocks, kv_blocks, nsl, slot, H, hd, out.data_ptr(),
+                                      scratch.data_ptr(), scratch.numel(), None)
+    assert rc == 0, rc
+    o = out.double().cpu()
+    assert torch_finite(o)
+    err = (o - ref).abs()
+    assert (err <= 1e-2 * (1 + ref.abs())).all().item(), err.max().item()
