@@ -57,7 +57,7 @@ def attention_traffic_ratio():
     """DRAM traffic / algorithmic bytes of the decode-attention kernel from the
     committed ncu summary, if it was captured from the current source."""
     import hashlib
-    prof = os.path.join(ROOT, "profiles", "k_attn_ouro_decode.md")
+    prof = os.path.join(ROOT, "profiles", "k_attn_tma_ouro_decode.md")
     src = os.path.join(ROOT, "continuous_depth_batching_gb300", "csrc", "attention.cu")
     if not (os.path.exists(prof) and os.path.exists(src)):
         return None

@@ -59,8 +59,9 @@ def main():
                 done += 1
 
     # Per decode step (one decode-attention launch per step with one layer):
-    # the attention launch's index among all attention launches and its
-    # algorithmic bytes, so an ncu capture (-k k_attn -s INDEX) can be matched.
+    # the launch's index among the decode-attention launches (prefill chunks
+    # use their own kernel) and its algorithmic bytes, so an ncu capture
+    # (-k k_attn_tma -s INDEX) can be matched.
     eng.profile_enable(True)
     n_attn = 0
     per_step = []
@@ -68,7 +69,6 @@ def main():
     for i in range(args.warmup + args.steps):
         advance(1)
         st = eng.profile_read()
-        n_attn += st["prefill_attention"]["launches"]
         if st["attention"]["launches"]:
             per_step.append({"step": i, "attn_index": n_attn, "attn_launches": st["attention"]["launches"],
                              "attn_bytes": st["attention"]["bytes"], "attn_ms": st["attention"]["ms"]})
