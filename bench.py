@@ -72,6 +72,14 @@ def attention_traffic_ratio():
     return float(kv["traffic_ratio_dram_over_algorithmic"])
 
 
+def weight_gb(shape):
+    """Bytes of weights one core step streams (every core layer, plus the adapter), in GB."""
+    d, f = shape.d_model, shape.ffn
+    per_layer = 4 * d * d + 3 * d * f
+    n = shape.n_core * per_layer + (2 * d * d if shape.has_adapter else 0)
+    return n * shape.elem_bytes / 1e9
+
+
 def peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -313,7 +321,7 @@ def run_ours(args):
     traffic = ratio * st["bytes"] / st["launches"] if ratio is not None else None
     roof.update({"kernel": dom, "traffic": traffic, "peak_source": src,
                  "traffic_source": ("ncu dram__bytes_read+write of one captured launch over its algorithmic "
-                                    "bytes (profiles/k_attn_ouro_decode.md), times this window's algorithmic "
+                                    "bytes (profiles/k_attn_tma_ouro_decode.md), times this window's algorithmic "
                                     "bytes per launch") if traffic is not None else None,
                  "window": f"{pcores} core steps right after the timed ones, CUDA events on the compute stream",
                  "share_of_step": st["ms"] / prof_ms,
@@ -393,7 +401,8 @@ def run_ours(args):
         line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
                 "warmup": args.warmup, "ms_per_step": ms / max(cores, 1), "higher_is_better": True,
                 "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-                "config": _config(wl, shape, args.mode, "inputs larger than L2 (2.5 GB of weights per step)"),
+                "config": _config(wl, shape, args.mode,
+                                  f"inputs larger than L2 ({weight_gb(shape):.1f} GB of weights per step)"),
                 "roofline": roof, "cpu_baseline": cpu, "e2e": e2e, "modes": modes, "gpu_launches": launches,
                 "clocks": clocks, "tokens_in_window": tot_toks, "core_steps": cores}
         print(json.dumps(line), flush=True)

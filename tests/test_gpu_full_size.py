@@ -1,4 +1,4 @@
-"""Parity at full size, in the launch configuration bench.py times.
+"""Parity at full size, in the launch configuration bench.py times, and at Huginn's widths.
 
 The Ouro-shaped model (1.4 G parameters, bf16) decodes the whole 256-request
 workload in refill mode with W = 64, M = 8192, K = 1.  The CPU oracle decodes
@@ -89,3 +89,53 @@ def test_ouro_full_workload_matches_oracle_sample():
         assert e_l.max() <= LOGIT_TOL, e_l.max()
         assert max(per_t) <= HIDDEN_TOL, per_t
         assert e_z.max() <= GATE_TOL, e_z.max()
+
+
+def test_huginn_widths_match_oracle():
+    """Huginn's layer widths (d 5280, 55 heads x 96, SwiGLU 17920, adapter,
+    65536-token vocabulary) with one prelude, one core and one coda layer at
+    r_max 4, so the oracle decodes every sequence.  Exercises the head-dim-96
+    kernels (64-byte swizzle), a partial head group (55 = 13 x 4 + 3), the
+    adapter's split-K fold, single-slot prelude/coda layers and chunked
+    prefill across sequences; W = 4 forces refills."""
+    import dataclasses
+
+    from continuous_depth_batching_gb300 import binding
+    from continuous_depth_batching_gb300.build import build
+    from oracle.model import OracleModel, decode_sequence
+
+    build()
+    shape = dataclasses.replace(model_shape("huginn"), name="huginn_widths", n_prelude=1, n_core=1, n_coda=1,
+                                r_max=4, r_min=2)
+    wts = make_weights(shape)
+    rng = np.random.default_rng(41)
+    lens = [17, 20, 23, 26, 29, 32]
+    gen = 5
+    reqs = [dict(seq_id=i, prompt=rng.integers(0, shape.vocab, n).astype(np.int32), gen_len=gen)
+            for i, n in enumerate(lens)]
+    om = OracleModel(shape, wts)
+    ref = {r["seq_id"]: decode_sequence(om, r["prompt"], gen, keep_logits=gen, near_tol=GATE_BAND) for r in reqs}
+    del om
+    eng = binding.Engine(shape, binding.device_weights(shape, wts), mode="refill", W=4, M=48, K=2,
+                         max_ctx=48, max_new_cap=gen, trace_tokens=gen, trace_gate=True)
+    for r in reqs:
+        fe, ft = force_tables(ref[r["seq_id"]], gap_band=GAP_BAND)
+        eng.admit(r["seq_id"], r["prompt"], gen, fe, ft)
+    eng.run()
+    out = {o["seq_id"]: o for o in eng.drain(cap=len(reqs))}
+    eng.close()
+    assert sorted(out) == [r["seq_id"] for r in reqs]
+    depths = []
+    for sid, tr in ref.items():
+        o = out[sid]
+        assert list(o["tokens"]) == tr.tokens
+        assert list(o["exit_depths"]) == tr.exit_depths
+        depths += tr.exit_depths
+        lg, hd = np.array(tr.logits), np.array(tr.hidden)
+        assert np.abs(o["logits"] - lg).max() <= LOGIT_TOL
+        per_t = [float(np.abs(o["hidden"][t] - hd[t]).max() / np.sqrt((hd[t] ** 2).mean())) for t in range(gen)]
+        assert max(per_t) <= HIDDEN_TOL, per_t
+        z_ref = np.concatenate([np.array(z) for z in tr.gate_logits if z])
+        z_got = np.concatenate([o["gate_logits"][t, : len(z)] for t, z in enumerate(tr.gate_logits) if z])
+        assert np.abs(z_got - z_ref).max() <= GATE_TOL
+    print("exit depths seen", sorted(set(depths)))
