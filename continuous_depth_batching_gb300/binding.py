@@ -159,6 +159,11 @@ def model_desc(shape) -> ModelDesc:
                      math.log(q / (1.0 - q)), shape.gate_bias)
 
 
+def kv_bytes_per_token(shape) -> int:
+    """KV-cache bytes one token occupies for this model (every layer and loop step)."""
+    return int(lib().cdb_kv_bytes_per_token(C.byref(model_desc(shape))))
+
+
 def device_weights(shape, weights: dict, device="cuda") -> dict:
     """Move host weights (float32 or uint16 bf16 bit patterns) to device tensors."""
     import torch

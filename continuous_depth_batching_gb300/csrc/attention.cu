@@ -580,7 +580,7 @@ struct TmaGeo {
   static constexpr int KREG = NX * SLICE;               // K (or V) of one page
   static constexpr int QB = kWarps * HD * 2;            // q rows of the item
   static constexpr int STAGE = (2 * KREG + QB + 1023) / 1024 * 1024;
-  static constexpr int NS = 3;
+  static constexpr int NS = 2;
   static constexpr size_t SMEM = 1024 + (size_t)NS * STAGE + NS * (2 * 8 + sizeof(StageMeta));
   static_assert(HD % 32 == 0, "head dim");
 };

@@ -403,9 +403,11 @@ static int sm_count() {
   return n;
 }
 
-// Split count of a decode GEMM: as many CTAs as two per SM hold, at least
-// four 64-element K slabs per split, at most kGemmMaxSplits.  Depends only on
-// the weight shape (and the device), never on the number of rows.
+// Split count of a decode GEMM: at least four 64-element K slabs per split,
+// at most kGemmMaxSplits, and about two CTAs per SM for narrow weights (few
+// 128-row tiles) but one per SM for wide ones (at least 32 tiles), whose
+// consumers then fold half as many partials.  Depends only on the weight
+// shape (and the device), never on the number of rows.
 // CDB_GEMM_SPLIT_CAP (1..kGemmMaxSplits) lowers the cap, for tuning.
 static int split_cap() {
   static int cap = 0;
@@ -421,7 +423,7 @@ int gemm_tc_splits(int N, int K, bool decode) {
   if (!decode) return 1;
   const int tiles = (N + tc::BM - 1) / tc::BM;
   const int KT = (K + tc::BK - 1) / tc::BK;
-  int s = 2 * sm_count() / tiles;
+  int s = (tiles >= 32 ? 1 : 2) * sm_count() / tiles;
   if (s > KT / 4) s = KT / 4;
   if (s > split_cap()) s = split_cap();
   return s < 1 ? 1 : s;
