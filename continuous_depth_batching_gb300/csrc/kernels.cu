@@ -234,6 +234,25 @@ __global__ void k_concat(const float* __restrict__ E, int e_per_slot, const int*
 
 // Row i at position p and loop step r writes K,V into slot slot_base + r-1
 // (core layers, clamp=1) or slot_base (prelude / coda layers).
+template <typename T>
+__device__ __forceinline__ void store4(T* p, const T (&v)[4]);
+template <>
+__device__ __forceinline__ void store4<float>(float* p, const float (&v)[4]) {
+  *reinterpret_cast<float4*>(p) = make_float4(v[0], v[1], v[2], v[3]);
+}
+template <>
+__device__ __forceinline__ void store4<__nv_bfloat16>(__nv_bfloat16* p, const __nv_bfloat16 (&v)[4]) {
+  __nv_bfloat162 lo, hi;
+  lo.x = v[0];
+  lo.y = v[1];
+  hi.x = v[2];
+  hi.y = v[3];
+  uint2 u;
+  u.x = *reinterpret_cast<const uint32_t*>(&lo);
+  u.y = *reinterpret_cast<const uint32_t*>(&hi);
+  *reinterpret_cast<uint2*>(p) = u;
+}
+
 // QKV arrives as split-K partials (qkv.ns >= 1; one partial is the plain
 // GEMM output).
 template <typename T>
@@ -273,16 +292,24 @@ __global__ void k_rope_kv(Parts qkv, int rows, const int* __restrict__ mslot,
     const float ka_[4] = {ka.x, ka.y, ka.z, ka.w}, kb_[4] = {kb.x, kb.y, kb.z, kb.w};
     const float va_[4] = {va.x, va.y, va.z, va.w}, vb_[4] = {vb.x, vb.y, vb.z, vb.w};
     const size_t kofs = (size_t)h * 16 * hd + j0;
+    T qo[2][4], ko[2][4], vo[2][4];
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
-      const float c = cs[j0 + e].x, s = cs[j0 + e].y;
-      Q[(size_t)i * d + a + e] = from_f<T>(qa_[e] * c - qb_[e] * s);
-      Q[(size_t)i * d + b + e] = from_f<T>(qb_[e] * c + qa_[e] * s);
-      kdst[kofs + e] = from_f<T>(ka_[e] * c - kb_[e] * s);
-      kdst[kofs + half + e] = from_f<T>(kb_[e] * c + ka_[e] * s);
-      vdst[kofs + e] = from_f<T>(va_[e]);
-      vdst[kofs + half + e] = from_f<T>(vb_[e]);
+      const float2 r = cs[j0 + e];
+      qo[0][e] = from_f<T>(qa_[e] * r.x - qb_[e] * r.y);
+      qo[1][e] = from_f<T>(qb_[e] * r.x + qa_[e] * r.y);
+      ko[0][e] = from_f<T>(ka_[e] * r.x - kb_[e] * r.y);
+      ko[1][e] = from_f<T>(kb_[e] * r.x + ka_[e] * r.y);
+      vo[0][e] = from_f<T>(va_[e]);
+      vo[1][e] = from_f<T>(vb_[e]);
     }
+    // Four consecutive elements per store (8 bytes for bf16, 16 for fp32).
+    store4(Q + (size_t)i * d + a, qo[0]);
+    store4(Q + (size_t)i * d + b, qo[1]);
+    store4(kdst + kofs, ko[0]);
+    store4(kdst + kofs + half, ko[1]);
+    store4(vdst + kofs, vo[0]);
+    store4(vdst + kofs + half, vo[1]);
   }
 }
 
@@ -576,9 +603,9 @@ void launch_rope_kv(cudaStream_t s, const float* QKV, int ns, int rows, const in
                     int hd, const float2* rope, int* status) {
   Parts qkv{QKV, ns < 1 ? 1 : ns, (size_t)rows * 3 * kv.d, 3 * kv.d};
   const int quads = H * (hd / 2) / 4;
-  const int gy = (quads + 127) / 128;
+  const int gy = (quads + 63) / 64;
   if (rows > 0)
-    count_launch(), launch_pdl(k_rope_kv<T>, dim3(rows, gy), dim3(128), 0, s, qkv, rows, mslot, mpos, mdepth, depth_uniform, slot_base, clamp, Q,
+    count_launch(), launch_pdl(k_rope_kv<T>, dim3(rows, gy), dim3(64), 0, s, qkv, rows, mslot, mpos, mdepth, depth_uniform, slot_base, clamp, Q,
                                       kv, H, hd, rope, status);
 }
 template <typename T>
