@@ -510,13 +510,25 @@ __global__ void k_argmax(const float* __restrict__ logits, int rows, int V, RowM
   float best = -INFINITY;
   int bi = V;
   bool nan = false;
-  for (int j = threadIdx.x; j < V; j += blockDim.x) {
-    const float v = lg[j];
+  auto take = [&](float v, int j) {
     if (v != v) nan = true;
-    if (v > best) {
+    if (v > best) {  // strict: the lowest index wins a tie within a thread
       best = v;
       bi = j;
     }
+  };
+  if ((V & 3) == 0) {  // rows are 16-byte aligned: four logits per load, all loads in flight
+    const float4* lg4 = reinterpret_cast<const float4*>(lg);
+#pragma unroll 4
+    for (int j = threadIdx.x; j < V / 4; j += blockDim.x) {
+      const float4 v = lg4[j];
+      take(v.x, 4 * j);
+      take(v.y, 4 * j + 1);
+      take(v.z, 4 * j + 2);
+      take(v.w, 4 * j + 3);
+    }
+  } else {
+    for (int j = threadIdx.x; j < V; j += blockDim.x) take(lg[j], j);
   }
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
 #pragma unroll
