@@ -367,7 +367,8 @@ struct Acc<T, HD, false> {
 template <typename T, int HD>
 __global__ void __launch_bounds__((attn::kWarps + 1) * 32)
     k_attn(const T* __restrict__ Q, int rows, const int* __restrict__ mslot, const int* __restrict__ mpos,
-           const int* __restrict__ mdepth, int depth_uniform, KvGeom kv, int slot_base, int clamp, int H, int split,
+           const int* __restrict__ mdepth, int depth_uniform, KvGeom kv, int slot_base, int clamp, int perkey, int H,
+           int split,
            int max_splits, T* __restrict__ O, float* __restrict__ part_o, float* __restrict__ part_ml,
            int* status) {
   using Gm = attn::Geo<T, HD>;
@@ -449,11 +450,13 @@ __global__ void __launch_bounds__((attn::kWarps + 1) * 32)
         int kidx = -1;
         if (key < k_hi) {
           const int blk = bt[key >> 4];
-          // clamp 0: the layer's single slot; 1: step min(r, e_j) from the
-          // exit-depth table; 2: step r for every key (no table read).
+          // clamp 0: the layer's single slot; else step min(r, clamp), and
+          // with perkey also at most e_j from the exit-depth table.
           int dr = 1;
-          if (clamp == 1 && blk >= 0 && blk < kv.kv_blocks) dr = min(r, (int)kv.etab[(size_t)blk * 16 + (key & 15)]);
-          else if (clamp == 2) dr = r;
+          if (clamp > 0) {
+            dr = min(r, clamp);
+            if (perkey && blk >= 0 && blk < kv.kv_blocks) dr = min(dr, (int)kv.etab[(size_t)blk * 16 + (key & 15)]);
+          }
           const int sl = slot_base + dr - 1;
           if (blk < 0 || blk >= kv.kv_blocks || dr < 1 || sl >= kv.nsl) {
             if (lane < 16) atomicOr(status, kStatusBadDepth);
@@ -650,7 +653,7 @@ __global__ void __launch_bounds__((attn::kWarps + 1) * 32)
   if (warp == G) {
     // ---------------- producer warp ----------------
     const int r = depth_uniform > 0 ? depth_uniform : mdepth[row] + 1;
-    const int sl = slot_base + (clamp ? r - 1 : 0);
+    const int sl = slot_base + (clamp ? min(r, clamp) - 1 : 0);
     const int* bt = kv.bt + mslot[row] * kv.max_blocks;
     uint64_t pol;
     asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
@@ -1139,10 +1142,9 @@ static void attn_hd(cudaStream_t s, const T* Q, int rows, const int* mslot, cons
     }
     const long long items = (long long)max_splits * rows * ((H + attn::kWarps - 1) / attn::kWarps);
     const int grid = (int)(items < ctas ? items : ctas);
-    const int mode = (uniform && clamp) ? 2 : clamp;  // uniform reads never touch the exit-depth table
-    count_launch();
+    count_launch();  // uniform reads never touch the exit-depth table
     launch_pdl(k_attn<T, HD>, dim3(grid), dim3((attn::kWarps + 1) * 32), Gm::SMEM, s, Q, rows, mslot, mpos, mdepth,
-               depth_uniform, kv, slot_base, mode, H, split, max_splits, O, part_o, part_ml, status);
+               depth_uniform, kv, slot_base, clamp, uniform ? 0 : 1, H, split, max_splits, O, part_o, part_ml, status);
   }
   if (max_splits > 1)
     count_launch(), launch_pdl(k_attn_combine<T>, dim3(rows * H), dim3(128), 0, s, rows, mpos, H, HD, kv.d, split,

@@ -88,10 +88,11 @@ int cdb_attention_noalloc(const void* q, int rows, const int32_t* slot, const in
   g.d = n_heads * head_dim;
   if (dtype == CDB_BF16)
     cdb::launch_attention<__nv_bfloat16>(s, static_cast<const __nv_bfloat16*>(q), rows, slot, pos, depth, 0, g,
-                                         slot_base, 1, n_heads, head_dim, split, (int)splits,
+                                         slot_base, cdb::kNoSlotCap, n_heads, head_dim, split, (int)splits,
                                          static_cast<__nv_bfloat16*>(out), part_o, part_ml, status, false);
   else
-    cdb::launch_attention<float>(s, static_cast<const float*>(q), rows, slot, pos, depth, 0, g, slot_base, 1,
+    cdb::launch_attention<float>(s, static_cast<const float*>(q), rows, slot, pos, depth, 0, g, slot_base,
+                                 cdb::kNoSlotCap,
                                  n_heads, head_dim, split, (int)splits, static_cast<float*>(out), part_o, part_ml,
                                  status, false);
   if (cudaGetLastError() != cudaSuccess || cudaStreamSynchronize(s) != cudaSuccess) return CDB_ERR_CUDA;

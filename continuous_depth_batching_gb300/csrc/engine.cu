@@ -43,12 +43,17 @@ struct Layout {
   int es, nsl, max_blocks, max_splits, split, R, S, cap;
 };
 
+// KV slots per token of one recurrent-core layer: s of App. E.1.
+static int core_slots(const cdb_model_desc* m) {
+  return m->kv_slots <= 0 || m->kv_slots > m->r_max ? m->r_max : m->kv_slots;
+}
+
 static bool plan_layout(const cdb_model_desc* m, const cdb_sched_cfg* c, Layout* L) {
   const int es = m->dtype == CDB_BF16 ? 2 : 4;
   const size_t d = m->d_model, H = m->n_heads, hd = m->head_dim, f = m->ffn, V = m->vocab;
   const size_t W = c->W, M = c->M;
   L->es = es;
-  L->nsl = m->n_prelude + m->n_core * m->r_max + m->n_coda;
+  L->nsl = m->n_prelude + m->n_core * core_slots(m) + m->n_coda;
   L->max_blocks = (c->max_ctx + 15) / 16;
   L->split = c->attn_split > 0 ? c->attn_split : 128;
   L->max_splits = (c->max_ctx + L->split - 1) / L->split;
@@ -392,7 +397,8 @@ class GpuExecutor : public Executor {
     bool done = false;
     if (!decode && sizeof(T) == 2 && pf_tiles_ > 0 && depth_uniform > 0)
       done = launch_prefill_attention(s, (const __nv_bfloat16*)Q, L.R, at<int4>(x, L.ptiles), pf_tiles_, kv,
-                                      slot_base + (clamp ? depth_uniform - 1 : 0), H, hd, (__nv_bfloat16*)O, st);
+                                      slot_base + (clamp ? std::min(depth_uniform, clamp) - 1 : 0), H, hd,
+                                      (__nv_bfloat16*)O, st);
     if (!done)
       launch_attention<T>(s, Q, rows, mslot, mpos, mdepth, depth_uniform, kv, slot_base, clamp, H, hd, split, msp,
                           O, at<float>(x, L.part_o), at<float>(x, L.part_ml), st, true);
@@ -481,6 +487,7 @@ class GpuExecutor : public Executor {
                             at<int>(x, L.status));
     double sumL = 0;
     for (int i = 0; i < n; ++i) sumL += b[i] + 1;
+    const int sc = core_slots(&x->m);
     for (int i = 0; i < x->m.n_prelude; ++i) block<T>(x->pre[i], Xp, n, rslot, rpos, nullptr, 1, i, 0, false, sumL);
     flush<T>();
     float* Ep = at<float>(x, L.Ep);
@@ -491,9 +498,9 @@ class GpuExecutor : public Executor {
     for (int r = 1; r <= x->m.r_max; ++r) {
       if (x->m.has_adapter) adapter_step<T>(Xp, n, Ep, 0, rslot);
       for (int l = 0; l < x->m.n_core; ++l)
-        block<T>(x->core[l], Xp, n, rslot, rpos, nullptr, r, x->m.n_prelude + l * x->m.r_max, 1, false, sumL);
+        block<T>(x->core[l], Xp, n, rslot, rpos, nullptr, r, x->m.n_prelude + l * sc, sc, false, sumL);
     }
-    const int cbase = x->m.n_prelude + x->m.n_core * x->m.r_max;
+    const int cbase = x->m.n_prelude + x->m.n_core * sc;
     for (int j = 0; j < x->m.n_coda; ++j)
       block<T>(x->coda[j], Xp, n, rslot, rpos, nullptr, 1, cbase + j, 0, false, sumL);
     flush<T>();
@@ -559,7 +566,8 @@ class GpuExecutor : public Executor {
     double sumL = 0;
     for (const Tok& t : *p.rows) sumL += t.pos + 1;
     for (int l = 0; l < x->m.n_core; ++l)
-      block<T>(x->core[l], X, B, mx.slot, mx.pos, mx.depth, 0, x->m.n_prelude + l * x->m.r_max, 1, true, sumL);
+      block<T>(x->core[l], X, B, mx.slot, mx.pos, mx.depth, 0, x->m.n_prelude + l * core_slots(&x->m),
+               core_slots(&x->m), true, sumL);
     flush<T>();
     const int ri = (int)(p.step % kRing);
     uint8_t* ring = at<uint8_t>(x, L.ring) + (size_t)ri * x->c.W;
@@ -568,7 +576,9 @@ class GpuExecutor : public Executor {
                    at<int>(x, L.pend_new), ring, x->c.trace_gate ? at<float>(x, L.gtrace) : nullptr);
     launch_compact(x->cs, X, mx, at<int>(x, L.pend_new), B, d, x->m.r_max, p.qc_off, at<float>(x, L.rows[1]),
                    meta_at(x, L.meta[1]), at<float>(x, L.rows[3]), meta_at(x, L.meta[3]), geom(),
-                   at<int8_t>(x, L.out_depth), x->c.max_new_cap, x->m.n_core, x->m.n_prelude, x->m.head_dim,
+                   at<int8_t>(x, L.out_depth), x->c.max_new_cap,
+                   core_slots(&x->m) == x->m.r_max ? x->m.n_core : 0,  // gaps exist only with one slot per step
+                   x->m.n_prelude, x->m.head_dim,
                    (int)sizeof(T), at<int>(x, L.status));
     CK(cudaGetLastError());
     // Lookahead flags to the host on the prep stream.
@@ -603,7 +613,7 @@ class GpuExecutor : public Executor {
     if (x->m.n_coda > 0) {
       float* Tc = at<float>(x, L.rows[4]);
       launch_copy_rows(x->cs, Cb, Tc, n, d);
-      const int cbase = x->m.n_prelude + x->m.n_core * x->m.r_max;
+      const int cbase = x->m.n_prelude + x->m.n_core * core_slots(&x->m);
       double sumL = 0;
       for (const Tok& t : rows) sumL += t.pos + 1;
       for (int j = 0; j < x->m.n_coda; ++j)
@@ -739,7 +749,7 @@ size_t cdb_arena_bytes(const cdb_model_desc* m, const cdb_sched_cfg* c) {
 size_t cdb_kv_bytes_per_token(const cdb_model_desc* m) {
   if (!m) return 0;
   const size_t es = m->dtype == CDB_BF16 ? 2 : 4;
-  const size_t slots = (size_t)m->n_prelude + m->n_coda + (size_t)m->n_core * m->r_max;
+  const size_t slots = (size_t)m->n_prelude + m->n_coda + (size_t)m->n_core * core_slots(m);
   return slots * 2 * (size_t)m->d_model * es;
 }
 
@@ -748,7 +758,8 @@ int cdb_init(const cdb_model_desc* m, const cdb_weights* w, const cdb_sched_cfg*
   *out = nullptr;
   if (m->vocab < 2 || m->d_model < 4 || m->n_heads < 1 || m->d_model != m->n_heads * m->head_dim ||
       m->d_model % 4 != 0 || !valid_hd(m->head_dim) || m->ffn < 1 || m->n_core < 1 || m->n_prelude < 0 ||
-      m->n_coda < 0 || m->r_min < 2 || m->r_max < m->r_min || m->r_max > CDB_MAX_DEPTH ||
+      m->n_coda < 0 || m->r_min < 2 || m->r_max < m->r_min || m->r_max > CDB_MAX_DEPTH || m->kv_slots < 0 ||
+      m->kv_slots > m->r_max ||
       (m->dtype != CDB_FP32 && m->dtype != CDB_BF16) || (m->has_adapter && !w->adapter))
     return CDB_ERR_ARG;
   if (c->W < 1 || c->M < 1 || c->K < 1 || c->kv_blocks < 1 || c->max_ctx < 1 || c->max_new_cap < 1 ||
@@ -1071,10 +1082,10 @@ static int test_attention(const void* q, int rows, const int32_t* slot, const in
   g.nsl = n_kv_slots;
   g.d = n_heads * head_dim;
   if (dtype == CDB_BF16)
-    launch_attention<__nv_bfloat16>(s, (const __nv_bfloat16*)q, rows, slot, pos, depth, 0, g, slot_base, 1, n_heads,
+    launch_attention<__nv_bfloat16>(s, (const __nv_bfloat16*)q, rows, slot, pos, depth, 0, g, slot_base, kNoSlotCap, n_heads,
                                     head_dim, split, (int)ms, (__nv_bfloat16*)out, part_o, part_ml, status, uniform);
   else
-    launch_attention<float>(s, (const float*)q, rows, slot, pos, depth, 0, g, slot_base, 1, n_heads, head_dim,
+    launch_attention<float>(s, (const float*)q, rows, slot, pos, depth, 0, g, slot_base, kNoSlotCap, n_heads, head_dim,
                             split, (int)ms, (float*)out, part_o, part_ml, status, uniform);
   if (cudaGetLastError() != cudaSuccess || cudaStreamSynchronize(s) != cudaSuccess) return CDB_ERR_CUDA;
   int st = 0;

@@ -233,7 +233,8 @@ __global__ void k_concat(const float* __restrict__ E, int e_per_slot, const int*
 // ---------------------------------------------------------------------------
 
 // Row i at position p and loop step r writes K,V into slot slot_base + r-1
-// (core layers, clamp=1) or slot_base (prelude / coda layers).
+// (core layers; slot_base + min(r, clamp) - 1 with a shared layout) or
+// slot_base (prelude / coda layers, clamp = 0).
 template <typename T>
 __device__ __forceinline__ void store4(T* p, const T (&v)[4]);
 template <>
@@ -268,7 +269,7 @@ __global__ void k_rope_kv(Parts qkv, int rows, const int* __restrict__ mslot,
   const int pos = mpos[i];
   const int r = depth_uniform > 0 ? depth_uniform : mdepth[i] + 1;
   const int blk = kv.bt[mslot[i] * kv.max_blocks + pos / 16];
-  const int sl = slot_base + (clamp ? r - 1 : 0);
+  const int sl = slot_base + (clamp ? min(r, clamp) - 1 : 0);
   if (blk < 0 || blk >= kv.kv_blocks || sl < 0 || sl >= kv.nsl) {
     if (threadIdx.x == 0) atomicOr(status, kStatusBadBlock);
     return;

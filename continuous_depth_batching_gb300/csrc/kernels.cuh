@@ -110,6 +110,11 @@ void launch_argmax(cudaStream_t s, const float* logits, int rows, int V, RowMeta
 void launch_rope_table(cudaStream_t s, float2* tab, int max_ctx, int hd, float theta);
 void launch_copy_rows(cudaStream_t s, const float* src, float* dst, int rows, int d);
 
+// Slot of a row at loop step r in a layer whose cache starts at slot_base:
+// clamp (the slot cap, s of App. E.1) 0 = the layer's single slot, else
+// slot_base + min(r, clamp) - 1.  kNoSlotCap: one slot per loop step.
+constexpr int kNoSlotCap = 1 << 20;
+
 // ---- attention (attention.cu) ----
 // Decode (and prefill) attention.  uniform: every key of a row is read from
 // one slot (slot_base + r - 1 with clamp, slot_base without), which holds

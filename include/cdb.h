@@ -82,6 +82,13 @@ typedef struct {
   int dtype;        /* cdb_dtype: weights, activations and KV cache */
   float rms_eps, rope_theta;
   float gate_threshold, gate_bias;
+  /* KV slots per token of each recurrent-core layer, s (App. E.1): 0 or
+   * r_max = the depth-indexed cache (loop step d writes and reads slot d);
+   * 1 = single-slot sharing (every step overwrites one slot); 2 =
+   * first-then-shared (step 1 keeps a private slot, steps >= 2 share the
+   * second); in general step d uses slot min(d, s).  A prompt split across
+   * prefill chunks then reads its earlier chunks at their last loop step. */
+  int kv_slots;
 } cdb_model_desc;
 
 /* One transformer block; device pointers, row-major [out, in] like nn.Linear.

@@ -102,15 +102,20 @@ class OracleModel:
         # RoPE inverse frequencies theta^(-2i/hd), i < hd/2.
         self.inv_freq = m.rope_theta ** (-2.0 * np.arange(half, dtype=np.float64) / m.head_dim)
 
-    # -- slots of the depth-indexed cache (§4.2; App. E.1 counts l0 + lr*s) --
+    # -- cache slots (§4.2; App. E.1: l0 + lr * s entries per token) --
+    # Core layer l keeps s slots per position.  Loop step d writes and reads
+    # slot min(d, s): s = r_max is the depth-indexed cache (one slot per step),
+    # s = 1 the single-slot shared cache (every step overwrites the slot), s = 2
+    # first-then-shared (step 1 private, steps >= 2 share the second slot).
     def slot_prelude(self, i: int) -> int:
         return i
 
-    def slot_core(self, l: int, depth: int) -> int:
-        return self.m.n_prelude + l * self.m.r_max + (depth - 1)
+    def slot_core(self, l: int, depth):
+        s = self.m.slots_per_core_layer
+        return self.m.n_prelude + l * s + (np.minimum(depth, s) - 1)
 
     def slot_coda(self, j: int) -> int:
-        return self.m.n_prelude + self.m.n_core * self.m.r_max + j
+        return self.m.n_prelude + self.m.n_core * self.m.slots_per_core_layer + j
 
     # -- elementary ops --
     def rmsnorm(self, x, g):
@@ -306,9 +311,10 @@ def iter_decode(model: OracleModel, prompt, gen_len: int, mode: str = "adaptive"
         for d in range(1, m.r_max + 1):
             x = model.adapter(emb, s) if m.has_adapter else s
             # Depth clamp: key j is read at min(d, e_j); e_p = r_max in flight.
+            # With a shared layout the slot of that step holds j's latest write.
             read_depth = np.minimum(d, e[:p + 1])
             for l in range(m.n_core):
-                key_slots = model.slot_core(l, 1) + read_depth - 1
+                key_slots = model.slot_core(l, read_depth)
                 x = model.block(f"core.{l}.", x, ppos, kv, model.slot_core(l, d),
                                 key_slots, "core")
             s = x

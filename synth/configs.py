@@ -62,6 +62,11 @@ class ModelShape:
     rope_theta: float = 10000.0
     init_std: float = 0.02
     weight_seed: int = 0
+    kv_slots: int = 0  # KV slots per recurrent layer s (App. E.1): 0 = r_max (depth-indexed), 1, 2 = shared
+
+    @property
+    def slots_per_core_layer(self) -> int:
+        return self.r_max if self.kv_slots <= 0 else min(self.kv_slots, self.r_max)
 
     @property
     def gate_threshold_logit(self) -> float:
@@ -70,8 +75,8 @@ class ModelShape:
 
     @property
     def n_kv_slots(self) -> int:
-        """KV entries per token with a depth-indexed cache: l0 + lr * r_max."""
-        return self.n_prelude + self.n_coda + self.n_core * self.r_max
+        """KV entries per token, l0 + lr * s (App. E.1; s = r_max for the depth-indexed cache)."""
+        return self.n_prelude + self.n_coda + self.n_core * self.slots_per_core_layer
 
     @property
     def elem_bytes(self) -> int:

@@ -30,7 +30,11 @@ def _w64(a):
 
 class BruteForceLM:
     def __init__(self, shape, weights, prompt, gen_len, exit_depth_of_token):
-        """exit_depth_of_token(t) -> exit depth of decode forward t (1-based)."""
+        """exit_depth_of_token(t) -> exit depth of decode forward t (1-based).
+
+        shape.kv_slots selects the cache layout of App. E.1 (0 or r_max:
+        depth-indexed; 1: single slot; 2: first-then-shared); see visible_step.
+        """
         self.m = shape
         self.w = {k: _w64(v) for k, v in weights.items()}
         self.P = len(prompt)
@@ -125,10 +129,29 @@ class BruteForceLM:
         pre = f"core.{l - 1}."
 
         def kv_of(j):
-            dj = d if j == i else min(d, self.exit_depth(j))
-            return self._kv(pre, self.core_in(j, dj, l - 1), j)
+            return self._kv(pre, self.core_in(j, self.visible_step(i, j, d), l - 1), j)
 
         return self._layer(pre, self.core_in(i, d, l - 1), i, kv_of)
+
+    def visible_step(self, i, j, d):
+        """Loop step of key j whose K/V position i sees at its loop step d.
+
+        Depth-indexed cache: step d of j, or j's last step e_j if it left
+        earlier (the depth clamp).  Shared layouts keep fewer slots, so a key
+        shows whatever step last wrote the slot step d reads: with s slots,
+        steps below s have private slots (step d itself); the last slot holds
+        the key's latest step, which is d while the prompt runs its loop steps
+        together in prefill and e_j once the key's token has finished.
+        """
+        m = self.m
+        if j == i:
+            return d
+        s = m.r_max if m.kv_slots <= 0 else min(m.kv_slots, m.r_max)
+        if s == m.r_max:
+            return min(d, self.exit_depth(j))
+        if d < s:
+            return d
+        return d if i < self.P else self.exit_depth(j)
 
     @functools.lru_cache(maxsize=None)
     def coda_in(self, i, l):

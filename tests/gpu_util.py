@@ -33,7 +33,7 @@ def force_tables(tr, replay=None, gap_band=NEAR):
 
 
 def gpu_run(shape, dev_w, reqs, traces, *, mode="refill", W=4, M=8192, K=1, S=0, max_ctx=None,
-            trace_tokens=0, trace_gate=False, attn_split=0, force=True):
+            trace_tokens=0, trace_gate=False, attn_split=0, force=True, gap_band=NEAR):
     from continuous_depth_batching_gb300 import binding
     if max_ctx is None:
         max_ctx = max(len(r["prompt"]) + r["gen_len"] for r in reqs)
@@ -44,7 +44,7 @@ def gpu_run(shape, dev_w, reqs, traces, *, mode="refill", W=4, M=8192, K=1, S=0,
     for r in reqs:
         fe = ft = None
         if force and traces is not None:
-            fe, ft = force_tables(traces[r["seq_id"]], r.get("replay"))
+            fe, ft = force_tables(traces[r["seq_id"]], r.get("replay"), gap_band)
         elif r.get("replay") is not None:
             fe = np.asarray(r["replay"], dtype=np.int8)
         eng.admit(r["seq_id"], r["prompt"], r["gen_len"], fe, ft)

@@ -44,18 +44,20 @@ def test_every_declared_symbol_is_exported(L):
         assert hasattr(L, n), n
 
 
-# Table 4 prints KiB per token rounded to whole KiB; slots s = r_max for the
-# depth-indexed cache, and the single-slot / first-then-shared rows follow the
-# same l0 + lr * s count (App. E.1).
-TABLE4 = [("ouro", 4, 768), ("ouro", 1, 192), ("ouro", 2, 384),
-          ("huginn", 16, 1402), ("huginn", 1, 165), ("huginn", 2, 248)]
+# Table 4 prints KiB per token rounded to whole KiB: the depth-indexed cache
+# (s = r_max; Huginn at the paper's r_max 16), single-slot (s = 1) and
+# first-then-shared (s = 2) layouts, l0 + lr * s entries (App. E.1).  The
+# shared rows go through the kv_slots field with the model's own r_max.
+TABLE4 = [("ouro", 0, 4, 768), ("ouro", 1, 4, 192), ("ouro", 2, 4, 384),
+          ("huginn", 0, 16, 1402), ("huginn", 1, 32, 165), ("huginn", 2, 32, 248)]
 
 
-@pytest.mark.parametrize("name,s,kib", TABLE4)
-def test_kv_bytes_per_token_table4(L, name, s, kib):
-    shape = dataclasses.replace(model_shape(name), r_max=s, r_min=min(2, s))
+@pytest.mark.parametrize("name,s,r_max,kib", TABLE4)
+def test_kv_bytes_per_token_table4(L, name, s, r_max, kib):
+    shape = dataclasses.replace(model_shape(name), r_max=r_max, kv_slots=s)
     desc = binding.model_desc(shape)
     assert abs(L.cdb_kv_bytes_per_token(C.byref(desc)) / 1024 - kib) <= 0.5
+    assert abs(shape.n_kv_slots * 2 * shape.d_model * shape.elem_bytes / 1024 - kib) <= 0.5
 
 
 def test_core_parameter_counts():

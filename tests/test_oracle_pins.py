@@ -6,7 +6,9 @@
   sequence, cache-free causal forward computed with torch's own attention.
 * With early exits, the oracle must equal a recursive, cache-free
   recomputation that applies the depth-clamp reading directly
-  (tests/brute_force.py), including prelude/coda layers and the adapter.
+  (tests/brute_force.py), including prelude/coda layers and the adapter; the
+  same holds for the shared cache layouts of App. E.1, where the brute force
+  states which loop step of each key is visible instead of using slots.
 * Gate extremes: an always-positive gate exits every token at r_min (§4.3,
   lookahead: r_min = 2), an always-negative gate reproduces fixed depth.
 * bf16 rounding equals torch's float32 -> bfloat16 conversion.
@@ -149,6 +151,30 @@ def test_brute_force_detects_wrong_clamp():
     wrong_lg = wrong.run()[1]
     np.testing.assert_allclose(tr.logits[-1], honest[-1], atol=2e-5, rtol=0)
     assert np.max(np.abs(tr.logits[-1] - wrong_lg[-1])) > 1e-3
+
+
+@pytest.mark.parametrize("kv_slots", [1, 2])
+@pytest.mark.parametrize("variant", ["looped", "huginn_like"])
+def test_shared_kv_layouts_match_brute_force(variant, kv_slots):
+    """Single-slot and first-then-shared caches (App. E.1): the oracle's slot
+    overwrites equal the brute force's explicit visible-step rule."""
+    if variant == "looped":
+        shape = micro(r_max=4, kv_slots=kv_slots)
+    else:
+        shape = micro(r_max=4, n_prelude=1, n_core=1, n_coda=1, has_adapter=True, kv_slots=kv_slots)
+    wts = make_weights(shape)
+    prompt = prompt_for(shape, 5, seed=13)
+    gen = 6
+    depths = np.array([2, 4, 3, 2, 4], dtype=np.int8)
+    tr = decode_sequence(OracleModel(shape, wts), prompt, gen, force_exit=depths, keep_logits=gen)
+    toks, lg = BruteForceLM(shape, wts, prompt, gen, lambda t: int(depths[t - 1])).run()
+    assert tr.tokens == toks
+    for t in range(gen):
+        np.testing.assert_allclose(tr.logits[t], lg[t], atol=2e-5, rtol=0)
+    # The layout matters: the depth-indexed cache gives other logits.
+    deep = decode_sequence(OracleModel(dataclasses.replace(shape, kv_slots=0), wts), prompt, gen,
+                           force_exit=depths, keep_logits=gen)
+    assert max(np.abs(np.array(deep.logits) - np.array(tr.logits)).max(axis=1)) > 1e-3
 
 
 # ---------------------------------------------------------------------------
