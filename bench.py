@@ -22,6 +22,7 @@ host cores, one generated token per step.
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import json
 import os
 import statistics
@@ -50,6 +51,8 @@ def parse():
     ap.add_argument("--no-modes", action="store_true", help="skip the no-refill and fixed-depth full jobs")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=20.0)
+    ap.add_argument("--kv-slots", type=int, default=0,
+                    help="KV slots per core layer: 0 = r_max (depth-indexed), 1 single-slot, 2 first-then-shared")
     return ap.parse_args()
 
 
@@ -189,7 +192,7 @@ def run_reference(args):
     from oracle.model import OracleModel, iter_decode
     from synth import make_requests, make_weights, model_shape, workload
     wl = workload(args.workload)
-    shape = model_shape(wl.model)
+    shape = dataclasses.replace(model_shape(wl.model), kv_slots=args.kv_slots)
     wts = make_weights(shape)
     reqs = sorted(make_requests(wl, shape.vocab, shape.r_max, shape.r_min), key=lambda r: len(r["prompt"]))
     om = OracleModel(shape, wts)
@@ -224,6 +227,8 @@ def _config(wl, shape, mode, flush):
             "model": f"{shape.name}: d{shape.d_model} {shape.n_heads}x{shape.head_dim} ffn{shape.ffn} "
                      f"{shape.n_prelude}-{shape.n_core}-{shape.n_coda} r_max{shape.r_max} {shape.dtype}",
             "mode": mode, "global_batch": wl.W, "seq_len": wl.prompt_hi + wl.gen_hi,
+            "kv_layout": {0: "depth-indexed", 1: "single-slot", 2: "first-then-shared"}.get(
+                shape.kv_slots if shape.kv_slots < shape.r_max else 0, f"{shape.kv_slots} slots"),
             "parallelism": "replicas", "l2": flush}
 
 
@@ -242,7 +247,7 @@ def run_ours(args):
         dist.init_process_group("nccl", device_id=torch.device("cuda", local))
     build()
     wl = workload(args.workload)
-    shape = model_shape(wl.model)
+    shape = dataclasses.replace(model_shape(wl.model), kv_slots=args.kv_slots)
     wts = make_weights(shape)
     dw = binding.device_weights(shape, wts)
     reqs = make_requests(wl, shape.vocab, shape.r_max, shape.r_min)

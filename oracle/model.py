@@ -37,6 +37,13 @@ before an untied LM head, greedy argmax with ties to the lowest index, exit
 gate z = w_g . rmsnorm(h) + b_g compared with logit(q) (a token exits when
 sigmoid(z) > q; z == logit(q) does not exit).  Huginn-shaped models enter every
 loop step through x = A [e; s_{d-1}] with s_0 = 0 and e the prelude output.
+
+Convergence exit (App. E.2, Huginn's training-free criterion): after loop step
+d the statistic is c_d = ||s_d - s_{d-1}||_2 / ||s_d||_2, with s_{d-1} the
+state that entered step d (s_0 = 0 with an adapter, else the prelude output),
+and the token exits when c_d < tau (c_d == tau does not exit).  It goes through
+the same lookahead as the linear gate, so with r_min = 3 the first deciding
+comparison is c_2 (App. E.2: minimum loop count 3 for this criterion).
 """
 
 from __future__ import annotations
@@ -97,7 +104,8 @@ class OracleModel:
         self.w = {k: _decode_weight(v) for k, v in weights.items()}
         self.flops = FlopCount()
         m = shape
-        self.theta = math.log(m.gate_q / (1.0 - m.gate_q))
+        self.convergence_gate = getattr(m, "gate_kind", "probe") == "convergence"
+        self.theta = m.conv_tau if self.convergence_gate else math.log(m.gate_q / (1.0 - m.gate_q))
         half = m.head_dim // 2
         # RoPE inverse frequencies theta^(-2i/hd), i < hd/2.
         self.inv_freq = m.rope_theta ** (-2.0 * np.arange(half, dtype=np.float64) / m.head_dim)
@@ -197,6 +205,17 @@ class OracleModel:
         hn = h / np.sqrt(ms + m.rms_eps)
         return _f32(hn @ self.w["gate_w"] + m.gate_bias)
 
+    def convergence(self, s, s_prev):
+        """c = ||s - s_prev||_2 / ||s||_2 per row, float32 result (inf when s = 0)."""
+        num = np.sqrt(np.sum((s - s_prev) ** 2, axis=-1))
+        den = np.sqrt(np.sum(s * s, axis=-1))
+        with np.errstate(divide="ignore", invalid="ignore"):
+            return _f32(np.where(den > 0, num / np.where(den > 0, den, 1.0), np.inf))
+
+    def gate_fires(self, z):
+        """Exit decision of one gate value: z > logit(q) for the probe, c < tau for convergence."""
+        return z < self.theta if self.convergence_gate else z > self.theta
+
     def logits(self, h):
         u = self.store(self.rmsnorm(h, self.w["final_norm"]))
         return _f32(self.linear(u, self.w["lm_head"], "coda"))
@@ -216,7 +235,7 @@ class SeqTrace:
     """Everything the oracle decided for one sequence."""
     tokens: list = field(default_factory=list)          # generated ids, token 0 from prefill
     exit_depths: list = field(default_factory=list)     # per decode forward (gen_len - 1)
-    gate_logits: list = field(default_factory=list)     # per decode forward: z_1..z_{e-1}
+    gate_logits: list = field(default_factory=list)     # per decode forward: z_1..z_{e-1} (c_d for convergence)
     near_gate: list = field(default_factory=list)       # per decode forward: |z_d - theta| < tol at a deciding d
     top2_gap: list = field(default_factory=list)        # per generated token
     logits: list = field(default_factory=list)          # per generated token (if kept)
@@ -313,6 +332,7 @@ def iter_decode(model: OracleModel, prompt, gen_len: int, mode: str = "adaptive"
             # Depth clamp: key j is read at min(d, e_j); e_p = r_max in flight.
             # With a shared layout the slot of that step holds j's latest write.
             read_depth = np.minimum(d, e[:p + 1])
+            s_prev = s
             for l in range(m.n_core):
                 key_slots = model.slot_core(l, read_depth)
                 x = model.block(f"core.{l}.", x, ppos, kv, model.slot_core(l, d),
@@ -320,13 +340,16 @@ def iter_decode(model: OracleModel, prompt, gen_len: int, mode: str = "adaptive"
             s = x
             if d == exit_at:
                 break
-            z = float(model.gate_logit(s)[0])
+            if model.convergence_gate:
+                z = float(model.convergence(s, s_prev)[0])
+            else:
+                z = float(model.gate_logit(s)[0])
             zs.append(z)
             deciding = m.r_min - 1 <= d <= m.r_max - 2
             if deciding and not decided and not (mode == "adaptive" and forced):
                 if abs(z - model.theta) < near_tol:
                     near = True
-                if mode == "adaptive" and not decided and z > model.theta:
+                if mode == "adaptive" and not decided and model.gate_fires(z):
                     exit_at = d + 1
                     decided = True
         e[p] = d

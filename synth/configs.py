@@ -63,6 +63,11 @@ class ModelShape:
     init_std: float = 0.02
     weight_seed: int = 0
     kv_slots: int = 0  # KV slots per recurrent layer s (App. E.1): 0 = r_max (depth-indexed), 1, 2 = shared
+    # Exit policy: "probe" (the linear gate above) or "convergence" (Huginn's
+    # training-free criterion, App. E.2: exit once the normalised L2 distance
+    # between consecutive loop states falls below conv_tau).
+    gate_kind: str = "probe"
+    conv_tau: float = 0.0
 
     @property
     def slots_per_core_layer(self) -> int:

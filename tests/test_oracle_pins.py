@@ -15,6 +15,11 @@
 * RoPE scores depend only on the relative position.
 * Executed FLOPs equal the closed form used by §5 eq. (1).
 * Exit gaps of the depth-indexed cache are never written.
+* Convergence exit (App. E.2): the oracle's statistics and exit depths equal
+  the normalised L2 distances of the brute force's loop states with the
+  lookahead rule applied to them; c = 1 exactly at step 1 when s_0 = 0; a
+  threshold above every statistic exits at r_min = 3, a zero threshold
+  reproduces fixed depth.
 """
 
 import dataclasses
@@ -275,3 +280,85 @@ def test_exit_gaps_never_written():
             for t, e in enumerate(depths, start=1):
                 written = np.all(np.isfinite(K[sl, P + t - 1]))
                 assert written == (dpt <= e)
+
+
+# ---------------------------------------------------------------------------
+# convergence exit (App. E.2)
+# ---------------------------------------------------------------------------
+
+def conv_micro(variant, **kw):
+    base = dict(r_max=6, r_min=3, gate_kind="convergence")
+    if variant == "huginn_like":
+        base.update(n_prelude=1, n_core=1, n_coda=1, has_adapter=True)
+    base.update(kw)
+    return micro(**base)
+
+
+def test_convergence_statistic_closed_form():
+    om = OracleModel(conv_micro("looped"), make_weights(conv_micro("looped")))
+    c = om.convergence(np.array([[3.0, 4.0], [3.0, 4.0], [0.0, 0.0]]),
+                       np.array([[0.0, 0.0], [3.0, 0.0], [1.0, 1.0]]))
+    assert c[0] == 1.0 and c[1] == pytest.approx(0.8, abs=1e-7) and np.isinf(c[2])
+    assert om.gate_fires(om.theta - 1e-3) and not om.gate_fires(om.theta)
+
+
+@pytest.mark.parametrize("variant", ["looped", "huginn_like"])
+def test_convergence_gate_matches_brute_force(variant):
+    shape0 = conv_micro(variant, conv_tau=0.0)
+    wts = make_weights(shape0)
+    prompt = prompt_for(shape0, 5, seed=17)
+    gen = 7
+    # Statistics of a run that never exits fix a threshold inside their range.
+    free = decode_sequence(OracleModel(shape0, wts), prompt, gen)
+    deciding = np.array([z for zs in free.gate_logits for z in zs[shape0.r_min - 2:shape0.r_max - 2]])
+    tau = float(np.median(deciding))
+    shape = dataclasses.replace(shape0, conv_tau=tau)
+    tr = decode_sequence(OracleModel(shape, wts), prompt, gen, keep_logits=gen)
+    assert len(set(tr.exit_depths)) >= 2, tr.exit_depths
+
+    P = len(prompt)
+    bf = None
+
+    def c_of(i, d):
+        a, b = bf.state(i, d), bf.state(i, d - 1)
+        return float(np.linalg.norm(a - b) / np.linalg.norm(a))
+
+    def exit_of(t):
+        # Lookahead: a statistic below tau after step d (r_min-1 <= d <= r_max-2)
+        # makes the token run step d+1 and leave.
+        i = P + t - 1
+        for d in range(shape.r_min - 1, shape.r_max - 1):
+            if c_of(i, d) < tau:
+                return d + 1
+        return shape.r_max
+
+    bf = BruteForceLM(shape, wts, prompt, gen, exit_of)
+    toks, lg = bf.run()
+    assert tr.exit_depths == [exit_of(t) for t in range(1, gen)]
+    assert tr.tokens == toks
+    for t in range(1, gen):
+        i = P + t - 1
+        want = [c_of(i, d) for d in range(1, tr.exit_depths[t - 1])]
+        np.testing.assert_allclose(tr.gate_logits[t - 1], want, rtol=1e-5, atol=0)
+        margin = min(abs(c - tau) for c in want[shape.r_min - 2:])
+        assert margin > 1e-5 or tr.exit_depths[t - 1] == shape.r_min  # no decision within rounding of tau
+    for t in range(gen):
+        np.testing.assert_allclose(tr.logits[t], lg[t], atol=2e-5, rtol=0)
+
+
+def test_convergence_gate_extremes():
+    shape = conv_micro("huginn_like")
+    wts = make_weights(shape)
+    prompt = prompt_for(shape, 6)
+    gen = 6
+    hi = decode_sequence(OracleModel(dataclasses.replace(shape, conv_tau=10.0), wts), prompt, gen)
+    assert hi.exit_depths == [3] * (gen - 1)
+    lo = decode_sequence(OracleModel(dataclasses.replace(shape, conv_tau=0.0), wts), prompt, gen,
+                         keep_logits=gen)
+    fx = decode_sequence(OracleModel(shape, wts), prompt, gen, mode="fixed", keep_logits=gen)
+    assert lo.exit_depths == [shape.r_max] * (gen - 1)
+    assert lo.tokens == fx.tokens
+    for a, b in zip(lo.logits, fx.logits):
+        np.testing.assert_array_equal(a, b)
+    # s_0 = 0 with the adapter: the first statistic is exactly 1.
+    assert all(zs[0] == 1.0 for zs in lo.gate_logits)
