@@ -28,7 +28,7 @@ class ModelDesc(C.Structure):
                 ("ffn", C.c_int), ("n_prelude", C.c_int), ("n_core", C.c_int), ("n_coda", C.c_int),
                 ("r_max", C.c_int), ("r_min", C.c_int), ("has_adapter", C.c_int), ("dtype", C.c_int),
                 ("rms_eps", C.c_float), ("rope_theta", C.c_float), ("gate_threshold", C.c_float),
-                ("gate_bias", C.c_float), ("kv_slots", C.c_int)]
+                ("gate_bias", C.c_float), ("kv_slots", C.c_int), ("gate_kind", C.c_int)]
 
 
 class LayerWeights(C.Structure):
@@ -153,10 +153,12 @@ def model_desc(shape) -> ModelDesc:
     """cdb_model_desc from a shape object with the fields of synth.ModelShape."""
     import math
     q = shape.gate_q
+    conv = getattr(shape, "gate_kind", "probe") == "convergence"
     return ModelDesc(shape.vocab, shape.d_model, shape.n_heads, shape.head_dim, shape.ffn, shape.n_prelude,
                      shape.n_core, shape.n_coda, shape.r_max, shape.r_min, int(shape.has_adapter),
                      1 if shape.dtype == "bf16" else 0, shape.rms_eps, shape.rope_theta,
-                     math.log(q / (1.0 - q)), shape.gate_bias, int(getattr(shape, "kv_slots", 0)))
+                     shape.conv_tau if conv else math.log(q / (1.0 - q)), shape.gate_bias,
+                     int(getattr(shape, "kv_slots", 0)), 1 if conv else 0)
 
 
 def kv_bytes_per_token(shape) -> int:

@@ -32,7 +32,7 @@ static size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
 
 struct Layout {
   size_t total = 0;
-  size_t pool, etab, bt, out_tok, ftok, fexit, out_depth, gtrace, ltrace, htrace, estore, rope;
+  size_t pool, etab, bt, out_tok, ftok, fexit, out_depth, gtrace, ltrace, htrace, estore, rope, sprev;
   size_t rows[5], meta[5];  // X, Xc, Pb, Cb, Tp
   size_t pend_new, ring, status;
   size_t Xp, Ep, rslot, rpos, rtok, ptiles, done_idx, Cp, Cp_meta;
@@ -78,6 +78,7 @@ static bool plan_layout(const cdb_model_desc* m, const cdb_sched_cfg* c, Layout*
   L->ltrace = take(W * T * V * 4);
   L->htrace = take(W * T * d * 4);
   L->estore = take(m->has_adapter ? W * d * 4 : 0);
+  L->sprev = take(m->gate_kind == CDB_GATE_CONVERGENCE ? W * d * 4 : 0);  // s_{d-1} of each core row
   L->rope = take((size_t)c->max_ctx * (hd / 2) * 8);
   for (int i = 0; i < 5; ++i) {
     L->rows[i] = take(W * d * 4);
@@ -560,8 +561,10 @@ class GpuExecutor : public Executor {
     const int d = x->m.d_model, B = p.B;
     float* X = at<float>(x, L.rows[0]);
     RowMeta mx = meta_at(x, L.meta[0]);
+    const bool conv = x->m.gate_kind == CDB_GATE_CONVERGENCE;
+    float* sprev = conv ? at<float>(x, L.sprev) : nullptr;  // s_{d-1}, kept for the convergence exit
     launch_gather_core(x->cs, at<float>(x, L.rows[1]), meta_at(x, L.meta[1]), p.B_cont, at<float>(x, L.rows[2]),
-                       meta_at(x, L.meta[2]), p.n_ref, X, mx, d);
+                       meta_at(x, L.meta[2]), p.n_ref, X, mx, d, sprev);
     if (x->m.has_adapter) adapter_step<T>(X, B, at<float>(x, L.estore), 1, mx.slot);
     double sumL = 0;
     for (const Tok& t : *p.rows) sumL += t.pos + 1;
@@ -571,8 +574,8 @@ class GpuExecutor : public Executor {
     flush<T>();
     const int ri = (int)(p.step % kRing);
     uint8_t* ring = at<uint8_t>(x, L.ring) + (size_t)ri * x->c.W;
-    launch_gate<T>(x->cs, X, (const T*)x->gate_w, x->m.gate_bias, x->m.gate_threshold, x->m.rms_eps, B, d, mx,
-                   x->c.mode, x->m.r_min, x->m.r_max, at<int8_t>(x, L.fexit), x->c.max_new_cap,
+    launch_gate<T>(x->cs, X, sprev, (const T*)x->gate_w, x->m.gate_bias, x->m.gate_threshold, x->m.rms_eps, B, d,
+                   mx, x->c.mode, x->m.r_min, x->m.r_max, at<int8_t>(x, L.fexit), x->c.max_new_cap,
                    at<int>(x, L.pend_new), ring, x->c.trace_gate ? at<float>(x, L.gtrace) : nullptr);
     launch_compact(x->cs, X, mx, at<int>(x, L.pend_new), B, d, x->m.r_max, p.qc_off, at<float>(x, L.rows[1]),
                    meta_at(x, L.meta[1]), at<float>(x, L.rows[3]), meta_at(x, L.meta[3]), geom(),
@@ -759,14 +762,16 @@ int cdb_init(const cdb_model_desc* m, const cdb_weights* w, const cdb_sched_cfg*
   if (m->vocab < 2 || m->d_model < 4 || m->n_heads < 1 || m->d_model != m->n_heads * m->head_dim ||
       m->d_model % 4 != 0 || !valid_hd(m->head_dim) || m->ffn < 1 || m->n_core < 1 || m->n_prelude < 0 ||
       m->n_coda < 0 || m->r_min < 2 || m->r_max < m->r_min || m->r_max > CDB_MAX_DEPTH || m->kv_slots < 0 ||
-      m->kv_slots > m->r_max ||
+      m->kv_slots > m->r_max || m->gate_kind < CDB_GATE_PROBE || m->gate_kind > CDB_GATE_CONVERGENCE ||
+      (m->gate_kind == CDB_GATE_CONVERGENCE && m->r_min < 3) ||
       (m->dtype != CDB_FP32 && m->dtype != CDB_BF16) || (m->has_adapter && !w->adapter))
     return CDB_ERR_ARG;
   if (c->W < 1 || c->M < 1 || c->K < 1 || c->kv_blocks < 1 || c->max_ctx < 1 || c->max_new_cap < 1 ||
       c->mode < 0 || c->mode > 2 || c->trace_tokens < 0 || !c->arena || ((uintptr_t)c->arena % kAlign) != 0 ||
       c->attn_split < 0 || c->attn_split % 16 != 0 || (c->S > c->W))
     return CDB_ERR_ARG;
-  if (!w->embed || !w->lm_head || !w->final_norm || !w->gate_w || (m->n_core > 0 && !w->core) ||
+  if (!w->embed || !w->lm_head || !w->final_norm || (m->gate_kind == CDB_GATE_PROBE && !w->gate_w) ||
+      (m->n_core > 0 && !w->core) ||
       (m->n_prelude > 0 && !w->prelude) || (m->n_coda > 0 && !w->coda))
     return CDB_ERR_ARG;
   std::unique_ptr<cdb_ctx> x(new cdb_ctx);

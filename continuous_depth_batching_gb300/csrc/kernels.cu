@@ -336,7 +336,8 @@ __global__ void k_rope_table(float2* tab, int max_ctx, int hd, float theta) {
 // after step r+1: live gate -> z > thr and r >= r_min-1; a forced exit depth
 // e -> r + 1 == e; fixed-depth mode never sets it.
 template <typename T>
-__global__ void k_gate(const float* __restrict__ X, const T* __restrict__ w, float bias, float thr,
+__global__ void k_gate(const float* __restrict__ X, const float* __restrict__ Sp, const T* __restrict__ w,
+                       float bias, float thr,
                        float eps, int rows, int d, RowMeta m, int mode, int r_min, int r_max,
                        const int8_t* __restrict__ fexit, int cap, int* __restrict__ pend_new,
                        uint8_t* __restrict__ ring, float* __restrict__ gtrace) {
@@ -347,21 +348,31 @@ __global__ void k_gate(const float* __restrict__ X, const T* __restrict__ w, flo
   if (i >= rows) return;
   const float* x = X + (size_t)i * d;
   float ss = 0.f, dot = 0.f;
-  for (int c = threadIdx.x; c < d; c += blockDim.x) {
-    ss = fmaf(x[c], x[c], ss);
-    dot = fmaf(x[c], to_f(w[c]), dot);
+  if (Sp) {  // convergence statistic: dot accumulates ||s_d - s_{d-1}||^2
+    const float* xp = Sp + (size_t)i * d;
+    for (int c = threadIdx.x; c < d; c += blockDim.x) {
+      const float df = x[c] - xp[c];
+      ss = fmaf(x[c], x[c], ss);
+      dot = fmaf(df, df, dot);
+    }
+  } else {
+    for (int c = threadIdx.x; c < d; c += blockDim.x) {
+      ss = fmaf(x[c], x[c], ss);
+      dot = fmaf(x[c], to_f(w[c]), dot);
+    }
   }
   ss = block_sum(ss, sh);
   dot = block_sum(dot, sh);
   if (threadIdx.x != 0) return;
-  const float z = dot / sqrtf(ss / (float)d + eps) + bias;
+  const float z = Sp ? (ss > 0.f ? sqrtf(dot) / sqrtf(ss) : __int_as_float(0x7f800000))
+                     : dot / sqrtf(ss / (float)d + eps) + bias;
   const int slot = m.slot[i], t = m.t[i];
   const int r = m.depth[i] + 1;
   int p = 0;
   if (mode != 2) {
     const int fe = fexit[slot * cap + t - 1];
     if (fe > 0) p = (r + 1 == fe);
-    else p = (z > thr) && (r >= r_min - 1);
+    else p = (Sp ? z < thr : z > thr) && (r >= r_min - 1);
   }
   if (r + 1 >= r_max) p = 0;
   pend_new[i] = p;
@@ -445,7 +456,7 @@ __global__ void k_compact(const float* __restrict__ X, RowMeta m, const int* __r
 // Batch re-formation: continuing rows first, then refill rows (slot order).
 __global__ void k_gather_core(const float* __restrict__ Xc, RowMeta mc, int B_cont,
                               const float* __restrict__ Pb, RowMeta mp, int n_ref,
-                              float* __restrict__ X, RowMeta mx, int d) {
+                              float* __restrict__ X, RowMeta mx, int d, float* __restrict__ Sprev) {
   pdl_wait();
   pdl_trigger();
   const int i = blockIdx.x;
@@ -455,7 +466,16 @@ __global__ void k_gather_core(const float* __restrict__ Xc, RowMeta mc, int B_co
   const float* src = (c ? Xc : Pb) + (size_t)j * d;
   const float4* s4 = reinterpret_cast<const float4*>(src);
   float4* d4 = reinterpret_cast<float4*>(X + (size_t)i * d);
-  for (int u = threadIdx.x; u < d / 4; u += blockDim.x) d4[u] = s4[u];
+  if (Sprev) {
+    float4* p4 = reinterpret_cast<float4*>(Sprev + (size_t)i * d);
+    for (int u = threadIdx.x; u < d / 4; u += blockDim.x) {
+      const float4 v = s4[u];
+      d4[u] = v;
+      p4[u] = v;
+    }
+  } else {
+    for (int u = threadIdx.x; u < d / 4; u += blockDim.x) d4[u] = s4[u];
+  }
   if (threadIdx.x == 0) {
     const RowMeta& s = c ? mc : mp;
     mx.slot[i] = s.slot[j];
@@ -622,12 +642,12 @@ void launch_rope_kv(cudaStream_t s, const float* QKV, int ns, int rows, const in
                                       kv, H, hd, rope, status);
 }
 template <typename T>
-void launch_gate(cudaStream_t s, const float* X, const T* w, float bias, float thr, float eps, int rows,
-                 int d, RowMeta meta, int mode, int r_min, int r_max, const int8_t* fexit, int cap,
+void launch_gate(cudaStream_t s, const float* X, const float* Sprev, const T* w, float bias, float thr, float eps,
+                 int rows, int d, RowMeta meta, int mode, int r_min, int r_max, const int8_t* fexit, int cap,
                  int* pend_new, uint8_t* ring, float* gtrace) {
   if (rows > 0)
-    count_launch(), launch_pdl(k_gate<T>, dim3(rows), dim3(256), 0, s, X, w, bias, thr, eps, rows, d, meta, mode, r_min, r_max, fexit, cap,
-                                   pend_new, ring, gtrace);
+    count_launch(), launch_pdl(k_gate<T>, dim3(rows), dim3(256), 0, s, X, Sprev, w, bias, thr, eps, rows, d, meta, mode,
+                               r_min, r_max, fexit, cap, pend_new, ring, gtrace);
 }
 void launch_compact(cudaStream_t s, const float* X, RowMeta m, const int* pend_new, int B, int d, int r_max,
                     int qc_off, float* Xc, RowMeta mc, float* Cb, RowMeta mb, KvGeom kv, int8_t* out_depth,
@@ -637,9 +657,10 @@ void launch_compact(cudaStream_t s, const float* X, RowMeta m, const int* pend_n
                                Xc, mc, Cb, mb, kv, out_depth, cap, core_slot0, hd, es, status);
 }
 void launch_gather_core(cudaStream_t s, const float* Xc, RowMeta mc, int B_cont, const float* Pb, RowMeta mp,
-                        int n_ref, float* X, RowMeta mx, int d) {
+                        int n_ref, float* X, RowMeta mx, int d, float* Sprev) {
   if (B_cont + n_ref > 0)
-    count_launch(), launch_pdl(k_gather_core, dim3(B_cont + n_ref), dim3(256), 0, s, Xc, mc, B_cont, Pb, mp, n_ref, X, mx, d);
+    count_launch(), launch_pdl(k_gather_core, dim3(B_cont + n_ref), dim3(256), 0, s, Xc, mc, B_cont, Pb, mp, n_ref, X, mx, d,
+                               Sprev);
 }
 void launch_gather_rows(cudaStream_t s, const float* src, const int* idx, const int* rslot, const int* rpos,
                         int n, float* dst, RowMeta md, int d) {
@@ -671,8 +692,8 @@ void launch_copy_rows(cudaStream_t s, const float* src, float* dst, int rows, in
   template void launch_concat<T>(cudaStream_t, const float*, int, const int*, const float*, T*, int, int);  \
   template void launch_rope_kv<T>(cudaStream_t, const float*, int, int, const int*, const int*, const int*,  \
                                   int, int, int, T*, KvGeom, int, int, const float2*, int*);                  \
-  template void launch_gate<T>(cudaStream_t, const float*, const T*, float, float, float, int, int,        \
-                               RowMeta, int, int, int, const int8_t*, int, int*, uint8_t*, float*);
+  template void launch_gate<T>(cudaStream_t, const float*, const float*, const T*, float, float, float, int, \
+                               int, RowMeta, int, int, int, const int8_t*, int, int*, uint8_t*, float*);
 CDB_INST(float)
 CDB_INST(__nv_bfloat16)
 #undef CDB_INST

@@ -89,8 +89,10 @@ void launch_rope_kv(cudaStream_t s, const float* QKV, int ns, int rows, const in
                     const int* mpos, const int* mdepth, int depth_uniform, int slot_base,
                     int clamp, T* Q, KvGeom kv, int H, int hd, const float2* rope,
                     int* status);
+// Exit gate after a loop step.  Sprev == nullptr: linear probe z = w . rmsnorm(X) + bias, fires
+// when z > thr; otherwise the convergence statistic c = ||X - Sprev|| / ||X||, fires when c < thr.
 template <typename T>
-void launch_gate(cudaStream_t s, const float* X, const T* w, float bias, float thr, float eps,
+void launch_gate(cudaStream_t s, const float* X, const float* Sprev, const T* w, float bias, float thr, float eps,
                  int rows, int d, RowMeta meta, int mode, int r_min, int r_max,
                  const int8_t* fexit, int max_new_cap, int* pend_new, uint8_t* ring,
                  float* gtrace);
@@ -100,8 +102,9 @@ void launch_compact(cudaStream_t s, const float* X, RowMeta m, const int* pend_n
                     int d, int r_max, int qc_off, float* Xc, RowMeta mc, float* Cb,
                     RowMeta mb, KvGeom kv, int8_t* out_depth, int max_new_cap, int n_core,
                     int core_slot0, int hd, int es, int* status);
+// Core batch = continuing rows then refills; Sprev (nullable) receives a copy of the gathered states.
 void launch_gather_core(cudaStream_t s, const float* Xc, RowMeta mc, int B_cont, const float* Pb,
-                        RowMeta mp, int n_ref, float* X, RowMeta mx, int d);
+                        RowMeta mp, int n_ref, float* X, RowMeta mx, int d, float* Sprev);
 void launch_gather_rows(cudaStream_t s, const float* src, const int* idx, const int* rslot,
                         const int* rpos, int n, float* dst, RowMeta md, int d);
 void launch_argmax(cudaStream_t s, const float* logits, int rows, int V, RowMeta m,

@@ -67,6 +67,12 @@ typedef enum {
   CDB_STAGE_CODA = 4
 } cdb_stage;
 
+/* Exit policies (gate_kind). */
+typedef enum {
+  CDB_GATE_PROBE = 0,       /* z = gate_w . rmsnorm(h) + gate_bias; exit when z > gate_threshold */
+  CDB_GATE_CONVERGENCE = 1  /* c = ||s_d - s_{d-1}|| / ||s_d||; exit when c < gate_threshold */
+} cdb_gate_kind;
+
 /* Model shape.  A pre-norm block is RMSNorm -> QKV (RoPE on q,k) -> causal
  * attention -> O-proj + residual -> RMSNorm -> SwiGLU MLP + residual.  The
  * exit gate is z = gate_w . rmsnorm(h) + gate_bias (unit gain) on the core
@@ -89,6 +95,17 @@ typedef struct {
    * second); in general step d uses slot min(d, s).  A prompt split across
    * prefill chunks then reads its earlier chunks at their last loop step. */
   int kv_slots;
+  /* cdb_gate_kind.  CDB_GATE_CONVERGENCE is Huginn's training-free exit
+   * ("Depth-adaptive Inference of Looped Language Models via Continuous Depth
+   * Batching", App. E.2): after loop step d, c_d = ||s_d - s_{d-1}||_2 /
+   * ||s_d||_2 over the fp32 core state, s_{d-1} being the state that entered
+   * step d (s_0 = 0 with an adapter, else the prelude output); the token
+   * exits when c_d < gate_threshold (equality does not exit; c is +inf when
+   * s_d = 0).  gate_w and gate_bias are unused (gate_w may be NULL) and
+   * r_min must be >= 3: the lookahead decision after step d takes effect at
+   * d + 2 and the first comparison that does not involve s_0 is after step
+   * 2.  gate_logits traces then hold c_d. */
+  int gate_kind;
 } cdb_model_desc;
 
 /* One transformer block; device pointers, row-major [out, in] like nn.Linear.

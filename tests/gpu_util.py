@@ -9,12 +9,12 @@ from oracle.model import OracleModel, decode_sequence
 NEAR = 1e-3  # gate logits / top-2 gaps closer than this are forced to the oracle's decision
 
 
-def oracle_traces(shape, wts, reqs, mode="adaptive", keep_logits=0):
+def oracle_traces(shape, wts, reqs, mode="adaptive", keep_logits=0, near_tol=NEAR):
     om = OracleModel(shape, wts)
     out = {}
     for r in reqs:
         out[r["seq_id"]] = decode_sequence(om, r["prompt"], r["gen_len"], mode, r.get("replay"),
-                                           None, keep_logits=keep_logits)
+                                           None, keep_logits=keep_logits, near_tol=near_tol)
     return out
 
 

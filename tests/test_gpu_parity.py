@@ -166,3 +166,42 @@ def test_huginn_like_single_slot_cache_matches_oracle():
     out, _ = gpu_run(shape, binding.device_weights(shape, wts), reqs, ref, mode="refill", W=3, K=2,
                      trace_tokens=8, trace_gate=True, attn_split=16, gap_band=BF16_GAP)
     compare(out, ref, BF16_TOL, check_gate=True)
+
+
+@pytest.mark.parametrize("variant,dtype,tol,kv_slots", [("looped", "fp32", FP32_TOL, 0),
+                                                         ("huginn_like", "bf16", BF16_TOL, 1)])
+def test_convergence_gate_matches_oracle(variant, dtype, tol, kv_slots):
+    """Huginn's convergence exit (App. E.2) decided live on the GPU: the
+    statistics c_d, exit depths and tokens match the oracle.  The bf16 case is
+    the pages' Huginn setting: convergence exit over a single-slot cache.  A
+    statistic within the gate tolerance of the threshold takes the oracle's
+    decision (each side's c may be off by that much).
+
+    With random weights c_d clusters tightly by loop step.  fp32 resolves
+    tokens inside a cluster, so its threshold is the median of the deciding
+    statistics (exit depths differ between tokens); in bf16 such a threshold
+    would make every decision a rounding-noise tie, so the threshold sits in
+    the gap between the step-2 and step-3 clusters (every token exits at 4)."""
+    from continuous_depth_batching_gb300 import binding
+    kw = dict(r_min=3, r_max=6, gate_kind="convergence", kv_slots=kv_slots)
+    if variant == "huginn_like":
+        kw.update(d_model=192, n_heads=2, head_dim=96, ffn=384, n_prelude=1, n_core=2, n_coda=1,
+                  has_adapter=True)
+    shape0 = _mini(dtype, conv_tau=0.0, **kw)
+    wts = make_weights(shape0)
+    reqs = _reqs(shape0, 5, 10, 40, 8, seed=23)
+    free = oracle_traces(shape0, wts, reqs[:2])  # never exits: the statistics' range
+    zs = np.array([z for tr in free.values() for z in tr.gate_logits])  # [forwards][r_max - 1]
+    if dtype == "fp32":
+        tau = float(np.median(zs[:, shape0.r_min - 2:shape0.r_max - 2]))
+    else:
+        tau = float(np.sqrt(zs[:, 1].min() * zs[:, 2].max()))
+    shape = dataclasses.replace(shape0, conv_tau=tau)
+    band = 1e-3 if dtype == "fp32" else BF16_TOL
+    ref = oracle_traces(shape, wts, reqs, "adaptive", keep_logits=8, near_tol=band)
+    out, _ = gpu_run(shape, binding.device_weights(shape, wts), reqs, ref, mode="refill", W=3, K=2,
+                     trace_tokens=8, trace_gate=True, attn_split=16, gap_band=GAP[dtype])
+    compare(out, ref, tol, check_gate=True)
+    depths = [e for tr in ref.values() for e in tr.exit_depths]
+    assert min(depths) >= 3 and len(set(depths)) >= (2 if dtype == "fp32" else 1), depths
+    assert sum(sum(tr.near_gate) for tr in ref.values()) <= len(depths) // 4

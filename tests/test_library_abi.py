@@ -89,3 +89,10 @@ def test_sim_rejects_bad_force_exit(L):
         sim.admit(0, 4, 3, np.array([1, 3], dtype=np.int8))  # depth 1 < r_min
     with pytest.raises(binding.CdbError):
         sim.admit(1, 4, 3, np.array([5, 3], dtype=np.int8))  # depth > r_max
+
+
+def test_convergence_gate_descriptor():
+    shape = dataclasses.replace(model_shape("huginn"), r_min=3, gate_kind="convergence", conv_tau=0.25)
+    desc = binding.model_desc(shape)
+    assert desc.gate_kind == 1 and desc.gate_threshold == pytest.approx(0.25)
+    assert binding.model_desc(model_shape("huginn")).gate_kind == 0
