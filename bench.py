@@ -334,6 +334,19 @@ def run_ours(args):
                                  "GBps": (v["bytes"] / (v["ms"] / 1e3) / 1e9) if v["ms"] else None,
                                  "TFps": (v["flops"] / (v["ms"] / 1e3) / 1e12) if v["ms"] else None}
                              for k, v in prof.items()}})
+    # Whole core step (the metric's "core-step % of roofline"): the algorithmic
+    # bytes and FLOPs of every kernel class per core step, averaged over the
+    # profile window, against the unprofiled time per core step of the timed
+    # window; the roofline time is max(bytes / HBM peak, FLOPs / tensor peak).
+    by_step = sum(v["bytes"] for v in prof.values()) / max(pcores, 1)
+    fl_step = sum(v["flops"] for v in prof.values()) / max(pcores, 1)
+    t_step = ms / max(cores, 1) / 1e3
+    t_roof = max(by_step / (hbm * 1e9), fl_step / (tf * 1e12))
+    core_step = {"bytes_per_step": by_step, "flops_per_step": fl_step, "s_per_step": t_step,
+                 "achieved_GBps": by_step / t_step / 1e9, "achieved_TFps": fl_step / t_step / 1e12,
+                 "roofline_s": t_roof, "frac": t_roof / t_step,
+                 "bound": "hbm" if by_step / (hbm * 1e9) >= fl_step / (tf * 1e12) else "tensor",
+                 "peaks": {"hbm_GBps": hbm, "tensor_TFps": tf, "source": src}}
 
     def full_job(mode):
         """The whole offline job through the public API: admit host prompts ... drain host results.
@@ -408,7 +421,8 @@ def run_ours(args):
                 "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
                 "config": _config(wl, shape, args.mode,
                                   f"inputs larger than L2 ({weight_gb(shape):.1f} GB of weights per step)"),
-                "roofline": roof, "cpu_baseline": cpu, "e2e": e2e, "modes": modes, "gpu_launches": launches,
+                "roofline": roof, "core_step_roofline": core_step, "cpu_baseline": cpu, "e2e": e2e,
+                "modes": modes, "gpu_launches": launches,
                 "clocks": clocks, "tokens_in_window": tot_toks, "core_steps": cores}
         print(json.dumps(line), flush=True)
     if world > 1:

@@ -53,7 +53,7 @@ class StepInfo(C.Structure):
     _fields_ = [("stage", C.c_int), ("batch", C.c_int), ("prefill_tokens", C.c_int), ("stage2", C.c_int),
                 ("batch2", C.c_int), ("exits", C.c_int), ("q_r", C.c_int), ("q_c", C.c_int), ("q_p", C.c_int),
                 ("q_d", C.c_int), ("depth_hist", C.c_int * MAX_DEPTH), ("step_index", C.c_int64),
-                ("new_tokens", C.c_int)]
+                ("new_tokens", C.c_int), ("ctx", C.c_int64), ("ctx2", C.c_int64)]
 
     def as_dict(self):
         d = {f: getattr(self, f) for f, _ in self._fields_ if f != "depth_hist"}
@@ -125,6 +125,12 @@ def lib(path: str | None = None) -> C.CDLL:
     L.cdb_sim_finished.argtypes = [C.c_void_p, C.POINTER(C.c_int64), C.c_int, C.POINTER(C.c_int)]
     L.cdb_sim_free.argtypes = [C.c_void_p]
     L.cdb_sim_free.restype = None
+    L.cdb_predict_job.argtypes = [C.POINTER(Job), C.c_int, C.c_int, C.POINTER(LatencyModel), C.POINTER(Prediction)]
+    L.cdb_roofline_latency.argtypes = [C.POINTER(ModelDesc), C.c_double, C.c_double, C.c_double,
+                                       C.POINTER(LatencyModel)]
+    L.cdb_select_schedule.argtypes = [C.POINTER(Job), C.POINTER(LatencyModel), C.POINTER(C.c_int),
+                                      C.POINTER(C.c_int), C.POINTER(Prediction), C.POINTER(C.c_double),
+                                      C.POINTER(C.c_double)]
     _lib = L
     return L
 
@@ -403,3 +409,101 @@ class Sim:
             self.L.cdb_sim_free(self.h)
         except Exception:
             pass
+
+
+# ---------------------------------------------------------------------------
+# latency planner (include/cdb_plan.h)
+# ---------------------------------------------------------------------------
+
+STAGES = ("prefill", "prelude", "core", "coda")
+
+
+class StageCost(C.Structure):
+    _fields_ = [("delta", C.c_double), ("gamma", C.c_double), ("alpha", C.c_double)]
+
+
+class LatencyModel(C.Structure):
+    _fields_ = [(s, StageCost) for s in STAGES]
+
+    def as_dict(self):
+        return {s: {k: getattr(getattr(self, s), k) for k in ("delta", "gamma", "alpha")} for s in STAGES}
+
+    @classmethod
+    def from_dict(cls, d):
+        lm = cls()
+        for s in STAGES:
+            c = d.get(s, {})
+            setattr(lm, s, StageCost(float(c.get("delta", 0.0)), float(c.get("gamma", 0.0)),
+                                     float(c.get("alpha", 0.0))))
+        return lm
+
+
+class Job(C.Structure):
+    _fields_ = [("n_seqs", C.c_int), ("prompt_len", C.POINTER(C.c_int32)), ("gen_len", C.POINTER(C.c_int32)),
+                ("exit_depths", C.POINTER(C.c_int8)), ("W", C.c_int), ("M", C.c_int), ("S", C.c_int),
+                ("r_max", C.c_int), ("r_min", C.c_int), ("kv_blocks", C.c_int), ("kv_headroom", C.c_float),
+                ("max_ctx", C.c_int), ("max_new_cap", C.c_int)]
+
+
+class Prediction(C.Structure):
+    _fields_ = [("seconds", C.c_double), ("prefill_seconds", C.c_double), ("prelude_seconds", C.c_double),
+                ("core_seconds", C.c_double), ("coda_seconds", C.c_double), ("prefill_stages", C.c_int64),
+                ("prelude_stages", C.c_int64), ("core_steps", C.c_int64), ("coda_stages", C.c_int64),
+                ("tokens", C.c_int64), ("core_token_steps", C.c_int64), ("mean_core_batch", C.c_double),
+                ("mean_coda_batch", C.c_double)]
+
+    def as_dict(self):
+        return {f: getattr(self, f) for f, _ in self._fields_}
+
+
+class PlanJob:
+    """An offline job for the planner: requests with prompt / output lengths and exit depths."""
+
+    def __init__(self, reqs, W, M=8192, S=0, r_max=4, r_min=2, kv_blocks=1 << 22, kv_headroom=0.0,
+                 max_ctx=None, max_new_cap=None):
+        import numpy as np
+        self._p = np.ascontiguousarray([len(r["prompt"]) if "prompt" in r else r["prompt_len"] for r in reqs],
+                                       dtype=np.int32)
+        self._g = np.ascontiguousarray([r["gen_len"] for r in reqs], dtype=np.int32)
+        ex = [np.asarray(r["replay"] if r.get("replay") is not None else r.get("exit_depths", []), dtype=np.int8)
+              for r in reqs]
+        for e, g in zip(ex, self._g):
+            if len(e) != g - 1:
+                raise ValueError("every request needs gen_len - 1 exit depths")
+        self._e = np.ascontiguousarray(np.concatenate(ex) if ex else np.zeros(0, np.int8), dtype=np.int8)
+        mc = int(max_ctx or int((self._p + self._g - 1).max()))
+        mn = int(max_new_cap or int(self._g.max()))
+        self.job = Job(len(reqs), self._p.ctypes.data_as(C.POINTER(C.c_int32)),
+                       self._g.ctypes.data_as(C.POINTER(C.c_int32)), self._e.ctypes.data_as(C.POINTER(C.c_int8)),
+                       W, M, S, r_max, r_min, kv_blocks, kv_headroom, mc, mn)
+
+
+def predict_job(job: PlanJob, mode, K, lm: LatencyModel) -> dict:
+    out = Prediction()
+    rc = lib().cdb_predict_job(C.byref(job.job), MODES[mode] if isinstance(mode, str) else mode, K, C.byref(lm),
+                               C.byref(out))
+    if rc != OK:
+        raise CdbError(rc, "cdb_predict_job")
+    return out.as_dict()
+
+
+def roofline_latency(shape, hbm_gbps, tensor_tflops, launch_s=0.0) -> LatencyModel:
+    lm = LatencyModel()
+    desc = model_desc(shape)
+    rc = lib().cdb_roofline_latency(C.byref(desc), hbm_gbps, tensor_tflops, launch_s, C.byref(lm))
+    if rc != OK:
+        raise CdbError(rc, "cdb_roofline_latency")
+    return lm
+
+
+def select_schedule(job: PlanJob, lm: LatencyModel) -> dict:
+    mode, K = C.c_int(), C.c_int()
+    best = Prediction()
+    r_s, n_s = C.c_double(), C.c_double()
+    rc = lib().cdb_select_schedule(C.byref(job.job), C.byref(lm), C.byref(mode), C.byref(K), C.byref(best),
+                                   C.byref(r_s), C.byref(n_s))
+    if rc != OK:
+        raise CdbError(rc, "cdb_select_schedule")
+    names = {v: k for k, v in MODES.items()}
+    return {"mode": names[mode.value], "K": K.value, "prediction": best.as_dict(),
+            "refill_seconds": r_s.value, "no_refill_seconds": n_s.value}

@@ -25,6 +25,7 @@ LIB = os.path.join(BUILD, "libcdb.so")
 SOURCES = [
     "sched.cpp",
     "sim.cpp",
+    "planner.cpp",
     "engine.cu",
     "kernels.cu",
     "attention.cu",

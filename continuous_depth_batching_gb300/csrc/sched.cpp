@@ -126,12 +126,16 @@ int Scheduler::run_prelude(std::vector<Tok>& rows, cdb_step_info* info, bool sec
   refill_ += (int)rows.size();
   record(CDB_STAGE_PRELUDE, (int)rows.size(), 0, 0, nullptr);
   if (info) {
+    int64_t ctx = 0;
+    for (auto& t : rows) ctx += t.pos + 1;
     if (second) {
       info->stage2 = CDB_STAGE_PRELUDE;
       info->batch2 = (int)rows.size();
+      info->ctx2 = ctx;
     } else {
       info->stage = CDB_STAGE_PRELUDE;
       info->batch = (int)rows.size();
+      info->ctx = ctx;
     }
   }
   return CDB_OK;
@@ -179,6 +183,7 @@ int Scheduler::run_prefill(cdb_step_info* info) {
     info->batch = plan.n_seqs;
     info->prefill_tokens = (int)plan.rows.size();
     info->new_tokens = (int)plan.done_seqs.size();
+    for (auto& r : plan.rows) info->ctx += r.pos + 1;
   }
   std::vector<Tok> next;
   for (int si : plan.done_seqs) {
@@ -218,6 +223,7 @@ int Scheduler::run_coda(cdb_step_info* info) {
     info->stage = CDB_STAGE_CODA;
     info->batch = (int)rows.size();
     info->new_tokens = (int)rows.size();
+    for (auto& t : rows) info->ctx += t.pos + 1;
   }
   std::vector<Tok> next;
   for (auto& t : rows) {
@@ -310,6 +316,8 @@ int Scheduler::step_core(cdb_step_info* info) {
   int rc = ex_->core(p);
   if (rc < 0) return fail(rc, ex_->error());
   const int64_t this_step = steps_++;
+  int64_t ctx = 0;
+  for (auto& t : qr_) ctx += t.pos + 1;
 
   // Lookahead: the gate results of the previous step decide this step's exits.
   bool need = false;
@@ -348,6 +356,7 @@ int Scheduler::step_core(cdb_step_info* info) {
     info->stage = CDB_STAGE_LOOP;
     info->batch = p.B;
     info->exits = exits;
+    info->ctx = ctx;
     std::memcpy(info->depth_hist, hist, sizeof(hist));
   }
   fill_queues(info);

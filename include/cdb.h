@@ -152,6 +152,8 @@ typedef struct {
   int depth_hist[CDB_MAX_DEPTH]; /* loop: depth_hist[i] tokens ran loop step i+1 */
   int64_t step_index;            /* loop steps issued so far, this one included */
   int new_tokens;                /* tokens generated by this call (coda rows + prompts completed) */
+  int64_t ctx, ctx2;             /* context entries of stage / stage2: the sum over its rows of
+                                    (position + 1), the keys their attention reads per layer */
 } cdb_step_info;
 
 /* One finished sequence.  The caller sets the pointers before cdb_drain; the

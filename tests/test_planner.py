@@ -1,0 +1,120 @@
+"""The latency planner (include/cdb_plan.h) against closed forms of the schedule.
+
+"Depth-adaptive Inference of Looped Language Models via Continuous Depth
+Batching", §5 (t = delta + gamma N_b + alpha N_c per recurrent step), §6.4 /
+Fig. 7 (minimum coda batch K) and Algorithms 1-2.  With one cost term switched
+on at a time the predicted time counts something the schedule fixes:
+
+* core gamma: loop-step tokens, the sum of all exit depths (any mode);
+* core alpha: sum over decode forwards of depth x (position + 1);
+* prefill gamma / alpha: prompt tokens / causal pairs sum P (P + 1) / 2;
+* coda gamma and prelude gamma: decode forwards, sum (gen_len - 1);
+* core delta: core steps.  No-refill with one cohort (W >= requests, equal
+  output lengths) runs, per generated token, as many steps as the deepest
+  token of the cohort; refill with K = 1 and W >= requests never makes a
+  token wait, so it runs as many steps as the longest chain of exit depths.
+"""
+
+import dataclasses
+
+import numpy as np
+import pytest
+
+from continuous_depth_batching_gb300 import binding
+from synth import model_shape
+
+
+def _reqs(n, gen, r_min, r_max, seed=3, plo=5, phi=40):
+    rng = np.random.default_rng(seed)
+    return [dict(prompt_len=int(rng.integers(plo, phi + 1)), gen_len=gen,
+                 exit_depths=rng.integers(r_min, r_max + 1, gen - 1).astype(np.int8)) for _ in range(n)]
+
+
+def _lm(**terms):
+    d = {}
+    for k, v in terms.items():
+        stage, term = k.split("_")
+        d.setdefault(stage, {})[term] = v
+    return binding.LatencyModel.from_dict(d)
+
+
+@pytest.mark.parametrize("mode", ["refill", "no_refill", "fixed_depth"])
+def test_cost_terms_count_the_schedule(mode):
+    r_min, r_max = 2, 6
+    reqs = _reqs(7, 9, r_min, r_max)
+    job = binding.PlanJob(reqs, W=4, M=64, r_max=r_max, r_min=r_min)
+    depth = [np.full(r["gen_len"] - 1, r_max) if mode == "fixed_depth" else r["exit_depths"] for r in reqs]
+    want_steps = sum(int(e.sum()) for e in depth)
+    want_ctx = sum(int((e * (r["prompt_len"] + np.arange(len(e)) + 1)).sum()) for e, r in zip(depth, reqs))
+    fwd = sum(r["gen_len"] - 1 for r in reqs)
+    P = np.array([r["prompt_len"] for r in reqs])
+    assert binding.predict_job(job, mode, 1, _lm(core_gamma=1.0))["seconds"] == want_steps
+    assert binding.predict_job(job, mode, 1, _lm(core_alpha=1.0))["seconds"] == want_ctx
+    assert binding.predict_job(job, mode, 1, _lm(prefill_gamma=1.0))["seconds"] == P.sum()
+    assert binding.predict_job(job, mode, 1, _lm(prefill_alpha=1.0))["seconds"] == (P * (P + 1) // 2).sum()
+    assert binding.predict_job(job, mode, 1, _lm(coda_gamma=1.0))["seconds"] == fwd
+    assert binding.predict_job(job, mode, 1, _lm(prelude_gamma=1.0))["seconds"] == fwd
+    p = binding.predict_job(job, mode, 1, _lm(core_gamma=1.0))
+    assert p["tokens"] == sum(r["gen_len"] for r in reqs)
+    assert p["core_token_steps"] == want_steps
+
+
+def test_core_steps_of_one_cohort_and_of_refill():
+    r_min, r_max = 2, 5
+    reqs = _reqs(6, 8, r_min, r_max, seed=11)
+    job = binding.PlanJob(reqs, W=8, M=4096, S=1, r_max=r_max, r_min=r_min)
+    E = np.stack([r["exit_depths"] for r in reqs])          # [request][decode forward]
+    nr = binding.predict_job(job, "no_refill", 1, _lm(core_delta=1.0))
+    assert nr["core_steps"] == E.max(axis=0).sum()
+    rf = binding.predict_job(job, "refill", 1, _lm(core_delta=1.0))
+    assert rf["core_steps"] == E.sum(axis=1).max()
+    fx = binding.predict_job(job, "fixed_depth", 1, _lm(core_delta=1.0))
+    assert fx["core_steps"] == r_max * E.shape[1]
+
+
+def test_roofline_model_of_the_ouro_shape():
+    shape = model_shape("ouro")
+    lm = binding.roofline_latency(shape, 6000.0, 1500.0).as_dict()
+    d, f = shape.d_model, shape.ffn
+    core_bytes = shape.n_core * (4 * d * d + 3 * d * f) * 2
+    assert lm["core"]["delta"] == pytest.approx(core_bytes / 6000e9)
+    assert lm["core"]["alpha"] == pytest.approx(shape.n_core * 2 * d * 2 / 6000e9)
+    assert lm["core"]["gamma"] == pytest.approx(2 * core_bytes / 2 / 1500e12)
+    assert lm["coda"]["delta"] == pytest.approx(shape.vocab * d * 2 / 6000e9)
+    assert lm["prelude"]["delta"] == 0.0
+    # Launch cost adds to delta only.
+    lm2 = binding.roofline_latency(shape, 6000.0, 1500.0, launch_s=1e-6).as_dict()
+    assert lm2["core"]["delta"] > lm["core"]["delta"] and lm2["core"]["gamma"] == lm["core"]["gamma"]
+
+
+def test_selection_follows_the_regime():
+    """Memory-bound core steps (delta dominates): refill wins (§5).  Costly
+    boundary stages with compute-bound core steps: no-refill wins (§6.2,
+    Huginn).  Costly coda with refill forced on: a larger K wins (§6.4)."""
+    r_min, r_max = 2, 8
+    reqs = _reqs(32, 12, r_min, r_max, seed=5)
+    job = binding.PlanJob(reqs, W=16, M=4096, r_max=r_max, r_min=r_min)
+    mem = binding.select_schedule(job, _lm(core_delta=1.0, core_gamma=0.001))
+    assert mem["mode"] == "refill" and mem["refill_seconds"] < mem["no_refill_seconds"]
+    heavy = binding.select_schedule(job, _lm(core_gamma=0.01, coda_delta=1.0, prelude_delta=1.0))
+    assert heavy["mode"] == "no_refill" and heavy["refill_seconds"] >= heavy["no_refill_seconds"]
+    ks = {K: binding.predict_job(job, "refill", K, _lm(core_delta=0.1, core_gamma=0.01, coda_delta=1.0))["seconds"]
+          for K in (1, 4, 16)}
+    assert ks[4] < ks[1]
+
+
+def test_planner_rejects_bad_jobs():
+    reqs = _reqs(2, 4, 2, 4)
+    job = binding.PlanJob(reqs, W=2, r_max=4, r_min=2)
+    with pytest.raises(binding.CdbError):
+        binding.predict_job(job, "refill", 0, _lm(core_delta=1.0))
+    with pytest.raises(binding.CdbError):
+        binding.predict_job(job, "refill", 1, _lm(core_delta=-1.0))
+    bad = [dict(r, exit_depths=np.full(3, 9, np.int8)) for r in reqs]
+    with pytest.raises(binding.CdbError):
+        binding.predict_job(binding.PlanJob(bad, W=2, r_max=4, r_min=2), "refill", 1, _lm(core_delta=1.0))
+    with pytest.raises(ValueError):
+        binding.PlanJob([dict(reqs[0], exit_depths=np.zeros(1, np.int8))], W=2)
+    huginn = dataclasses.replace(model_shape("huginn"), d_model=0)
+    with pytest.raises(binding.CdbError):
+        binding.roofline_latency(huginn, 1.0, 1.0)
