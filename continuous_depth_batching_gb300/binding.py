@@ -415,7 +415,7 @@ class Sim:
 # latency planner (include/cdb_plan.h)
 # ---------------------------------------------------------------------------
 
-STAGES = ("prefill", "prelude", "core", "coda")
+COST_STAGES = ("prefill", "prelude", "core", "coda")
 
 
 class StageCost(C.Structure):
@@ -423,15 +423,15 @@ class StageCost(C.Structure):
 
 
 class LatencyModel(C.Structure):
-    _fields_ = [(s, StageCost) for s in STAGES]
+    _fields_ = [(s, StageCost) for s in COST_STAGES]
 
     def as_dict(self):
-        return {s: {k: getattr(getattr(self, s), k) for k in ("delta", "gamma", "alpha")} for s in STAGES}
+        return {s: {k: getattr(getattr(self, s), k) for k in ("delta", "gamma", "alpha")} for s in COST_STAGES}
 
     @classmethod
     def from_dict(cls, d):
         lm = cls()
-        for s in STAGES:
+        for s in COST_STAGES:
             c = d.get(s, {})
             setattr(lm, s, StageCost(float(c.get("delta", 0.0)), float(c.get("gamma", 0.0)),
                                      float(c.get("alpha", 0.0))))
