@@ -118,16 +118,18 @@ struct Parts {
   size_t ss;  // floats between consecutive splits
   int ld;     // floats between consecutive rows
   // Sum of columns c..c+3 of `row` (c and ld multiples of 4): every partial
-  // is loaded before the first add, then added in split order.
-  __device__ __forceinline__ float4 sum4(int row, int c) const {
+  // is loaded before the first add, then added in split order.  The loop is
+  // unrolled for at most S partials (S >= ns).
+  template <int S>
+  __device__ __forceinline__ float4 sum4_upto(int row, int c) const {
     const float4* p = reinterpret_cast<const float4*>(P + (size_t)row * ld + c);
     const size_t s4 = ss / 4;
-    float4 v[kGemmMaxSplits];
+    float4 v[S];
 #pragma unroll
-    for (int q = 0; q < kGemmMaxSplits; ++q) v[q] = q < ns ? p[q * s4] : make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int q = 0; q < S; ++q) v[q] = q < ns ? p[q * s4] : make_float4(0.f, 0.f, 0.f, 0.f);
     float4 g = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-    for (int q = 0; q < kGemmMaxSplits; ++q)
+    for (int q = 0; q < S; ++q)
       if (q < ns) {
         g.x += v[q].x;
         g.y += v[q].y;
@@ -136,11 +138,59 @@ struct Parts {
       }
     return g;
   }
+  // The same sum; the unroll depth follows ns (uniform across the grid).
+  __device__ __forceinline__ float4 sum4(int row, int c) const {
+    if (ns <= 4) return sum4_upto<4>(row, c);
+    if (ns <= 8) return sum4_upto<8>(row, c);
+    return sum4_upto<kGemmMaxSplits>(row, c);
+  }
 };
+
+// Four consecutive elements in one access (8 bytes for bf16, 16 for fp32).
+template <typename T>
+__device__ __forceinline__ void store4(T* p, const T (&v)[4]);
+template <>
+__device__ __forceinline__ void store4<float>(float* p, const float (&v)[4]) {
+  *reinterpret_cast<float4*>(p) = make_float4(v[0], v[1], v[2], v[3]);
+}
+template <>
+__device__ __forceinline__ void store4<__nv_bfloat16>(__nv_bfloat16* p, const __nv_bfloat16 (&v)[4]) {
+  __nv_bfloat162 lo, hi;
+  lo.x = v[0];
+  lo.y = v[1];
+  hi.x = v[2];
+  hi.y = v[3];
+  uint2 u;
+  u.x = *reinterpret_cast<const uint32_t*>(&lo);
+  u.y = *reinterpret_cast<const uint32_t*>(&hi);
+  *reinterpret_cast<uint2*>(p) = u;
+}
+template <typename T>
+__device__ __forceinline__ void load4(const T* p, T (&v)[4]);
+template <>
+__device__ __forceinline__ void load4<float>(const float* p, float (&v)[4]) {
+  const float4 f = *reinterpret_cast<const float4*>(p);
+  v[0] = f.x;
+  v[1] = f.y;
+  v[2] = f.z;
+  v[3] = f.w;
+}
+template <>
+__device__ __forceinline__ void load4<__nv_bfloat16>(const __nv_bfloat16* p, __nv_bfloat16 (&v)[4]) {
+  const uint2 u = *reinterpret_cast<const uint2*>(p);
+  const __nv_bfloat162 lo = *reinterpret_cast<const __nv_bfloat162*>(&u.x);
+  const __nv_bfloat162 hi = *reinterpret_cast<const __nv_bfloat162*>(&u.y);
+  v[0] = lo.x;
+  v[1] = lo.y;
+  v[2] = hi.x;
+  v[3] = hi.y;
+}
 
 // With pending partials (mode 1: residual, X += sum; mode 2: store, X = sum)
 // X is updated first, then normalised.
-template <typename T>
+// One block per row; each thread keeps KV four-column groups of the row in
+// registers from the fold to the normalised store (d and lda multiples of 4).
+template <typename T, int KV>
 __global__ void k_rmsnorm(float* __restrict__ X, const T* __restrict__ g, T* __restrict__ A, int rows, int d,
                           float eps, int lda, Parts pp, int mode) {
   pdl_wait();
@@ -149,33 +199,51 @@ __global__ void k_rmsnorm(float* __restrict__ X, const T* __restrict__ g, T* __r
   const int i = blockIdx.x;
   if (i >= rows) return;
   float* x = X + (size_t)i * d;
-  float ss = 0.f;
-  if (pp.ns > 0) {  // d is a multiple of 4 whenever partials exist (bf16 models)
-    for (int c = threadIdx.x * 4; c < d; c += blockDim.x * 4) {
-      const float4 v = pp.sum4(i, c);
-      float4 o = *reinterpret_cast<const float4*>(x + c);
-      if (mode == 1) {
-        o.x += v.x;
-        o.y += v.y;
-        o.z += v.z;
-        o.w += v.w;
-      } else {
-        o = v;
+  const int n4 = d / 4;
+  const bool keep = !(pp.ns > 0 && mode == 2);  // mode 2 replaces X by the sum
+  float4 o[KV];
+#pragma unroll
+  for (int k = 0; k < KV; ++k) {
+    const int u = threadIdx.x + k * blockDim.x;
+    o[k] = u < n4 && keep ? *reinterpret_cast<const float4*>(x + 4 * u) : make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+  if (pp.ns > 0) {
+#pragma unroll
+    for (int k = 0; k < KV; ++k) {
+      const int u = threadIdx.x + k * blockDim.x;
+      if (u < n4) {
+        const float4 v = pp.sum4(i, 4 * u);
+        o[k].x += v.x;
+        o[k].y += v.y;
+        o[k].z += v.z;
+        o[k].w += v.w;
+        *reinterpret_cast<float4*>(x + 4 * u) = o[k];
       }
-      *reinterpret_cast<float4*>(x + c) = o;
-      ss = fmaf(o.x, o.x, ss);
-      ss = fmaf(o.y, o.y, ss);
-      ss = fmaf(o.z, o.z, ss);
-      ss = fmaf(o.w, o.w, ss);
     }
-  } else {
-    for (int c = threadIdx.x; c < d; c += blockDim.x) ss = fmaf(x[c], x[c], ss);
+  }
+  float ss = 0.f;
+#pragma unroll
+  for (int k = 0; k < KV; ++k) {
+    ss = fmaf(o[k].x, o[k].x, ss);
+    ss = fmaf(o[k].y, o[k].y, ss);
+    ss = fmaf(o[k].z, o[k].z, ss);
+    ss = fmaf(o[k].w, o[k].w, ss);
   }
   ss = block_sum(ss, sh);
   const float inv = 1.0f / sqrtf(ss / (float)d + eps);
   if (A == nullptr) return;
-  for (int c = threadIdx.x; c < d; c += blockDim.x)
-    A[(size_t)i * lda + c] = from_f<T>(x[c] * inv * to_f(g[c]));
+#pragma unroll
+  for (int k = 0; k < KV; ++k) {
+    const int u = threadIdx.x + k * blockDim.x;
+    if (u < n4) {
+      const float w[4] = {o[k].x, o[k].y, o[k].z, o[k].w};
+      T gv[4], out[4];
+      load4(g + 4 * u, gv);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) out[e] = from_f<T>(w[e] * inv * to_f(gv[e]));
+      store4(A + (size_t)i * lda + 4 * u, out);
+    }
+  }
 }
 
 // C[i][c] (row stride ldc) = sum of the partials (mode 2) or C + sum (mode 1).
@@ -234,28 +302,8 @@ __global__ void k_concat(const float* __restrict__ E, int e_per_slot, const int*
 
 // Row i at position p and loop step r writes K,V into slot slot_base + r-1
 // (core layers; slot_base + min(r, clamp) - 1 with a shared layout) or
-// slot_base (prelude / coda layers, clamp = 0).
-template <typename T>
-__device__ __forceinline__ void store4(T* p, const T (&v)[4]);
-template <>
-__device__ __forceinline__ void store4<float>(float* p, const float (&v)[4]) {
-  *reinterpret_cast<float4*>(p) = make_float4(v[0], v[1], v[2], v[3]);
-}
-template <>
-__device__ __forceinline__ void store4<__nv_bfloat16>(__nv_bfloat16* p, const __nv_bfloat16 (&v)[4]) {
-  __nv_bfloat162 lo, hi;
-  lo.x = v[0];
-  lo.y = v[1];
-  hi.x = v[2];
-  hi.y = v[3];
-  uint2 u;
-  u.x = *reinterpret_cast<const uint32_t*>(&lo);
-  u.y = *reinterpret_cast<const uint32_t*>(&hi);
-  *reinterpret_cast<uint2*>(p) = u;
-}
-
-// QKV arrives as split-K partials (qkv.ns >= 1; one partial is the plain
-// GEMM output).
+// slot_base (prelude / coda layers, clamp = 0).  QKV arrives as split-K
+// partials (qkv.ns >= 1; one partial is the plain GEMM output).
 template <typename T>
 __global__ void k_rope_kv(Parts qkv, int rows, const int* __restrict__ mslot,
                           const int* __restrict__ mpos, const int* __restrict__ mdepth,
@@ -280,37 +328,34 @@ __global__ void k_rope_kv(Parts qkv, int rows, const int* __restrict__ mslot,
   T* kdst = pool + (((size_t)blk * kv.nsl + sl) * 2 + 0) * 16 * d + (size_t)(pos & 15) * hd;
   T* vdst = kdst + (size_t)16 * d;
   const float2* cs = rope + (size_t)pos * half;
-  // Four consecutive rotation pairs (j, j + half) per thread; half is a
-  // multiple of 4 for every supported head dim.
+  // blockIdx.z: 0 = q (rotated, to Q), 1 = k (rotated, to the K page), 2 = v
+  // (to the V page).  Four consecutive rotation pairs (j, j + half) per
+  // thread; half is a multiple of 4 for every supported head dim.
+  const int part = blockIdx.z;
   const int quads = H * half / 4;
   for (int u = blockIdx.y * blockDim.x + threadIdx.x; u < quads; u += gridDim.y * blockDim.x) {
     const int h = u / (half / 4), j0 = (u % (half / 4)) * 4;
     const int a = h * hd + j0, b = a + half;
-    const float4 qa = qkv.sum4(i, a), qb = qkv.sum4(i, b);
-    const float4 ka = qkv.sum4(i, d + a), kb = qkv.sum4(i, d + b);
-    const float4 va = qkv.sum4(i, 2 * d + a), vb = qkv.sum4(i, 2 * d + b);
-    const float qa_[4] = {qa.x, qa.y, qa.z, qa.w}, qb_[4] = {qb.x, qb.y, qb.z, qb.w};
-    const float ka_[4] = {ka.x, ka.y, ka.z, ka.w}, kb_[4] = {kb.x, kb.y, kb.z, kb.w};
-    const float va_[4] = {va.x, va.y, va.z, va.w}, vb_[4] = {vb.x, vb.y, vb.z, vb.w};
-    const size_t kofs = (size_t)h * 16 * hd + j0;
-    T qo[2][4], ko[2][4], vo[2][4];
+    const float4 xa = qkv.sum4(i, part * d + a), xb = qkv.sum4(i, part * d + b);
+    const float a_[4] = {xa.x, xa.y, xa.z, xa.w}, b_[4] = {xb.x, xb.y, xb.z, xb.w};
+    T lo[4], hi[4];
+    if (part < 2) {
 #pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const float2 r = cs[j0 + e];
-      qo[0][e] = from_f<T>(qa_[e] * r.x - qb_[e] * r.y);
-      qo[1][e] = from_f<T>(qb_[e] * r.x + qa_[e] * r.y);
-      ko[0][e] = from_f<T>(ka_[e] * r.x - kb_[e] * r.y);
-      ko[1][e] = from_f<T>(kb_[e] * r.x + ka_[e] * r.y);
-      vo[0][e] = from_f<T>(va_[e]);
-      vo[1][e] = from_f<T>(vb_[e]);
+      for (int e = 0; e < 4; ++e) {
+        const float2 r = cs[j0 + e];
+        lo[e] = from_f<T>(a_[e] * r.x - b_[e] * r.y);
+        hi[e] = from_f<T>(b_[e] * r.x + a_[e] * r.y);
+      }
+    } else {
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        lo[e] = from_f<T>(a_[e]);
+        hi[e] = from_f<T>(b_[e]);
+      }
     }
-    // Four consecutive elements per store (8 bytes for bf16, 16 for fp32).
-    store4(Q + (size_t)i * d + a, qo[0]);
-    store4(Q + (size_t)i * d + b, qo[1]);
-    store4(kdst + kofs, ko[0]);
-    store4(kdst + kofs + half, ko[1]);
-    store4(vdst + kofs, vo[0]);
-    store4(vdst + kofs + half, vo[1]);
+    T* dst = part == 0 ? Q + (size_t)i * d + a : (part == 1 ? kdst : vdst) + (size_t)h * 16 * hd + j0;
+    store4(dst, lo);
+    store4(dst + half, hi);
   }
 }
 
@@ -612,7 +657,18 @@ template <typename T>
 void launch_rmsnorm(cudaStream_t s, float* X, const T* g, T* A, int rows, int d, float eps, int lda,
                     const float* P, int ns, int mode) {
   Parts pp{P, ns, (size_t)rows * d, d};
-  if (rows > 0) count_launch(), launch_pdl(k_rmsnorm<T>, dim3(rows), dim3(256), 0, s, X, g, A, rows, d, eps, lda, pp, mode);
+  if (rows <= 0) return;
+  // d and lda are multiples of 4 (the model descriptor requires it of d_model).
+  const int n4 = d / 4;
+  const int kv = n4 <= 512 ? 1 : n4 <= 1024 ? 2 : n4 <= 2048 ? 4 : 8;
+  const int threads = ((n4 + kv - 1) / kv + 31) / 32 * 32;
+  count_launch();
+  switch (kv) {
+    case 1: launch_pdl(k_rmsnorm<T, 1>, dim3(rows), dim3(threads), 0, s, X, g, A, rows, d, eps, lda, pp, mode); break;
+    case 2: launch_pdl(k_rmsnorm<T, 2>, dim3(rows), dim3(threads), 0, s, X, g, A, rows, d, eps, lda, pp, mode); break;
+    case 4: launch_pdl(k_rmsnorm<T, 4>, dim3(rows), dim3(threads), 0, s, X, g, A, rows, d, eps, lda, pp, mode); break;
+    default: launch_pdl(k_rmsnorm<T, 8>, dim3(rows), dim3(threads), 0, s, X, g, A, rows, d, eps, lda, pp, mode); break;
+  }
 }
 void launch_fold(cudaStream_t s, const float* P, int ns, int rows, int n, float* C, int ldc, int mode) {
   Parts pp{P, ns, (size_t)rows * n, n};
@@ -638,7 +694,7 @@ void launch_rope_kv(cudaStream_t s, const float* QKV, int ns, int rows, const in
   const int quads = H * (hd / 2) / 4;
   const int gy = (quads + 63) / 64;
   if (rows > 0)
-    count_launch(), launch_pdl(k_rope_kv<T>, dim3(rows, gy), dim3(64), 0, s, qkv, rows, mslot, mpos, mdepth, depth_uniform, slot_base, clamp, Q,
+    count_launch(), launch_pdl(k_rope_kv<T>, dim3(rows, gy, 3), dim3(64), 0, s, qkv, rows, mslot, mpos, mdepth, depth_uniform, slot_base, clamp, Q,
                                       kv, H, hd, rope, status);
 }
 template <typename T>
