@@ -1071,28 +1071,72 @@ __global__ void __launch_bounds__(5 * 32)
 }
 
 // Merge split partials in split order: o = sum_s e^{m_s - m} acc_s / sum_s e^{m_s - m} l_s.
+// One warp per (row, head): lane j owns columns 4j..4j+3 (HDv <= 128).  The
+// split weights 2^(m_s - m) are computed once per split by the lane that
+// loaded (m_s, l_s) and broadcast; the output sums over splits in split order.
 template <typename T>
 __global__ void k_attn_combine(int rows, const int* __restrict__ mpos, int H, int HDv, int d, int split,
                                int max_splits, const float* __restrict__ part_o,
                                const float* __restrict__ part_ml, T* __restrict__ O) {
   pdl_wait();
   pdl_trigger();
-  const int row = blockIdx.x / H, h = blockIdx.x % H;
+  const int lane = threadIdx.x & 31;
+  const int item = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  const int row = item / H, h = item % H;
   if (row >= rows) return;
   const int L = mpos[row] + 1;
   const int nsp = (L + split - 1) / split;
   if (nsp <= 1) return;
   const size_t pi = ((size_t)row * H + h) * max_splits;
   float m = -INFINITY;
-  for (int s = 0; s < nsp; ++s) m = fmaxf(m, part_ml[(pi + s) * 2]);
+  for (int s = lane; s < nsp; s += 32) m = fmaxf(m, part_ml[(pi + s) * 2]);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+  const bool cols = 4 * lane < HDv;
+  float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
   float l = 0.f;
-  for (int s = 0; s < nsp; ++s) l += part_ml[(pi + s) * 2 + 1] * exp2f(part_ml[(pi + s) * 2] - m);
-  const float inv = 1.f / l;
-  for (int e = threadIdx.x; e < HDv; e += blockDim.x) {
-    float a = 0.f;
-    for (int s = 0; s < nsp; ++s) a += part_o[(pi + s) * HDv + e] * exp2f(part_ml[(pi + s) * 2] - m);
-    O[(size_t)row * d + h * HDv + e] = from_f<T>(a * inv);
+  for (int s0 = 0; s0 < nsp; s0 += 32) {
+    const int s = s0 + lane;
+    const float w = s < nsp ? exp2f(part_ml[(pi + s) * 2] - m) : 0.f;
+    const float ls = s < nsp ? part_ml[(pi + s) * 2 + 1] * w : 0.f;
+    // l and the output accumulate over the broadcast splits in split order.
+    const int n = min(32, nsp - s0);
+    int k = 0;
+    for (; k + 4 <= n; k += 4) {
+      float wk[4];
+      float4 v[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        wk[u] = __shfl_sync(0xffffffffu, w, k + u);
+        l += __shfl_sync(0xffffffffu, ls, k + u);
+        v[u] = cols ? *reinterpret_cast<const float4*>(part_o + (pi + s0 + k + u) * HDv + 4 * lane)
+                    : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        a.x += v[u].x * wk[u];
+        a.y += v[u].y * wk[u];
+        a.z += v[u].z * wk[u];
+        a.w += v[u].w * wk[u];
+      }
+    }
+    for (; k < n; ++k) {
+      const float wk = __shfl_sync(0xffffffffu, w, k);
+      l += __shfl_sync(0xffffffffu, ls, k);
+      const float4 v = cols ? *reinterpret_cast<const float4*>(part_o + (pi + s0 + k) * HDv + 4 * lane)
+                            : make_float4(0.f, 0.f, 0.f, 0.f);
+      a.x += v.x * wk;
+      a.y += v.y * wk;
+      a.z += v.z * wk;
+      a.w += v.w * wk;
+    }
   }
+  if (!cols) return;
+  const float inv = 1.f / l;
+  T out[4] = {from_f<T>(a.x * inv), from_f<T>(a.y * inv), from_f<T>(a.z * inv), from_f<T>(a.w * inv)};
+  T* dst = O + (size_t)row * d + h * HDv + 4 * lane;
+#pragma unroll
+  for (int e = 0; e < 4; ++e) dst[e] = out[e];
 }
 
 // Uniform-slot TMA path; false when the shape or pool does not fit it.
@@ -1147,8 +1191,8 @@ static void attn_hd(cudaStream_t s, const T* Q, int rows, const int* mslot, cons
                depth_uniform, kv, slot_base, clamp, uniform ? 0 : 1, H, split, max_splits, O, part_o, part_ml, status);
   }
   if (max_splits > 1)
-    count_launch(), launch_pdl(k_attn_combine<T>, dim3(rows * H), dim3(128), 0, s, rows, mpos, H, HD, kv.d, split,
-                               max_splits, part_o, part_ml, O);
+    count_launch(), launch_pdl(k_attn_combine<T>, dim3((rows * H + 3) / 4), dim3(128), 0, s, rows, mpos, H, HD, kv.d,
+                               split, max_splits, part_o, part_ml, O);
 }
 
 template <int HD>

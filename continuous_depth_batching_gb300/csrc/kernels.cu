@@ -190,16 +190,24 @@ __device__ __forceinline__ void load4<__nv_bfloat16>(const __nv_bfloat16* p, __n
 // X is updated first, then normalised.
 // One block per row; each thread keeps KV four-column groups of the row in
 // registers from the fold to the normalised store (d and lda multiples of 4).
+// The gain is a weight, never written while kernels run, so it is loaded
+// before waiting for the previous kernel.
 template <typename T, int KV>
 __global__ void k_rmsnorm(float* __restrict__ X, const T* __restrict__ g, T* __restrict__ A, int rows, int d,
                           float eps, int lda, Parts pp, int mode) {
+  const int n4 = d / 4;
+  T gv[KV][4];
+#pragma unroll
+  for (int k = 0; k < KV; ++k) {
+    const int u = threadIdx.x + k * blockDim.x;
+    if (A != nullptr && u < n4) load4(g + 4 * u, gv[k]);
+  }
   pdl_wait();
   pdl_trigger();
   __shared__ float sh[33];
   const int i = blockIdx.x;
   if (i >= rows) return;
   float* x = X + (size_t)i * d;
-  const int n4 = d / 4;
   const bool keep = !(pp.ns > 0 && mode == 2);  // mode 2 replaces X by the sum
   float4 o[KV];
 #pragma unroll
@@ -237,10 +245,9 @@ __global__ void k_rmsnorm(float* __restrict__ X, const T* __restrict__ g, T* __r
     const int u = threadIdx.x + k * blockDim.x;
     if (u < n4) {
       const float w[4] = {o[k].x, o[k].y, o[k].z, o[k].w};
-      T gv[4], out[4];
-      load4(g + 4 * u, gv);
+      T out[4];
 #pragma unroll
-      for (int e = 0; e < 4; ++e) out[e] = from_f<T>(w[e] * inv * to_f(gv[e]));
+      for (int e = 0; e < 4; ++e) out[e] = from_f<T>(w[e] * inv * to_f(gv[k][e]));
       store4(A + (size_t)i * lda + 4 * u, out);
     }
   }
@@ -336,15 +343,19 @@ __global__ void k_rope_kv(Parts qkv, int rows, const int* __restrict__ mslot,
   for (int u = blockIdx.y * blockDim.x + threadIdx.x; u < quads; u += gridDim.y * blockDim.x) {
     const int h = u / (half / 4), j0 = (u % (half / 4)) * 4;
     const int a = h * hd + j0, b = a + half;
+    float2 r[4];
+    if (part < 2) {
+#pragma unroll
+      for (int e = 0; e < 4; ++e) r[e] = cs[j0 + e];
+    }
     const float4 xa = qkv.sum4(i, part * d + a), xb = qkv.sum4(i, part * d + b);
     const float a_[4] = {xa.x, xa.y, xa.z, xa.w}, b_[4] = {xb.x, xb.y, xb.z, xb.w};
     T lo[4], hi[4];
     if (part < 2) {
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
-        const float2 r = cs[j0 + e];
-        lo[e] = from_f<T>(a_[e] * r.x - b_[e] * r.y);
-        hi[e] = from_f<T>(b_[e] * r.x + a_[e] * r.y);
+        lo[e] = from_f<T>(a_[e] * r[e].x - b_[e] * r[e].y);
+        hi[e] = from_f<T>(b_[e] * r[e].x + a_[e] * r[e].y);
       }
     } else {
 #pragma unroll
