@@ -155,9 +155,9 @@ struct Cfg {
   static constexpr int A_BYTES = BM * BK * 2;
   static constexpr int B_BYTES = BN * BK * 2;
   static constexpr int STAGE = A_BYTES * (SW ? 2 : 1) + B_BYTES;
-  // 64-row (decode) tiles keep two CTAs per SM, so one CTA's prologue and
-  // epilogue overlap the other's weight stream; 128-row tiles use one.
-  static constexpr int BUDGET = BN == 64 ? 104 * 1024 : 200 * 1024;
+  // Two CTAs per SM, so one CTA's prologue and epilogue overlap the other's
+  // main loop (decode: its weight stream; prefill: its MMAs).
+  static constexpr int BUDGET = BN == 64 ? 104 * 1024 : 100 * 1024;
   static constexpr int STAGES = BUDGET / STAGE > 8 ? 8 : BUDGET / STAGE;
   static constexpr int ACC = BN * (SW ? 2 : 1);
   static constexpr int TMEM_COLS = ACC <= 32 ? 32 : ACC <= 64 ? 64 : ACC <= 128 ? 128 : ACC <= 256 ? 256 : 512;
@@ -165,7 +165,7 @@ struct Cfg {
 };
 
 template <int BN, int EPI>
-__global__ void __launch_bounds__(128, BN == 64 ? 2 : 1)
+__global__ void __launch_bounds__(128, 2)
     k_gemm_tc(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmW2,
               const __grid_constant__ CUtensorMap tmA, int N, int K, int rows, int splits,
               float* __restrict__ Cf, __nv_bfloat16* __restrict__ Ct, int ldc, float* __restrict__ ws,
