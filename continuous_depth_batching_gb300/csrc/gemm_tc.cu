@@ -447,9 +447,18 @@ int launch_gemm_tc(cudaStream_t s, int epi, const __nv_bfloat16* A, int lda, int
       default: ok = tc::launch_bn<64, kEpiSwiglu>(s, A, lda, a_rows, W, W2, N, K, rows, splits, Cf, Ct, ldc, P, status); break;
     }
   } else {
+    // Prefill: 256-row tiles (twice the weight-tile reuse per staged byte)
+    // where one accumulator fits; SwiGLU keeps two and 128-row tiles.
+    const bool wide = rows > 128;
     switch (epi) {
-      case kEpiStore: ok = tc::launch_bn<128, kEpiStore>(s, A, lda, a_rows, W, W2, N, K, rows, 1, Cf, Ct, ldc, nullptr, status); break;
-      case kEpiResid: ok = tc::launch_bn<128, kEpiResid>(s, A, lda, a_rows, W, W2, N, K, rows, 1, Cf, Ct, ldc, nullptr, status); break;
+      case kEpiStore:
+        ok = wide ? tc::launch_bn<256, kEpiStore>(s, A, lda, a_rows, W, W2, N, K, rows, 1, Cf, Ct, ldc, nullptr, status)
+                  : tc::launch_bn<128, kEpiStore>(s, A, lda, a_rows, W, W2, N, K, rows, 1, Cf, Ct, ldc, nullptr, status);
+        break;
+      case kEpiResid:
+        ok = wide ? tc::launch_bn<256, kEpiResid>(s, A, lda, a_rows, W, W2, N, K, rows, 1, Cf, Ct, ldc, nullptr, status)
+                  : tc::launch_bn<128, kEpiResid>(s, A, lda, a_rows, W, W2, N, K, rows, 1, Cf, Ct, ldc, nullptr, status);
+        break;
       default: ok = tc::launch_bn<128, kEpiSwiglu>(s, A, lda, a_rows, W, W2, N, K, rows, 1, Cf, Ct, ldc, nullptr, status); break;
     }
   }
