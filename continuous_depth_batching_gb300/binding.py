@@ -105,6 +105,7 @@ def lib(path: str | None = None) -> C.CDLL:
     L.cdb_step_boundary.argtypes = [C.c_void_p, C.POINTER(StepInfo)]
     L.cdb_step_core.argtypes = [C.c_void_p, C.POINTER(StepInfo)]
     L.cdb_drain.argtypes = [C.c_void_p, C.POINTER(Result), C.c_int, C.POINTER(C.c_int)]
+    L.cdb_poll.argtypes = [C.c_void_p, C.POINTER(Result), C.c_int, C.POINTER(C.c_int)]
     L.cdb_sync.argtypes = [C.c_void_p]
     L.cdb_free.argtypes = [C.c_void_p]
     L.cdb_free.restype = None
@@ -260,6 +261,14 @@ class Engine:
         return self._check(self.L.cdb_sync(self.ctx))
 
     def drain(self, cap=4096):
+        """Finished sequences (waits for their results); see cdb_drain."""
+        return self._collect(self.L.cdb_drain, cap)
+
+    def poll(self, cap=16):
+        """Finished sequences whose results are already on the host (no wait); see cdb_poll."""
+        return self._collect(self.L.cdb_poll, cap)
+
+    def _collect(self, fn, cap):
         s = self.shape
         cap_new = self.max_new_cap
         bufs = []
@@ -278,7 +287,7 @@ class Engine:
                 res[i].hidden = b["hidden"].ctypes.data_as(C.POINTER(C.c_float))
             bufs.append(b)
         n = C.c_int()
-        self._check(self.L.cdb_drain(self.ctx, res, cap, C.byref(n)))
+        self._check(fn(self.ctx, res, cap, C.byref(n)))
         out = []
         for i in range(n.value):
             nt = res[i].n_tokens

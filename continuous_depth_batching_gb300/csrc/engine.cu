@@ -905,14 +905,14 @@ int cdb_sync(cdb_ctx* x) {
   return check_status(x);
 }
 
-int cdb_drain(cdb_ctx* x, cdb_result* buf, int cap, int* n_out) {
+static int drain_impl(cdb_ctx* x, cdb_result* buf, int cap, int* n_out, bool block) {
   if (!x || !n_out || (cap > 0 && !buf)) return CDB_ERR_ARG;
   *n_out = 0;
   if (x->dead) return CDB_ERR_STATE;
-  int rc = check_status(x);
+  int rc = block ? check_status(x) : CDB_OK;  // the status check synchronizes the stream
   if (rc < 0) return rc;
   for (int s = 0; s < x->c.W; ++s) {
-    rc = x->exec->harvest_slot(s, true);
+    rc = x->exec->harvest_slot(s, block);
     if (rc < 0) return rc;
   }
   int n = 0;
@@ -932,6 +932,10 @@ int cdb_drain(cdb_ctx* x, cdb_result* buf, int cap, int* n_out) {
   *n_out = n;
   return CDB_OK;
 }
+
+int cdb_drain(cdb_ctx* x, cdb_result* buf, int cap, int* n_out) { return drain_impl(x, buf, cap, n_out, true); }
+
+int cdb_poll(cdb_ctx* x, cdb_result* buf, int cap, int* n_out) { return drain_impl(x, buf, cap, n_out, false); }
 
 void cdb_free(cdb_ctx* x) {
   if (!x) return;

@@ -206,8 +206,18 @@ int cdb_step_boundary(cdb_ctx *ctx, cdb_step_info *info);
  * exit counts in info come from the previous step's lookahead flags. */
 int cdb_step_core(cdb_ctx *ctx, cdb_step_info *info);
 
-/* Copy up to cap finished sequences (finish order) into buf; *n_out set. */
+/* Copy up to cap finished sequences (finish order) into buf; *n_out set.
+ * Waits for the device copies of every finished sequence's results. */
 int cdb_drain(cdb_ctx *ctx, cdb_result *buf, int cap, int *n_out);
+
+/* cdb_drain without waiting: only sequences whose results have already
+ * reached host memory are returned (a sequence not ready now comes back from
+ * a later poll or drain), so an online driver can collect finished requests
+ * between steps without stalling the device queue.  Each finished sequence is
+ * returned exactly once by poll and drain together.  Unlike cdb_drain it does
+ * not read the device status word (that needs a stream synchronization);
+ * cdb_drain and cdb_sync report a failed bounds check. */
+int cdb_poll(cdb_ctx *ctx, cdb_result *buf, int cap, int *n_out);
 
 /* Block until all enqueued work has finished and check device-side status. */
 int cdb_sync(cdb_ctx *ctx);

@@ -205,3 +205,35 @@ def test_convergence_gate_matches_oracle(variant, dtype, tol, kv_slots):
     depths = [e for tr in ref.values() for e in tr.exit_depths]
     assert min(depths) >= 3 and len(set(depths)) >= (2 if dtype == "fp32" else 1), depths
     assert sum(sum(tr.near_gate) for tr in ref.values()) <= len(depths) // 4
+
+
+def test_poll_returns_each_finished_sequence_once(tiny, tiny_ref):
+    """cdb_poll between steps hands out finished sequences without waiting;
+    poll and the final drain together return every sequence exactly once, with
+    the tokens of a run that only drains at the end (the online-serving driver
+    relies on this)."""
+    from continuous_depth_batching_gb300 import binding
+    shape, _, dw, reqs = tiny
+    eng = binding.Engine(shape, dw, mode="refill", W=2, M=64, K=1, max_ctx=64, max_new_cap=16, attn_split=16)
+    for r in reqs:
+        eng.admit(r["seq_id"], r["prompt"], r["gen_len"])
+    seen = []
+    polled = 0
+    while True:
+        rc, _ = eng.step_boundary()
+        if rc == binding.DONE:
+            break
+        if rc == binding.IDLE:
+            eng.step_core()
+        got = eng.poll()
+        polled += len(got)
+        seen += got
+    eng.sync()
+    seen += eng.drain()
+    eng.close()
+    ids = [o["seq_id"] for o in seen]
+    assert sorted(ids) == sorted(r["seq_id"] for r in reqs) and len(set(ids)) == len(ids)
+    assert polled > 0, "sequences that finished early should come back from poll"
+    ref, _ = gpu_run(shape, dw, reqs, None, mode="refill", W=2, M=64, K=1, max_ctx=64, attn_split=16, force=False)
+    for o in seen:
+        assert list(o["tokens"]) == list(ref[o["seq_id"]]["tokens"])
