@@ -118,3 +118,34 @@ def test_planner_rejects_bad_jobs():
     huginn = dataclasses.replace(model_shape("huginn"), d_model=0)
     with pytest.raises(binding.CdbError):
         binding.roofline_latency(huginn, 1.0, 1.0)
+
+
+def test_latency_fit_recovers_a_known_model():
+    """The per-call regression of schedule_select (non-negative least squares on
+    the twelve stage features) returns the coefficients that generated the
+    times, including calls that ran a coda and a prelude together."""
+    pytest.importorskip("scipy")
+    from continuous_depth_batching_gb300.schedule_select import fit_latency
+    true = {"prefill": (1e-3, 2e-6, 1e-9), "prelude": (5e-5, 1e-6, 0.0), "core": (1.4e-3, 1.2e-5, 3e-9),
+            "coda": (2e-4, 3e-6, 1e-10)}
+    col = {"prefill": 0, "prelude": 3, "core": 6, "coda": 9}
+    coef = np.zeros(12)
+    for k, (d, g, a) in true.items():
+        coef[col[k]:col[k] + 3] = (d, g, a)
+    rng = np.random.default_rng(0)
+    rows = []
+    for _ in range(3000):
+        x = np.zeros(12)
+        st = col[("prefill", "prelude", "core", "coda")[rng.integers(0, 4)]]
+        x[st], x[st + 1] = 1, rng.integers(1, 64)
+        x[st + 2] = x[st + 1] * rng.integers(100, 1000)
+        if st == 9 and rng.random() < 0.5:      # coda followed by a prelude in one call
+            x[3], x[4], x[5] = 1, x[10], x[11] + x[10]
+        rows.append((x, float(x @ coef)))
+    model, rel = fit_latency(rows)
+    assert rel < 1e-6
+    for k, (d, g, a) in true.items():
+        got = model[k]
+        assert got["delta"] == pytest.approx(d, rel=1e-4, abs=1e-9)
+        assert got["gamma"] == pytest.approx(g, rel=1e-4, abs=1e-11)
+        assert got["alpha"] == pytest.approx(a, rel=1e-4, abs=1e-14)
