@@ -8,6 +8,15 @@ if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
 
+@pytest.fixture(scope="session", autouse=True)
+def _library_built():
+    """Compile libcdb.so once per session (nvcc cross-compiles without a GPU;
+    nothing is rebuilt when the objects are current), so that host-only tests
+    of the scheduler, the planner and the ABI find it on a fresh checkout."""
+    from continuous_depth_batching_gb300.build import build
+    build()
+
+
 def pytest_configure(config):
     config.addinivalue_line("markers", "gpu: needs a CUDA GPU (GB300) and the built library")
     config.addinivalue_line("markers", "slow: long-running CPU test")
