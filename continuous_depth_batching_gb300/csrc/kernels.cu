@@ -388,9 +388,12 @@ __global__ void k_rope_table(float2* tab, int max_ctx, int hd, float theta) {
 // lookahead exit gate (§4.3)
 // ---------------------------------------------------------------------------
 
-// z = w . rmsnorm(h) + b.  The flag set after step r makes the token exit
-// after step r+1: live gate -> z > thr and r >= r_min-1; a forced exit depth
-// e -> r + 1 == e; fixed-depth mode never sets it.
+// Probe gate (Sp == nullptr): z = w . rmsnorm(h) + b, fires when z > thr.
+// Convergence gate (Sp = the states that entered this step, App. E.2):
+// z = ||h - Sp|| / ||h||, fires when z < thr.  The flag set after step r makes
+// the token exit after step r+1: live gate -> it fires and r >= r_min-1; a
+// forced exit depth e -> r + 1 == e; fixed-depth mode never sets it.  z goes
+// to the gate trace in either case.
 template <typename T>
 __global__ void k_gate(const float* __restrict__ X, const float* __restrict__ Sp, const T* __restrict__ w,
                        float bias, float thr,
