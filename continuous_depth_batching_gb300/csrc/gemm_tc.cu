@@ -22,6 +22,7 @@
 #include <cuda.h>
 
 #include <cstdlib>
+#include <cstring>
 #include <unordered_map>
 
 #include "common.cuh"
@@ -313,6 +314,169 @@ __global__ void __launch_bounds__(128, 2)
 }
 
 // ---------------------------------------------------------------------------
+// Persistent prefill GEMM: one CTA per SM walks the output tiles (tile t, then
+// t + gridDim.x, ...).  Warp 0 streams operand slabs through a STAGES-deep
+// ring, warp 1 issues the MMAs, warps 2-5 drain accumulators.  Two TMEM
+// accumulator buffers alternate between tiles, so the epilogue of one tile
+// overlaps the main loop of the next: the MMA warp waits for `tempty[b]`
+// (all four epilogue warps done with buffer b) before reusing it, the
+// epilogue warps wait for `tfull[b]` (the tile's last MMA committed).  An
+// epilogue warp reads the TMEM lane quadrant its warp index selects
+// (warp % 4), i.e. output features n0 + 32 * (warp % 4) + lane.
+// ---------------------------------------------------------------------------
+template <int BN, bool SW>
+struct PfCfg {
+  static constexpr int A_BYTES = BM * BK * 2;
+  static constexpr int B_BYTES = BN * BK * 2;
+  static constexpr int STAGE = A_BYTES * (SW ? 2 : 1) + B_BYTES;
+  static constexpr int STAGES = (196 * 1024) / STAGE > 8 ? 8 : (196 * 1024) / STAGE;
+  static constexpr int ACC = BN * (SW ? 2 : 1);  // TMEM columns of one tile's accumulators
+  static constexpr int TMEM_COLS = 2 * ACC;      // two buffers
+  static constexpr int SMEM = STAGES * STAGE + 1024 + 256;
+  static_assert(TMEM_COLS <= 512, "two accumulator buffers must fit TMEM");
+};
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(su32(bar)) : "memory");
+}
+
+template <int BN, int EPI>
+__global__ void __launch_bounds__(192, 1)
+    k_gemm_pf(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmW2,
+              const __grid_constant__ CUtensorMap tmA, int N, int K, int rows, float* __restrict__ Cf,
+              __nv_bfloat16* __restrict__ Ct, int ldc, int* status) {
+  constexpr bool SW = EPI == kEpiSwiglu;
+  using C = PfCfg<BN, SW>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::STAGES * C::STAGE);
+  uint64_t* empty = full + C::STAGES;
+  uint64_t* tfull = empty + C::STAGES;
+  uint64_t* tempty = tfull + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tempty + 2);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int tiles_n = (N + BM - 1) / BM;
+  const int tiles = tiles_n * ((rows + BN - 1) / BN);
+  const int KT = (K + BK - 1) / BK;
+
+  if (threadIdx.x == 0) {
+    asm volatile("prefetch.tensormap [%0];" ::"l"(&tmW) : "memory");
+    asm volatile("prefetch.tensormap [%0];" ::"l"(&tmA) : "memory");
+    if (SW) asm volatile("prefetch.tensormap [%0];" ::"l"(&tmW2) : "memory");
+    for (int s = 0; s < C::STAGES; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&tfull[b], 1);
+      mbar_init(&tempty[b], 4);
+    }
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  }
+  if (warp == 0) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(su32(tmem_slot)),
+                 "r"(C::TMEM_COLS));
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+  }
+  fence_before();
+  __syncthreads();
+  fence_after();
+  const uint32_t tmem = *tmem_slot;
+  pdl_wait();  // activations, residual inputs and outputs belong to earlier kernels
+  pdl_trigger();
+  bool fail = false;
+  if (warp == 0) {
+    if (lane == 0) {
+      // TMA producer: k-slab `it` counts across all of this CTA's tiles.
+      uint32_t it = 0;
+      for (int t = blockIdx.x; t < tiles && !fail; t += gridDim.x) {
+        const int n0 = (t % tiles_n) * BM, m0 = (t / tiles_n) * BN;
+        for (int kt = 0; kt < KT; ++kt, ++it) {
+          const int s = it % C::STAGES;
+          if (it >= (uint32_t)C::STAGES && !mbar_wait(&empty[s], ((it / C::STAGES) - 1) & 1)) {
+            fail = true;
+            break;
+          }
+          uint8_t* st = smem + s * C::STAGE;
+          mbar_expect_tx(&full[s], C::STAGE);
+          tma_load(st, &tmW, &full[s], kt * BK, n0);
+          if (SW) tma_load(st + C::A_BYTES, &tmW2, &full[s], kt * BK, n0);
+          tma_load(st + C::A_BYTES * (SW ? 2 : 1), &tmA, &full[s], kt * BK, m0);
+        }
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // MMA issuer.
+      constexpr uint32_t id = idesc(BM, BN);
+      uint32_t it = 0, tl = 0;
+      for (int t = blockIdx.x; t < tiles && !fail; t += gridDim.x, ++tl) {
+        const uint32_t b = tl & 1, acc0 = tmem + b * C::ACC;
+        if (tl >= 2 && !mbar_wait(&tempty[b], ((tl / 2) - 1) & 1)) {
+          fail = true;
+          break;
+        }
+        fence_after();
+        for (int kt = 0; kt < KT; ++kt, ++it) {
+          const int s = it % C::STAGES;
+          if (!mbar_wait(&full[s], (it / C::STAGES) & 1)) {
+            fail = true;
+            break;
+          }
+          fence_after();
+          const uint32_t a = su32(smem + s * C::STAGE);
+          const uint32_t a2 = a + C::A_BYTES;
+          const uint32_t bb = a + C::A_BYTES * (SW ? 2 : 1);
+#pragma unroll
+          for (int kk = 0; kk < BK / UK; ++kk) {
+            const uint32_t accum = (kt > 0 || kk > 0) ? 1u : 0u;
+            mma(acc0, sdesc(a + kk * 32), sdesc(bb + kk * 32), id, accum);
+            if (SW) mma(acc0 + BN, sdesc(a2 + kk * 32), sdesc(bb + kk * 32), id, accum);
+          }
+          mma_commit(&empty[s]);
+        }
+        if (fail) break;
+        mma_commit(&tfull[b]);
+      }
+    }
+  } else {
+    // Epilogue warps 2-5: TMEM lane quadrant warp % 4.
+    const int q = warp & 3;
+    uint32_t tl = 0;
+    for (int t = blockIdx.x; t < tiles; t += gridDim.x, ++tl) {
+      const uint32_t b = tl & 1;
+      // Warp-uniform: tcgen05.ld below is a collective of the whole warp.
+      if (!__all_sync(0xffffffffu, mbar_wait(&tfull[b], (tl / 2) & 1))) {
+        fail = true;
+        break;
+      }
+      fence_after();
+      const int n0 = (t % tiles_n) * BM, m0 = (t / tiles_n) * BN;
+      const int f = n0 + q * 32 + lane;
+      const uint32_t lane_base = tmem + ((uint32_t)(q * 32) << 16) + b * C::ACC;
+#pragma unroll 1
+      for (int c0 = 0; c0 < BN; c0 += 16) {
+        float v[16], u[16];
+        tmem_ld16(lane_base + c0, v);
+        if (SW) tmem_ld16(lane_base + BN + c0, u);
+        const int jn = min(16, rows - (m0 + c0));
+        if (f < N && jn > 0) epilogue16<EPI>(v, u, jn, Cf, Ct, (size_t)(m0 + c0) * ldc + f, ldc);
+      }
+      fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&tempty[b]);
+    }
+  }
+  fence_before();
+  __syncthreads();
+  if (fail && lane == 0) atomicOr(status, kStatusTimeout);
+  if (warp == 0)
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(C::TMEM_COLS));
+}
+
+// ---------------------------------------------------------------------------
 // host side: tensor maps (cached), launch
 // ---------------------------------------------------------------------------
 
@@ -390,6 +554,30 @@ static bool launch_bn(cudaStream_t s, const __nv_bfloat16* A, int lda, int a_row
                     *mw, *mw2, *ma, N, K, rows, splits, Cf, Ct, ldc, ws, status) == cudaSuccess;
 }
 
+// Persistent prefill launch: min(tiles, max_ctas) CTAs of 192 threads.
+template <int BN, int EPI>
+static bool launch_pf(cudaStream_t s, const __nv_bfloat16* A, int lda, int a_rows, const __nv_bfloat16* W,
+                      const __nv_bfloat16* W2, int N, int K, int rows, float* Cf, __nv_bfloat16* Ct, int ldc,
+                      int max_ctas, int* status) {
+  using C = PfCfg<BN, EPI == kEpiSwiglu>;
+  const CUtensorMap* mw = get_map(W, K, N, (uint64_t)K * 2, BM);
+  const CUtensorMap* mw2 = EPI == kEpiSwiglu ? get_map(W2, K, N, (uint64_t)K * 2, BM) : mw;
+  const CUtensorMap* ma = get_map(A, K, a_rows, (uint64_t)lda * 2, BN);
+  if (!mw || !mw2 || !ma) return false;
+  static bool attr = false;
+  if (!attr) {
+    if (cudaFuncSetAttribute(k_gemm_pf<BN, EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) !=
+        cudaSuccess)
+      return false;
+    attr = true;
+  }
+  const long long tiles = (long long)((N + BM - 1) / BM) * ((rows + BN - 1) / BN);
+  const int grid = (int)(tiles < max_ctas ? tiles : max_ctas);
+  count_launch();
+  return launch_pdl(k_gemm_pf<BN, EPI>, dim3(grid), dim3(192), C::SMEM, s, *mw, *mw2, *ma, N, K, rows, Cf, Ct, ldc,
+                    status) == cudaSuccess;
+}
+
 }  // namespace tc
 
 static int sm_count() {
@@ -419,6 +607,17 @@ static int split_cap() {
   return cap;
 }
 
+// Prefill GEMMs run the persistent kernel unless CDB_PREFILL_GEMM=tiles
+// (one CTA per output tile, two per SM), kept for comparison.
+static bool persistent_prefill() {
+  static int p = -1;
+  if (p < 0) {
+    const char* e = std::getenv("CDB_PREFILL_GEMM");
+    p = e && std::strcmp(e, "tiles") == 0 ? 0 : 1;
+  }
+  return p == 1;
+}
+
 int gemm_tc_splits(int N, int K, bool decode) {
   if (!decode) return 1;
   const int tiles = (N + tc::BM - 1) / tc::BM;
@@ -445,6 +644,22 @@ int launch_gemm_tc(cudaStream_t s, int epi, const __nv_bfloat16* A, int lda, int
       case kEpiStore: ok = tc::launch_bn<64, kEpiStore>(s, A, lda, a_rows, W, W2, N, K, rows, splits, Cf, Ct, ldc, P, status); break;
       case kEpiResid: ok = tc::launch_bn<64, kEpiResid>(s, A, lda, a_rows, W, W2, N, K, rows, splits, Cf, Ct, ldc, P, status); break;
       default: ok = tc::launch_bn<64, kEpiSwiglu>(s, A, lda, a_rows, W, W2, N, K, rows, splits, Cf, Ct, ldc, P, status); break;
+    }
+  } else if (persistent_prefill()) {
+    // Prefill, persistent: one CTA per SM, double-buffered accumulators;
+    // 256-row tiles where one accumulator fits, 128-row tiles for SwiGLU.
+    const bool wide = rows > 128;
+    const int sm = sm_count();
+    switch (epi) {
+      case kEpiStore:
+        ok = wide ? tc::launch_pf<256, kEpiStore>(s, A, lda, a_rows, W, W2, N, K, rows, Cf, Ct, ldc, sm, status)
+                  : tc::launch_pf<128, kEpiStore>(s, A, lda, a_rows, W, W2, N, K, rows, Cf, Ct, ldc, sm, status);
+        break;
+      case kEpiResid:
+        ok = wide ? tc::launch_pf<256, kEpiResid>(s, A, lda, a_rows, W, W2, N, K, rows, Cf, Ct, ldc, sm, status)
+                  : tc::launch_pf<128, kEpiResid>(s, A, lda, a_rows, W, W2, N, K, rows, Cf, Ct, ldc, sm, status);
+        break;
+      default: ok = tc::launch_pf<128, kEpiSwiglu>(s, A, lda, a_rows, W, W2, N, K, rows, Cf, Ct, ldc, sm, status); break;
     }
   } else {
     // Prefill: 256-row tiles (twice the weight-tile reuse per staged byte)
