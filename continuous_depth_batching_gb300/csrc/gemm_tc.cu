@@ -17,6 +17,10 @@
 // the residual fold) sums the partials in split order while it reads them.
 // With one split the epilogue (store, residual add, SwiGLU) runs in place.
 //
+// Prefill (many rows, no split) runs a persistent variant, k_gemm_pf: one CTA
+// per SM walks the tiles with separate producer, MMA and epilogue warps and
+// two TMEM accumulators, so a tile's epilogue overlaps the next tile's MMAs.
+//
 // Every mbarrier wait is bounded by the global timer; on expiry the kernel
 // records kStatusTimeout, skips the epilogue, releases TMEM and returns.
 #include <cuda.h>
