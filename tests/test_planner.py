@@ -149,3 +149,22 @@ def test_latency_fit_recovers_a_known_model():
         assert got["delta"] == pytest.approx(d, rel=1e-4, abs=1e-9)
         assert got["gamma"] == pytest.approx(g, rel=1e-4, abs=1e-11)
         assert got["alpha"] == pytest.approx(a, rel=1e-4, abs=1e-14)
+
+
+def test_step_info_reports_context_entries():
+    """cdb_step_info.ctx / ctx2: the sum over a stage's rows of (position + 1),
+    the cached entries each row's attention reads per layer."""
+    P, gen = 10, 4
+    sim = binding.Sim("refill", W=1, M=64, K=1, r_max=3, r_min=2)
+    sim.admit(0, P, gen, np.array([2, 3, 2], np.int8))
+    rc, info = sim.step_boundary()                      # prefill + prelude of the first decode token
+    assert info.stage == 1 and info.ctx == P * (P + 1) // 2
+    assert info.stage2 == 2 and info.batch2 == 1 and info.ctx2 == P + 1
+    rc, info = sim.step_boundary()
+    assert rc == binding.IDLE
+    rc, info = sim.step_core()                          # the token at position P, loop step 1
+    assert info.stage == 3 and info.batch == 1 and info.ctx == P + 1
+    sim.step_boundary()
+    sim.step_core()                                     # step 2: it exits (depth 2)
+    rc, info = sim.step_boundary()                      # coda of position P, prelude of P + 1
+    assert info.stage == 4 and info.ctx == P + 1 and info.stage2 == 2 and info.ctx2 == P + 2
