@@ -129,6 +129,8 @@ def lib(path: str | None = None) -> C.CDLL:
     L.cdb_predict_job.argtypes = [C.POINTER(Job), C.c_int, C.c_int, C.POINTER(LatencyModel), C.POINTER(Prediction)]
     L.cdb_roofline_latency.argtypes = [C.POINTER(ModelDesc), C.c_double, C.c_double, C.c_double,
                                        C.POINTER(LatencyModel)]
+    L.cdb_predict_online.argtypes = [C.POINTER(Job), C.POINTER(C.c_double), C.c_int, C.c_int,
+                                     C.POINTER(LatencyModel), C.POINTER(C.c_double), C.POINTER(Prediction)]
     L.cdb_select_schedule.argtypes = [C.POINTER(Job), C.POINTER(LatencyModel), C.POINTER(C.c_int),
                                       C.POINTER(C.c_int), C.POINTER(Prediction), C.POINTER(C.c_double),
                                       C.POINTER(C.c_double)]
@@ -516,3 +518,19 @@ def select_schedule(job: PlanJob, lm: LatencyModel) -> dict:
     names = {v: k for k, v in MODES.items()}
     return {"mode": names[mode.value], "K": K.value, "prediction": best.as_dict(),
             "refill_seconds": r_s.value, "no_refill_seconds": n_s.value}
+
+
+def predict_online(job: PlanJob, arrival_s, mode, K, lm: LatencyModel):
+    """Predicted finish time of every request arriving at arrival_s (see cdb_predict_online)."""
+    import numpy as np
+    arr = np.ascontiguousarray(arrival_s, dtype=np.float64)
+    if arr.shape != (job.job.n_seqs,):
+        raise ValueError("one arrival time per request")
+    fin = np.zeros(job.job.n_seqs, dtype=np.float64)
+    out = Prediction()
+    rc = lib().cdb_predict_online(C.byref(job.job), arr.ctypes.data_as(C.POINTER(C.c_double)),
+                                  MODES[mode] if isinstance(mode, str) else mode, K, C.byref(lm),
+                                  fin.ctypes.data_as(C.POINTER(C.c_double)), C.byref(out))
+    if rc != OK:
+        raise CdbError(rc, "cdb_predict_online")
+    return fin, out.as_dict()

@@ -31,7 +31,9 @@ class CostExecutor : public ReplayExecutor {
   int prefill(const PrefillPlan& p, const std::vector<Seq>&) override {
     double ctx = 0;
     for (const PrefillRow& r : p.rows) ctx += r.pos + 1;
-    p_.prefill_seconds += stage_time(lm_.prefill, (double)p.rows.size(), ctx);
+    const double c = stage_time(lm_.prefill, (double)p.rows.size(), ctx);
+    p_.prefill_seconds += c;
+    call_ += c;
     ++p_.prefill_stages;
     p_.tokens += (int64_t)p.done_seqs.size();
     return CDB_OK;
@@ -39,14 +41,18 @@ class CostExecutor : public ReplayExecutor {
   int prelude(const PreludePlan& p) override {
     double ctx = 0;
     for (const Tok& t : p.rows) ctx += t.pos + 1;
-    p_.prelude_seconds += stage_time(lm_.prelude, (double)p.rows.size(), ctx);
+    const double c = stage_time(lm_.prelude, (double)p.rows.size(), ctx);
+    p_.prelude_seconds += c;
+    call_ += c;
     ++p_.prelude_stages;
     return CDB_OK;
   }
   int core(const CorePlan& p) override {
     double ctx = 0;
     for (const Tok& t : *p.rows) ctx += t.pos + 1;
-    p_.core_seconds += stage_time(lm_.core, (double)p.B, ctx);
+    const double c = stage_time(lm_.core, (double)p.B, ctx);
+    p_.core_seconds += c;
+    call_ += c;
     ++p_.core_steps;
     p_.core_token_steps += p.B;
     return ReplayExecutor::core(p);
@@ -54,12 +60,28 @@ class CostExecutor : public ReplayExecutor {
   int coda(const std::vector<Tok>& rows) override {
     double ctx = 0;
     for (const Tok& t : rows) ctx += t.pos + 1;
-    p_.coda_seconds += stage_time(lm_.coda, (double)rows.size(), ctx);
+    const double c = stage_time(lm_.coda, (double)rows.size(), ctx);
+    p_.coda_seconds += c;
+    call_ += c;
     ++p_.coda_stages;
     p_.tokens += (int64_t)rows.size();
     coda_rows_ += (int64_t)rows.size();
     return CDB_OK;
   }
+  // A finished sequence ends with the stage that produced its last token:
+  // record the cost of the current scheduler call up to that stage.
+  int finish(const Seq& s) override {
+    finished.push_back({s.id, call_});
+    return CDB_OK;
+  }
+  // Cost of the stages run since the last call, which it resets.
+  double take_call_cost() {
+    const double c = call_;
+    call_ = 0;
+    return c;
+  }
+  std::vector<std::pair<int64_t, double>> finished;  // (sequence id, cost into its call)
+
   cdb_prediction result() const {
     cdb_prediction r = p_;
     r.seconds = r.prefill_seconds + r.prelude_seconds + r.core_seconds + r.coda_seconds;
@@ -72,6 +94,7 @@ class CostExecutor : public ReplayExecutor {
   cdb_latency_model lm_;
   cdb_prediction p_;
   int64_t coda_rows_ = 0;
+  double call_ = 0;
 };
 
 bool cost_ok(const cdb_stage_cost& c) { return c.delta >= 0 && c.gamma >= 0 && c.alpha >= 0; }
@@ -86,6 +109,32 @@ bool job_ok(const cdb_job* j) {
         j->prompt_len[i] + j->gen_len[i] - 1 > j->max_ctx)
       return false;
   return true;
+}
+
+// Scheduler limits of a job; false for an inconsistent job.
+bool job_cfg(const cdb_job* job, int mode, int K, SchedCfg* c) {
+  c->mode = mode;
+  c->W = job->W;
+  c->M = job->M;
+  c->S = job->S > 0 ? job->S : (job->W / 8 > 1 ? job->W / 8 : 1);
+  c->K = K;
+  c->r_max = job->r_max;
+  c->r_min = job->r_min;
+  c->kv_blocks = job->kv_blocks;
+  c->kv_headroom = job->kv_headroom;
+  c->max_ctx = job->max_ctx;
+  c->max_new_cap = job->max_new_cap;
+  return c->S <= c->W;
+}
+
+// Exit depths of request i (offset `off` into the concatenated table), or
+// nullptr for fixed depth; `bad` is set when a depth is outside [r_min, r_max].
+const int8_t* job_exits(const cdb_job* job, int mode, int i, int64_t off, bool* bad) {
+  if (mode == CDB_MODE_FIXED_DEPTH || !job->exit_depths) return nullptr;
+  const int8_t* e = job->exit_depths + off;
+  for (int t = 0; t + 1 < job->gen_len[i]; ++t)
+    if (e[t] < job->r_min || e[t] > job->r_max) *bad = true;
+  return e;
 }
 
 }  // namespace
@@ -199,6 +248,64 @@ int cdb_select_schedule(const cdb_job* job, const cdb_latency_model* lm, int* mo
   if (refill_seconds) *refill_seconds = best_refill;
   if (no_refill_seconds) *no_refill_seconds = no_refill;
   return CDB_OK;
+}
+
+int cdb_predict_online(const cdb_job* job, const double* arrival_s, int mode, int K, const cdb_latency_model* lm,
+                       double* finish_s, cdb_prediction* out) {
+  using namespace cdb;
+  if (!job_ok(job) || !lm || !out || !finish_s || (job->n_seqs > 0 && !arrival_s) || K < 1 || mode < 0 ||
+      mode > 2 || !cost_ok(lm->prefill) || !cost_ok(lm->prelude) || !cost_ok(lm->core) || !cost_ok(lm->coda))
+    return CDB_ERR_ARG;
+  if (mode != CDB_MODE_FIXED_DEPTH && job->n_seqs > 0 && !job->exit_depths) return CDB_ERR_ARG;
+  for (int i = 0; i < job->n_seqs; ++i)
+    if (!(arrival_s[i] >= 0.0) || (i > 0 && arrival_s[i] < arrival_s[i - 1])) return CDB_ERR_ARG;
+  SchedCfg c;
+  if (!job_cfg(job, mode, K, &c)) return CDB_ERR_ARG;
+  CostExecutor ex(mode, job->W, job->r_max, *lm);
+  Scheduler sched(c, &ex);
+  ex.seqs = &sched.seqs();
+  std::vector<int64_t> off(job->n_seqs + 1, 0);
+  int64_t work = 64 + 2 * (int64_t)job->n_seqs;
+  for (int i = 0; i < job->n_seqs; ++i) {
+    bool bad = false;
+    job_exits(job, mode, i, off[i], &bad);
+    if (bad) return CDB_ERR_ARG;
+    off[i + 1] = off[i] + job->gen_len[i] - 1;
+    work += (int64_t)job->gen_len[i] * (job->r_max + 3) + job->prompt_len[i] / job->M + 2;
+    finish_s[i] = -1.0;
+  }
+  // Simulated clock: requests join when it passes their arrival time; each
+  // scheduler call advances it by the cost of the stages it ran; with nothing
+  // to run it jumps to the next arrival.
+  double T = 0.0;
+  int next = 0;
+  for (int64_t it = 0; it < 4 * work; ++it) {
+    while (next < job->n_seqs && arrival_s[next] <= T) {
+      bool bad = false;
+      const int8_t* e = job_exits(job, mode, next, off[next], &bad);
+      int rc = sched.admit(next, nullptr, job->prompt_len[next], job->gen_len[next], e, nullptr);
+      if (rc < 0) return rc;
+      ++next;
+    }
+    cdb_step_info info;
+    int rc = sched.step_boundary(&info);
+    if (rc < 0) return rc;
+    if (rc == CDB_IDLE) {
+      rc = sched.step_core(&info);
+      if (rc < 0) return rc;
+    }
+    for (const auto& f : ex.finished) finish_s[f.first] = T + f.second;
+    ex.finished.clear();
+    T += ex.take_call_cost();
+    if (rc == CDB_DONE) {
+      if (next >= job->n_seqs) {
+        *out = ex.result();
+        return CDB_OK;
+      }
+      if (arrival_s[next] > T) T = arrival_s[next];
+    }
+  }
+  return CDB_ERR_STATE;
 }
 
 }  // extern "C"

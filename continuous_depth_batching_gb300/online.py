@@ -118,6 +118,44 @@ def run_point(make_engine, reqs, arrive, window, mode, drain_limit=120.0):
             "normalized_latency": latency_stats(lat)}
 
 
+def predict_points(shape, lm, points, seed=4, depth_probs=None, kv_gb=150.0, modes=("refill", "no_refill",
+                                                                                      "fixed_depth")):
+    """Predicted online serving (include/cdb_plan.h, cdb_predict_online) at (target, rate, window) points.
+
+    The requests and arrivals are those the measured driver draws; exit
+    depths, which the live gate decides on the GPU, are drawn from
+    `depth_probs` over r_min, r_min + 1, ... (a stand-in with the measured
+    mean).  Returns one dict per (point, mode) with the predicted mean and
+    p50 normalised latency and the mean recurrent batch."""
+    from continuous_depth_batching_gb300 import binding
+    pool = make_online_requests(20000, shape.vocab, seed + 1)
+    rng = np.random.default_rng(seed + 2)
+    probs = np.asarray(depth_probs if depth_probs is not None else [1.0], np.float64)
+    probs = probs / probs.sum()
+    depths = np.arange(shape.r_min, shape.r_min + len(probs))
+    out = []
+    kv_tok = shape.n_kv_slots * 2 * shape.d_model * shape.elem_bytes
+    for target, rate, window in points:
+        arr = poisson_arrivals(rate, window, seed + 100 * target + 7)
+        reqs = []
+        for i in range(len(arr)):
+            g = pool[i]["gen_len"]
+            reqs.append(dict(prompt_len=len(pool[i]["prompt"]), gen_len=g,
+                             exit_depths=rng.choice(depths, g - 1, p=probs).astype(np.int8)))
+        W = min(512, max(64, 2 * target))
+        K = 1 if shape.n_prelude + shape.n_coda == 0 else max(1, W // 4)
+        job = binding.PlanJob(reqs, W=W, M=8192, r_max=shape.r_max, r_min=shape.r_min,
+                              kv_blocks=int(kv_gb * 1e9 / (16 * kv_tok)), max_ctx=2048 + 512, max_new_cap=512)
+        for mode in modes:
+            fin, pred = binding.predict_online(job, arr, mode, K, lm)
+            lat = normalized_latency(arr, fin, [r["gen_len"] for r in reqs])
+            st = latency_stats(lat)
+            out.append({"target_batch": target, "rate_per_s": rate, "mode": mode, "requests": len(reqs),
+                        "predicted_mean_ms": st.get("mean_ms"), "predicted_p50_ms": st.get("p50_ms"),
+                        "predicted_mean_core_batch": pred["mean_core_batch"]})
+    return out
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--model", default="ouro")
@@ -128,7 +166,27 @@ def main():
     ap.add_argument("--pilot", type=float, default=6.0)
     ap.add_argument("--kv-gb", type=float, default=150.0)
     ap.add_argument("--seed", type=int, default=4)
+    ap.add_argument("--predict-fit", default="",
+                    help="no GPU: predict with this latency fit (schedule_select --save-fit; 'roofline' for the "
+                         "roofline model) at --rates")
+    ap.add_argument("--rates", default="", help="target:rate pairs for --predict-fit, e.g. 8:6.86,32:21.83")
+    ap.add_argument("--depth-probs", default="0.45,0.39,0.16",
+                    help="exit-depth distribution from r_min up, for --predict-fit")
     args = ap.parse_args()
+
+    if args.predict_fit:
+        from continuous_depth_batching_gb300 import binding
+        from synth import model_shape
+        shape = model_shape(args.model)
+        if args.predict_fit == "roofline":
+            lm = binding.roofline_latency(shape, 6779.4, 1709.3)
+        else:
+            lm = binding.LatencyModel.from_dict(json.load(open(args.predict_fit))["fit"])
+        points = [(int(t), float(r), args.window) for t, r in (p.split(":") for p in args.rates.split(","))]
+        for row in predict_points(shape, lm, points, args.seed, [float(v) for v in args.depth_probs.split(",")],
+                                  args.kv_gb, tuple(args.modes.split(","))):
+            print(json.dumps(row), flush=True)
+        return
 
     from continuous_depth_batching_gb300 import binding
     from continuous_depth_batching_gb300.build import build

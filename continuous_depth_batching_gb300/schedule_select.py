@@ -112,6 +112,7 @@ def main():
     ap.add_argument("--seqs", type=int, default=0, help="first N requests of the workload (0: all)")
     ap.add_argument("--W", type=int, default=0)
     ap.add_argument("--ks", default="", help="K values of the refill sweep (default 1, W/8, W/4, W/2, W)")
+    ap.add_argument("--save-fit", default="", help="write the fitted latency model (JSON) to this path")
     args = ap.parse_args()
 
     import dataclasses
@@ -158,6 +159,9 @@ def main():
         print(json.dumps({"measured": name, "seconds": round(t, 4)}), flush=True)
     fitted, rel = fit_latency(fit_rows)
     print(json.dumps({"fit": fitted, "rms_rel_error_per_call": round(rel, 4), "calls": len(fit_rows)}), flush=True)
+    if args.save_fit:
+        with open(args.save_fit, "w") as fh:
+            json.dump({"model": shape.name, "fit": fitted}, fh)
 
     peaks = {"hbm_gbs": 6779.4, "bf16_tflops_sustained": 1709.3}
     pk = os.path.join(ROOT, "MEASURED_PEAKS.json")

@@ -86,6 +86,18 @@ int cdb_predict_job(const cdb_job *job, int mode, int K, const cdb_latency_model
 int cdb_roofline_latency(const cdb_model_desc *m, double hbm_gbps, double tensor_tflops, double launch_s,
                          cdb_latency_model *out);
 
+/* Online serving (§6.3): request i joins the scheduler when a simulated clock
+ * passes arrival_s[i] (HOST array, seconds, non-decreasing, >= 0); every
+ * scheduler call advances the clock by the cost of the stages it ran, and
+ * with nothing to run the clock jumps to the next arrival.  finish_s[i]
+ * (HOST, written) is the end of the stage that produced request i's last
+ * token, so (finish_s[i] - arrival_s[i]) / gen_len[i] is its normalised
+ * latency.  *out is filled as by cdb_predict_job (busy time; the makespan is
+ * the largest finish time).  Same errors as cdb_predict_job, plus CDB_ERR_ARG
+ * for missing or decreasing arrival times. */
+int cdb_predict_online(const cdb_job *job, const double *arrival_s, int mode, int K,
+                       const cdb_latency_model *lm, double *finish_s, cdb_prediction *out);
+
 /* Picks the schedule with the lowest predicted job latency among no-refill
  * and refill with K in {1, 2, 4, ..., W} (then K = W).  Writes the chosen
  * mode and K, its prediction (nullable) and the best refill and no-refill

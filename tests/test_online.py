@@ -47,3 +47,18 @@ def test_online_requests_have_the_stated_lengths():
     g = np.array([r["gen_len"] for r in reqs])
     assert p.min() >= 64 and p.max() <= 2048 and g.min() >= 32 and g.max() <= 512
     assert all(r["prompt"].max() < 1000 for r in reqs)
+
+
+def test_predicted_points_run_on_the_cpu():
+    """The planner's online prediction over the driver's own requests and arrivals."""
+    from continuous_depth_batching_gb300 import binding
+    from continuous_depth_batching_gb300.online import predict_points
+    from synth import model_shape
+    shape = model_shape("ouro")
+    lm = binding.roofline_latency(shape, 6779.4, 1709.3)
+    rows = predict_points(shape, lm, [(8, 5.0, 4.0)], depth_probs=[0.45, 0.39, 0.16])
+    assert [r["mode"] for r in rows] == ["refill", "no_refill", "fixed_depth"]
+    for r in rows:
+        assert r["requests"] > 0 and np.isfinite(r["predicted_mean_ms"]) and r["predicted_mean_ms"] > 0
+    by = {r["mode"]: r["predicted_mean_ms"] for r in rows}
+    assert by["fixed_depth"] >= by["refill"]   # fixed depth runs every token r_max loops

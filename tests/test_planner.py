@@ -168,3 +168,36 @@ def test_step_info_reports_context_entries():
     sim.step_core()                                     # step 2: it exits (depth 2)
     rc, info = sim.step_boundary()                      # coda of position P, prelude of P + 1
     assert info.stage == 4 and info.ctx == P + 1 and info.stage2 == 2 and info.ctx2 == P + 2
+
+
+@pytest.mark.parametrize("mode", ["refill", "no_refill", "fixed_depth"])
+def test_online_prediction_reduces_to_offline_and_to_isolated_requests(mode):
+    """All arrivals at 0: the online prediction is the offline one (same busy
+    time, the last request finishes at it).  Arrivals far apart: every request
+    runs alone, so its latency is the offline prediction of that request."""
+    r_min, r_max = 2, 5
+    reqs = _reqs(6, 7, r_min, r_max, seed=9)
+    lm = _lm(prefill_delta=1e-3, prefill_gamma=1e-6, core_delta=2e-3, core_gamma=1e-5, core_alpha=1e-8,
+             coda_delta=3e-4, prelude_delta=5e-5)
+    job = binding.PlanJob(reqs, W=4, M=64, r_max=r_max, r_min=r_min)
+    off = binding.predict_job(job, mode, 1, lm)
+    fin, on = binding.predict_online(job, np.zeros(len(reqs)), mode, 1, lm)
+    assert on["seconds"] == pytest.approx(off["seconds"]) and fin.max() == pytest.approx(off["seconds"])
+    assert (fin > 0).all()
+    gap = 10.0 * off["seconds"]
+    arr = gap * np.arange(len(reqs))
+    fin, _ = binding.predict_online(job, arr, mode, 1, lm)
+    for i, r in enumerate(reqs):
+        alone = binding.predict_job(binding.PlanJob([r], W=4, M=64, r_max=r_max, r_min=r_min), mode, 1, lm)
+        assert fin[i] - arr[i] == pytest.approx(alone["seconds"])
+
+
+def test_online_prediction_rejects_bad_arrivals():
+    reqs = _reqs(3, 4, 2, 4)
+    job = binding.PlanJob(reqs, W=2, r_max=4, r_min=2)
+    with pytest.raises(binding.CdbError):
+        binding.predict_online(job, [0.0, 2.0, 1.0], "refill", 1, _lm(core_delta=1.0))
+    with pytest.raises(binding.CdbError):
+        binding.predict_online(job, [-1.0, 0.0, 1.0], "refill", 1, _lm(core_delta=1.0))
+    with pytest.raises(ValueError):
+        binding.predict_online(job, [0.0, 1.0], "refill", 1, _lm(core_delta=1.0))
