@@ -149,27 +149,15 @@ int cdb_predict_job(const cdb_job* job, int mode, int K, const cdb_latency_model
     return CDB_ERR_ARG;
   if (mode != CDB_MODE_FIXED_DEPTH && job->n_seqs > 0 && !job->exit_depths) return CDB_ERR_ARG;
   SchedCfg c;
-  c.mode = mode;
-  c.W = job->W;
-  c.M = job->M;
-  c.S = job->S > 0 ? job->S : (job->W / 8 > 1 ? job->W / 8 : 1);
-  if (c.S > c.W) return CDB_ERR_ARG;
-  c.K = K;
-  c.r_max = job->r_max;
-  c.r_min = job->r_min;
-  c.kv_blocks = job->kv_blocks;
-  c.kv_headroom = job->kv_headroom;
-  c.max_ctx = job->max_ctx;
-  c.max_new_cap = job->max_new_cap;
+  if (!job_cfg(job, mode, K, &c)) return CDB_ERR_ARG;
   CostExecutor ex(mode, job->W, job->r_max, *lm);
   Scheduler sched(c, &ex);
   ex.seqs = &sched.seqs();
   int64_t off = 0, work = 64;
   for (int i = 0; i < job->n_seqs; ++i) {
-    const int8_t* e = mode == CDB_MODE_FIXED_DEPTH || !job->exit_depths ? nullptr : job->exit_depths + off;
-    if (e)
-      for (int t = 0; t + 1 < job->gen_len[i]; ++t)
-        if (e[t] < job->r_min || e[t] > job->r_max) return CDB_ERR_ARG;
+    bool bad = false;
+    const int8_t* e = job_exits(job, mode, i, off, &bad);
+    if (bad) return CDB_ERR_ARG;
     int rc = sched.admit(i, nullptr, job->prompt_len[i], job->gen_len[i], e, nullptr);
     if (rc < 0) return rc;
     off += job->gen_len[i] - 1;
