@@ -237,3 +237,23 @@ def test_poll_returns_each_finished_sequence_once(tiny, tiny_ref):
     ref, _ = gpu_run(shape, dw, reqs, None, mode="refill", W=2, M=64, K=1, max_ctx=64, attn_split=16, force=False)
     for o in seen:
         assert list(o["tokens"]) == list(ref[o["seq_id"]]["tokens"])
+
+
+def test_degenerate_requests_match_oracle(tiny):
+    """A one-token prompt, requests that only prefill (one generated token), a
+    prompt chunked across prefill batches whose context ends exactly at
+    max_ctx, mixed with ordinary requests; and an engine with nothing admitted."""
+    from continuous_depth_batching_gb300 import binding
+    shape, wts, dw, _ = tiny
+    rng = np.random.default_rng(7)
+    max_ctx = 48
+    spec = [(1, 5), (6, 1), (1, 1), (40, 9), (20, 3)]  # (prompt, generated); 40 + 9 - 1 = max_ctx
+    reqs = [dict(seq_id=i, prompt=rng.integers(0, shape.vocab, p).astype(np.int32), gen_len=g, replay=None)
+            for i, (p, g) in enumerate(spec)]
+    ref = oracle_traces(shape, wts, reqs, "adaptive")
+    out, _ = gpu_run(shape, dw, reqs, ref, mode="refill", W=2, M=16, K=1, max_ctx=max_ctx, attn_split=16)
+    compare(out, ref, FP32_TOL, check_logits=False)
+    assert [len(out[i]["tokens"]) for i in range(len(spec))] == [g for _, g in spec]
+    eng = binding.Engine(shape, dw, mode="refill", W=2, M=16, max_ctx=max_ctx, max_new_cap=4)
+    assert eng.step_boundary()[0] == binding.DONE and eng.drain() == []
+    eng.close()

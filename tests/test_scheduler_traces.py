@@ -163,3 +163,21 @@ def test_every_sequence_finishes_with_all_loop_work(mode):
     loops = [r for r in sim.trace() if r["stage"] == "loop"]
     assert sum(sum(r["hist"].values()) for r in loops) == total
     assert max(r["batch"] for r in loops) <= 7
+
+
+@pytest.mark.parametrize("mode", ["refill", "no_refill", "fixed_depth"])
+def test_degenerate_jobs(mode):
+    """No requests: the first call reports DONE.  Requests that generate one
+    token finish in prefill (the token comes from the prompt's last position,
+    App. A.5) and never reach the recurrent core."""
+    from continuous_depth_batching_gb300 import binding
+    sim = Sim(mode, W=2, M=16, S=1, K=1, r_max=4)
+    assert sim.step_boundary()[0] == binding.DONE
+    sim = Sim(mode, W=2, M=16, S=1, K=1, r_max=4)
+    for i, p in enumerate([1, 16, 33]):            # one token, exactly M, two chunks and a bit
+        sim.admit(i, p, 1, np.zeros(0, np.int8))
+    sim.run()
+    assert sorted(sim.finished()) == [0, 1, 2]
+    tr = sim.trace()
+    assert not any(r["stage"] in ("loop", "coda", "prelude") for r in tr)
+    assert sum(r["prefill_tokens"] for r in tr if r["stage"] == "prefill") == 1 + 16 + 33
