@@ -31,8 +31,6 @@ def main():
     ap.add_argument("--split", type=int, default=0, help="keys per split-KV partial (0: library default)")
     args = ap.parse_args()
 
-    import torch
-
     from continuous_depth_batching_gb300 import binding
     from continuous_depth_batching_gb300.build import build
     from synth import make_requests, make_weights, model_shape, workload

@@ -5,7 +5,6 @@ times, sum of their tokens) is checked with two gloo ranks on the CPU.
 
 import os
 
-import pytest
 import torch.multiprocessing as mp
 
 
