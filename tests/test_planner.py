@@ -201,3 +201,29 @@ def test_online_prediction_rejects_bad_arrivals():
         binding.predict_online(job, [-1.0, 0.0, 1.0], "refill", 1, _lm(core_delta=1.0))
     with pytest.raises(ValueError):
         binding.predict_online(job, [0.0, 1.0], "refill", 1, _lm(core_delta=1.0))
+
+
+def test_roofline_model_of_the_huginn_shape():
+    """Adapter in the core, two prelude and two coda blocks, the LM head in the coda."""
+    shape = model_shape("huginn")
+    lm = binding.roofline_latency(shape, 6000.0, 1500.0).as_dict()
+    d, f, V = shape.d_model, shape.ffn, shape.vocab
+    block = 4 * d * d + 3 * d * f
+    assert lm["core"]["delta"] == pytest.approx((shape.n_core * block + 2 * d * d) * 2 / 6000e9)
+    assert lm["prelude"]["delta"] == pytest.approx(shape.n_prelude * block * 2 / 6000e9)
+    assert lm["coda"]["delta"] == pytest.approx((shape.n_coda * block + V * d) * 2 / 6000e9)
+    assert lm["prelude"]["alpha"] == pytest.approx(shape.n_prelude * 2 * d * 2 / 6000e9)
+    applications = shape.n_prelude + shape.r_max * shape.n_core + shape.n_coda
+    assert lm["prefill"]["alpha"] == pytest.approx(4 * d * applications / 1500e12)
+
+
+def test_prefill_chunks_follow_the_token_budget():
+    """One prompt of P tokens with budget M is prefilled in ceil(P / M) chunks
+    (App. A.1), and the prefill context entries are the causal pairs."""
+    P = 100
+    for M in (16, 33, 100, 128):
+        job = binding.PlanJob([dict(prompt_len=P, gen_len=3, exit_depths=np.array([2, 2], np.int8))],
+                              W=1, M=M, r_max=3, r_min=2)
+        p = binding.predict_job(job, "refill", 1, _lm(prefill_delta=1.0, prefill_alpha=1e-9))
+        assert p["prefill_stages"] == -(-P // M)
+        assert p["prefill_seconds"] == pytest.approx(-(-P // M) + 1e-9 * P * (P + 1) / 2)
