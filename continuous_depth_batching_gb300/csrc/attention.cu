@@ -30,6 +30,8 @@
 // Scores are kept in the log2 domain (exp2).  With one split the warp writes
 // the normalised output; otherwise (m, l, acc) partials that k_attn_combine
 // merges in split order.
+#include <algorithm>
+
 #include "common.cuh"
 #include "kernels.cuh"
 #include "tmap.h"
@@ -364,6 +366,16 @@ struct Acc<T, HD, false> {
   }
 };
 
+namespace attn {
+// A row's last key position must lie inside both the split partials
+// (max_splits * split keys) and its block-table row (max_blocks pages), and
+// its sequence slot must be a table row.  Rows that fail are skipped and
+// flagged (kStatusBadRow), never read past those arrays.
+__device__ __forceinline__ bool row_in_bounds(int pos, int slot, int split, int max_splits, int max_blocks) {
+  return pos >= 0 && slot >= 0 && (long long)pos < (long long)split * max_splits && (pos >> 4) < max_blocks;
+}
+}  // namespace attn
+
 template <typename T, int HD>
 __global__ void __launch_bounds__((attn::kWarps + 1) * 32)
     k_attn(const T* __restrict__ Q, int rows, const int* __restrict__ mslot, const int* __restrict__ mpos,
@@ -407,7 +419,12 @@ __global__ void __launch_bounds__((attn::kWarps + 1) * 32)
           it = atomicAdd(counter, 1);
           if (it >= n_items) break;
           const int sp = it / per_sp, row = (it - sp * per_sp) / ngroups;
-          if (sp * split <= __ldg(&mpos[row])) break;  // split sp starts at or before the row's last key
+          const int p = __ldg(&mpos[row]);
+          if (!attn::row_in_bounds(p, __ldg(&mslot[row]), split, max_splits, kv.max_blocks)) {
+            if (sp == 0) atomicOr(status, kStatusBadRow);
+            continue;
+          }
+          if (sp * split <= p) break;  // split sp starts at or before the row's last key
         } while (true);
       }
       return __shfl_sync(0xffffffffu, it, 0);
@@ -644,6 +661,10 @@ __global__ void __launch_bounds__((attn::kWarps + 1) * 32)
   pdl_trigger();
   if (row >= rows) return;
   const int L = mpos[row] + 1;
+  if (!attn::row_in_bounds(L - 1, mslot[row], split, max_splits, kv.max_blocks)) {
+    if (threadIdx.x == 0 && sp == 0 && blockIdx.y == 0) atomicOr(status, kStatusBadRow);
+    return;
+  }
   const int nsp = (L + split - 1) / split;
   if (sp >= nsp) return;
   const int k_lo = sp * split, k_hi = min(L, k_lo + split);
@@ -1076,7 +1097,7 @@ __global__ void __launch_bounds__(5 * 32)
 // loaded (m_s, l_s) and broadcast; the output sums over splits in split order.
 template <typename T>
 __global__ void k_attn_combine(int rows, const int* __restrict__ mpos, int H, int HDv, int d, int split,
-                               int max_splits, const float* __restrict__ part_o,
+                               int max_splits, int max_keys, const float* __restrict__ part_o,
                                const float* __restrict__ part_ml, T* __restrict__ O) {
   pdl_wait();
   pdl_trigger();
@@ -1085,6 +1106,7 @@ __global__ void k_attn_combine(int rows, const int* __restrict__ mpos, int H, in
   const int row = item / H, h = item % H;
   if (row >= rows) return;
   const int L = mpos[row] + 1;
+  if (L < 1 || L > max_keys) return;  // skipped and flagged by the attention kernel
   const int nsp = (L + split - 1) / split;
   if (nsp <= 1) return;
   const size_t pi = ((size_t)row * H + h) * max_splits;
@@ -1149,12 +1171,13 @@ static bool attn_tma(cudaStream_t s, const __nv_bfloat16* Q, int rows, const int
   if (pool_rows + 16 * attn::kWarps >= (1ull << 31)) return false;  // tile row coordinates are int32
   const CUtensorMap* tm = tmap_bf16_2d(kv.pool, HD, pool_rows, (uint64_t)HD * 2, Gm::XW, Gm::ROWS, Gm::SWB);
   if (!tm) return false;
-  static bool set = false;
-  if (!set) {
+  static bool set[kMaxDevices] = {};
+  const int dev = current_device();
+  if (!set[dev]) {
     if (cudaFuncSetAttribute(k_attn_tma<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Gm::SMEM) !=
         cudaSuccess)
       return false;
-    set = true;
+    set[dev] = true;
   }
   dim3 grid(max_splits, (H + attn::kWarps - 1) / attn::kWarps, rows);
   count_launch();
@@ -1175,24 +1198,27 @@ static void attn_hd(cudaStream_t s, const T* Q, int rows, const int* mslot, cons
   }
   if (!done) {
     using Gm = attn::Geo<T, HD>;
-    static int ctas = 0;
-    if (!ctas) {
+    // Grid size (SMs x resident CTAs) and the shared-memory attribute, per device.
+    static int ctas[kMaxDevices] = {};
+    const int dev = current_device();
+    if (!ctas[dev]) {
       cudaFuncSetAttribute(k_attn<T, HD>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Gm::SMEM);
-      int dev = 0, sms = 0, per_sm = 0;
-      cudaGetDevice(&dev);
+      int sms = 0, per_sm = 0;
       cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
       cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_attn<T, HD>, (attn::kWarps + 1) * 32, Gm::SMEM);
-      ctas = sms * (per_sm > 0 ? per_sm : 1);
+      ctas[dev] = (sms > 0 ? sms : 1) * (per_sm > 0 ? per_sm : 1);
     }
     const long long items = (long long)max_splits * rows * ((H + attn::kWarps - 1) / attn::kWarps);
-    const int grid = (int)(items < ctas ? items : ctas);
+    const int grid = (int)(items < ctas[dev] ? items : ctas[dev]);
     count_launch();  // uniform reads never touch the exit-depth table
     launch_pdl(k_attn<T, HD>, dim3(grid), dim3((attn::kWarps + 1) * 32), Gm::SMEM, s, Q, rows, mslot, mpos, mdepth,
                depth_uniform, kv, slot_base, clamp, uniform ? 0 : 1, H, split, max_splits, O, part_o, part_ml, status);
   }
   if (max_splits > 1)
     count_launch(), launch_pdl(k_attn_combine<T>, dim3((rows * H + 3) / 4), dim3(128), 0, s, rows, mpos, H, HD, kv.d,
-                               split, max_splits, part_o, part_ml, O);
+                               split, max_splits, (int)std::min<long long>((long long)split * max_splits,
+                                                                           (long long)kv.max_blocks * 16),
+                               part_o, part_ml, O);
 }
 
 template <int HD>
@@ -1204,12 +1230,13 @@ static bool prefill_hd(cudaStream_t s, const __nv_bfloat16* Q, int q_rows, const
   const CUtensorMap* tk = tmap_bf16_2d(kv.pool, HD, pool_rows, (uint64_t)HD * 2, Pg::XW, 16, Pg::SWB);
   const CUtensorMap* tq = tmap_bf16_2d(Q, (uint64_t)kv.d, q_rows, (uint64_t)kv.d * 2, Pg::XW, attn::kPfRows, Pg::SWB);
   if (!tk || !tq) return false;
-  static bool set = false;
-  if (!set) {
+  static bool set[kMaxDevices] = {};
+  const int dev = current_device();
+  if (!set[dev]) {
     if (cudaFuncSetAttribute(k_attn_prefill<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Pg::SMEM) !=
         cudaSuccess)
       return false;
-    set = true;
+    set[dev] = true;
   }
   count_launch();
   return launch_pdl(k_attn_prefill<HD>, dim3(n_tiles, H), dim3(5 * 32), Pg::SMEM, s, *tq, *tk, tiles, kv, slot, H, O,

@@ -7,6 +7,15 @@
 
 namespace cdb {
 
+// Per-device caches of kernel attributes and launch geometry are indexed by
+// the current device (a process may drive several GPUs, one context each).
+constexpr int kMaxDevices = 64;
+inline int current_device() {
+  int d = 0;
+  if (cudaGetDevice(&d) != cudaSuccess || d < 0 || d >= kMaxDevices) d = 0;
+  return d;
+}
+
 // Programmatic dependent launch.  Every kernel of the decode path is launched
 // so that it may start while the previous kernel in the stream finishes; it
 // calls pdl_wait() before its first access to memory another kernel writes

@@ -546,12 +546,13 @@ static bool launch_bn(cudaStream_t s, const __nv_bfloat16* A, int lda, int a_row
   const CUtensorMap* mw2 = EPI == kEpiSwiglu ? get_map(W2, K, N, (uint64_t)K * 2, BM) : mw;
   const CUtensorMap* ma = get_map(A, K, a_rows, (uint64_t)lda * 2, BN);
   if (!mw || !mw2 || !ma) return false;
-  static bool attr = false;
-  if (!attr) {
+  static bool attr[kMaxDevices] = {};
+  const int dev = current_device();
+  if (!attr[dev]) {
     if (cudaFuncSetAttribute(k_gemm_tc<BN, EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) !=
         cudaSuccess)
       return false;
-    attr = true;
+    attr[dev] = true;
   }
   count_launch();
   return launch_pdl(k_gemm_tc<BN, EPI>, dim3((N + BM - 1) / BM, (rows + BN - 1) / BN, splits), dim3(128), C::SMEM, s,
@@ -568,12 +569,13 @@ static bool launch_pf(cudaStream_t s, const __nv_bfloat16* A, int lda, int a_row
   const CUtensorMap* mw2 = EPI == kEpiSwiglu ? get_map(W2, K, N, (uint64_t)K * 2, BM) : mw;
   const CUtensorMap* ma = get_map(A, K, a_rows, (uint64_t)lda * 2, BN);
   if (!mw || !mw2 || !ma) return false;
-  static bool attr = false;
-  if (!attr) {
+  static bool attr[kMaxDevices] = {};
+  const int dev = current_device();
+  if (!attr[dev]) {
     if (cudaFuncSetAttribute(k_gemm_pf<BN, EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) !=
         cudaSuccess)
       return false;
-    attr = true;
+    attr[dev] = true;
   }
   const long long tiles = (long long)((N + BM - 1) / BM) * ((rows + BN - 1) / BN);
   const int grid = (int)(tiles < max_ctas ? tiles : max_ctas);
@@ -585,14 +587,14 @@ static bool launch_pf(cudaStream_t s, const __nv_bfloat16* A, int lda, int a_row
 }  // namespace tc
 
 static int sm_count() {
-  static int n = 0;
-  if (!n) {
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) !=
-                                                  cudaSuccess || n <= 0)
-      n = 1;
+  static int n[kMaxDevices] = {};
+  const int dev = current_device();
+  if (!n[dev]) {
+    int v = 0;
+    if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || v <= 0) v = 1;
+    n[dev] = v;
   }
-  return n;
+  return n[dev];
 }
 
 // Split count of a decode GEMM: at least four 64-element K slabs per split,
@@ -600,35 +602,13 @@ static int sm_count() {
 // 128-row tiles) but one per SM for wide ones (at least 32 tiles), whose
 // consumers then fold half as many partials.  Depends only on the weight
 // shape (and the device), never on the number of rows.
-// CDB_GEMM_SPLIT_CAP (1..kGemmMaxSplits) lowers the cap, for tuning.
-static int split_cap() {
-  static int cap = 0;
-  if (!cap) {
-    const char* e = std::getenv("CDB_GEMM_SPLIT_CAP");
-    const int v = e ? std::atoi(e) : 0;
-    cap = v >= 1 && v <= kGemmMaxSplits ? v : kGemmMaxSplits;
-  }
-  return cap;
-}
-
-// Prefill GEMMs run the persistent kernel unless CDB_PREFILL_GEMM=tiles
-// (one CTA per output tile, two per SM), kept for comparison.
-static bool persistent_prefill() {
-  static int p = -1;
-  if (p < 0) {
-    const char* e = std::getenv("CDB_PREFILL_GEMM");
-    p = e && std::strcmp(e, "tiles") == 0 ? 0 : 1;
-  }
-  return p == 1;
-}
-
 int gemm_tc_splits(int N, int K, bool decode) {
   if (!decode) return 1;
   const int tiles = (N + tc::BM - 1) / tc::BM;
   const int KT = (K + tc::BK - 1) / tc::BK;
   int s = (tiles >= 32 ? 1 : 2) * sm_count() / tiles;
   if (s > KT / 4) s = KT / 4;
-  if (s > split_cap()) s = split_cap();
+  if (s > kGemmMaxSplits) s = kGemmMaxSplits;
   return s < 1 ? 1 : s;
 }
 
@@ -649,7 +629,7 @@ int launch_gemm_tc(cudaStream_t s, int epi, const __nv_bfloat16* A, int lda, int
       case kEpiResid: ok = tc::launch_bn<64, kEpiResid>(s, A, lda, a_rows, W, W2, N, K, rows, splits, Cf, Ct, ldc, P, status); break;
       default: ok = tc::launch_bn<64, kEpiSwiglu>(s, A, lda, a_rows, W, W2, N, K, rows, splits, Cf, Ct, ldc, P, status); break;
     }
-  } else if (persistent_prefill()) {
+  } else {
     // Prefill, persistent: one CTA per SM, double-buffered accumulators;
     // 256-row tiles where one accumulator fits, 128-row tiles for SwiGLU.
     const bool wide = rows > 128;
@@ -664,21 +644,6 @@ int launch_gemm_tc(cudaStream_t s, int epi, const __nv_bfloat16* A, int lda, int
                   : tc::launch_pf<128, kEpiResid>(s, A, lda, a_rows, W, W2, N, K, rows, Cf, Ct, ldc, sm, status);
         break;
       default: ok = tc::launch_pf<128, kEpiSwiglu>(s, A, lda, a_rows, W, W2, N, K, rows, Cf, Ct, ldc, sm, status); break;
-    }
-  } else {
-    // Prefill: 256-row tiles (twice the weight-tile reuse per staged byte)
-    // where one accumulator fits; SwiGLU keeps two and 128-row tiles.
-    const bool wide = rows > 128;
-    switch (epi) {
-      case kEpiStore:
-        ok = wide ? tc::launch_bn<256, kEpiStore>(s, A, lda, a_rows, W, W2, N, K, rows, 1, Cf, Ct, ldc, nullptr, status)
-                  : tc::launch_bn<128, kEpiStore>(s, A, lda, a_rows, W, W2, N, K, rows, 1, Cf, Ct, ldc, nullptr, status);
-        break;
-      case kEpiResid:
-        ok = wide ? tc::launch_bn<256, kEpiResid>(s, A, lda, a_rows, W, W2, N, K, rows, 1, Cf, Ct, ldc, nullptr, status)
-                  : tc::launch_bn<128, kEpiResid>(s, A, lda, a_rows, W, W2, N, K, rows, 1, Cf, Ct, ldc, nullptr, status);
-        break;
-      default: ok = tc::launch_bn<128, kEpiSwiglu>(s, A, lda, a_rows, W, W2, N, K, rows, 1, Cf, Ct, ldc, nullptr, status); break;
     }
   }
   if (!ok) return -1;

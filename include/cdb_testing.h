@@ -100,9 +100,16 @@ int cdb_test_attention_prefill(const void *q, int rows, const int32_t *row_slot,
  * Nothing is allocated: no cudaMalloc, cudaFree or allocating library call.
  * The first call on a device looks up the array's device address (once per
  * device, with that device current); make that first call before any stream
- * capture.  All calls share the one array and it keeps the previous call's
- * contents, so calls that overlap on the GPU (other streams, other host
- * threads) race; issue them one after another.  Synchronizes the stream. */
+ * capture.  With CUDA's lazy module loading (the default) the library's device
+ * code, and with it the array, is loaded onto a device the first time any
+ * kernel or symbol of this library is used there; if that is this call, the
+ * driver takes the array's memory then.  A caller that must keep every call
+ * free of that cost makes one warm-up call on each device at set-up (or runs
+ * with CUDA_MODULE_LOADING=EAGER).  All calls share the one array and it keeps
+ * the previous call's contents, so calls that overlap on the GPU (other
+ * streams, other host threads) race; issue them one after another.  A row
+ * whose position lies past max_ctx's block table or split partials is skipped
+ * and the call returns CDB_ERR_DEVICE_BOUNDS.  Synchronizes the stream. */
 int cdb_attention_noalloc(const void *q, int rows, const int32_t *slot, const int32_t *pos,
                           const int32_t *depth, const void *kv_pool, const int32_t *block_table,
                           int max_blocks, const uint8_t *exit_table, int kv_blocks, int n_kv_slots,

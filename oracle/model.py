@@ -194,7 +194,7 @@ class OracleModel:
         return _f32(self.w["embed"][np.asarray(tokens)])
 
     def adapter(self, e, s):
-        """Huginn-shaped loop input x = A [e; s] (BASELINE config: concat 2d -> d)."""
+        """Huginn-shaped loop input x = A [e; s]: the concatenation of the prelude output and the loop state (2d -> d)."""
         x = self.store(np.concatenate([e, s], axis=-1))
         return _f32(self.linear(x, self.w["adapter"], "core"))
 

@@ -5,9 +5,10 @@ whose host program owns all device memory or a latency-critical path that
 cannot absorb an allocation's synchronisation; its scratch lives in a 16 MiB
 array built into the library.  This file checks, through the C ABI, that two
 calls in a row (different shapes and dtypes, so the second call starts from
-the first call's leftover scratch) each match cdb_test_attention, the same
-kernel run with caller-provided scratch, within the attention tests'
-tolerance; and that a request too large for the built-in scratch is refused.
+the first call's leftover scratch) each equal cdb_test_attention, the same
+kernels with the same split order run on caller-provided scratch, bit for
+bit; that a request too large for the built-in scratch is refused; and that a
+row positioned past the block table is skipped and reported.
 Collected last so a failure here cannot stop the other GPU tests.
 """
 
@@ -64,22 +65,17 @@ def without_allocation(L, cs, d, split):
     return out
 
 
-def close(a, b, dtype):
-    tol = 2e-5 if dtype == 0 else 1e-2  # the attention tests' tolerances (fp32, bf16)
-    a, b = a.double(), b.double()
-    return bool(((a - b).abs() <= tol * (1 + b.abs())).all().item())
-
-
 def test_two_calls_in_a_row_match_the_caller_scratch_entry_point(L):
-    first = make_case(1, 16, 128, rows=9, max_ctx=1300, seed=21)   # bf16, 5 splits of 256
+    import torch
+    first = make_case(1, 16, 128, rows=9, max_ctx=1300, seed=21)   # bf16, 6 splits of 256
     second = make_case(0, 4, 64, rows=5, max_ctx=200, seed=22)     # fp32, 13 splits of 16
     d1, d2 = device_inputs(first), device_inputs(second)
     ref1 = with_caller_scratch(L, first, d1, 256)
     ref2 = with_caller_scratch(L, second, d2, 16)
     got1 = without_allocation(L, first, d1, 256)
     got2 = without_allocation(L, second, d2, 16)
-    assert close(got1, ref1, 1)
-    assert close(got2, ref2, 0)
+    assert torch.equal(got1, ref1)
+    assert torch.equal(got2, ref2)
 
 
 def test_request_beyond_the_built_in_scratch_is_refused(L):
@@ -89,3 +85,23 @@ def test_request_beyond_the_built_in_scratch_is_refused(L):
     a[1] = 4096          # rows: 4096 * 16 heads * 4 splits * 130 floats > 16 MiB
     a[16] = 64
     assert L.cdb_attention_noalloc(*a, d["q"].data_ptr(), None) == -1
+
+
+def test_row_past_the_block_table_is_reported(L):
+    """pos == max_ctx with max_ctx a multiple of 16 and of the split: the row's
+    page is past its block-table row and its last split past the partials, so
+    the kernels skip it and the call reports CDB_ERR_DEVICE_BOUNDS (-5)."""
+    import torch
+    cs = make_case(1, 4, 64, rows=3, max_ctx=512, seed=24)
+    cs["pos"][2] = cs["max_ctx"]
+    d = device_inputs(cs)
+    out = torch.zeros(3, cs["H"] * cs["hd"], dtype=cs["q"].dtype, device="cuda")
+    assert L.cdb_attention_noalloc(*args(cs, d, 256), out.data_ptr(), None) == -5
+    nb = L.cdb_test_attention_scratch_bytes(3, cs["H"], cs["hd"], 256, cs["max_ctx"])
+    scratch = torch.empty(nb, dtype=torch.uint8, device="cuda")
+    assert L.cdb_test_attention(*args(cs, d, 256), out.data_ptr(), scratch.data_ptr(), nb, None) == -5
+    # The valid rows are still computed, and the next call starts clean.
+    cs["pos"][2] = cs["max_ctx"] - 1
+    d = device_inputs(cs)
+    ref = with_caller_scratch(L, cs, d, 256)
+    assert torch.equal(without_allocation(L, cs, d, 256), ref)
