@@ -153,6 +153,15 @@ class BruteForceLM:
             return d
         return d if i < self.P else self.exit_depth(j)
 
+    def probe_logit(self, i, d):
+        """Linear exit probe on the state after loop step d: the state scaled to
+        unit root-mean-square (eps inside the root, unit gain), dotted with the
+        gate vector, plus the bias."""
+        s = self.state(i, d)
+        rms = math.sqrt(sum(float(x) * float(x) for x in s) / len(s) + self.m.rms_eps)
+        w = self.w["gate_w"]
+        return sum(float(w[c]) * float(s[c]) for c in range(len(s))) / rms + self.m.gate_bias
+
     @functools.lru_cache(maxsize=None)
     def coda_in(self, i, l):
         if l == 0:

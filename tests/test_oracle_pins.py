@@ -15,6 +15,13 @@
 * RoPE scores depend only on the relative position.
 * Executed FLOPs equal the closed form used by §5 eq. (1).
 * Exit gaps of the depth-indexed cache are never written.
+* Probe gate (§4.3): a closed form of the probe on a 2-element state, and the
+  oracle's gate logits and exit depths equal the probe applied to the brute
+  force's loop states (after the step) with the lookahead rule.
+* bf16 storage (Table 1, bfloat16): at fixed depth the oracle's bf16 logits
+  equal a full-sequence torch forward that casts through torch.bfloat16 at the
+  same storage points, and dropping any one point moves the logits far outside
+  that tolerance.
 * Convergence exit (App. E.2): the oracle's statistics and exit depths equal
   the normalised L2 distances of the brute force's loop states with the
   lookahead rule applied to them; c = 1 exactly at step 1 when s_0 = 0; a
@@ -23,6 +30,7 @@
 """
 
 import dataclasses
+import functools
 import math
 
 import numpy as np
@@ -362,3 +370,186 @@ def test_convergence_gate_extremes():
         np.testing.assert_array_equal(a, b)
     # s_0 = 0 with the adapter: the first statistic is exactly 1.
     assert all(zs[0] == 1.0 for zs in lo.gate_logits)
+
+
+# ---------------------------------------------------------------------------
+# probe gate (§4.3): closed form, and logits from the brute force's loop states
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("eps,want", [(0.0, 0.1 + math.sqrt(2.0)), (12.5, 1.1)])
+def test_probe_logit_closed_form(eps, want):
+    """h = [3, 4] has mean square 12.5.  With w = [1, 0.5], b = 0.1 and eps = 0
+    the unit-RMS state is [3, 4] / sqrt(12.5), so z = 0.1 + 5 / sqrt(12.5) =
+    0.1 + sqrt(2); with eps = 12.5 inside the root the divisor is 5 and
+    z = 0.1 + 1.  Dropping the normalisation (z = 5.1), adding eps outside the
+    root, or a gain other than one gives other values."""
+    shape = micro(d_model=2, n_heads=1, head_dim=2, rms_eps=eps, gate_bias=0.1)
+    om = OracleModel(shape, {"gate_w": np.array([1.0, 0.5], dtype=np.float32)})
+    z = om.gate_logit(np.array([[3.0, 4.0]]))
+    assert z.shape == (1,)
+    assert z[0] == pytest.approx(want, abs=1e-6)
+
+
+@pytest.mark.parametrize("variant", ["looped", "huginn_like"])
+def test_probe_gate_matches_brute_force(variant):
+    """The oracle's gate logits and exit depths equal the probe applied to the
+    brute force's cache-free loop states (the state after step d), with the
+    lookahead rule applied to them: a logit above logit(q) = 0 after step d,
+    r_min - 1 <= d <= r_max - 2, makes the token run step d + 1 and leave."""
+    kw = dict(r_max=5)
+    if variant == "huginn_like":
+        kw.update(n_prelude=1, n_core=1, n_coda=1, has_adapter=True)
+    shape0 = micro(**kw)
+    wts = make_weights(shape0)
+    prompt = prompt_for(shape0, 5, seed=29)
+    gen = 7
+    # Logits of a run that never exits place the threshold inside their range.
+    free = decode_sequence(OracleModel(shape0, wts), prompt, gen, mode="fixed")
+    deciding = [z for zs in free.gate_logits for z in zs[shape0.r_min - 2:shape0.r_max - 2]]
+    shape = dataclasses.replace(shape0, gate_bias=-float(np.median(deciding)))
+    tr = decode_sequence(OracleModel(shape, wts), prompt, gen, keep_logits=gen)
+    assert len(set(tr.exit_depths)) >= 3, tr.exit_depths
+
+    P = len(prompt)
+    bf = None
+
+    @functools.lru_cache(maxsize=None)
+    def exit_of(t):
+        i = P + t - 1
+        for d in range(shape.r_min - 1, shape.r_max - 1):
+            if bf.probe_logit(i, d) > 0.0:
+                return d + 1
+        return shape.r_max
+
+    bf = BruteForceLM(shape, wts, prompt, gen, exit_of)
+    toks, lg = bf.run()
+    assert tr.exit_depths == [exit_of(t) for t in range(1, gen)]
+    assert tr.tokens == toks
+    for t in range(1, gen):
+        i = P + t - 1
+        want = [bf.probe_logit(i, d) for d in range(1, tr.exit_depths[t - 1])]
+        np.testing.assert_allclose(tr.gate_logits[t - 1], want, rtol=0, atol=2e-5)
+        # no decision within rounding distance of the threshold
+        assert min(abs(z) for z in want[shape.r_min - 2:]) > 1e-4
+    for t in range(gen):
+        np.testing.assert_allclose(tr.logits[t], lg[t], atol=2e-5, rtol=0)
+
+
+def test_probe_gate_reads_the_state_after_the_step():
+    """Sensitivity of the brute-force pin: the probe on the state that entered
+    step d (before it) gives other logits than the oracle records for step d."""
+    shape = micro(r_max=4)
+    wts = make_weights(shape)
+    prompt = prompt_for(shape, 5, seed=29)
+    depths = np.array([4, 4, 4], dtype=np.int8)
+    tr = decode_sequence(OracleModel(shape, wts), prompt, 4, force_exit=depths)
+    bf = BruteForceLM(shape, wts, prompt, 4, lambda t: int(depths[t - 1]))
+    i = len(prompt)
+    after = [bf.probe_logit(i, d) for d in range(1, 4)]
+    state, bf.state = bf.state, lambda j, d: state(j, d - 1)
+    before = [bf.probe_logit(i, d) for d in range(1, 4)]
+    np.testing.assert_allclose(tr.gate_logits[0], after, atol=2e-5, rtol=0)
+    assert np.max(np.abs(np.array(tr.gate_logits[0]) - np.array(before))) > 1e-2
+
+
+# ---------------------------------------------------------------------------
+# bf16 storage points (Table 1, bfloat16): an independent torch forward
+# ---------------------------------------------------------------------------
+
+# Values the method stores in bf16 (the rest stays float32): the normalised
+# inputs of the QKV, gate/up and LM-head products, q, k and v after RoPE (so
+# the KV cache), the attention output, the SwiGLU product and the adapter input.
+BF16_POINTS = ("attn_norm", "q", "k", "v", "attn_out", "mlp_norm", "swiglu", "adapter_in", "head_in")
+
+
+def torch_bf16_fixed_depth_logits(shape, weights, tokens, skip=None):
+    """Cache-free causal forward of the whole sequence at fixed depth (every
+    token runs r_max loop steps, so with a depth-indexed cache this is the
+    unrolled transformer).  Arithmetic in float64 through torch's own ops;
+    every result stored as float32, and cast through torch.bfloat16 from
+    float32 at the points of BF16_POINTS except `skip` (to show that each point
+    matters).  Returns float32-valued logits for every position."""
+    w = {k: torch.from_numpy(v.view(np.int16)).view(torch.bfloat16).to(torch.float64)
+         for k, v in weights.items()}
+    T = len(tokens)
+    d, H, hd = shape.d_model, shape.n_heads, shape.head_dim
+
+    def f32(t):
+        return t.to(torch.float32).to(torch.float64)
+
+    def bf(t, point):
+        return f32(t) if point == skip else t.to(torch.float32).to(torch.bfloat16).to(torch.float64)
+
+    inv = shape.rope_theta ** (-torch.arange(0, hd, 2, dtype=torch.float64) / hd)
+    ang = torch.arange(T, dtype=torch.float64)[:, None] * inv[None, :]
+    cos, sin = torch.cos(ang), torch.sin(ang)
+
+    def rope(t):  # [H, T, hd]
+        a, b = t[..., : hd // 2], t[..., hd // 2:]
+        return torch.cat([a * cos - b * sin, b * cos + a * sin], dim=-1)
+
+    def norm(t, g, point):
+        return bf(F.rms_norm(t, (d,), g, eps=shape.rms_eps), point)
+
+    def block(p, x):
+        u = norm(x, w[p + "attn_norm"], "attn_norm")
+        q, k, v = f32(F.linear(u, w[p + "wqkv"])).split(d, dim=-1)
+        q = bf(rope(q.view(T, H, hd).transpose(0, 1)), "q")
+        k = bf(rope(k.view(T, H, hd).transpose(0, 1)), "k")
+        v = bf(v.view(T, H, hd).transpose(0, 1), "v")
+        o = F.scaled_dot_product_attention(q, k, v, is_causal=True)
+        o = bf(o.transpose(0, 1).reshape(T, d), "attn_out")
+        x = f32(x + F.linear(o, w[p + "wo"]))
+        u = norm(x, w[p + "mlp_norm"], "mlp_norm")
+        mid = bf(f32(F.silu(f32(F.linear(u, w[p + "wg"]))) * f32(F.linear(u, w[p + "wu"]))), "swiglu")
+        return f32(x + F.linear(mid, w[p + "wd"]))
+
+    x = w["embed"][torch.as_tensor(tokens, dtype=torch.long)]
+    for i in range(shape.n_prelude):
+        x = block(f"prelude.{i}.", x)
+    e = x
+    s = torch.zeros_like(e) if shape.has_adapter else e
+    for _ in range(shape.r_max):
+        if shape.has_adapter:
+            s = f32(F.linear(bf(torch.cat([e, s], dim=-1), "adapter_in"), w["adapter"]))
+        for l in range(shape.n_core):
+            s = block(f"core.{l}.", s)
+    y = s
+    for j in range(shape.n_coda):
+        y = block(f"coda.{j}.", y)
+    return f32(F.linear(norm(y, w["final_norm"], "head_in"), w["lm_head"])).numpy()
+
+
+def _bf16_case(variant, r_max):
+    kw = dict(dtype="bf16", r_max=r_max, r_min=min(2, r_max))
+    if variant == "huginn_like":
+        kw.update(n_prelude=1, n_core=1, n_coda=1, has_adapter=True)
+    shape = micro(**kw)
+    wts = make_weights(shape)
+    prompt = prompt_for(shape, 8, seed=31)
+    gen = 5
+    tr = decode_sequence(OracleModel(shape, wts), prompt, gen, mode="fixed", keep_logits=gen)
+    seq = np.concatenate([prompt, np.array(tr.tokens[:-1], dtype=np.int32)])
+    return shape, wts, seq, tr, len(prompt) - 1
+
+
+@pytest.mark.parametrize("r_max", [1, 3])
+@pytest.mark.parametrize("variant", ["looped", "huginn_like"])
+def test_bf16_storage_points_match_torch(variant, r_max):
+    shape, wts, seq, tr, p0 = _bf16_case(variant, r_max)
+    ref = torch_bf16_fixed_depth_logits(shape, wts, seq)
+    for t in range(len(tr.tokens)):
+        np.testing.assert_allclose(tr.logits[t], ref[p0 + t], atol=1e-5, rtol=0)
+
+
+@pytest.mark.parametrize("variant", ["looped", "huginn_like"])
+def test_each_bf16_storage_point_matters(variant):
+    """Dropping any one rounding point moves the logits far outside the
+    tolerance above, so an oracle that missed (or added) one would fail it."""
+    shape, wts, seq, tr, p0 = _bf16_case(variant, 3)
+    got = np.array(tr.logits)
+    for point in BF16_POINTS:
+        if point == "adapter_in" and not shape.has_adapter:
+            continue
+        ref = torch_bf16_fixed_depth_logits(shape, wts, seq, skip=point)[p0:p0 + len(got)]
+        assert np.max(np.abs(got - ref)) > 1e-4, point
