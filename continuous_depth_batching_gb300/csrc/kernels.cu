@@ -446,7 +446,10 @@ __global__ void k_gate(const float* __restrict__ X, const float* __restrict__ Sp
 // Row i exits after this step if its previous-step flag was set or it reached
 // r_max.  Exits keep slot order and go to the coda rows after qc_off; the
 // rest keep slot order at the front of the continuing rows.  One block per
-// row; each block ranks its row with a block-wide count over the earlier rows.
+// row; its destination is the exclusive prefix sum of the exit flags at row
+// i, taken as a block-wide population count of the flags of rows j < i
+// (__syncthreads_count, blockDim rows per round), and the row moves in
+// 16-byte vectors.
 // blockIdx.y == 0 compacts row blockIdx.x; blockIdx.y = 1 + l fills the exit
 // gaps of core layer l: a row leaving after loop step r < r_max copies its
 // slot-r K and V into slots r+1 .. r_max of that layer.  A later reader at
@@ -459,7 +462,6 @@ __global__ void k_compact(const float* __restrict__ X, RowMeta m, const int* __r
                           int cap, int core_slot0, int hd, int es, int* status) {
   pdl_wait();
   pdl_trigger();
-  __shared__ float sh[33];
   const int i = blockIdx.x;
   if (i >= B) return;
   auto exits = [&](int j) { return (m.depth[j] >= 1 && m.pend[j]) || (m.depth[j] + 1 >= r_max); };
@@ -487,14 +489,18 @@ __global__ void k_compact(const float* __restrict__ X, RowMeta m, const int* __r
     }
     return;
   }
-  float before = 0.f;
-  for (int j = threadIdx.x; j < i; j += blockDim.x) before += exits(j) ? 1.f : 0.f;
-  const int n_exit_before = (int)(block_sum(before, sh) + 0.5f);
+  int n_exit_before = 0;
+  for (int j0 = 0; j0 < i; j0 += blockDim.x) {  // i is uniform across the block
+    const int j = j0 + threadIdx.x;
+    n_exit_before += __syncthreads_count(j < i && exits(j));
+  }
   const bool ex = exits(i);
   const int r = m.depth[i] + 1;
   const int dst = ex ? qc_off + n_exit_before : i - n_exit_before;
-  float* out = ex ? Cb : Xc;
-  for (int c = threadIdx.x; c < d; c += blockDim.x) out[(size_t)dst * d + c] = X[(size_t)i * d + c];
+  // Rows are d fp32 values, d a multiple of 4, at 256-byte aligned buffers.
+  const float4* src4 = reinterpret_cast<const float4*>(X + (size_t)i * d);
+  float4* dst4 = reinterpret_cast<float4*>((ex ? Cb : Xc) + (size_t)dst * d);
+  for (int c = threadIdx.x; c < d / 4; c += blockDim.x) dst4[c] = src4[c];
   if (threadIdx.x == 0) {
     RowMeta o = ex ? mb : mc;
     const int slot = m.slot[i], pos = m.pos[i], t = m.t[i];

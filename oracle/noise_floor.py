@@ -11,6 +11,9 @@ derives its tolerances and forcing bands from it.
 Measured (16-core box and 8-core container agree): logits 0.050, hidden
 0.69 (RMS 9.7), gate logit 0.013 max abs; tokens and exit depths equal.
 
+``floor`` computes the same disagreement for any model and request list; the
+bf16 parity tests take their tolerances from it.
+
 Usage: python -m oracle.noise_floor
 """
 
@@ -20,13 +23,13 @@ from synth import make_requests, make_weights, model_shape, workload
 from oracle.model import OracleModel, decode_sequence
 
 
-def main(T=8):
-    wl = workload("ouro")
-    shape = model_shape("ouro")
-    wts = make_weights(shape)
-    r = sorted(make_requests(wl, shape.vocab), key=lambda r: len(r["prompt"]))[0]
-    om = OracleModel(shape, wts)
-    a = decode_sequence(om, r["prompt"], T, keep_logits=T)
+def floor(shape, weights, requests, T):
+    """Largest disagreement of the two oracles over the first T generated
+    tokens of each request: dict with max abs logit, hidden-state and gate
+    differences and the hidden-state RMS.  The float32-reduction run follows
+    the float64 run's exit depths and tokens (requests may carry replayed
+    depths under "replay"), so both see the same sequence."""
+    om = OracleModel(shape, weights)
     w32 = {id(v): v.astype(np.float32) for v in om.w.values()}
 
     class Fp32Reductions(OracleModel):
@@ -35,15 +38,30 @@ def main(T=8):
 
     om2 = Fp32Reductions.__new__(Fp32Reductions)
     om2.__dict__.update(om.__dict__)
-    b = decode_sequence(om2, r["prompt"], T, keep_logits=T)
-    la, lb = np.array(a.logits), np.array(b.logits)
-    ha, hb = np.array(a.hidden), np.array(b.hidden)
-    za = np.concatenate([np.array(z) for z in a.gate_logits if z])
-    zb = np.concatenate([np.array(z) for z in b.gate_logits if z])
-    print("sequence", r["seq_id"], "prompt", len(r["prompt"]), "tokens equal", a.tokens == b.tokens,
-          "exits equal", a.exit_depths == b.exit_depths)
-    print("logits max abs", float(np.abs(la - lb).max()), "hidden max abs", float(np.abs(ha - hb).max()),
-          "hidden rms", float(np.sqrt((ha ** 2).mean())), "gate max abs", float(np.abs(za - zb).max()))
+    out = dict(logits=0.0, hidden=0.0, gate=0.0, hidden_rms=0.0)
+    for r in requests:
+        n = min(T, r["gen_len"])
+        a = decode_sequence(om, r["prompt"], n, keep_logits=n, force_exit=r.get("replay"))
+        b = decode_sequence(om2, r["prompt"], n, keep_logits=n, force_exit=np.array(a.exit_depths, np.int8),
+                            force_token=np.array(a.tokens, np.int32))
+        ha = np.array(a.hidden)
+        out["logits"] = max(out["logits"], float(np.abs(np.array(a.logits) - np.array(b.logits)).max()))
+        out["hidden"] = max(out["hidden"], float(np.abs(ha - np.array(b.hidden)).max()))
+        out["hidden_rms"] = max(out["hidden_rms"], float(np.sqrt((ha ** 2).mean())))
+        za = [z for zs in a.gate_logits for z in zs]
+        zb = [z for zs in b.gate_logits for z in zs]
+        if za:
+            out["gate"] = max(out["gate"], float(np.abs(np.array(za) - np.array(zb)).max()))
+    return out
+
+
+def main(T=8):
+    wl = workload("ouro")
+    shape = model_shape("ouro")
+    wts = make_weights(shape)
+    r = sorted(make_requests(wl, shape.vocab), key=lambda r: len(r["prompt"]))[0]
+    f = floor(shape, wts, [dict(prompt=r["prompt"], gen_len=T)], T)
+    print("sequence", r["seq_id"], "prompt", len(r["prompt"]), f)
 
 
 if __name__ == "__main__":

@@ -55,6 +55,30 @@ def gpu_run(shape, dev_w, reqs, traces, *, mode="refill", W=4, M=8192, K=1, S=0,
     return out, trace
 
 
+def forced_counts(traces, replays=None, gap_band=NEAR):
+    """(forced exits, live gate decisions, forced tokens, tokens) of the forcing
+    tables force_tables builds for these traces; replayed sequences decide no
+    exit live, so their decisions are not counted."""
+    fe = ne = ft = nt = 0
+    for sid, tr in traces.items():
+        if replays is None or replays.get(sid) is None:
+            fe += int(sum(tr.near_gate))
+            ne += len(tr.exit_depths)
+        ft += int(sum(g < gap_band for g in tr.top2_gap))
+        nt += len(tr.tokens)
+    return fe, ne, ft, nt
+
+
+def check_forced(traces, replays=None, gap_band=NEAR, max_frac=0.05, label=""):
+    """Print the forced decisions and bound them: at most max_frac of the live
+    gate decisions and of the tokens (at least one of each is allowed)."""
+    fe, ne, ft, nt = forced_counts(traces, replays, gap_band)
+    print(f"{label} forced exits {fe}/{ne}, forced tokens {ft}/{nt} (gap band {gap_band:g})")
+    assert fe <= max(1, int(max_frac * ne)), (fe, ne)
+    assert ft <= max(1, int(max_frac * nt)), (ft, nt)
+    return fe, ne, ft, nt
+
+
 def compare(out, traces, tol, check_logits=True, check_gate=False):
     """Tokens and exit depths exact; logits / hidden / gate logits within tol."""
     worst = 0.0

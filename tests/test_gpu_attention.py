@@ -252,3 +252,63 @@ def test_prefill_tiles_match_causal_reference(L, H, hd):
     assert torch_finite(o)
     err = (o - ref).abs()
     assert (err <= 1e-2 * (1 + ref.abs())).all().item(), err.max().item()
+
+
+@pytest.mark.parametrize("uniform", [False, True])
+def test_long_context_matches_reference(L, uniform):
+    """8320 keys (an 8192-token prompt plus 128 generated tokens): 65 splits of
+    128 keys per row, merged by the split-KV combine."""
+    cs = (make_uniform_case if uniform else make_case)(1, 4, 128, rows=3, max_ctx=8320, seed=13,
+                                                      **({} if uniform else dict(n_core=1, layer=0)))
+    out = (run_uniform if uniform else run)(L, cs, 128).double().cpu()
+    ref = reference(cs)
+    assert torch_finite(out)
+    err = (out - ref).abs()
+    assert (err <= 1e-2 * (1 + ref.abs())).all().item(), err.max().item()
+
+
+def test_prefill_tiles_long_prompt_match_causal_reference(L):
+    """One 8192-row prompt chunk (128 query tiles of 64 rows) and a chunk that
+    continues another prompt from position 700, against a float64 causal
+    reference over each sequence's whole key range."""
+    import torch
+    L.cdb_test_attention_prefill.argtypes = ([C.c_void_p, C.c_int, C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p] +
+                                             [C.c_int] * 6 + [C.c_void_p, C.c_void_p, C.c_size_t, C.c_void_p])
+    rng = np.random.default_rng(19)
+    H, hd = 2, 128
+    d = H * hd
+    nsl, slot = 2, 1
+    runs = [(0, 0, 8192), (1, 700, 300)]
+    max_blocks = 512
+    kv_blocks = 2 * max_blocks + 3
+    perm = rng.permutation(kv_blocks)[: 2 * max_blocks].reshape(2, max_blocks)
+    bt = torch.from_numpy(perm.astype(np.int32))
+    pool = torch.from_numpy(rng.standard_normal((kv_blocks, nsl, 2, H, 16, hd)).astype(np.float32)).to(torch.bfloat16)
+    row_slot = np.concatenate([np.full(n, sq, np.int32) for sq, p0, n in runs])
+    row_pos = np.concatenate([np.arange(p0, p0 + n, dtype=np.int32) for sq, p0, n in runs])
+    rows = len(row_pos)
+    q = torch.from_numpy(rng.standard_normal((rows, d)).astype(np.float32)).to(torch.bfloat16)
+    ref = torch.zeros(rows, d, dtype=torch.float64)
+    r0 = 0
+    for sq, p0, n in runs:
+        T = p0 + n
+        j = torch.arange(T)
+        blk = bt[sq][j // 16].long()
+        K = pool[blk, slot, 0, :, j % 16].double().transpose(0, 1)  # [H, T, hd]
+        V = pool[blk, slot, 1, :, j % 16].double().transpose(0, 1)
+        Q = q[r0:r0 + n].double().view(n, H, hd).transpose(0, 1)    # rows at positions p0..T-1
+        s = Q @ K.transpose(1, 2) / np.sqrt(hd)                       # [H, n, T]
+        s = s.masked_fill(j[None, None, :] > torch.arange(p0, T)[None, :, None], float("-inf"))
+        ref[r0:r0 + n] = (torch.softmax(s, -1) @ V).transpose(0, 1).reshape(n, d)
+        r0 += n
+    out = torch.zeros(rows, d, dtype=torch.bfloat16, device="cuda")
+    scratch = torch.zeros(256 + 16 * (rows + 1), dtype=torch.uint8, device="cuda")
+    dq, dp, dbt = q.cuda(), pool.cuda(), bt.cuda()
+    rc = L.cdb_test_attention_prefill(dq.data_ptr(), rows, row_slot.ctypes.data, row_pos.ctypes.data, dp.data_ptr(),
+                                      dbt.data_ptr(), max_blocks, kv_blocks, nsl, slot, H, hd, out.data_ptr(),
+                                      scratch.data_ptr(), scratch.numel(), None)
+    assert rc == 0, rc
+    o = out.double().cpu()
+    assert torch_finite(o)
+    err = (o - ref).abs()
+    assert (err <= 1e-2 * (1 + ref.abs())).all().item(), err.max().item()

@@ -2,7 +2,7 @@
 
 The Ouro-shaped model (1.4 G parameters, bf16) decodes the whole 256-request
 workload in refill mode with W = 64, M = 8192, K = 1.  The CPU oracle decodes
-the two shortest-prompt sequences alone for their first 8 generated tokens;
+the eight shortest-prompt sequences alone for their first 16 generated tokens;
 tokens and exit depths must match exactly.  Every sequence must finish with
 256 tokens and exit depths in [r_min, r_max].
 
@@ -12,18 +12,23 @@ already differ by 0.050 in logits, 0.69 in hidden states (RMS 9.7, about 4%)
 and 0.013 in gate logits.  The bounds below are about twice that floor, and
 gate logits within 0.05 of the threshold and top-2 logit gaps below 0.1 are
 forced to the oracle's decision (about 3x and 2x the floor), since a
-narrower band would leave decisions to rounding noise.
+narrower band would leave decisions to rounding noise.  With a noise floor of
+about 5% of the logit spread and 49152 candidates, a large share of argmaxes
+falls inside that band (the oracle's own top-2 gaps: a third to a half below
+0.1), so the forced tokens and exits are counted and printed; tokens outside
+the band and every exit decision outside the gate band are compared exactly.
 """
 
 import numpy as np
 import pytest
 
 from synth import make_requests, make_weights, model_shape, workload
-from tests.gpu_util import force_tables
+from tests.gpu_util import check_forced, force_tables
 
 pytestmark = pytest.mark.gpu
 
-T = 8
+T = 16
+N_SAMPLE = 8
 LOGIT_TOL = 0.1        # absolute
 HIDDEN_TOL = 0.1       # relative to the token's hidden-state RMS
 GATE_TOL = 0.04        # absolute
@@ -41,7 +46,7 @@ def test_ouro_full_workload_matches_oracle_sample():
     shape = model_shape(wl.model)
     wts = make_weights(shape)
     reqs = make_requests(wl, shape.vocab, shape.r_max, shape.r_min)
-    sample = sorted(reqs, key=lambda r: len(r["prompt"]))[:2]
+    sample = sorted(reqs, key=lambda r: len(r["prompt"]))[:N_SAMPLE]
     om = OracleModel(shape, wts)
     ref = {r["seq_id"]: decode_sequence(om, r["prompt"], T, keep_logits=T, near_tol=GATE_BAND) for r in sample}
     del om
@@ -69,6 +74,7 @@ def test_ouro_full_workload_matches_oracle_sample():
         assert o["exit_depths"].min() >= shape.r_min and o["exit_depths"].max() <= shape.r_max
     depths = np.concatenate([o["exit_depths"] for o in out.values()])
     assert 2.5 < depths.mean() < 3.5, depths.mean()
+    check_forced(ref, None, GAP_BAND, max_frac=0.6, label="ouro full size")
 
     for sid, tr in ref.items():
         o = out[sid]
@@ -138,4 +144,5 @@ def test_huginn_widths_match_oracle():
         z_ref = np.concatenate([np.array(z) for z in tr.gate_logits if z])
         z_got = np.concatenate([o["gate_logits"][t, : len(z)] for t, z in enumerate(tr.gate_logits) if z])
         assert np.abs(z_got - z_ref).max() <= GATE_TOL
+    check_forced(ref, None, GAP_BAND, max_frac=0.6, label="huginn widths")
     print("exit depths seen", sorted(set(depths)))

@@ -13,17 +13,25 @@ import numpy as np
 import pytest
 
 from synth import make_requests, make_weights, model_shape, workload
-from tests.gpu_util import compare, gpu_run, oracle_traces
+from tests.gpu_util import check_forced, compare, gpu_run, oracle_traces
 
 pytestmark = pytest.mark.gpu
 
 FP32_TOL = 1e-4
 BF16_TOL = 2e-2
-# A bf16 run may pick either token of a top-2 pair closer than twice the
-# logit tolerance (each logit may be off by BF16_TOL); such argmaxes are
-# pinned to the oracle's choice and the logits are still compared.
-BF16_GAP = 2 * BF16_TOL
+# A bf16 run may pick either token of a top-2 pair closer than the arithmetic
+# noise between two correct implementations: the oracle-only noise floor of
+# these two-layer bf16 models (float64 against float32 reductions,
+# oracle/noise_floor.py) is 0.0034 in logits and 0.0010 in gate logits.  Such
+# argmaxes (top-2 gap below three times the floor) are pinned to the oracle's
+# choice, counted, and their logits still compared.
+BF16_GAP = 1e-2
 GAP = {"fp32": 1e-3, "bf16": BF16_GAP}
+# Largest share of forced decisions (gate decisions, tokens).  The bands cover
+# 0-3% of the tokens of these random-weight models in fp32 and 0-15% in bf16
+# (measured on GB300; the single-slot model repeats tokens with small top-2
+# gaps and is the highest).
+MAX_FORCED = {"fp32": 0.05, "bf16": 0.15}
 
 
 @pytest.fixture(scope="module")
@@ -48,6 +56,7 @@ def test_tiny_refill_matches_oracle(tiny, tiny_ref):
     out, trace = gpu_run(shape, dw, reqs, tiny_ref, mode="refill", W=4, K=1, trace_tokens=16,
                          trace_gate=True, attn_split=16)
     err = compare(out, tiny_ref, FP32_TOL, check_gate=True)
+    check_forced(tiny_ref, None, GAP["fp32"], MAX_FORCED["fp32"], label="tiny")
     depths = np.concatenate([o["exit_depths"] for o in out.values()])
     assert set(depths.tolist()) >= {2, 3, 4, 8}, "exit depths should spread"
     assert any(len(r["hist"]) > 1 for r in trace if r["stage"] == "loop"), "refill mixes depths"
@@ -118,6 +127,7 @@ def test_bf16_model_matches_oracle():
     out, _ = gpu_run(shape, binding.device_weights(shape, wts), reqs, ref, mode="refill", W=3, K=1,
                      trace_tokens=10, trace_gate=True, attn_split=32, gap_band=BF16_GAP)
     err = compare(out, ref, BF16_TOL, check_gate=True)
+    check_forced(ref, None, BF16_GAP, MAX_FORCED["bf16"], label="bf16 mini")
     print("bf16 mini max err", err)
 
 
@@ -135,7 +145,10 @@ def test_huginn_like_model_matches_oracle(dtype, tol):
     ref = oracle_traces(shape, wts, reqs, "adaptive", keep_logits=8)
     out, _ = gpu_run(shape, binding.device_weights(shape, wts), reqs, ref, mode="refill", W=3, K=2,
                      trace_tokens=8, trace_gate=True, attn_split=16, gap_band=GAP[dtype])
-    compare(out, ref, tol, check_gate=True)
+    err = compare(out, ref, tol, check_gate=True)
+    check_forced(ref, {r["seq_id"]: r["replay"] for r in reqs}, GAP[dtype], MAX_FORCED[dtype],
+                 label=f"huginn-like {dtype}")
+    print("huginn-like", dtype, "max err", err)
 
 
 @pytest.mark.parametrize("kv_slots", [1, 2])
@@ -152,7 +165,9 @@ def test_shared_kv_layouts_match_oracle(kv_slots, dtype, tol):
     ref = oracle_traces(shape, wts, reqs, "adaptive", keep_logits=10)
     out, _ = gpu_run(shape, binding.device_weights(shape, wts), reqs, ref, mode="refill", W=3, K=1,
                      trace_tokens=10, trace_gate=True, attn_split=32, gap_band=GAP[dtype])
-    compare(out, ref, tol, check_gate=True)
+    err = compare(out, ref, tol, check_gate=True)
+    check_forced(ref, None, GAP[dtype], MAX_FORCED[dtype], label=f"shared kv s={kv_slots} {dtype}")
+    print("shared kv", kv_slots, dtype, "max err", err)
 
 
 def test_huginn_like_single_slot_cache_matches_oracle():
@@ -165,7 +180,9 @@ def test_huginn_like_single_slot_cache_matches_oracle():
     ref = oracle_traces(shape, wts, reqs, "adaptive", keep_logits=8)
     out, _ = gpu_run(shape, binding.device_weights(shape, wts), reqs, ref, mode="refill", W=3, K=2,
                      trace_tokens=8, trace_gate=True, attn_split=16, gap_band=BF16_GAP)
-    compare(out, ref, BF16_TOL, check_gate=True)
+    err = compare(out, ref, BF16_TOL, check_gate=True)
+    check_forced(ref, None, BF16_GAP, MAX_FORCED["bf16"], label="huginn-like single slot")
+    print("huginn-like single slot max err", err)
 
 
 @pytest.mark.parametrize("variant,dtype,tol,kv_slots", [("looped", "fp32", FP32_TOL, 0),
@@ -201,7 +218,9 @@ def test_convergence_gate_matches_oracle(variant, dtype, tol, kv_slots):
     ref = oracle_traces(shape, wts, reqs, "adaptive", keep_logits=8, near_tol=band)
     out, _ = gpu_run(shape, binding.device_weights(shape, wts), reqs, ref, mode="refill", W=3, K=2,
                      trace_tokens=8, trace_gate=True, attn_split=16, gap_band=GAP[dtype])
-    compare(out, ref, tol, check_gate=True)
+    err = compare(out, ref, tol, check_gate=True)
+    check_forced(ref, None, GAP[dtype], 0.25, label=f"convergence {variant} {dtype}")
+    print("convergence", variant, dtype, "max err", err)
     depths = [e for tr in ref.values() for e in tr.exit_depths]
     assert min(depths) >= 3 and len(set(depths)) >= (2 if dtype == "fp32" else 1), depths
     assert sum(sum(tr.near_gate) for tr in ref.values()) <= len(depths) // 4
