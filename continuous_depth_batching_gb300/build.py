@@ -29,6 +29,7 @@ SOURCES = [
     "engine.cu",
     "kernels.cu",
     "attention.cu",
+    "attention_prefill_tc.cu",
     "gemm_simt.cu",
     "gemm_tc.cu",
     "attention_noalloc.cu",

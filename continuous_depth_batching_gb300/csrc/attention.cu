@@ -1248,11 +1248,25 @@ bool launch_prefill_attention(cudaStream_t s, const __nv_bfloat16* Q, int q_rows
   if (n_tiles <= 0) return true;
   switch (hd) {
     case 32: return prefill_hd<32>(s, Q, q_rows, tiles, n_tiles, kv, slot, H, O, status);
-    case 64: return prefill_hd<64>(s, Q, q_rows, tiles, n_tiles, kv, slot, H, O, status);
+    case 64:
+    case 128: return launch_prefill_attention_tc(s, Q, q_rows, tiles, n_tiles, kv, slot, H, hd, O, status);
     case 96: return prefill_hd<96>(s, Q, q_rows, tiles, n_tiles, kv, slot, H, O, status);
-    case 128: return prefill_hd<128>(s, Q, q_rows, tiles, n_tiles, kv, slot, H, O, status);
     default: return false;
   }
+}
+
+std::vector<int4> prefill_tiles(const int32_t* row_slot, const int32_t* row_pos, int rows, int hd) {
+  const int T = prefill_tile_rows(hd);
+  std::vector<int4> tiles;
+  for (int i = 0; i < rows;) {
+    int j = i + 1;
+    while (j < rows && j - i < T && row_slot[j] == row_slot[i] && row_pos[j] == row_pos[i] + (j - i)) ++j;
+    tiles.push_back(make_int4(i, j - i, row_slot[i], row_pos[i]));
+    i = j;
+  }
+  // Work of a tile grows with its last position (keys 0 .. p0 + rows - 1).
+  std::stable_sort(tiles.begin(), tiles.end(), [](const int4& a, const int4& b) { return a.w + a.y > b.w + b.y; });
+  return tiles;
 }
 
 template <typename T>

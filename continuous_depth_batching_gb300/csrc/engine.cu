@@ -473,14 +473,8 @@ class GpuExecutor : public Executor {
     if ((rc = upload(x, rpos, b.data(), n * 4)) < 0) return rc;
     if ((rc = upload(x, rtok, c.data(), n * 4)) < 0) return rc;
     // Query tiles for the prefill attention: runs of consecutive positions of
-    // one sequence, at most kPrefillTileRows rows each.
-    std::vector<int4> tiles;
-    for (int i = 0; i < n;) {
-      int j = i + 1;
-      while (j < n && j - i < kPrefillTileRows && a[j] == a[i] && b[j] == b[i] + (j - i)) ++j;
-      tiles.push_back(make_int4(i, j - i, a[i], b[i]));
-      i = j;
-    }
+    // one sequence, at most prefill_tile_rows(head_dim) rows each.
+    const std::vector<int4> tiles = prefill_tiles(a.data(), b.data(), n, x->m.head_dim);
     if ((rc = upload(x, at<int4>(x, L.ptiles), tiles.data(), tiles.size() * sizeof(int4))) < 0) return rc;
     pf_tiles_ = (int)tiles.size();
     float* Xp = at<float>(x, L.Xp);
@@ -1109,15 +1103,9 @@ int cdb_test_attention_prefill(const void* q, int rows, const int32_t* row_slot,
   if (!q || rows < 1 || !row_slot || !row_pos || !kv_pool || !block_table || max_blocks < 1 || kv_blocks < 1 ||
       n_kv_slots < 1 || slot < 0 || slot >= n_kv_slots || n_heads < 1 || !out || !scratch)
     return CDB_ERR_ARG;
-  std::vector<int4> tiles;
-  for (int i = 0; i < rows;) {
+  for (int i = 0; i < rows; ++i)
     if (row_slot[i] < 0 || row_pos[i] < 0 || row_pos[i] >= max_blocks * 16) return CDB_ERR_ARG;
-    int j = i + 1;
-    while (j < rows && j - i < kPrefillTileRows && row_slot[j] == row_slot[i] && row_pos[j] == row_pos[i] + (j - i))
-      ++j;
-    tiles.push_back(make_int4(i, j - i, row_slot[i], row_pos[i]));
-    i = j;
-  }
+  const std::vector<int4> tiles = prefill_tiles(row_slot, row_pos, rows, head_dim);
   if (scratch_bytes < 256 + tiles.size() * sizeof(int4)) return CDB_ERR_ARG;
   cudaStream_t s = (cudaStream_t)stream;
   int* status = (int*)scratch;

@@ -20,6 +20,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <vector>
+
 namespace cdb {
 
 // Kernel launches issued by the launchers below (process-wide).
@@ -130,13 +132,23 @@ void launch_attention(cudaStream_t s, const T* Q, int rows, const int* mslot, co
                       float* part_o, float* part_ml, int* status, bool uniform);
 
 // Causal prefill attention over query tiles (bf16, head_dim 32/64/96/128):
-// tiles[t] = (first row, rows <= 64, sequence slot, position of the first
-// row); rows of a tile are consecutive positions of one sequence, and every
-// key is read from KV slot `slot`.  Q and O are [q_rows][d].  Returns false
-// (nothing launched) for shapes it does not cover.
+// tiles[t] = (first row, rows <= prefill_tile_rows(hd), sequence slot,
+// position of the first row); rows of a tile are consecutive positions of one
+// sequence, and every key is read from KV slot `slot`.  Q and O are
+// [q_rows][d].  head_dim 64 and 128 run on the tensor cores (tcgen05, 128-row
+// tiles, attention_prefill_tc.cu); 32 and 96 on warp-level MMAs (64-row
+// tiles).  Returns false (nothing launched) for shapes it does not cover.
 constexpr int kPrefillTileRows = 64;
+constexpr int kPrefillTileRowsTc = 128;
+inline int prefill_tile_rows(int hd) { return hd == 64 || hd == 128 ? kPrefillTileRowsTc : kPrefillTileRows; }
 bool launch_prefill_attention(cudaStream_t s, const __nv_bfloat16* Q, int q_rows, const int4* tiles, int n_tiles,
                               KvGeom kv, int slot, int H, int hd, __nv_bfloat16* O, int* status);
+bool launch_prefill_attention_tc(cudaStream_t s, const __nv_bfloat16* Q, int q_rows, const int4* tiles, int n_tiles,
+                                 KvGeom kv, int slot, int H, int hd, __nv_bfloat16* O, int* status);
+// Query tiles of a prefill chunk (rows given by sequence slot and position,
+// runs of consecutive positions of one sequence), longest key range first so
+// the heaviest tiles start first.
+std::vector<int4> prefill_tiles(const int32_t* row_slot, const int32_t* row_pos, int rows, int hd);
 
 // ---- GEMM (gemm_simt.cu) ----
 enum GemmEpi { kEpiStore = 0, kEpiResid = 1, kEpiSwiglu = 2 };

@@ -12,7 +12,9 @@ min(r_max, 1 + min{d in [r_min-1, r_max-2] : z_d + b > logit(q)}).
 
 * tiny: the bias that spreads exit depths most evenly over 2..r_max
   (largest entropy of the depth histogram on a grid of step 0.005).
-* ouro: the bias whose mean exit depth is closest to 3.
+* ouro: the bias whose live-gate mean exit depth over a sample of the job
+  (8 sequences spread over its prompt lengths, 64 generated tokens each) is
+  closest to 3.
 * huginn: exit depths are replayed (App. C.2), the bias stays 0.
 
 Usage: python -m oracle.calibrate_gate [tiny|ouro ...]
@@ -69,12 +71,58 @@ def calibrate(name: str) -> float:
                 best, best_h = float(b), h
         return round(best, 3)
     if name == "ouro":
-        Z = pilot_logits(name, 2, 24)
-        bs = np.arange(-3.0, 3.0, 0.005)
-        means = [exit_depths(Z, b, shape.r_min, shape.r_max,
-                             shape.gate_threshold_logit).mean() for b in bs]
-        return round(float(bs[int(np.argmin(np.abs(np.array(means) - 3.0)))]), 3)
+        return calibrate_mean(name, 3.0)
     raise KeyError(name)
+
+
+def job_sample(name: str, n_seqs: int):
+    """n_seqs requests spread evenly over the workload's sequence ids (prompt
+    lengths are independent draws, so this spans the prompt-length range)."""
+    wl = workload(name)
+    reqs = make_requests(wl, model_shape(name).vocab)
+    step = max(1, wl.n_seqs // n_seqs)
+    return [reqs[i] for i in range(0, wl.n_seqs, step)][:n_seqs]
+
+
+def adaptive_mean(shape, weights, reqs, gen: int, b: float) -> float:
+    """Mean exit depth of the live gate with bias b (each request decoded alone)."""
+    om = OracleModel(_replace(shape, gate_bias=b), weights)
+    e = []
+    for r in reqs:
+        e += decode_sequence(om, r["prompt"], gen).exit_depths
+    return float(np.mean(e))
+
+
+def calibrate_mean(name: str, target: float, n_seqs: int = 8, gen: int = 64) -> float:
+    """Bias whose mean exit depth over a sample of the job is closest to target.
+
+    A fixed-depth pilot gives every token's logits z_1..z_{r_max-1}, hence the
+    mean exit depth m(b) of any bias under the lookahead rule.  Exits change
+    later tokens' states through the depth clamp, so the live-gate mean at the
+    pilot's bias b0 is measured with adaptive runs and the bias is moved along
+    the pilot's m(b) curve by the difference (one correction step, then the
+    better of the two)."""
+    shape = _replace(model_shape(name), gate_bias=0.0)
+    weights = make_weights(shape)
+    reqs = job_sample(name, n_seqs)
+    om = OracleModel(shape, weights)
+    Z = []
+    for r in reqs:
+        Z += decode_sequence(om, r["prompt"], gen, mode="fixed").gate_logits
+    Z = np.array(Z)
+    del om
+    bs = np.arange(-3.0, 3.0, 0.005)
+    curve = np.array([exit_depths(Z, b, shape.r_min, shape.r_max, shape.gate_threshold_logit).mean() for b in bs])
+
+    def bias_for(m):
+        return float(bs[int(np.argmin(np.abs(curve - m)))])
+
+    b0 = bias_for(target)
+    m0 = adaptive_mean(shape, weights, reqs, gen, b0)
+    b1 = bias_for(target + (target - m0))
+    m1 = adaptive_mean(shape, weights, reqs, gen, b1)
+    print(f"{name}: pilot bias {b0:.3f} -> live mean {m0:.3f}; corrected bias {b1:.3f} -> live mean {m1:.3f}")
+    return round(b0 if abs(m0 - target) <= abs(m1 - target) else b1, 3)
 
 
 def main(names):
