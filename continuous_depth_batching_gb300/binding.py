@@ -113,6 +113,7 @@ def lib(path: str | None = None) -> C.CDLL:
     L.cdb_last_error.restype = C.c_char_p
     L.cdb_trace_enable.argtypes = [C.c_void_p, C.c_int]
     L.cdb_profile_enable.argtypes = [C.c_void_p, C.c_int]
+    L.cdb_profile_repeat.argtypes = [C.c_void_p, C.c_int]
     L.cdb_profile_read.argtypes = [C.c_void_p, C.POINTER(KernelStat), C.c_int, C.POINTER(C.c_int)]
     L.cdb_kernel_launches.restype = C.c_int64
     L.cdb_kernel_launches.argtypes = []
@@ -304,8 +305,13 @@ class Engine:
             out.append(r)
         return out
 
-    def profile_enable(self, on=True):
-        self._check(self.L.cdb_profile_enable(self.ctx, int(on)))
+    def profile_enable(self, on=True, core_only=False):
+        self._check(self.L.cdb_profile_enable(self.ctx, (2 if core_only else 1) if on else 0))
+
+    def profile_repeat(self, cls=None):
+        """Relaunch one kernel class inside every core step (None stops)."""
+        code = -1 if cls is None else {"attention": 0, "gemm": 1, "rowwise": 3}[cls]
+        self._check(self.L.cdb_profile_repeat(self.ctx, code))
 
     def profile_read(self):
         st = (KernelStat * 8)()

@@ -161,8 +161,11 @@ struct cdb_ctx {
   std::string err;
   bool dead = false;
   int64_t io_h2d = 0, io_d2h = 0;
-  // kernel timing (cdb_profile_enable)
+  // kernel timing (cdb_profile_enable, cdb_profile_repeat)
   bool prof_on = false;
+  bool prof_core_only = false;  // time launches of core steps only
+  int prof_repeat = -1;         // class relaunched inside core steps (step-delta cost), -1 none
+  bool in_core = false;         // a core step is being enqueued
   struct ProfEv {
     int cls;
     cudaEvent_t a, b;
@@ -254,7 +257,7 @@ static cudaEvent_t pool_event(cdb_ctx* x) {
 
 // Bracket one launch with events when timing is on; returns a handle or -1.
 static int prof_begin(cdb_ctx* x, int cls) {
-  if (!x->prof_on) return -1;
+  if (!x->prof_on || (x->prof_core_only && !x->in_core)) return -1;
   cdb_ctx::ProfEv ev{cls, pool_event(x), pool_event(x), 0, 0};
   cudaEventRecord(ev.a, x->cs);
   x->prof_live.push_back(ev);
@@ -330,6 +333,12 @@ class GpuExecutor : public Executor {
     if (ns < 0) {
       launch_gemm<T>(x->cs, epi, A, lda, (const T*)W, (const T*)W2, N, K, rows, Cf, Ct, ldc);
       ns = 0;
+    } else if (repeat(1) && !(ns == 0 && epi == kEpiResid)) {
+      // Step-delta timing: the same launch again writes the same partials
+      // (or the same stored output); an in-place residual is not repeated.
+      launch_gemm_tc(x->cs, epi, (const __nv_bfloat16*)A, lda, x->L.R, (const __nv_bfloat16*)W,
+                     (const __nv_bfloat16*)W2, N, K, rows, Cf, (__nv_bfloat16*)Ct, ldc, decode_tiles_,
+                     parts ? at<float>(x, x->L.gpart) : nullptr, x->L.gpart_floats, at<int>(x, x->L.status));
     }
     const double out_b = epi == kEpiSwiglu ? es : (epi == kEpiResid ? 8.0 : 4.0);
     prof_end(x, h, nw * N * (double)K * es + (double)rows * K * es + (double)rows * N * out_b,
@@ -387,8 +396,9 @@ class GpuExecutor : public Executor {
     norm<T>(X, lw.attn_norm, A, rows);
     int ns = gemm<T>(kEpiStore, A, d, lw.wqkv, nullptr, 3 * d, d, rows, QKV, nullptr, 3 * d, true);
     int hr = prof_begin(x, 3);
-    launch_rope_kv<T>(s, ns ? GP : QKV, ns, rows, mslot, mpos, mdepth, depth_uniform, slot_base, clamp, Q, kv, H, hd,
-                      at<float2>(x, L.rope), st);
+    for (int rr = repeat(3) ? 2 : 1; rr > 0; --rr)
+      launch_rope_kv<T>(s, ns ? GP : QKV, ns, rows, mslot, mpos, mdepth, depth_uniform, slot_base, clamp, Q, kv, H,
+                        hd, at<float2>(x, L.rope), st);
     prof_end(x, hr, (double)rows * d * (12.0 + 3.0 * es), 0.0);  // q, k, v in; q, K, V rows out
     const int split = decode ? L.split : (1 << 30);
     const int msp = decode ? L.max_splits : 1;
@@ -401,17 +411,20 @@ class GpuExecutor : public Executor {
                                       slot_base + (clamp ? std::min(depth_uniform, clamp) - 1 : 0), H, hd,
                                       (__nv_bfloat16*)O, st);
     if (!done)
-      launch_attention<T>(s, Q, rows, mslot, mpos, mdepth, depth_uniform, kv, slot_base, clamp, H, hd, split, msp,
-                          O, at<float>(x, L.part_o), at<float>(x, L.part_ml), st, true);
-    // Each key row (K and V, d elements each) is read once; q in, o out.
-    prof_end(x, ha, sumL * 2.0 * d * es + 2.0 * rows * d * es, 4.0 * d * sumL);
+      for (int rr = repeat(0) ? 2 : 1; rr > 0; --rr)
+        launch_attention<T>(s, Q, rows, mslot, mpos, mdepth, depth_uniform, kv, slot_base, clamp, H, hd, split, msp,
+                            O, at<float>(x, L.part_o), at<float>(x, L.part_ml), st, true);
+    // Decode: each row reads each of its key rows (K and V, d elements each)
+    // once.  Prefill tiles: each tile reads the keys up to its last position
+    // once for all of its rows.  Plus q in, o out.
+    prof_end(x, ha, (done ? pf_key_rows_ : sumL) * 2.0 * d * es + 2.0 * rows * d * es, 4.0 * d * sumL);
     ns = gemm<T>(kEpiResid, O, d, lw.wo, nullptr, d, d, rows, X, nullptr, d, true);
     if (ns) pend_ = Pending{X, rows, ns, 1};
     norm<T>(X, lw.mlp_norm, A, rows);
     ns = gemm<T>(kEpiSwiglu, A, d, lw.wg, lw.wu, f, d, rows, nullptr, Mid, f, true);
     if (ns) {
       hr = prof_begin(x, 3);
-      launch_swiglu_combine<T>(s, GP, ns, rows, f, Mid);
+      for (int rr = repeat(3) ? 2 : 1; rr > 0; --rr) launch_swiglu_combine<T>(s, GP, ns, rows, f, Mid);
       prof_end(x, hr, (double)rows * f * (8.0 + es), 0.0);
     }
     ns = gemm<T>(kEpiResid, Mid, f, lw.wd, nullptr, d, f, rows, X, nullptr, d, true);
@@ -477,6 +490,8 @@ class GpuExecutor : public Executor {
     const std::vector<int4> tiles = prefill_tiles(a.data(), b.data(), n, x->m.head_dim);
     if ((rc = upload(x, at<int4>(x, L.ptiles), tiles.data(), tiles.size() * sizeof(int4))) < 0) return rc;
     pf_tiles_ = (int)tiles.size();
+    pf_key_rows_ = 0;
+    for (const int4& t : tiles) pf_key_rows_ += (double)t.w + t.y;
     float* Xp = at<float>(x, L.Xp);
     launch_embed_prefill<T>(x->cs, (const T*)x->embed, d, x->m.vocab, rslot, rpos, rtok, n, Xp, geom(), x->m.r_max,
                             at<int>(x, L.status));
@@ -508,6 +523,7 @@ class GpuExecutor : public Executor {
       head<T>(Cp, nd, cm);
     }
     pf_tiles_ = 0;
+    pf_key_rows_ = 0;
     CK(cudaGetLastError());
     return CDB_OK;
   }
@@ -556,6 +572,11 @@ class GpuExecutor : public Executor {
     float* X = at<float>(x, L.rows[0]);
     RowMeta mx = meta_at(x, L.meta[0]);
     const bool conv = x->m.gate_kind == CDB_GATE_CONVERGENCE;
+    x->in_core = true;
+    struct CoreScope {
+      cdb_ctx* c;
+      ~CoreScope() { c->in_core = false; }
+    } scope{x};
     float* sprev = conv ? at<float>(x, L.sprev) : nullptr;  // s_{d-1}, kept for the convergence exit
     launch_gather_core(x->cs, at<float>(x, L.rows[1]), meta_at(x, L.meta[1]), p.B_cont, at<float>(x, L.rows[2]),
                        meta_at(x, L.meta[2]), p.n_ref, X, mx, d, sprev);
@@ -711,6 +732,9 @@ class GpuExecutor : public Executor {
   cdb_ctx* x_;
   bool decode_tiles_ = true;  // GEMM tiling for the rows being processed
   int pf_tiles_ = 0;          // query tiles of the prefill chunk being processed
+  double pf_key_rows_ = 0;    // key rows those tiles read (each tile: its last position + 1)
+  // Relaunch the kernels of class cls in this core step (cdb_profile_repeat).
+  bool repeat(int cls) const { return x_->in_core && x_->prof_repeat == cls; }
 };
 
 static int check_status(cdb_ctx* x) {
@@ -965,8 +989,15 @@ int cdb_io_bytes(const cdb_ctx* x, int64_t* h2d, int64_t* d2h) {
 }
 
 int cdb_profile_enable(cdb_ctx* x, int on) {
-  if (!x) return CDB_ERR_ARG;
+  if (!x || on < 0 || on > 2) return CDB_ERR_ARG;
   x->prof_on = on != 0;
+  x->prof_core_only = on == 2;
+  return CDB_OK;
+}
+
+int cdb_profile_repeat(cdb_ctx* x, int cls) {
+  if (!x || !(cls == -1 || cls == 0 || cls == 1 || cls == 3)) return CDB_ERR_ARG;
+  x->prof_repeat = cls;
   return CDB_OK;
 }
 

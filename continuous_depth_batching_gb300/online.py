@@ -165,6 +165,8 @@ def main():
     ap.add_argument("--pilot", type=float, default=6.0)
     ap.add_argument("--kv-gb", type=float, default=150.0)
     ap.add_argument("--seed", type=int, default=4)
+    ap.add_argument("--kv-slots", type=int, default=0,
+                    help="KV slots per core layer (App. E.1): 0 depth-indexed, 1 single slot, 2 first-then-shared")
     ap.add_argument("--predict-fit", default="",
                     help="no GPU: predict with this latency fit (schedule_select --save-fit; 'roofline' for the "
                          "roofline model) at --rates")
@@ -192,7 +194,8 @@ def main():
     from synth import make_weights, model_shape
 
     build()
-    shape = model_shape(args.model)
+    import dataclasses
+    shape = dataclasses.replace(model_shape(args.model), kv_slots=args.kv_slots)
     dw = binding.device_weights(shape, make_weights(shape))
     max_ctx, gen_cap = 2048 + 512, 512
     kv_tok = binding.kv_bytes_per_token(shape)
@@ -220,7 +223,8 @@ def main():
         arr = poisson_arrivals(rate, window, args.seed + 100 * target + 7)
         for mode in args.modes.split(","):
             res = run_point(make_engine, pool, arr, window, mode)
-            res.update(target_batch=target, rate_per_s=rate, window_s=window, W=W, K=K, model=shape.name)
+            res.update(target_batch=target, rate_per_s=rate, window_s=window, W=W, K=K, model=shape.name,
+                       kv_slots=shape.kv_slots)
             print(json.dumps(res), flush=True)
 
 

@@ -29,6 +29,10 @@ def main():
     ap.add_argument("--warmup", type=int, default=2)
     ap.add_argument("--workload", default="ouro")
     ap.add_argument("--split", type=int, default=0, help="keys per split-KV partial (0: library default)")
+    ap.add_argument("--W", type=int, default=0, help="core slots (0: the workload's)")
+    ap.add_argument("--prompt-len", type=int, default=0, help="every prompt this long (0: the workload's lengths)")
+    ap.add_argument("--gen", type=int, default=0, help="tokens generated per request (0: the workload's)")
+    ap.add_argument("--kv-slots", type=int, default=0)
     args = ap.parse_args()
 
     from continuous_depth_batching_gb300 import binding
@@ -37,7 +41,15 @@ def main():
 
     build()
     wl = workload(args.workload)
-    shape = dataclasses.replace(model_shape(wl.model), n_core=args.layers)
+    over = {}
+    if args.W:
+        over.update(W=args.W, n_seqs=max(wl.n_seqs, args.W))
+    if args.prompt_len:
+        over.update(prompt_lo=args.prompt_len, prompt_hi=args.prompt_len)
+    if args.gen:
+        over.update(gen_lo=args.gen, gen_hi=args.gen)
+    wl = wl.with_(**over)
+    shape = dataclasses.replace(model_shape(wl.model), n_core=args.layers, kv_slots=args.kv_slots)
     dw = binding.device_weights(shape, make_weights(shape))
     reqs = make_requests(wl, shape.vocab, shape.r_max, shape.r_min)
     max_ctx = (wl.prompt_hi + wl.gen_hi - 1 + 15) // 16 * 16

@@ -100,6 +100,8 @@ def main():
     ap.add_argument("--contexts", default="128,512,2048,8192")
     ap.add_argument("--kv-gb", type=float, default=220.0, help="KV budget per cell")
     ap.add_argument("--tokens", type=int, default=16)
+    ap.add_argument("--kv-slots", type=int, default=0,
+                    help="KV slots per core layer (App. E.1): 0 depth-indexed, 1 single slot, 2 first-then-shared")
     args = ap.parse_args()
 
     from continuous_depth_batching_gb300 import binding
@@ -107,7 +109,8 @@ def main():
     from synth import make_weights, model_shape
 
     build()
-    shape = model_shape(args.model)
+    import dataclasses
+    shape = dataclasses.replace(model_shape(args.model), kv_slots=args.kv_slots)
     dw = binding.device_weights(shape, make_weights(shape))
     kv_tok = binding.kv_bytes_per_token(shape)
     peaks = json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json"))) if os.path.exists(

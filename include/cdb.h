@@ -240,8 +240,20 @@ typedef struct {
   int64_t launches;
   double ms, bytes, flops;
 } cdb_kernel_stat;
+/* on: 0 off, 1 launches of every stage, 2 launches of core steps only. */
 int cdb_profile_enable(cdb_ctx *ctx, int on);
 int cdb_profile_read(cdb_ctx *ctx, cdb_kernel_stat *out, int cap, int *n_out);
+
+/* Step-delta timing of a kernel class inside the recurrent-core step: while
+ * set, every core step launches the class's kernels twice (class 0 decode
+ * attention with its combine, 1 projection GEMMs, 3 RoPE + KV write and the
+ * SwiGLU combine; -1 stops).  The repeated launches write the same values
+ * again (an in-place residual GEMM epilogue is never repeated), so results are
+ * unchanged; the difference between the time of such a step and of a plain
+ * one is the class's live cost with programmatic dependent launch in effect.
+ * For measurement only: the extra launches cost time.  CDB_ERR_ARG for other
+ * classes. */
+int cdb_profile_repeat(cdb_ctx *ctx, int cls);
 
 /* Kernel launches issued by the library in this process, all contexts. */
 int64_t cdb_kernel_launches(void);

@@ -33,7 +33,7 @@ def force_tables(tr, replay=None, gap_band=NEAR):
 
 
 def gpu_run(shape, dev_w, reqs, traces, *, mode="refill", W=4, M=8192, K=1, S=0, max_ctx=None,
-            trace_tokens=0, trace_gate=False, attn_split=0, force=True, gap_band=NEAR):
+            trace_tokens=0, trace_gate=False, attn_split=0, force=True, gap_band=NEAR, repeat=None):
     from continuous_depth_batching_gb300 import binding
     if max_ctx is None:
         max_ctx = max(len(r["prompt"]) + r["gen_len"] for r in reqs)
@@ -41,6 +41,8 @@ def gpu_run(shape, dev_w, reqs, traces, *, mode="refill", W=4, M=8192, K=1, S=0,
     eng = binding.Engine(shape, dev_w, mode=mode, W=W, M=M, K=K, S=S, max_ctx=max_ctx, max_new_cap=cap,
                          trace_tokens=trace_tokens, trace_gate=trace_gate, attn_split=attn_split)
     eng.trace_enable(True)
+    if repeat is not None:
+        eng.profile_repeat(repeat)
     for r in reqs:
         fe = ft = None
         if force and traces is not None:

@@ -166,3 +166,21 @@ def test_bf16_modes_agree_bit_exactly():
         for sid in runs[0]:
             for key in ("tokens", "exit_depths", "logits", "hidden", "gate_logits"):
                 np.testing.assert_array_equal(runs[0][sid][key], other[sid][key], err_msg=f"{sid} {key}")
+
+
+def test_step_delta_repeats_leave_results_unchanged():
+    """cdb_profile_repeat relaunches a kernel class inside every core step for
+    step-delta timing; the repeated kernels write the same values, so tokens,
+    exit depths, logits, coda inputs and gate logits are bit-identical."""
+    from continuous_depth_batching_gb300 import binding
+    shape = _shape(r_max=5)
+    wts = make_weights(shape)
+    reqs = _reqs(shape, 6, 20, 70, 6, 6, seed=47)
+    ref = oracle_traces(shape, wts, reqs, "adaptive", keep_logits=6)
+    dw = binding.device_weights(shape, wts)
+    runs = [gpu_run(shape, dw, reqs, ref, mode="refill", W=3, trace_tokens=6, trace_gate=True, gap_band=BF16_GAP,
+                    repeat=cls)[0] for cls in (None, "attention", "gemm", "rowwise")]
+    for other in runs[1:]:
+        for sid in runs[0]:
+            for key in ("tokens", "exit_depths", "logits", "hidden", "gate_logits"):
+                np.testing.assert_array_equal(runs[0][sid][key], other[sid][key], err_msg=f"{sid} {key}")
