@@ -50,12 +50,13 @@ struct Geo {
   static constexpr int PBUF = 2 * PPART;
   static constexpr int OFF_KV = QBYTES;
   static constexpr int OFF_P = OFF_KV + kStages * STAGE;
-  static constexpr int OFF_BAR = OFF_P + 2 * PBUF;
-  static constexpr int NBAR = 2 + 2 * kStages + 10;  // q, done, kv full/empty, s full/free, p full, o full/free
+  static constexpr int OFF_XCH = OFF_P + 2 * PBUF;   // fp32 [6][kRows]: row maxima, then row sums
+  static constexpr int OFF_BAR = OFF_XCH + 6 * kRows * 4;
+  static constexpr int NBAR = 2 + 2 * kStages + 8 + 12;  // q, done, kv full/empty, s full/free, p full, o done, pairs
   static constexpr size_t SMEM = 1024 + OFF_BAR + NBAR * 8 + 16;
   static constexpr int S_COL = 0;                // two score buffers of kKeys columns
-  static constexpr int O_COL = 2 * kKeys;        // two output buffers of HD columns
-  static constexpr int TMEM_COLS = O_COL + 2 * HD <= 256 ? 256 : 512;
+  static constexpr int O_COL = 2 * kKeys;        // the output accumulator, HD columns
+  static constexpr int TMEM_COLS = O_COL + HD <= 256 ? 256 : 512;
 };
 
 __device__ __forceinline__ uint32_t su32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
@@ -146,6 +147,22 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float* v) {
 #pragma unroll
   for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
 }
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const float* v) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
+      "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+      "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])), "r"(__float_as_uint(v[3])),
+      "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])), "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7])),
+      "r"(__float_as_uint(v[8])), "r"(__float_as_uint(v[9])), "r"(__float_as_uint(v[10])), "r"(__float_as_uint(v[11])),
+      "r"(__float_as_uint(v[12])), "r"(__float_as_uint(v[13])), "r"(__float_as_uint(v[14])),
+      "r"(__float_as_uint(v[15])), "r"(__float_as_uint(v[16])), "r"(__float_as_uint(v[17])),
+      "r"(__float_as_uint(v[18])), "r"(__float_as_uint(v[19])), "r"(__float_as_uint(v[20])),
+      "r"(__float_as_uint(v[21])), "r"(__float_as_uint(v[22])), "r"(__float_as_uint(v[23])),
+      "r"(__float_as_uint(v[24])), "r"(__float_as_uint(v[25])), "r"(__float_as_uint(v[26])),
+      "r"(__float_as_uint(v[27])), "r"(__float_as_uint(v[28])), "r"(__float_as_uint(v[29])),
+      "r"(__float_as_uint(v[30])), "r"(__float_as_uint(v[31]))
+      : "memory");
+}
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<const uint32_t*>(&v);
@@ -157,17 +174,19 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t
 }  // namespace pftc
 
 template <int HD>
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(320, 1)
     k_attn_prefill_tc(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
                       const int4* __restrict__ tiles, KvGeom kv, int slot, int H, __nv_bfloat16* __restrict__ O,
                       int* status) {
   using namespace pftc;
   using G = Geo<HD>;
+  constexpr int HH = HD / 2;  // output columns of one softmax warp
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* qs = smem;
   uint8_t* kvs = smem + G::OFF_KV;
   uint8_t* ps = smem + G::OFF_P;
+  float* xch = reinterpret_cast<float*>(smem + G::OFF_XCH);  // [2 parities][2 halves][128 rows] maxima, then sums
   uint64_t* qbar = reinterpret_cast<uint64_t*>(smem + G::OFF_BAR);
   uint64_t* done = qbar + 1;
   uint64_t* kv_full = done + 1;
@@ -175,9 +194,9 @@ __global__ void __launch_bounds__(192, 1)
   uint64_t* s_full = kv_empty + kStages;
   uint64_t* s_free = s_full + 2;
   uint64_t* p_full = s_free + 2;
-  uint64_t* o_full = p_full + 2;
-  uint64_t* o_free = o_full + 2;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(o_free + 2);
+  uint64_t* o_done = p_full + 2;
+  uint64_t* pair = o_done + 2;  // [quadrant][parity] exchange barriers, then one per quadrant for the sums
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(pair + 12);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int h = blockIdx.y;
@@ -192,15 +211,15 @@ __global__ void __launch_bounds__(192, 1)
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&s_full[b], 1);
-      mbar_init(&s_free[b], 4);
-      mbar_init(&p_full[b], 4);
-      mbar_init(&o_full[b], 1);
-      mbar_init(&o_free[b], 4);
+      mbar_init(&s_free[b], 8);
+      mbar_init(&p_full[b], 8);
+      mbar_init(&o_done[b], 1);
     }
+    for (int i = 0; i < 12; ++i) mbar_init(&pair[i], 64);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
   }
-  if (warp == 5) {
+  if (warp == 9) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(su32(tmem_slot)),
                  "r"(G::TMEM_COLS));
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
@@ -217,7 +236,7 @@ __global__ void __launch_bounds__(192, 1)
   const int nb = kmax / kKeys + 1;
   const int npg = kmax / 16 + 1;
 
-  if (warp == 4) {
+  if (warp == 8) {
     // ---------------- TMA producer ----------------
     if (lane == 0) {
       uint64_t pol;  // keys and values are read again by the sequence's later tiles
@@ -272,7 +291,7 @@ __global__ void __launch_bounds__(192, 1)
       for (int j = issued - kStages < 0 ? 0 : issued - kStages; j < issued; ++j)
         mbar_wait(&kv_full[j % kStages], (j / kStages) & 1);
     }
-  } else if (warp == 5) {
+  } else if (warp == 9) {
     // ---------------- MMA issuer ----------------
     if (lane == 0) {
       constexpr uint32_t idS = idesc(kRows, kKeys, false), idO = idesc(kRows, HD, true);
@@ -296,19 +315,19 @@ __global__ void __launch_bounds__(192, 1)
         if (j + 1 < nb && !(ok = issue_qk(j + 1))) break;
         const int s = j % kStages, b = j & 1;
         if (!(ok = mbar_wait(&p_full[b], (j >> 1) & 1))) break;
-        if (j >= 2 && !(ok = mbar_wait(&o_free[b], ((j - 2) >> 1) & 1))) break;
         fence_after();
         const uint32_t pb = su32(ps + b * G::PBUF);
         const uint32_t vb = su32(kvs + (size_t)s * G::STAGE + G::KVB);
-        const uint32_t od = tmem + G::O_COL + b * HD;
-        // O_j = P_hi V_j + P_lo V_j over the block's four 16-key steps.
+        // O += P_hi V_j + P_lo V_j over the block's four 16-key steps; block 0
+        // starts the accumulator.
 #pragma unroll
         for (int kk = 0; kk < kKeys / 16; ++kk)
-          mma(od, desc_k(pb + kk * 32), desc_mn(vb + kk * 2048, G::KSLICE), idO, kk > 0 ? 1u : 0u);
+          mma(tmem + G::O_COL, desc_k(pb + kk * 32), desc_mn(vb + kk * 2048, G::KSLICE), idO,
+              (j > 0 || kk > 0) ? 1u : 0u);
 #pragma unroll
         for (int kk = 0; kk < kKeys / 16; ++kk)
-          mma(od, desc_k(pb + G::PPART + kk * 32), desc_mn(vb + kk * 2048, G::KSLICE), idO, 1u);
-        commit(&o_full[b]);
+          mma(tmem + G::O_COL, desc_k(pb + G::PPART + kk * 32), desc_mn(vb + kk * 2048, G::KSLICE), idO, 1u);
+        commit(&o_done[b]);
         commit(&kv_empty[s]);
       }
       if (!ok) atomicOr(status, kStatusTimeout);
@@ -317,116 +336,138 @@ __global__ void __launch_bounds__(192, 1)
       mbar_wait(done, 0);
     }
   } else {
-    // ---------------- softmax warps: query row r = TMEM lane r ----------------
-    const int r = warp * 32 + lane;
+    // ---------------- softmax warps ----------------
+    // Warps w and w + 4 share query rows 32 (w % 4) .. + 31 (TMEM lanes of
+    // that quadrant): warp half hf = w / 4 takes keys 32 hf .. + 31 of each
+    // block and output columns hf * HD / 2 .. + HD / 2.  The pair exchanges
+    // its row maxima through shared memory behind a bounded mbarrier.
+    const int q4 = warp & 3, hf = warp >> 2;
+    const int r = q4 * 32 + lane;
     const int lim = min(p0 + r, kmax);  // last key of row r (rows past the tile end stop at kmax)
     const float scale = 1.4426950408889634f / sqrtf((float)HD);
-    const uint32_t trow = tmem + ((uint32_t)(warp * 32) << 16);
+    constexpr float kTau = 8.f;  // rescale O only when the row maximum grows by more than 2^8
+    const uint32_t trow = tmem + ((uint32_t)(q4 * 32) << 16);
     const uint32_t pbase = su32(ps) + (uint32_t)(r >> 3) * 1024 + (uint32_t)(r & 7) * 128;
-    float o[HD];
-#pragma unroll
-    for (int c = 0; c < HD; ++c) o[c] = 0.f;
-    float m = -INFINITY, l = 0.f;
-
-    // Scores of block j -> P_j (hi, lo) in shared memory; returns the
-    // rescale factor of the running sums, exp2(m_old - m_new).
-    auto softmax_block = [&](int j, float& corr) -> bool {
+    float m = -INFINITY, l = 0.f;  // m: log2-domain maximum the weights are taken against
+    bool ok = true;
+    for (int j = 0; j < nb; ++j) {
       const int b = j & 1;
-      if (!mbar_wait(&s_full[b], (j >> 1) & 1)) return false;
+      if (!(ok = __all_sync(0xffffffffu, mbar_wait(&s_full[b], (j >> 1) & 1)))) break;
       fence_after();
-      float sv[kKeys];
-      tmem_ld32(trow + G::S_COL + b * kKeys, sv);
-      tmem_ld32(trow + G::S_COL + b * kKeys + 32, sv + 32);
+      float sv[32];
+      tmem_ld32(trow + G::S_COL + b * kKeys + hf * 32, sv);
       fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&s_free[b]);
-      const int k0 = j * kKeys;
+      const int k0 = j * kKeys + hf * 32;
       float mx = -INFINITY;
+      if (k0 + 31 <= p0) {  // every key of this half block precedes every row of the tile
 #pragma unroll
-      for (int c = 0; c < kKeys; ++c) {
-        sv[c] = k0 + c <= lim ? sv[c] * scale : -INFINITY;
-        mx = fmaxf(mx, sv[c]);
+        for (int c = 0; c < 32; ++c) mx = fmaxf(mx, sv[c]);
+      } else {
+#pragma unroll
+        for (int c = 0; c < 32; ++c) {
+          sv[c] = k0 + c <= lim ? sv[c] : -INFINITY;
+          mx = fmaxf(mx, sv[c]);
+        }
       }
-      const float mn = fmaxf(m, mx);  // finite: key 0 is visible to every row
-      corr = exp2f(m - mn);
-      float sum = 0.f;
+      mx *= scale;
+      xch[(b * 2 + hf) * kRows + r] = mx;
+      mbar_arrive(&pair[q4 * 2 + b]);
+      if (!(ok = __all_sync(0xffffffffu, mbar_wait(&pair[q4 * 2 + b], (j >> 1) & 1)))) break;
+      mx = fmaxf(mx, xch[(b * 2 + (hf ^ 1)) * kRows + r]);  // finite: key 0 is visible to every row
+      const float mnew = mx > m + kTau ? mx : m;
+      const float factor = exp2f(m - mnew);  // 1 without a rescale, 0 for the first block
+      if (j > 0 && __any_sync(0xffffffffu, mnew != m)) {
+        // O holds blocks 0 .. j-1 against the old maximum: wait for P_{j-1} V_{j-1}.
+        if (!(ok = __all_sync(0xffffffffu, mbar_wait(&o_done[(j - 1) & 1], ((j - 1) >> 1) & 1))))
+          break;
+        fence_after();
+#pragma unroll
+        for (int c0 = 0; c0 < HH; c0 += 32) {
+          float v[32];
+          tmem_ld32(trow + G::O_COL + hf * HH + c0, v);
+#pragma unroll
+          for (int e = 0; e < 32; ++e) v[e] *= factor;
+          tmem_st32(trow + G::O_COL + hf * HH + c0, v);
+        }
+        asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+      }
+      l *= factor;
+      m = mnew;
+      // P buffer b was last read by P_{j-2} V_{j-2}.
+      if (j >= 2 && !(ok = __all_sync(0xffffffffu, mbar_wait(&o_done[b], ((j - 2) >> 1) & 1)))) break;
       const uint32_t ph = pbase + b * G::PBUF, pl = ph + G::PPART;
 #pragma unroll
-      for (int c = 0; c < kKeys / 8; ++c) {
+      for (int cc = 0; cc < 4; ++cc) {
         uint32_t hi[4], lo[4];
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
-          const float x0 = exp2f(sv[8 * c + 2 * e] - mn), x1 = exp2f(sv[8 * c + 2 * e + 1] - mn);
-          sum += x0 + x1;
-          const float h0 = __bfloat162float(__float2bfloat16_rn(x0)), h1 = __bfloat162float(__float2bfloat16_rn(x1));
-          hi[e] = pack_bf16(h0, h1);
+          const float x0 = exp2f(fmaf(sv[8 * cc + 2 * e], scale, -m));
+          const float x1 = exp2f(fmaf(sv[8 * cc + 2 * e + 1], scale, -m));
+          l += x0 + x1;
+          hi[e] = pack_bf16(x0, x1);
+          const float h0 = __uint_as_float(hi[e] << 16), h1 = __uint_as_float(hi[e] & 0xFFFF0000u);
           lo[e] = pack_bf16(x0 - h0, x1 - h1);
         }
-        const uint32_t off = (uint32_t)((c ^ (r & 7)) * 16);
+        const uint32_t off = (uint32_t)(((hf * 4 + cc) ^ (r & 7)) * 16);
         st_shared_v4(ph + off, hi[0], hi[1], hi[2], hi[3]);
         st_shared_v4(pl + off, lo[0], lo[1], lo[2], lo[3]);
       }
-      l = l * corr + sum;
-      m = mn;
-      if (j == nb - 1 && kmax - k0 < kKeys - 1) {
+      if (j == nb - 1 && kmax - j * kKeys < kKeys - 1) {
         // Keys past the tile's last position: their weights are 0, but their
         // V rows may hold NaN (unwritten positions) or a previous block's
         // keys; zero them so that 0 * NaN never reaches the accumulator.
         const int s = j % kStages;
-        if (!mbar_wait(&kv_full[s], (j / kStages) & 1)) return false;
+        if (!(ok = __all_sync(0xffffffffu, mbar_wait(&kv_full[s], (j / kStages) & 1)))) break;
         uint8_t* vt = kvs + (size_t)s * G::STAGE + G::KVB;
-        const int first = kmax - k0 + 1;
-        for (int u = r; u < (kKeys - first) * G::NX * 8; u += kRows) {
+        const int first = kmax - j * kKeys + 1;
+        for (int u = warp * 32 + lane; u < (kKeys - first) * G::NX * 8; u += 256) {
           const int row = first + u / (G::NX * 8), rem = u % (G::NX * 8);
           *reinterpret_cast<uint4*>(vt + (size_t)(rem / 8) * G::KSLICE + (size_t)row * 128 + (rem % 8) * 16) =
               make_uint4(0, 0, 0, 0);
         }
       }
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&p_full[b]);
-      return true;
-    };
-
-    float corr_j = 0.f;
-    bool ok = softmax_block(0, corr_j);
-    for (int j = 0; ok && j < nb; ++j) {
-      float corr_next = 1.f;
-      if (j + 1 < nb && !(ok = softmax_block(j + 1, corr_next))) break;
-      const int b = j & 1;
-      if (!(ok = mbar_wait(&o_full[b], (j >> 1) & 1))) break;
-      fence_after();
-#pragma unroll
-      for (int c0 = 0; c0 < HD; c0 += 32) {
-        float v[32];
-        tmem_ld32(trow + G::O_COL + b * HD + c0, v);
-#pragma unroll
-        for (int e = 0; e < 32; ++e) o[c0 + e] = fmaf(o[c0 + e], corr_j, v[e]);
-      }
       fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&o_free[b]);
-      corr_j = corr_next;
+      if (lane == 0) mbar_arrive(&p_full[b]);
+    }
+    if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&o_done[(nb - 1) & 1], ((nb - 1) >> 1) & 1));
+    float lt = 0.f;
+    if (ok) {
+      xch[(4 + hf) * kRows + r] = l;  // sums: a region the maxima never use
+      mbar_arrive(&pair[8 + q4]);
+      ok = __all_sync(0xffffffffu, mbar_wait(&pair[8 + q4], 0));
+      lt = l + xch[(4 + (hf ^ 1)) * kRows + r];
     }
     if (!ok) {
       if (lane == 0) atomicOr(status, kStatusTimeout);
-    } else if (r < nq) {
-      const float inv = 1.f / l;
-      __nv_bfloat16* dst = O + (size_t)(row0 + r) * kv.d + (size_t)h * HD;
+    } else {
+      fence_after();
+      const float inv = 1.f / lt;
+      __nv_bfloat16* dst = O + (size_t)(row0 + r) * kv.d + (size_t)h * HD + hf * HH;
 #pragma unroll
-      for (int c = 0; c < HD; c += 8) {
-        uint4 u;
-        u.x = pack_bf16(o[c] * inv, o[c + 1] * inv);
-        u.y = pack_bf16(o[c + 2] * inv, o[c + 3] * inv);
-        u.z = pack_bf16(o[c + 4] * inv, o[c + 5] * inv);
-        u.w = pack_bf16(o[c + 6] * inv, o[c + 7] * inv);
-        *reinterpret_cast<uint4*>(dst + c) = u;
+      for (int c0 = 0; c0 < HH; c0 += 32) {
+        float v[32];
+        tmem_ld32(trow + G::O_COL + hf * HH + c0, v);
+        if (r < nq) {
+#pragma unroll
+          for (int c = 0; c < 32; c += 8) {
+            uint4 u;
+            u.x = pack_bf16(v[c] * inv, v[c + 1] * inv);
+            u.y = pack_bf16(v[c + 2] * inv, v[c + 3] * inv);
+            u.z = pack_bf16(v[c + 4] * inv, v[c + 5] * inv);
+            u.w = pack_bf16(v[c + 6] * inv, v[c + 7] * inv);
+            *reinterpret_cast<uint4*>(dst + c0 + c) = u;
+          }
+        }
       }
     }
   }
   fence_before();
   __syncthreads();
-  if (warp == 5) {
+  if (warp == 9) {
     fence_after();
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(G::TMEM_COLS));
   }
@@ -450,7 +491,7 @@ static bool prefill_tc_hd(cudaStream_t s, const __nv_bfloat16* Q, int q_rows, co
     set[dev] = true;
   }
   count_launch();
-  return launch_pdl(k_attn_prefill_tc<HD>, dim3(n_tiles, H), dim3(192), G::SMEM, s, *tq, *tk, tiles, kv, slot, H, O,
+  return launch_pdl(k_attn_prefill_tc<HD>, dim3(n_tiles, H), dim3(320), G::SMEM, s, *tq, *tk, tiles, kv, slot, H, O,
                     status) == cudaSuccess;
 }
 
