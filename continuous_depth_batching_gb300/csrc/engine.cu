@@ -24,6 +24,7 @@
 namespace cdb {
 
 static constexpr int kRing = 8;           // lookahead flag ring (core steps)
+static constexpr int kWideBatch = 256;    // engines with at least this many slots skip split-K
 static constexpr size_t kAlign = 256;
 static constexpr size_t kStageSeg = 1 << 20;  // pinned upload segment
 static constexpr int kStageSegs = 8;
@@ -108,7 +109,8 @@ static bool plan_layout(const cdb_model_desc* m, const cdb_sched_cfg* c, Layout*
   L->part_o = take(W * H * L->max_splits * hd * 4);
   L->part_ml = take(W * H * L->max_splits * 2 * 4);
   // Split-K partials of one decode GEMM ([split][row][ldp], ldp <= max(3d, 2f)).
-  L->gpart_floats = (size_t)kGemmMaxSplits * W * std::max(3 * d, 2 * f);
+  // Split-K partials exist only for engines below kWideBatch slots.
+  L->gpart_floats = W < kWideBatch ? (size_t)kGemmMaxSplits * W * std::max(3 * d, 2 * f) : 64;
   L->gpart = take(L->gpart_floats * 4);
   L->total = o;
   return true;
@@ -326,10 +328,17 @@ class GpuExecutor : public Executor {
     const double es = sizeof(T), nw = W2 ? 2.0 : 1.0;
     const int h = prof_begin(x, decode_tiles_ ? 1 : 4);
     int ns = -1;
+    // Decode tiling (64-row tiles, split-K fixed by the weight shape) for
+    // engines of fewer than kWideBatch slots; wider engines run every
+    // projection on the persistent kernel without split partials, whose
+    // traffic grows with the rows (about 200 MB per Ouro-shaped layer at 512
+    // rows).  Either way a row's result does not depend on the other rows.
+    const bool split_tiles = decode_tiles_ && x->c.W < kWideBatch;
     if (sizeof(T) == 2)
       ns = launch_gemm_tc(x->cs, epi, (const __nv_bfloat16*)A, lda, x->L.R, (const __nv_bfloat16*)W,
-                          (const __nv_bfloat16*)W2, N, K, rows, Cf, (__nv_bfloat16*)Ct, ldc, decode_tiles_,
-                          parts ? at<float>(x, x->L.gpart) : nullptr, x->L.gpart_floats, at<int>(x, x->L.status));
+                          (const __nv_bfloat16*)W2, N, K, rows, Cf, (__nv_bfloat16*)Ct, ldc, split_tiles,
+                          parts && split_tiles ? at<float>(x, x->L.gpart) : nullptr, x->L.gpart_floats,
+                          at<int>(x, x->L.status));
     if (ns < 0) {
       launch_gemm<T>(x->cs, epi, A, lda, (const T*)W, (const T*)W2, N, K, rows, Cf, Ct, ldc);
       ns = 0;
@@ -337,8 +346,9 @@ class GpuExecutor : public Executor {
       // Step-delta timing: the same launch again writes the same partials
       // (or the same stored output); an in-place residual is not repeated.
       launch_gemm_tc(x->cs, epi, (const __nv_bfloat16*)A, lda, x->L.R, (const __nv_bfloat16*)W,
-                     (const __nv_bfloat16*)W2, N, K, rows, Cf, (__nv_bfloat16*)Ct, ldc, decode_tiles_,
-                     parts ? at<float>(x, x->L.gpart) : nullptr, x->L.gpart_floats, at<int>(x, x->L.status));
+                     (const __nv_bfloat16*)W2, N, K, rows, Cf, (__nv_bfloat16*)Ct, ldc, split_tiles,
+                     parts && split_tiles ? at<float>(x, x->L.gpart) : nullptr, x->L.gpart_floats,
+                     at<int>(x, x->L.status));
     }
     const double out_b = epi == kEpiSwiglu ? es : (epi == kEpiResid ? 8.0 : 4.0);
     prof_end(x, h, nw * N * (double)K * es + (double)rows * K * es + (double)rows * N * out_b,
@@ -378,7 +388,7 @@ class GpuExecutor : public Executor {
 
   template <typename T>
   int block(const LayerW& lw, float* X, int rows, const int* mslot, const int* mpos, const int* mdepth,
-            int depth_uniform, int slot_base, int clamp, bool decode, double sumL) {
+            int depth_uniform, int slot_base, int clamp, bool decode, double sumL, int maxL = 0) {
     cdb_ctx* x = x_;
     const Layout& L = x->L;
     const int d = x->m.d_model, f = x->m.ffn, H = x->m.n_heads, hd = x->m.head_dim;
@@ -401,7 +411,12 @@ class GpuExecutor : public Executor {
                         hd, at<float2>(x, L.rope), st);
     prof_end(x, hr, (double)rows * d * (12.0 + 3.0 * es), 0.0);  // q, k, v in; q, K, V rows out
     const int split = decode ? L.split : (1 << 30);
-    const int msp = decode ? L.max_splits : 1;
+    // Split partials per (row, head): enough for the longest context in this
+    // batch (maxL keys; the arena holds max_ctx), which also decides whether
+    // the combine runs.  A row's own arithmetic does not depend on it.
+    const int msp = decode ? std::max(1, std::min(L.max_splits, maxL > 0 ? (maxL + split - 1) / split
+                                                                         : L.max_splits))
+                           : 1;
     const int ha = prof_begin(x, decode ? 0 : 2);
     // Exit gaps are filled at compaction, so every key of a row is read from
     // the row's own slot.  Prefill chunks go through query tiles.
@@ -552,8 +567,10 @@ class GpuExecutor : public Executor {
     launch_embed_prelude<T>(x->cs, (const T*)x->embed, d, x->m.vocab, ls, lt, lp, n, at<int>(x, L.out_tok),
                             x->c.max_new_cap, Tp, tm, geom(), x->m.r_max, at<int>(x, L.status));
     double sumL = 0;
-    for (int i = 0; i < n; ++i) sumL += c[i] + 1;
-    for (int i = 0; i < x->m.n_prelude; ++i) block<T>(x->pre[i], Tp, n, tm.slot, tm.pos, nullptr, 1, i, 0, true, sumL);
+    int maxL = 0;
+    for (int i = 0; i < n; ++i) sumL += c[i] + 1, maxL = std::max(maxL, c[i] + 1);
+    for (int i = 0; i < x->m.n_prelude; ++i)
+      block<T>(x->pre[i], Tp, n, tm.slot, tm.pos, nullptr, 1, i, 0, true, sumL, maxL);
     flush<T>();
     launch_prelude_finish(x->cs, Tp, tm, n, at<float>(x, L.rows[2]), meta_at(x, L.meta[2]), p.dst_off,
                           x->m.has_adapter ? at<float>(x, L.estore) : nullptr, d, x->m.has_adapter);
@@ -582,10 +599,11 @@ class GpuExecutor : public Executor {
                        meta_at(x, L.meta[2]), p.n_ref, X, mx, d, sprev);
     if (x->m.has_adapter) adapter_step<T>(X, B, at<float>(x, L.estore), 1, mx.slot);
     double sumL = 0;
-    for (const Tok& t : *p.rows) sumL += t.pos + 1;
+    int maxL = 0;
+    for (const Tok& t : *p.rows) sumL += t.pos + 1, maxL = std::max(maxL, t.pos + 1);
     for (int l = 0; l < x->m.n_core; ++l)
       block<T>(x->core[l], X, B, mx.slot, mx.pos, mx.depth, 0, x->m.n_prelude + l * core_slots(&x->m),
-               core_slots(&x->m), true, sumL);
+               core_slots(&x->m), true, sumL, maxL);
     flush<T>();
     const int ri = (int)(p.step % kRing);
     uint8_t* ring = at<uint8_t>(x, L.ring) + (size_t)ri * x->c.W;
@@ -633,9 +651,10 @@ class GpuExecutor : public Executor {
       launch_copy_rows(x->cs, Cb, Tc, n, d);
       const int cbase = x->m.n_prelude + x->m.n_core * core_slots(&x->m);
       double sumL = 0;
-      for (const Tok& t : rows) sumL += t.pos + 1;
+      int maxL = 0;
+      for (const Tok& t : rows) sumL += t.pos + 1, maxL = std::max(maxL, t.pos + 1);
       for (int j = 0; j < x->m.n_coda; ++j)
-        block<T>(x->coda[j], Tc, n, mb.slot, mb.pos, nullptr, 1, cbase + j, 0, true, sumL);
+        block<T>(x->coda[j], Tc, n, mb.slot, mb.pos, nullptr, 1, cbase + j, 0, true, sumL, maxL);
       flush<T>();
       Hrows = Tc;
     }
