@@ -256,16 +256,20 @@ def live_core_costs(eng, stream, binding, n_steps):
     import torch
     classes = [None, "attention", "gemm", "rowwise"]
     times = {c: [] for c in classes}
+    bound = {}  # boundary calls that did work, by stage: (events, count)
     i = 0
     while i < n_steps * len(classes):
         cls = classes[i % len(classes)]
         eng.profile_repeat(cls)
         a = torch.cuda.Event(enable_timing=True)
         b = torch.cuda.Event(enable_timing=True)
-        rc, _ = eng.step_boundary()
+        a.record(stream)
+        rc, info = eng.step_boundary()
         if rc == binding.DONE:
             break
         if rc != binding.IDLE:
+            b.record(stream)
+            bound.setdefault(binding.STAGES.get(info.stage, str(info.stage)), []).append((a, b))
             continue
         a.record(stream)
         eng.step_core()
@@ -276,7 +280,11 @@ def live_core_costs(eng, stream, binding, n_steps):
     torch.cuda.synchronize()
     mean = {c: (sum(a.elapsed_time(b) for a, b in v) / len(v)) if v else float("nan") for c, v in times.items()}
     base = mean[None]
-    out = {"core_step_ms": base, "steps_per_class": min(len(v) for v in times.values())}
+    n_core = sum(len(v) for v in times.values())
+    out = {"core_step_ms": base, "steps_per_class": min(len(v) for v in times.values()),
+           "boundary_ms_per_core_step": {k: sum(a.elapsed_time(b) for a, b in v) / max(n_core, 1)
+                                         for k, v in bound.items()},
+           "boundary_calls_per_core_step": {k: len(v) / max(n_core, 1) for k, v in bound.items()}}
     for c in classes[1:]:
         out[c] = mean[c] - base
     out["rowwise_note"] = "RoPE + KV write and the SwiGLU combine; RMSNorm folds are in other"

@@ -24,7 +24,7 @@
 namespace cdb {
 
 static constexpr int kRing = 8;           // lookahead flag ring (core steps)
-static constexpr int kWideBatch = 256;    // engines with at least this many slots skip split-K
+static constexpr int kWideBatch = 384;    // engines with at least this many slots skip split-K
 static constexpr size_t kAlign = 256;
 static constexpr size_t kStageSeg = 1 << 20;  // pinned upload segment
 static constexpr int kStageSegs = 8;
@@ -334,9 +334,10 @@ class GpuExecutor : public Executor {
     // traffic grows with the rows (about 200 MB per Ouro-shaped layer at 512
     // rows).  Either way a row's result does not depend on the other rows.
     const bool split_tiles = decode_tiles_ && x->c.W < kWideBatch;
+    const int tiling = split_tiles ? kTileSplit : decode_tiles_ ? kTileWide : kTilePrefill;
     if (sizeof(T) == 2)
       ns = launch_gemm_tc(x->cs, epi, (const __nv_bfloat16*)A, lda, x->L.R, (const __nv_bfloat16*)W,
-                          (const __nv_bfloat16*)W2, N, K, rows, Cf, (__nv_bfloat16*)Ct, ldc, split_tiles,
+                          (const __nv_bfloat16*)W2, N, K, rows, Cf, (__nv_bfloat16*)Ct, ldc, tiling,
                           parts && split_tiles ? at<float>(x, x->L.gpart) : nullptr, x->L.gpart_floats,
                           at<int>(x, x->L.status));
     if (ns < 0) {
@@ -346,7 +347,7 @@ class GpuExecutor : public Executor {
       // Step-delta timing: the same launch again writes the same partials
       // (or the same stored output); an in-place residual is not repeated.
       launch_gemm_tc(x->cs, epi, (const __nv_bfloat16*)A, lda, x->L.R, (const __nv_bfloat16*)W,
-                     (const __nv_bfloat16*)W2, N, K, rows, Cf, (__nv_bfloat16*)Ct, ldc, split_tiles,
+                     (const __nv_bfloat16*)W2, N, K, rows, Cf, (__nv_bfloat16*)Ct, ldc, tiling,
                      parts && split_tiles ? at<float>(x, x->L.gpart) : nullptr, x->L.gpart_floats,
                      at<int>(x, x->L.status));
     }
@@ -1074,7 +1075,7 @@ size_t cdb_test_gemm_ws_bytes(int N, int K, int rows, int tiling, int epi) {
 
 int cdb_test_gemm(int epi, int tiling, const void* A, int lda, int a_rows, const void* W, const void* W2, int N,
                   int K, int rows, float* Cf, void* Ct, int ldc, void* ws, size_t ws_bytes, void* stream) {
-  if (epi < 0 || epi > 2 || tiling < 0 || tiling > 2 || !A || !W || (epi == 2 && (!W2 || !Ct)) ||
+  if (epi < 0 || epi > 2 || tiling < 0 || tiling > 3 || !A || !W || (epi == 2 && (!W2 || !Ct)) ||
       (epi != 2 && !Cf) || !ws || ws_bytes < cdb_test_gemm_ws_bytes(N, K, rows, tiling, epi))
     return CDB_ERR_ARG;
   cudaStream_t s = (cudaStream_t)stream;
@@ -1088,7 +1089,8 @@ int cdb_test_gemm(int epi, int tiling, const void* A, int lda, int a_rows, const
     // The decode tiling leaves split-K partials for a consumer; fold them here
     // the way the engine's consumers do (split order, then the epilogue).
     const int ns = launch_gemm_tc(s, epi, (const __nv_bfloat16*)A, lda, a_rows, (const __nv_bfloat16*)W,
-                                  (const __nv_bfloat16*)W2, N, K, rows, Cf, (__nv_bfloat16*)Ct, ldc, tiling == 0,
+                                  (const __nv_bfloat16*)W2, N, K, rows, Cf, (__nv_bfloat16*)Ct, ldc,
+                                  tiling == 0 ? kTileSplit : tiling == 1 ? kTilePrefill : kTileWide,
                                   tiling == 0 ? parts : nullptr, (ws_bytes - 256) / 4, status);
     if (ns < 0) return CDB_ERR_ARG;
     if (ns > 0) {

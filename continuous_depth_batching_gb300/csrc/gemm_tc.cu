@@ -614,8 +614,9 @@ int gemm_tc_splits(int N, int K, bool decode) {
 
 int launch_gemm_tc(cudaStream_t s, int epi, const __nv_bfloat16* A, int lda, int a_rows, const __nv_bfloat16* W,
                    const __nv_bfloat16* W2, int N, int K, int rows, float* Cf, __nv_bfloat16* Ct, int ldc,
-                   bool decode, float* ws, size_t ws_floats, int* status) {
+                   int tiling, float* ws, size_t ws_floats, int* status) {
   if (rows <= 0) return 0;
+  const bool decode = tiling == kTileSplit;
   if ((K * 2) % 16 != 0 || (lda * 2) % 16 != 0 || rows > a_rows) return -1;
   int splits = ws ? gemm_tc_splits(N, K, decode) : 1;
   const size_t ldp = epi == kEpiSwiglu ? 2 * (size_t)N : (size_t)N;
@@ -630,9 +631,10 @@ int launch_gemm_tc(cudaStream_t s, int epi, const __nv_bfloat16* A, int lda, int
       default: ok = tc::launch_bn<64, kEpiSwiglu>(s, A, lda, a_rows, W, W2, N, K, rows, splits, Cf, Ct, ldc, P, status); break;
     }
   } else {
-    // Prefill, persistent: one CTA per SM, double-buffered accumulators;
+    // Persistent: one CTA per SM, double-buffered accumulators.  Prefill:
     // 256-row tiles where one accumulator fits, 128-row tiles for SwiGLU.
-    const bool wide = rows > 128;
+    // Wide decode batches: 128-row tiles always.
+    const bool wide = tiling == kTilePrefill && rows > 128;
     const int sm = sm_count();
     switch (epi) {
       case kEpiStore:

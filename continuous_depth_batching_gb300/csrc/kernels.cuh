@@ -168,10 +168,15 @@ void launch_gemm(cudaStream_t s, int epi, const T* A, int lda, const T* W, const
 // when the epilogue was applied in place, -1 when the shape is unsupported.
 // a_rows: rows allocated in A (TMA bounds).
 constexpr int kGemmMaxSplits = 16;
+// Tilings: kTileSplit = 64-row tiles with split-K (decode batches below the
+// wide threshold); kTilePrefill = persistent, 256-row tiles (128 for SwiGLU)
+// when rows > 128; kTileWide = persistent, 128-row tiles at any row count
+// (wide decode batches: the tile shape never depends on the rows).
+enum GemmTiling { kTileSplit = 0, kTilePrefill = 1, kTileWide = 2 };
 int gemm_tc_splits(int N, int K, bool decode);
 int launch_gemm_tc(cudaStream_t s, int epi, const __nv_bfloat16* A, int lda, int a_rows,
                    const __nv_bfloat16* W, const __nv_bfloat16* W2, int N, int K, int rows,
-                   float* Cf, __nv_bfloat16* Ct, int ldc, bool decode, float* ws, size_t ws_floats,
+                   float* Cf, __nv_bfloat16* Ct, int ldc, int tiling, float* ws, size_t ws_floats,
                    int* status);
 
 }  // namespace cdb

@@ -19,8 +19,11 @@ extern "C" {
  *   tiling 0: tensor cores, decode tiles (64 rows, split-K fixed by N and K;
  *             the fp32 partials are summed in split order by a second kernel,
  *             as the engine's consumer kernels do, then the epilogue applied)
- *   tiling 1: tensor cores, prefill tiles (128 rows, no split)
+ *   tiling 1: tensor cores, persistent prefill tiles (256 rows, 128 for
+ *             SwiGLU, when rows > 128; else 128), no split
  *   tiling 2: the CUDA-core kernel (fp32 FMA), for comparison
+ *   tiling 3: tensor cores, persistent 128-row tiles at any row count, no
+ *             split (what engines of 384 or more slots run in decode)
  * a_rows: rows allocated in A (>= rows).  ws: device memory of at least
  * cdb_test_gemm_ws_bytes() bytes: the kernel's status word, then the split-K
  * partials.  stream: cudaStream_t or NULL.

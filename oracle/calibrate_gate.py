@@ -13,8 +13,9 @@ min(r_max, 1 + min{d in [r_min-1, r_max-2] : z_d + b > logit(q)}).
 * tiny: the bias that spreads exit depths most evenly over 2..r_max
   (largest entropy of the depth histogram on a grid of step 0.005).
 * ouro: the bias whose live-gate mean exit depth over a sample of the job
-  (8 sequences spread over its prompt lengths, 64 generated tokens each) is
-  closest to 3.
+  (6 sequences spread over its prompt lengths, each decoded for all 256
+  generated tokens, since exits grow shallower along a sequence) is closest
+  to 3.
 * huginn: exit depths are replayed (App. C.2), the bias stays 0.
 
 Usage: python -m oracle.calibrate_gate [tiny|ouro ...]
@@ -93,7 +94,7 @@ def adaptive_mean(shape, weights, reqs, gen: int, b: float) -> float:
     return float(np.mean(e))
 
 
-def calibrate_mean(name: str, target: float, n_seqs: int = 8, gen: int = 64) -> float:
+def calibrate_mean(name: str, target: float, n_seqs: int = 6, gen: int = 256) -> float:
     """Bias whose mean exit depth over a sample of the job is closest to target.
 
     A fixed-depth pilot gives every token's logits z_1..z_{r_max-1}, hence the

@@ -17,7 +17,7 @@ must reproduce the sequence-alone oracle for each configuration's shape:
   rows), with the single-slot cache that makes such batches fit.
 * bf16 refill, no-refill and one-slot runs give identical bits (the same
   invariance on the tensor-core GEMMs, the TMA decode attention and the tiled
-  prefill attention), and so do engines of 256 and more slots, which run the
+  prefill attention), and so do engines of 384 and more slots, which run the
   projections without split-K, among themselves.
 
 Bars as in the other parity tests: tokens and exit depths identical, gate
@@ -188,17 +188,17 @@ def test_step_delta_repeats_leave_results_unchanged():
 
 
 def test_wide_engines_agree_bit_exactly():
-    """Engines of 256 or more slots run the projections without split-K (the
-    persistent GEMM, 128- or 256-row tiles chosen by the step's rows); a
-    token's bits still do not depend on the batch: W = 256 and W = 512 refill
-    runs and a W = 320 no-refill run of the same requests agree bit for bit."""
+    """Engines of 384 or more slots run the projections without split-K (the
+    persistent GEMM, 128-row tiles at any row count); a token's bits still do
+    not depend on the batch: W = 384 and W = 512 refill runs and a W = 448
+    no-refill run of the same requests agree bit for bit."""
     from continuous_depth_batching_gb300 import binding
     shape = _shape(r_max=5)
     wts = make_weights(shape)
     reqs = _reqs(shape, 600, 4, 24, 3, 8, seed=53)
     dw = binding.device_weights(shape, wts)
     runs = [gpu_run(shape, dw, reqs, None, mode=m, W=w, trace_tokens=3, trace_gate=True, force=False)[0]
-            for m, w in [("refill", 256), ("refill", 512), ("no_refill", 320)]]
+            for m, w in [("refill", 384), ("refill", 512), ("no_refill", 448)]]
     for other in runs[1:]:
         for sid in runs[0]:
             for key in ("tokens", "exit_depths", "logits", "hidden", "gate_logits"):
