@@ -50,7 +50,7 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-modes", action="store_true", help="skip the no-refill and fixed-depth full jobs")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--cpu-seconds", type=float, default=20.0)
+    ap.add_argument("--cpu-seconds", type=float, default=30.0)
     ap.add_argument("--kv-slots", type=int, default=0,
                     help="KV slots per core layer: 0 = r_max (depth-indexed), 1 single-slot, 2 first-then-shared")
     return ap.parse_args()
@@ -161,38 +161,38 @@ def aggregate(ms: float, tokens: float, world: int, device: str = "cuda"):
     return float(mx[0]), float(sm[0])
 
 
-def cpu_baseline(shape, wts, reqs, seconds):
-    """The oracle as it stands, on a bounded sample: shortest prompts, prefill + leading tokens.
+def cpu_baseline(shape, wts, reqs, seconds, n_seqs=4, n_tokens=16):
+    """The oracle as it stands, on a bounded sample of the same workload.
 
-    A prefill is not interruptible, so prompts are cut to the length whose
-    prefill takes about half the budget, estimated from an untimed 16-token
-    prefill (long-context workloads would otherwise spend tens of minutes in
-    one prompt); the sample says so when it cuts."""
+    n_seqs sequences at evenly spaced quantiles of the workload's prompt
+    lengths, each decoded alone: prefill, then its first n_tokens generated
+    tokens.  A prefill is not interruptible, so prompts are cut to the length
+    whose prefills take about half the budget together, estimated from an
+    untimed 16-token prefill (long-context workloads would otherwise spend
+    tens of minutes in one prompt); the sample says so when it cuts."""
     import numpy as np  # noqa: F401
     from oracle.model import OracleModel, iter_decode
     om = OracleModel(shape, wts)
     order = sorted(reqs, key=lambda r: len(r["prompt"]))
+    picks = [order[min(len(order) - 1, int((k + 0.5) * len(order) / n_seqs))] for k in range(n_seqs)]
     t = time.perf_counter()
     next(iter_decode(om, order[0]["prompt"][:16], 2))
     per_tok = (time.perf_counter() - t) / 16
-    pmax = max(16, int(0.5 * seconds / max(per_tok, 1e-9)))
+    pmax = max(16, int(0.5 * seconds / n_seqs / max(per_tok, 1e-9)))
     t0 = time.perf_counter()
     tokens, done = 0, []
-    for r in order:
+    for r in picks:
         n = 0
-        for _ in iter_decode(om, r["prompt"][:pmax], r["gen_len"]):
+        for _ in iter_decode(om, r["prompt"][:pmax], min(n_tokens, r["gen_len"])):
             n += 1
             tokens += 1
-            if time.perf_counter() - t0 > seconds:
-                break
         done.append((r["seq_id"], len(r["prompt"]), n))
-        if time.perf_counter() - t0 > seconds:
-            break
     dt = time.perf_counter() - t0
     desc = "; ".join(f"seq {s} (prompt {p}{f', first {pmax} tokens' if p > pmax else ''}): prefill + {n} "
                      f"generated tokens" for s, p, n in done)
     return {"value": tokens / dt, "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
-            "sample": desc + f", {dt:.1f} s, fp64 numpy oracle"}
+            "sample": f"{n_seqs} sequences at the prompt-length quantiles: " + desc +
+                      f", {dt:.1f} s, fp64 numpy oracle"}
 
 
 def run_reference(args):
