@@ -602,6 +602,9 @@ struct TmaGeo {
   static constexpr int STAGE = (2 * KREG + QB + 1023) / 1024 * 1024;
   static constexpr int NS = 2;
   static constexpr size_t SMEM = 1024 + (size_t)NS * STAGE + NS * (2 * 8 + sizeof(StageMeta));
+  // Fused RoPE / KV write: q, k and v rows (bf16) of each consumer warp's head.
+  static constexpr size_t XOFF = ((size_t)NS * STAGE + NS * (2 * 8 + sizeof(StageMeta)) + 15) / 16 * 16;
+  static constexpr size_t SMEM_FUSED = 1024 + XOFF + (size_t)kWarps * 3 * HD * 2;
   static_assert(HD % 32 == 0, "head dim");
 };
 
@@ -631,13 +634,18 @@ __device__ __forceinline__ uint32_t swz(uint32_t slice, int row, int c) {
 
 }  // namespace attn
 
-template <int HD>
+// FUSE: the row's query is not read from Q but formed here from the QKV
+// GEMM's split-K partials (RoPE, then bf16), and the CTA holding the row's
+// last split also forms the token's own K and V rows: it stores them in the
+// pool for later steps and writes them into the tile of its last page, whose
+// copy from the pool may predate them.  Same arithmetic as k_rope_kv.
+template <int HD, bool FUSE>
 __global__ void __launch_bounds__((attn::kWarps + 1) * 32)
     k_attn_tma(const __grid_constant__ CUtensorMap tm, const __nv_bfloat16* __restrict__ Q, int rows,
                const int* __restrict__ mslot, const int* __restrict__ mpos, const int* __restrict__ mdepth,
                int depth_uniform, KvGeom kv, int slot_base, int clamp, int H, int split, int max_splits,
                __nv_bfloat16* __restrict__ O, float* __restrict__ part_o, float* __restrict__ part_ml,
-               int* status) {
+               int* status, Parts qkv, const float2* __restrict__ rope) {
   using Gm = attn::TmaGeo<HD>;
   constexpr int G = attn::kWarps, NS = Gm::NS, NT = HD / 16;
   extern __shared__ uint8_t smem_raw[];
@@ -703,7 +711,7 @@ __global__ void __launch_bounds__((attn::kWarps + 1) * 32)
         const int nk = min(16, k_hi - key0);
         meta[s].flags = (pg == 0 ? attn::kFirst : 0) | (pg == npg - 1 ? attn::kLast : 0);
         meta[s].mask = ok ? (int)((1u << nk) - 1u) : 0;
-        const uint32_t qb = (uint32_t)Gc * HD * 2;
+        const uint32_t qb = FUSE ? 0u : (uint32_t)Gc * HD * 2;
         const uint32_t st = attn::su32(smem + (size_t)s * Gm::STAGE);
         attn::mbar_arrive_tx(&full[s], (ok ? 2u * Gm::KREG : 0u) + (pg == 0 ? qb : 0u));
         if (ok) {
@@ -713,7 +721,8 @@ __global__ void __launch_bounds__((attn::kWarps + 1) * 32)
             for (int j = 0; j < Gm::NX; ++j)
               attn::tma_2d(st + kvh * Gm::KREG + j * Gm::SLICE, &tm, &full[s], j * Gm::XW, y0 + kvh * H * 16, pol);
         }
-        if (pg == 0) attn::bulk_1d(st + 2 * Gm::KREG, Q + (size_t)row * kv.d + (size_t)h0 * HD, qb, &full[s]);
+        if (!FUSE && pg == 0)
+          attn::bulk_1d(st + 2 * Gm::KREG, Q + (size_t)row * kv.d + (size_t)h0 * HD, qb, &full[s]);
       }
       __syncwarp();
     }
@@ -723,6 +732,56 @@ __global__ void __launch_bounds__((attn::kWarps + 1) * 32)
 
   // ---------------- consumer warps: warp w handles head h0 + w ----------------
   const int h = h0 + warp;
+  // Fused RoPE / KV write: this warp's q (and, in the row's last split, k
+  // and v) rows, rotated and rounded, in xs = [q | k | v] of HD each.
+  __nv_bfloat16* xs = reinterpret_cast<__nv_bfloat16*>(smem + Gm::XOFF) + warp * 3 * HD;
+  const bool own = FUSE && sp == nsp - 1 && h < H;
+  if constexpr (FUSE) {
+    if (h < H) {
+      const int pos = L - 1;
+      const float2* cs = rope + (size_t)pos * (HD / 2);
+      constexpr int QU = HD / 8;  // four-pair groups per part
+      for (int u = lane; u < (own ? 3 : 1) * QU; u += 32) {
+        const int part = u / QU, j0 = (u - part * QU) * 4;
+        const int c = part * kv.d + h * HD + j0;
+        const float4 xa = qkv.sum4(row, c), xb = qkv.sum4(row, c + HD / 2);
+        const float a_[4] = {xa.x, xa.y, xa.z, xa.w}, b_[4] = {xb.x, xb.y, xb.z, xb.w};
+        float lo[4], hi[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          if (part < 2) {
+            rope_pair(a_[e], b_[e], cs[j0 + e], lo[e], hi[e]);
+          } else {
+            lo[e] = a_[e];
+            hi[e] = b_[e];
+          }
+        }
+        __nv_bfloat16* dst = xs + part * HD + j0;
+        *reinterpret_cast<uint2*>(dst) = make_uint2(attn::pack_bf16(lo[0], lo[1]), attn::pack_bf16(lo[2], lo[3]));
+        *reinterpret_cast<uint2*>(dst + HD / 2) =
+            make_uint2(attn::pack_bf16(hi[0], hi[1]), attn::pack_bf16(hi[2], hi[3]));
+      }
+      __syncwarp();
+      if (own) {
+        // The token's K and V rows go to its page at this layer's slot.
+        const int r = depth_uniform > 0 ? depth_uniform : mdepth[row] + 1;
+        const int sl = slot_base + (clamp ? min(r, clamp) - 1 : 0);
+        const int blk = kv.bt[mslot[row] * kv.max_blocks + (pos >> 4)];
+        if (blk >= 0 && blk < kv.kv_blocks && sl >= 0 && sl < kv.nsl) {
+          __nv_bfloat16* kdst = reinterpret_cast<__nv_bfloat16*>(kv.pool) +
+                                (((size_t)blk * kv.nsl + sl) * 2) * 16 * kv.d + (size_t)h * 16 * HD +
+                                (size_t)(pos & 15) * HD;
+          for (int u = lane; u < HD / 4; u += 32) {
+            *reinterpret_cast<uint2*>(kdst + 4 * u) = *reinterpret_cast<const uint2*>(xs + HD + 4 * u);
+            *reinterpret_cast<uint2*>(kdst + (size_t)16 * kv.d + 4 * u) =
+                *reinterpret_cast<const uint2*>(xs + 2 * HD + 4 * u);
+          }
+        } else if (lane == 0) {
+          atomicOr(status, kStatusBadBlock);
+        }
+      }
+    }
+  }
   const float scale = 1.4426950408889634f / sqrtf((float)HD);
   const bool real = (lane & 3) == 0;
   uint32_t qb[NT][2];
@@ -744,8 +803,9 @@ __global__ void __launch_bounds__((attn::kWarps + 1) * 32)
     const int flags = meta[s].flags;
     const uint32_t st = base + (uint32_t)s * Gm::STAGE;
     if (flags & attn::kFirst) {
-      const uint32_t* qs = reinterpret_cast<const uint32_t*>(smem + (size_t)s * Gm::STAGE + 2 * Gm::KREG) +
-                           warp * (HD / 2);
+      const uint32_t* qs =
+          FUSE ? reinterpret_cast<const uint32_t*>(xs)
+               : reinterpret_cast<const uint32_t*>(smem + (size_t)s * Gm::STAGE + 2 * Gm::KREG) + warp * (HD / 2);
 #pragma unroll
       for (int t = 0; t < NT; ++t) {
         qb[t][0] = (lane < 4 && warp < Gc) ? qs[t * 8 + lane] : 0u;
@@ -764,6 +824,20 @@ __global__ void __launch_bounds__((attn::kWarps + 1) * 32)
         const int j = rem / (Gm::SWB / 16), c = rem % (Gm::SWB / 16);
         *reinterpret_cast<uint4*>(vt + (size_t)j * Gm::SLICE + (size_t)(warp * 16 + k) * Gm::SWB + c * 16) =
             make_uint4(0, 0, 0, 0);
+      }
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      __syncwarp();
+    }
+    if (own && (flags & attn::kLast) && mask != 0u) {
+      // Lanes 0-15: the K row, 16-31: the V row, one 16-byte chunk each (HD <= 128).
+      const int kk = (L - 1) & 15;
+      const int part = lane >> 4, e = (lane & 15) * 8;
+      if (e < HD) {
+        const int j = e / Gm::XW, c = (e % Gm::XW) / 8;
+        const uint32_t dst = attn::swz<Gm::SWB>(st + part * Gm::KREG + j * Gm::SLICE, warp * 16 + kk, c);
+        const uint4 v = *reinterpret_cast<const uint4*>(xs + (1 + part) * HD + e);
+        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(dst), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
+                     : "memory");
       }
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
       __syncwarp();
@@ -1162,11 +1236,14 @@ __global__ void k_attn_combine(int rows, const int* __restrict__ mpos, int H, in
 }
 
 // Uniform-slot TMA path; false when the shape or pool does not fit it.
-template <int HD>
+// FUSE: q, k and v from the QKV partials (see k_attn_tma), Q unused.
+template <int HD, bool FUSE>
 static bool attn_tma(cudaStream_t s, const __nv_bfloat16* Q, int rows, const int* mslot, const int* mpos,
                      const int* mdepth, int depth_uniform, KvGeom kv, int slot_base, int clamp, int H, int split,
-                     int max_splits, __nv_bfloat16* O, float* part_o, float* part_ml, int* status) {
+                     int max_splits, __nv_bfloat16* O, float* part_o, float* part_ml, int* status, Parts qkv,
+                     const float2* rope) {
   using Gm = attn::TmaGeo<HD>;
+  constexpr size_t smem = FUSE ? Gm::SMEM_FUSED : Gm::SMEM;
   const uint64_t pool_rows = (uint64_t)kv.kv_blocks * kv.nsl * 2 * H * 16;
   if (pool_rows + 16 * attn::kWarps >= (1ull << 31)) return false;  // tile row coordinates are int32
   const CUtensorMap* tm = tmap_bf16_2d(kv.pool, HD, pool_rows, (uint64_t)HD * 2, Gm::XW, Gm::ROWS, Gm::SWB);
@@ -1174,16 +1251,27 @@ static bool attn_tma(cudaStream_t s, const __nv_bfloat16* Q, int rows, const int
   static bool set[kMaxDevices] = {};
   const int dev = current_device();
   if (!set[dev]) {
-    if (cudaFuncSetAttribute(k_attn_tma<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Gm::SMEM) !=
+    if (cudaFuncSetAttribute(k_attn_tma<HD, FUSE>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
         cudaSuccess)
       return false;
     set[dev] = true;
   }
   dim3 grid(max_splits, (H + attn::kWarps - 1) / attn::kWarps, rows);
   count_launch();
-  launch_pdl(k_attn_tma<HD>, grid, dim3((attn::kWarps + 1) * 32), Gm::SMEM, s, *tm, Q, rows, mslot, mpos, mdepth,
-             depth_uniform, kv, slot_base, clamp, H, split, max_splits, O, part_o, part_ml, status);
+  launch_pdl(k_attn_tma<HD, FUSE>, grid, dim3((attn::kWarps + 1) * 32), smem, s, *tm, Q, rows, mslot, mpos, mdepth,
+             depth_uniform, kv, slot_base, clamp, H, split, max_splits, O, part_o, part_ml, status, qkv, rope);
   return true;
+}
+
+// Merge of the split partials (rows whose keys span more than one split).
+template <typename T>
+static void attn_combine(cudaStream_t s, int rows, const int* mpos, int H, int hd, KvGeom kv, int split,
+                         int max_splits, const float* part_o, const float* part_ml, T* O) {
+  if (max_splits > 1)
+    count_launch(), launch_pdl(k_attn_combine<T>, dim3((rows * H + 3) / 4), dim3(128), 0, s, rows, mpos, H, hd, kv.d,
+                               split, max_splits, (int)std::min<long long>((long long)split * max_splits,
+                                                                           (long long)kv.max_blocks * 16),
+                               part_o, part_ml, O);
 }
 
 template <typename T, int HD>
@@ -1193,8 +1281,8 @@ static void attn_hd(cudaStream_t s, const T* Q, int rows, const int* mslot, cons
   bool done = false;
   if constexpr (sizeof(T) == 2 && HD % 32 == 0) {
     if (uniform)
-      done = attn_tma<HD>(s, Q, rows, mslot, mpos, mdepth, depth_uniform, kv, slot_base, clamp, H, split, max_splits,
-                          O, part_o, part_ml, status);
+      done = attn_tma<HD, false>(s, Q, rows, mslot, mpos, mdepth, depth_uniform, kv, slot_base, clamp, H, split,
+                                 max_splits, O, part_o, part_ml, status, Parts{nullptr, 0, 0, 0}, nullptr);
   }
   if (!done) {
     using Gm = attn::Geo<T, HD>;
@@ -1214,11 +1302,32 @@ static void attn_hd(cudaStream_t s, const T* Q, int rows, const int* mslot, cons
     launch_pdl(k_attn<T, HD>, dim3(grid), dim3((attn::kWarps + 1) * 32), Gm::SMEM, s, Q, rows, mslot, mpos, mdepth,
                depth_uniform, kv, slot_base, clamp, uniform ? 0 : 1, H, split, max_splits, O, part_o, part_ml, status);
   }
-  if (max_splits > 1)
-    count_launch(), launch_pdl(k_attn_combine<T>, dim3((rows * H + 3) / 4), dim3(128), 0, s, rows, mpos, H, HD, kv.d,
-                               split, max_splits, (int)std::min<long long>((long long)split * max_splits,
-                                                                           (long long)kv.max_blocks * 16),
-                               part_o, part_ml, O);
+  attn_combine<T>(s, rows, mpos, H, HD, kv, split, max_splits, part_o, part_ml, O);
+}
+
+bool attention_rope_fusable(KvGeom kv, int H, int hd, int split) {
+  const uint64_t pool_rows = (uint64_t)kv.kv_blocks * kv.nsl * 2 * H * 16;
+  return (hd == 32 || hd == 64 || hd == 96 || hd == 128) && split % 16 == 0 &&
+         pool_rows + 16 * attn::kWarps < (1ull << 31);
+}
+
+bool launch_attention_rope(cudaStream_t s, const float* QKV, int ns, int rows, const int* mslot, const int* mpos,
+                           const int* mdepth, int depth_uniform, KvGeom kv, int slot_base, int clamp, int H, int hd,
+                           int split, int max_splits, const float2* rope, __nv_bfloat16* O, float* part_o,
+                           float* part_ml, int* status) {
+  if (rows <= 0) return true;
+  if (split % 16 != 0) return false;
+  const Parts qkv{QKV, ns < 1 ? 1 : ns, (size_t)rows * 3 * kv.d, 3 * kv.d};
+  bool done = false;
+  switch (hd) {
+    case 32: done = attn_tma<32, true>(s, nullptr, rows, mslot, mpos, mdepth, depth_uniform, kv, slot_base, clamp, H, split, max_splits, O, part_o, part_ml, status, qkv, rope); break;
+    case 64: done = attn_tma<64, true>(s, nullptr, rows, mslot, mpos, mdepth, depth_uniform, kv, slot_base, clamp, H, split, max_splits, O, part_o, part_ml, status, qkv, rope); break;
+    case 96: done = attn_tma<96, true>(s, nullptr, rows, mslot, mpos, mdepth, depth_uniform, kv, slot_base, clamp, H, split, max_splits, O, part_o, part_ml, status, qkv, rope); break;
+    case 128: done = attn_tma<128, true>(s, nullptr, rows, mslot, mpos, mdepth, depth_uniform, kv, slot_base, clamp, H, split, max_splits, O, part_o, part_ml, status, qkv, rope); break;
+    default: return false;
+  }
+  if (done) attn_combine<__nv_bfloat16>(s, rows, mpos, H, hd, kv, split, max_splits, part_o, part_ml, O);
+  return done;
 }
 
 template <int HD>

@@ -80,7 +80,7 @@ static bool plan_layout(const cdb_model_desc* m, const cdb_sched_cfg* c, Layout*
   L->htrace = take(W * T * d * 4);
   L->estore = take(m->has_adapter ? W * d * 4 : 0);
   L->sprev = take(m->gate_kind == CDB_GATE_CONVERGENCE ? W * d * 4 : 0);  // s_{d-1} of each core row
-  L->rope = take((size_t)c->max_ctx * (hd / 2) * 8);
+  L->rope = take((size_t)L->max_blocks * 16 * (hd / 2) * 8);  // every position a block table can hold
   for (int i = 0; i < 5; ++i) {
     L->rows[i] = take(W * d * 4);
     L->meta[i] = take(W * 5 * 4);
@@ -406,11 +406,6 @@ class GpuExecutor : public Executor {
     decode_tiles_ = decode;
     norm<T>(X, lw.attn_norm, A, rows);
     int ns = gemm<T>(kEpiStore, A, d, lw.wqkv, nullptr, 3 * d, d, rows, QKV, nullptr, 3 * d, true);
-    int hr = prof_begin(x, 3);
-    for (int rr = repeat(3) ? 2 : 1; rr > 0; --rr)
-      launch_rope_kv<T>(s, ns ? GP : QKV, ns, rows, mslot, mpos, mdepth, depth_uniform, slot_base, clamp, Q, kv, H,
-                        hd, at<float2>(x, L.rope), st);
-    prof_end(x, hr, (double)rows * d * (12.0 + 3.0 * es), 0.0);  // q, k, v in; q, K, V rows out
     const int split = decode ? L.split : (1 << 30);
     // Split partials per (row, head): enough for the longest context in this
     // batch (maxL keys; the arena holds max_ctx), which also decides whether
@@ -418,28 +413,48 @@ class GpuExecutor : public Executor {
     const int msp = decode ? std::max(1, std::min(L.max_splits, maxL > 0 ? (maxL + split - 1) / split
                                                                          : L.max_splits))
                            : 1;
-    const int ha = prof_begin(x, decode ? 0 : 2);
-    // Exit gaps are filled at compaction, so every key of a row is read from
-    // the row's own slot.  Prefill chunks go through query tiles.
-    bool done = false;
-    if (!decode && sizeof(T) == 2 && pf_tiles_ > 0 && depth_uniform > 0)
-      done = launch_prefill_attention(s, (const __nv_bfloat16*)Q, L.R, at<int4>(x, L.ptiles), pf_tiles_, kv,
-                                      slot_base + (clamp ? std::min(depth_uniform, clamp) - 1 : 0), H, hd,
-                                      (__nv_bfloat16*)O, st);
-    if (!done)
-      for (int rr = repeat(0) ? 2 : 1; rr > 0; --rr)
-        launch_attention<T>(s, Q, rows, mslot, mpos, mdepth, depth_uniform, kv, slot_base, clamp, H, hd, split, msp,
-                            O, at<float>(x, L.part_o), at<float>(x, L.part_ml), st, true);
-    // Decode: each row reads each of its key rows (K and V, d elements each)
-    // once.  Prefill tiles: each tile reads the keys up to its last position
-    // once for all of its rows.  Plus q in, o out.
-    prof_end(x, ha, (done ? pf_key_rows_ : sumL) * 2.0 * d * es + 2.0 * rows * d * es, 4.0 * d * sumL);
+    // bf16 decode: RoPE and the KV write run inside the attention kernel,
+    // which reads q, k and v from the QKV partials.
+    bool fused = decode && sizeof(T) == 2 && attention_rope_fusable(kv, H, hd, split);
+    if (fused) {
+      const int ha = prof_begin(x, 0);
+      for (int rr = repeat(0) ? 2 : 1; rr > 0 && fused; --rr)
+        fused = launch_attention_rope(s, ns ? GP : QKV, ns, rows, mslot, mpos, mdepth, depth_uniform, kv, slot_base,
+                                      clamp, H, hd, split, msp, at<float2>(x, L.rope), (__nv_bfloat16*)O,
+                                      at<float>(x, L.part_o), at<float>(x, L.part_ml), st);
+      // Each row reads each of its key rows (K and V, d elements each) once,
+      // reads its q, k, v partials, writes its K, V rows and its output.
+      prof_end(x, ha, sumL * 2.0 * d * es + rows * d * (12.0 * std::max(ns, 1) + 3.0 * es), 4.0 * d * sumL);
+    }
+    if (!fused) {
+      int hr = prof_begin(x, 3);
+      for (int rr = repeat(3) ? 2 : 1; rr > 0; --rr)
+        launch_rope_kv<T>(s, ns ? GP : QKV, ns, rows, mslot, mpos, mdepth, depth_uniform, slot_base, clamp, Q, kv, H,
+                          hd, at<float2>(x, L.rope), st);
+      prof_end(x, hr, (double)rows * d * (12.0 + 3.0 * es), 0.0);  // q, k, v in; q, K, V rows out
+      const int ha = prof_begin(x, decode ? 0 : 2);
+      // Exit gaps are filled at compaction, so every key of a row is read from
+      // the row's own slot.  Prefill chunks go through query tiles.
+      bool done = false;
+      if (!decode && sizeof(T) == 2 && pf_tiles_ > 0 && depth_uniform > 0)
+        done = launch_prefill_attention(s, (const __nv_bfloat16*)Q, L.R, at<int4>(x, L.ptiles), pf_tiles_, kv,
+                                        slot_base + (clamp ? std::min(depth_uniform, clamp) - 1 : 0), H, hd,
+                                        (__nv_bfloat16*)O, st);
+      if (!done)
+        for (int rr = repeat(0) ? 2 : 1; rr > 0; --rr)
+          launch_attention<T>(s, Q, rows, mslot, mpos, mdepth, depth_uniform, kv, slot_base, clamp, H, hd, split, msp,
+                              O, at<float>(x, L.part_o), at<float>(x, L.part_ml), st, true);
+      // Decode: each row reads each of its key rows (K and V, d elements each)
+      // once.  Prefill tiles: each tile reads the keys up to its last position
+      // once for all of its rows.  Plus q in, o out.
+      prof_end(x, ha, (done ? pf_key_rows_ : sumL) * 2.0 * d * es + 2.0 * rows * d * es, 4.0 * d * sumL);
+    }
     ns = gemm<T>(kEpiResid, O, d, lw.wo, nullptr, d, d, rows, X, nullptr, d, true);
     if (ns) pend_ = Pending{X, rows, ns, 1};
     norm<T>(X, lw.mlp_norm, A, rows);
     ns = gemm<T>(kEpiSwiglu, A, d, lw.wg, lw.wu, f, d, rows, nullptr, Mid, f, true);
     if (ns) {
-      hr = prof_begin(x, 3);
+      const int hr = prof_begin(x, 3);
       for (int rr = repeat(3) ? 2 : 1; rr > 0; --rr) launch_swiglu_combine<T>(s, GP, ns, rows, f, Mid);
       prof_end(x, hr, (double)rows * f * (8.0 + es), 0.0);
     }
@@ -873,7 +888,7 @@ int cdb_init(const cdb_model_desc* m, const cdb_weights* w, const cdb_sched_cfg*
   CKI(cudaMemsetAsync(x->base + L.pool, 0xFF, L.etab - L.pool, x->cs));
   CKI(cudaMemsetAsync(x->base + L.etab, 0, L.total - L.etab, x->cs));
   CKI(cudaMemsetAsync(x->base + L.bt, 0xFF, (size_t)c->W * L.max_blocks * 4, x->cs));
-  launch_rope_table(x->cs, at<float2>(xp, L.rope), c->max_ctx, m->head_dim, m->rope_theta);
+  launch_rope_table(x->cs, at<float2>(xp, L.rope), L.max_blocks * 16, m->head_dim, m->rope_theta);
   CKI(cudaGetLastError());
   CKI(cudaStreamSynchronize(x->cs));
 #undef CKI

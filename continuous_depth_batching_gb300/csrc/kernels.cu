@@ -109,43 +109,6 @@ __global__ void k_prelude_finish(const float* __restrict__ Tp, RowMeta tm, int r
 // RMSNorm -> GEMM operand; adapter concat
 // ---------------------------------------------------------------------------
 
-// Split-K partials of a GEMM output: P[split][row][ld] with split stride ss;
-// their sum in split order (the reduction every consumer uses, so a value is
-// the same whichever kernel folds it).
-struct Parts {
-  const float* P;
-  int ns;     // number of partials (<= kGemmMaxSplits); 0 = nothing to fold
-  size_t ss;  // floats between consecutive splits
-  int ld;     // floats between consecutive rows
-  // Sum of columns c..c+3 of `row` (c and ld multiples of 4): every partial
-  // is loaded before the first add, then added in split order.  The loop is
-  // unrolled for at most S partials (S >= ns).
-  template <int S>
-  __device__ __forceinline__ float4 sum4_upto(int row, int c) const {
-    const float4* p = reinterpret_cast<const float4*>(P + (size_t)row * ld + c);
-    const size_t s4 = ss / 4;
-    float4 v[S];
-#pragma unroll
-    for (int q = 0; q < S; ++q) v[q] = q < ns ? p[q * s4] : make_float4(0.f, 0.f, 0.f, 0.f);
-    float4 g = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-    for (int q = 0; q < S; ++q)
-      if (q < ns) {
-        g.x += v[q].x;
-        g.y += v[q].y;
-        g.z += v[q].z;
-        g.w += v[q].w;
-      }
-    return g;
-  }
-  // The same sum; the unroll depth follows ns (uniform across the grid).
-  __device__ __forceinline__ float4 sum4(int row, int c) const {
-    if (ns <= 4) return sum4_upto<4>(row, c);
-    if (ns <= 8) return sum4_upto<8>(row, c);
-    return sum4_upto<kGemmMaxSplits>(row, c);
-  }
-};
-
 // Four consecutive elements in one access (8 bytes for bf16, 16 for fp32).
 template <typename T>
 __device__ __forceinline__ void store4(T* p, const T (&v)[4]);
@@ -322,6 +285,10 @@ __global__ void k_rope_kv(Parts qkv, int rows, const int* __restrict__ mslot,
   if (i >= rows) return;
   const int d = kv.d, half = hd / 2;
   const int pos = mpos[i];
+  if (pos < 0 || (pos >> 4) >= kv.max_blocks || mslot[i] < 0) {  // past the block table (and the RoPE table)
+    if (threadIdx.x == 0) atomicOr(status, kStatusBadRow);
+    return;
+  }
   const int r = depth_uniform > 0 ? depth_uniform : mdepth[i] + 1;
   const int blk = kv.bt[mslot[i] * kv.max_blocks + pos / 16];
   const int sl = slot_base + (clamp ? min(r, clamp) - 1 : 0);
@@ -354,8 +321,10 @@ __global__ void k_rope_kv(Parts qkv, int rows, const int* __restrict__ mslot,
     if (part < 2) {
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
-        lo[e] = from_f<T>(a_[e] * r[e].x - b_[e] * r[e].y);
-        hi[e] = from_f<T>(b_[e] * r[e].x + a_[e] * r[e].y);
+        float l, h;
+        rope_pair(a_[e], b_[e], r[e], l, h);
+        lo[e] = from_f<T>(l);
+        hi[e] = from_f<T>(h);
       }
     } else {
 #pragma unroll

@@ -130,6 +130,19 @@ void launch_attention(cudaStream_t s, const T* Q, int rows, const int* mslot, co
                       const int* mdepth, int depth_uniform, KvGeom kv, int slot_base,
                       int clamp, int H, int hd, int split, int max_splits, T* O,
                       float* part_o, float* part_ml, int* status, bool uniform);
+// The same decode attention (bf16, every key of a row from one slot) with the
+// RoPE / KV write of its rows folded in: q, k and v come from the QKV GEMM's
+// ns split-K partials [split][row][3d] (ns <= 1: the plain output), rotated
+// and rounded exactly as launch_rope_kv does; the token's K and V rows are
+// stored in the pool.  Returns false (nothing launched) for shapes the fused
+// kernel does not cover; the caller then runs launch_rope_kv and
+// launch_attention.  attention_rope_fusable: whether it covers this cache
+// geometry (decided once per engine, so every step takes the same path).
+bool attention_rope_fusable(KvGeom kv, int H, int hd, int split);
+bool launch_attention_rope(cudaStream_t s, const float* QKV, int ns, int rows, const int* mslot, const int* mpos,
+                           const int* mdepth, int depth_uniform, KvGeom kv, int slot_base, int clamp, int H, int hd,
+                           int split, int max_splits, const float2* rope, __nv_bfloat16* O, float* part_o,
+                           float* part_ml, int* status);
 
 // Causal prefill attention over query tiles (bf16, head_dim 32/64/96/128):
 // tiles[t] = (first row, rows <= prefill_tile_rows(hd), sequence slot,
@@ -168,6 +181,52 @@ void launch_gemm(cudaStream_t s, int epi, const T* A, int lda, const T* W, const
 // when the epilogue was applied in place, -1 when the shape is unsupported.
 // a_rows: rows allocated in A (TMA bounds).
 constexpr int kGemmMaxSplits = 16;
+
+// Split-K partials of a GEMM output: P[split][row][ld] with split stride ss;
+// their sum in split order (the reduction every consumer uses, so a value is
+// the same whichever kernel folds it).
+struct Parts {
+  const float* P;
+  int ns;     // number of partials (<= kGemmMaxSplits); 0 = nothing to fold
+  size_t ss;  // floats between consecutive splits
+  int ld;     // floats between consecutive rows
+  // Sum of columns c..c+3 of `row` (c and ld multiples of 4): every partial
+  // is loaded before the first add, then added in split order.  The loop is
+  // unrolled for at most S partials (S >= ns).
+  template <int S>
+  __device__ __forceinline__ float4 sum4_upto(int row, int c) const {
+    const float4* p = reinterpret_cast<const float4*>(P + (size_t)row * ld + c);
+    const size_t s4 = ss / 4;
+    float4 v[S];
+#pragma unroll
+    for (int q = 0; q < S; ++q) v[q] = q < ns ? p[q * s4] : make_float4(0.f, 0.f, 0.f, 0.f);
+    float4 g = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int q = 0; q < S; ++q)
+      if (q < ns) {
+        g.x += v[q].x;
+        g.y += v[q].y;
+        g.z += v[q].z;
+        g.w += v[q].w;
+      }
+    return g;
+  }
+  // The same sum; the unroll depth follows ns (uniform across the grid).
+  __device__ __forceinline__ float4 sum4(int row, int c) const {
+    if (ns <= 4) return sum4_upto<4>(row, c);
+    if (ns <= 8) return sum4_upto<8>(row, c);
+    return sum4_upto<kGemmMaxSplits>(row, c);
+  }
+};
+
+// Rotate-half RoPE of the pair (a, b) = (x_j, x_{j + hd/2}) by the angle whose
+// (cos, sin) is cs.  Both products are rounded before the add, so every kernel
+// that rotates a value gets the same bits.
+__device__ __forceinline__ void rope_pair(float a, float b, float2 cs, float& lo, float& hi) {
+  lo = __fsub_rn(__fmul_rn(a, cs.x), __fmul_rn(b, cs.y));
+  hi = __fadd_rn(__fmul_rn(b, cs.x), __fmul_rn(a, cs.y));
+}
+
 // Tilings: kTileSplit = 64-row tiles with split-K (decode batches below the
 // wide threshold); kTilePrefill = persistent, 256-row tiles (128 for SwiGLU)
 // when rows > 128; kTileWide = persistent, 128-row tiles at any row count
