@@ -155,28 +155,31 @@ __device__ __forceinline__ void epilogue16(const float* v, const float* u, int n
   }
 }
 
-template <int BN, bool SW>
+template <int BN, bool SW, bool DEEP>
 struct Cfg {
   static constexpr int A_BYTES = BM * BK * 2;
   static constexpr int B_BYTES = BN * BK * 2;
   static constexpr int STAGE = A_BYTES * (SW ? 2 : 1) + B_BYTES;
-  // Two CTAs per SM, so one CTA's prologue and epilogue overlap the other's
-  // main loop (decode: its weight stream; prefill: its MMAs).
-  static constexpr int BUDGET = BN == 64 ? 104 * 1024 : 100 * 1024;
+  // DEEP: one CTA per SM with a 160 KB ring (six weight slabs in flight, four
+  // for SwiGLU), for grids of at most one wave: a decode split streams only
+  // 5-11 slabs, so the bytes it requests before its first MMA set its
+  // bandwidth.  Otherwise two CTAs per SM, so one CTA's prologue and
+  // epilogue overlap the other's main loop.
+  static constexpr int BUDGET = DEEP ? 160 * 1024 : BN == 64 ? 104 * 1024 : 100 * 1024;
   static constexpr int STAGES = BUDGET / STAGE > 8 ? 8 : BUDGET / STAGE;
   static constexpr int ACC = BN * (SW ? 2 : 1);
   static constexpr int TMEM_COLS = ACC <= 32 ? 32 : ACC <= 64 ? 64 : ACC <= 128 ? 128 : ACC <= 256 ? 256 : 512;
   static constexpr int SMEM = STAGES * STAGE + 1024 + 256;
 };
 
-template <int BN, int EPI>
-__global__ void __launch_bounds__(128, 2)
+template <int BN, int EPI, bool DEEP>
+__global__ void __launch_bounds__(128, DEEP ? 1 : 2)
     k_gemm_tc(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmW2,
               const __grid_constant__ CUtensorMap tmA, int N, int K, int rows, int splits,
               float* __restrict__ Cf, __nv_bfloat16* __restrict__ Ct, int ldc, float* __restrict__ ws,
               int* status) {
   constexpr bool SW = EPI == kEpiSwiglu;
-  using C = Cfg<BN, SW>;
+  using C = Cfg<BN, SW, DEEP>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::STAGES * C::STAGE);
@@ -537,26 +540,37 @@ static const CUtensorMap* get_map(const void* p, uint64_t inner, uint64_t outer,
   return &cache.emplace(k, m).first->second;
 }
 
-template <int BN, int EPI>
-static bool launch_bn(cudaStream_t s, const __nv_bfloat16* A, int lda, int a_rows, const __nv_bfloat16* W,
-                      const __nv_bfloat16* W2, int N, int K, int rows, int splits, float* Cf,
-                      __nv_bfloat16* Ct, int ldc, float* ws, int* status) {
-  using C = Cfg<BN, EPI == kEpiSwiglu>;
-  const CUtensorMap* mw = get_map(W, K, N, (uint64_t)K * 2, BM);
-  const CUtensorMap* mw2 = EPI == kEpiSwiglu ? get_map(W2, K, N, (uint64_t)K * 2, BM) : mw;
-  const CUtensorMap* ma = get_map(A, K, a_rows, (uint64_t)lda * 2, BN);
-  if (!mw || !mw2 || !ma) return false;
+template <int BN, int EPI, bool DEEP>
+static bool launch_bn_cfg(cudaStream_t s, const CUtensorMap* mw, const CUtensorMap* mw2, const CUtensorMap* ma,
+                          int N, int K, int rows, int splits, float* Cf, __nv_bfloat16* Ct, int ldc, float* ws,
+                          int* status) {
+  using C = Cfg<BN, EPI == kEpiSwiglu, DEEP>;
   static bool attr[kMaxDevices] = {};
   const int dev = current_device();
   if (!attr[dev]) {
-    if (cudaFuncSetAttribute(k_gemm_tc<BN, EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) !=
+    if (cudaFuncSetAttribute(k_gemm_tc<BN, EPI, DEEP>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) !=
         cudaSuccess)
       return false;
     attr[dev] = true;
   }
   count_launch();
-  return launch_pdl(k_gemm_tc<BN, EPI>, dim3((N + BM - 1) / BM, (rows + BN - 1) / BN, splits), dim3(128), C::SMEM, s,
-                    *mw, *mw2, *ma, N, K, rows, splits, Cf, Ct, ldc, ws, status) == cudaSuccess;
+  return launch_pdl(k_gemm_tc<BN, EPI, DEEP>, dim3((N + BM - 1) / BM, (rows + BN - 1) / BN, splits), dim3(128),
+                    C::SMEM, s, *mw, *mw2, *ma, N, K, rows, splits, Cf, Ct, ldc, ws, status) == cudaSuccess;
+}
+
+// The ring depth changes neither the MMA order nor the split count, so a
+// row's result is the same whichever configuration runs.
+template <int BN, int EPI>
+static bool launch_bn(cudaStream_t s, const __nv_bfloat16* A, int lda, int a_rows, const __nv_bfloat16* W,
+                      const __nv_bfloat16* W2, int N, int K, int rows, int splits, float* Cf,
+                      __nv_bfloat16* Ct, int ldc, float* ws, int* status, int sms) {
+  const CUtensorMap* mw = get_map(W, K, N, (uint64_t)K * 2, BM);
+  const CUtensorMap* mw2 = EPI == kEpiSwiglu ? get_map(W2, K, N, (uint64_t)K * 2, BM) : mw;
+  const CUtensorMap* ma = get_map(A, K, a_rows, (uint64_t)lda * 2, BN);
+  if (!mw || !mw2 || !ma) return false;
+  const long long ctas = (long long)((N + BM - 1) / BM) * ((rows + BN - 1) / BN) * splits;
+  return ctas <= sms ? launch_bn_cfg<BN, EPI, true>(s, mw, mw2, ma, N, K, rows, splits, Cf, Ct, ldc, ws, status)
+                     : launch_bn_cfg<BN, EPI, false>(s, mw, mw2, ma, N, K, rows, splits, Cf, Ct, ldc, ws, status);
 }
 
 // Persistent prefill launch: min(tiles, max_ctas) CTAs of 192 threads.
@@ -598,15 +612,14 @@ static int sm_count() {
 }
 
 // Split count of a decode GEMM: at least four 64-element K slabs per split,
-// at most kGemmMaxSplits, and about two CTAs per SM for narrow weights (few
-// 128-row tiles) but one per SM for wide ones (at least 32 tiles), whose
-// consumers then fold half as many partials.  Depends only on the weight
-// shape (and the device), never on the number of rows.
+// at most kGemmMaxSplits, and about one CTA per SM for a 64-row tile of
+// activations.  Depends only on the weight shape (and the device), never on
+// the number of rows.
 int gemm_tc_splits(int N, int K, bool decode) {
   if (!decode) return 1;
   const int tiles = (N + tc::BM - 1) / tc::BM;
   const int KT = (K + tc::BK - 1) / tc::BK;
-  int s = (tiles >= 32 ? 1 : 2) * sm_count() / tiles;
+  int s = sm_count() / tiles;
   if (s > KT / 4) s = KT / 4;
   if (s > kGemmMaxSplits) s = kGemmMaxSplits;
   return s < 1 ? 1 : s;
@@ -626,9 +639,9 @@ int launch_gemm_tc(cudaStream_t s, int epi, const __nv_bfloat16* A, int lda, int
   bool ok;
   if (decode) {
     switch (epi) {
-      case kEpiStore: ok = tc::launch_bn<64, kEpiStore>(s, A, lda, a_rows, W, W2, N, K, rows, splits, Cf, Ct, ldc, P, status); break;
-      case kEpiResid: ok = tc::launch_bn<64, kEpiResid>(s, A, lda, a_rows, W, W2, N, K, rows, splits, Cf, Ct, ldc, P, status); break;
-      default: ok = tc::launch_bn<64, kEpiSwiglu>(s, A, lda, a_rows, W, W2, N, K, rows, splits, Cf, Ct, ldc, P, status); break;
+      case kEpiStore: ok = tc::launch_bn<64, kEpiStore>(s, A, lda, a_rows, W, W2, N, K, rows, splits, Cf, Ct, ldc, P, status, sm_count()); break;
+      case kEpiResid: ok = tc::launch_bn<64, kEpiResid>(s, A, lda, a_rows, W, W2, N, K, rows, splits, Cf, Ct, ldc, P, status, sm_count()); break;
+      default: ok = tc::launch_bn<64, kEpiSwiglu>(s, A, lda, a_rows, W, W2, N, K, rows, splits, Cf, Ct, ldc, P, status, sm_count()); break;
     }
   } else {
     // Persistent: one CTA per SM, double-buffered accumulators.  Prefill:
