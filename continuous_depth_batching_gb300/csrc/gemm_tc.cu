@@ -648,15 +648,22 @@ int launch_gemm_tc(cudaStream_t s, int epi, const __nv_bfloat16* A, int lda, int
     // 256-row tiles where one accumulator fits, 128-row tiles for SwiGLU.
     // Wide decode batches: 128-row tiles always.
     const bool wide = tiling == kTilePrefill && rows > 128;
+    // Wide decode batches, narrow weights (fewer than 32 tiles of 128
+    // features: the O and down projections): 64-row tiles, so the tiles
+    // outnumber the SMs.  Without split-K a row's result is the same for
+    // any tile width.
+    const bool narrow = tiling == kTileWide && (N + tc::BM - 1) / tc::BM < 32;
     const int sm = sm_count();
     switch (epi) {
       case kEpiStore:
-        ok = wide ? tc::launch_pf<256, kEpiStore>(s, A, lda, a_rows, W, W2, N, K, rows, Cf, Ct, ldc, sm, status)
-                  : tc::launch_pf<128, kEpiStore>(s, A, lda, a_rows, W, W2, N, K, rows, Cf, Ct, ldc, sm, status);
+        ok = wide     ? tc::launch_pf<256, kEpiStore>(s, A, lda, a_rows, W, W2, N, K, rows, Cf, Ct, ldc, sm, status)
+             : narrow ? tc::launch_pf<64, kEpiStore>(s, A, lda, a_rows, W, W2, N, K, rows, Cf, Ct, ldc, sm, status)
+                      : tc::launch_pf<128, kEpiStore>(s, A, lda, a_rows, W, W2, N, K, rows, Cf, Ct, ldc, sm, status);
         break;
       case kEpiResid:
-        ok = wide ? tc::launch_pf<256, kEpiResid>(s, A, lda, a_rows, W, W2, N, K, rows, Cf, Ct, ldc, sm, status)
-                  : tc::launch_pf<128, kEpiResid>(s, A, lda, a_rows, W, W2, N, K, rows, Cf, Ct, ldc, sm, status);
+        ok = wide     ? tc::launch_pf<256, kEpiResid>(s, A, lda, a_rows, W, W2, N, K, rows, Cf, Ct, ldc, sm, status)
+             : narrow ? tc::launch_pf<64, kEpiResid>(s, A, lda, a_rows, W, W2, N, K, rows, Cf, Ct, ldc, sm, status)
+                      : tc::launch_pf<128, kEpiResid>(s, A, lda, a_rows, W, W2, N, K, rows, Cf, Ct, ldc, sm, status);
         break;
       default: ok = tc::launch_pf<128, kEpiSwiglu>(s, A, lda, a_rows, W, W2, N, K, rows, Cf, Ct, ldc, sm, status); break;
     }

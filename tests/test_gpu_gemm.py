@@ -1,7 +1,8 @@
 """Tensor-core projection GEMM (include/cdb_testing.h) against a float64 product.
 
-Checks every epilogue (store, residual add, SwiGLU), both tilings (decode:
-64-row tiles with split-K fixed by the weight shape; prefill: 128-row tiles),
+Checks every epilogue (store, residual add, SwiGLU), every tensor-core tiling
+(decode: 64-row tiles with split-K fixed by the weight shape; prefill: 128-
+and 256-row tiles; wide decode: 128-row tiles, 64 for narrow weights),
 ragged N and K tails, the split-K shapes of the Ouro-shaped core, agreement
 with the CUDA-core kernel, and that a row's result does not depend on how
 many other rows are in the batch (bit-exact).
@@ -59,7 +60,7 @@ SHAPES = [(5, 256, 192), (7, 200, 200), (64, 6144, 2048), (64, 2048, 5632), (33,
 
 
 @pytest.mark.parametrize("rows,N,K", SHAPES)
-@pytest.mark.parametrize("tiling", [0, 1])
+@pytest.mark.parametrize("tiling", [0, 1, 3])
 def test_store_and_residual(L, rows, N, K, tiling):
     import torch
     A = rnd(rows, K, seed=1)
@@ -73,7 +74,7 @@ def test_store_and_residual(L, rows, N, K, tiling):
 
 
 @pytest.mark.parametrize("rows,N,K", [(5, 256, 192), (64, 5632, 2048), (200, 300, 128)])
-@pytest.mark.parametrize("tiling", [0, 1])
+@pytest.mark.parametrize("tiling", [0, 1, 3])
 def test_swiglu(L, rows, N, K, tiling):
     import torch
     A = rnd(rows, K, seed=3)
@@ -96,10 +97,12 @@ def test_matches_cuda_core_kernel(L):
 
 
 @pytest.mark.parametrize("N,K", [(6144, 2048), (2048, 5632), (49152, 2048)])
-def test_row_result_independent_of_batch(L, N, K):
-    A = rnd(64, K, seed=8)
+@pytest.mark.parametrize("tiling", [0, 3])
+def test_row_result_independent_of_batch(L, N, K, tiling):
+    rows = 64 if tiling == 0 else 300
+    A = rnd(rows, K, seed=8)
     W = rnd(N, K, std=1.0 / np.sqrt(K), seed=9)
-    full, _ = run(L, 0, 0, A, W, a_rows=64)
+    full, _ = run(L, 0, tiling, A, W, a_rows=rows)
     for r in (1, 17):
-        part, _ = run(L, 0, 0, A[:r].contiguous(), W, a_rows=64)
+        part, _ = run(L, 0, tiling, A[:r].contiguous(), W, a_rows=rows)
         assert (part == full[:r]).all().item(), "row results must not depend on batch size"
