@@ -422,9 +422,10 @@ class GpuExecutor : public Executor {
         fused = launch_attention_rope(s, ns ? GP : QKV, ns, rows, mslot, mpos, mdepth, depth_uniform, kv, slot_base,
                                       clamp, H, hd, split, msp, at<float2>(x, L.rope), (__nv_bfloat16*)O,
                                       at<float>(x, L.part_o), at<float>(x, L.part_ml), st);
-      // Each row reads each of its key rows (K and V, d elements each) once,
-      // reads its q, k, v partials, writes its K, V rows and its output.
-      prof_end(x, ha, sumL * 2.0 * d * es + rows * d * (12.0 * std::max(ns, 1) + 3.0 * es), 4.0 * d * sumL);
+      // Algorithmic bytes: each row reads each of its key rows (K and V, d
+      // elements each) once and writes its own K and V rows and its output
+      // (the q, k, v partials it folds are the split-K GEMM's L2 traffic).
+      prof_end(x, ha, sumL * 2.0 * d * es + rows * d * 3.0 * es, 4.0 * d * sumL);
     }
     if (!fused) {
       int hr = prof_begin(x, 3);
