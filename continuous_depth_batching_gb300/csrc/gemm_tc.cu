@@ -166,6 +166,7 @@ struct Cfg {
   // bandwidth.  Otherwise two CTAs per SM, so one CTA's prologue and
   // epilogue overlap the other's main loop.
   static constexpr int BUDGET = DEEP ? 160 * 1024 : BN == 64 ? 104 * 1024 : 100 * 1024;
+  static_assert(DEEP || BN < 256, "256-row tiles run one CTA per SM (their SwiGLU accumulators fill TMEM)");
   static constexpr int STAGES = BUDGET / STAGE > 8 ? 8 : BUDGET / STAGE;
   static constexpr int ACC = BN * (SW ? 2 : 1);
   static constexpr int TMEM_COLS = ACC <= 32 ? 32 : ACC <= 64 ? 64 : ACC <= 128 ? 128 : ACC <= 256 ? 256 : 512;
@@ -569,8 +570,13 @@ static bool launch_bn(cudaStream_t s, const __nv_bfloat16* A, int lda, int a_row
   const CUtensorMap* ma = get_map(A, K, a_rows, (uint64_t)lda * 2, BN);
   if (!mw || !mw2 || !ma) return false;
   const long long ctas = (long long)((N + BM - 1) / BM) * ((rows + BN - 1) / BN) * splits;
-  return ctas <= sms ? launch_bn_cfg<BN, EPI, true>(s, mw, mw2, ma, N, K, rows, splits, Cf, Ct, ldc, ws, status)
-                     : launch_bn_cfg<BN, EPI, false>(s, mw, mw2, ma, N, K, rows, splits, Cf, Ct, ldc, ws, status);
+  if constexpr (BN == 256) {
+    if (ctas > sms) return false;  // the caller takes 256-row tiles only for one-wave grids
+    return launch_bn_cfg<BN, EPI, true>(s, mw, mw2, ma, N, K, rows, splits, Cf, Ct, ldc, ws, status);
+  } else {
+    return ctas <= sms ? launch_bn_cfg<BN, EPI, true>(s, mw, mw2, ma, N, K, rows, splits, Cf, Ct, ldc, ws, status)
+                       : launch_bn_cfg<BN, EPI, false>(s, mw, mw2, ma, N, K, rows, splits, Cf, Ct, ldc, ws, status);
+  }
 }
 
 // Persistent prefill launch: min(tiles, max_ctas) CTAs of 192 threads.
@@ -638,11 +644,29 @@ int launch_gemm_tc(cudaStream_t s, int epi, const __nv_bfloat16* A, int lda, int
   float* P = splits > 1 ? ws : nullptr;
   bool ok;
   if (decode) {
-    switch (epi) {
-      case kEpiStore: ok = tc::launch_bn<64, kEpiStore>(s, A, lda, a_rows, W, W2, N, K, rows, splits, Cf, Ct, ldc, P, status, sm_count()); break;
-      case kEpiResid: ok = tc::launch_bn<64, kEpiResid>(s, A, lda, a_rows, W, W2, N, K, rows, splits, Cf, Ct, ldc, P, status, sm_count()); break;
-      default: ok = tc::launch_bn<64, kEpiSwiglu>(s, A, lda, a_rows, W, W2, N, K, rows, splits, Cf, Ct, ldc, P, status, sm_count()); break;
+    // Activation tile height: the smallest of 64, 128 and 256 rows that holds
+    // the batch, while the grid stays one wave (else 128-row tiles).  The
+    // split count comes from the weight shape alone and a tile's height does
+    // not change the order in which a row's products are summed, so a row's
+    // result is the same for every batch size.
+    const int sm = sm_count();
+    const long long one_wave = (long long)((N + tc::BM - 1) / tc::BM) * splits;
+    int bn = rows <= 64 ? 64 : rows <= 128 ? 128 : rows <= 256 ? 256 : 128;
+    if (bn == 256 && one_wave > sm) bn = 128;
+#define CDB_BN(B)                                                                                                \
+  switch (epi) {                                                                                                 \
+    case kEpiStore: ok = tc::launch_bn<B, kEpiStore>(s, A, lda, a_rows, W, W2, N, K, rows, splits, Cf, Ct, ldc, P, status, sm); break; \
+    case kEpiResid: ok = tc::launch_bn<B, kEpiResid>(s, A, lda, a_rows, W, W2, N, K, rows, splits, Cf, Ct, ldc, P, status, sm); break; \
+    default: ok = tc::launch_bn<B, kEpiSwiglu>(s, A, lda, a_rows, W, W2, N, K, rows, splits, Cf, Ct, ldc, P, status, sm); break; \
+  }
+    if (bn == 64) {
+      CDB_BN(64)
+    } else if (bn == 128) {
+      CDB_BN(128)
+    } else {
+      CDB_BN(256)
     }
+#undef CDB_BN
   } else {
     // Persistent: one CTA per SM, double-buffered accumulators.  Prefill:
     // 256-row tiles where one accumulator fits, 128-row tiles for SwiGLU.

@@ -16,7 +16,8 @@ extern "C" {
  * fp32 accumulation, bf16 A and W (row-major, device pointers).
  *   epi 0: Cf[r][c] = acc (fp32 out)      epi 1: Cf[r][c] += acc
  *   epi 2: Ct[r][c] = bf16(silu(A.W^T) * (A.W2^T))   (SwiGLU, bf16 out)
- *   tiling 0: tensor cores, decode tiles (64 rows, split-K fixed by N and K;
+ *   tiling 0: tensor cores, decode tiles (64, 128 or 256 rows by the batch,
+ *             split-K fixed by N and K;
  *             the fp32 partials are summed in split order by a second kernel,
  *             as the engine's consumer kernels do, then the epilogue applied)
  *   tiling 1: tensor cores, persistent prefill tiles (256 rows, 128 for

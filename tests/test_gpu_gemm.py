@@ -1,8 +1,9 @@
 """Tensor-core projection GEMM (include/cdb_testing.h) against a float64 product.
 
 Checks every epilogue (store, residual add, SwiGLU), every tensor-core tiling
-(decode: 64-row tiles with split-K fixed by the weight shape; prefill: 128-
-and 256-row tiles; wide decode: 128-row tiles, 64 for narrow weights),
+(decode: 64-, 128- or 256-row tiles with split-K fixed by the weight shape;
+prefill: 128- and 256-row tiles; wide decode: 128-row tiles, 64 for narrow
+weights),
 ragged N and K tails, the split-K shapes of the Ouro-shaped core, agreement
 with the CUDA-core kernel, and that a row's result does not depend on how
 many other rows are in the batch (bit-exact).
@@ -56,7 +57,8 @@ def rnd(*shape, std=1.0, seed=0):
     return (torch.randn(*shape, generator=g) * std).to(torch.bfloat16).cuda()
 
 
-SHAPES = [(5, 256, 192), (7, 200, 200), (64, 6144, 2048), (64, 2048, 5632), (33, 384, 1000), (300, 384, 256)]
+SHAPES = [(5, 256, 192), (7, 200, 200), (64, 6144, 2048), (64, 2048, 5632), (33, 384, 1000), (300, 384, 256),
+          (100, 6144, 2048), (200, 2048, 5632)]
 
 
 @pytest.mark.parametrize("rows,N,K", SHAPES)
@@ -99,10 +101,12 @@ def test_matches_cuda_core_kernel(L):
 @pytest.mark.parametrize("N,K", [(6144, 2048), (2048, 5632), (49152, 2048)])
 @pytest.mark.parametrize("tiling", [0, 3])
 def test_row_result_independent_of_batch(L, N, K, tiling):
-    rows = 64 if tiling == 0 else 300
+    # Decode tiling: 200 rows run on 256-row tiles, 1-64 rows on 64-row tiles
+    # and 100 on 128-row tiles; the split count is the same for all of them.
+    rows = 200 if tiling == 0 else 300
     A = rnd(rows, K, seed=8)
     W = rnd(N, K, std=1.0 / np.sqrt(K), seed=9)
     full, _ = run(L, 0, tiling, A, W, a_rows=rows)
-    for r in (1, 17):
+    for r in (1, 17, 64, 100):
         part, _ = run(L, 0, tiling, A[:r].contiguous(), W, a_rows=rows)
         assert (part == full[:r]).all().item(), "row results must not depend on batch size"
