@@ -590,7 +590,10 @@ __global__ void __launch_bounds__((attn::kWarps + 1) * 32)
 // ---------------------------------------------------------------------------
 namespace attn {
 
-template <int HD>
+// NSTG: pages in flight per CTA (two at three CTAs per SM; six when the grid
+// has no more CTAs than the GPU has SMs, i.e. small decode batches, whose
+// few CTAs each walk a split's pages as a latency chain).
+template <int HD, int NSTG = 2>
 struct TmaGeo {
   static constexpr int SWB = HD % 64 == 0 ? 128 : 64;  // swizzle span = bytes of one slice row
   static constexpr int XW = SWB / 2;                    // elements per slice
@@ -600,7 +603,7 @@ struct TmaGeo {
   static constexpr int KREG = NX * SLICE;               // K (or V) of one page
   static constexpr int QB = kWarps * HD * 2;            // q rows of the item
   static constexpr int STAGE = (2 * KREG + QB + 1023) / 1024 * 1024;
-  static constexpr int NS = 2;
+  static constexpr int NS = NSTG;
   static constexpr size_t SMEM = 1024 + (size_t)NS * STAGE + NS * (2 * 8 + sizeof(StageMeta));
   // Fused RoPE / KV write: q, k and v rows (bf16) of each consumer warp's head.
   static constexpr size_t XOFF = ((size_t)NS * STAGE + NS * (2 * 8 + sizeof(StageMeta)) + 15) / 16 * 16;
@@ -639,14 +642,14 @@ __device__ __forceinline__ uint32_t swz(uint32_t slice, int row, int c) {
 // last split also forms the token's own K and V rows: it stores them in the
 // pool for later steps and writes them into the tile of its last page, whose
 // copy from the pool may predate them.  Same arithmetic as k_rope_kv.
-template <int HD, bool FUSE>
+template <int HD, bool FUSE, int NSTG>
 __global__ void __launch_bounds__((attn::kWarps + 1) * 32)
     k_attn_tma(const __grid_constant__ CUtensorMap tm, const __nv_bfloat16* __restrict__ Q, int rows,
                const int* __restrict__ mslot, const int* __restrict__ mpos, const int* __restrict__ mdepth,
                int depth_uniform, KvGeom kv, int slot_base, int clamp, int H, int split, int max_splits,
                __nv_bfloat16* __restrict__ O, float* __restrict__ part_o, float* __restrict__ part_ml,
                int* status, Parts qkv, const float2* __restrict__ rope) {
-  using Gm = attn::TmaGeo<HD>;
+  using Gm = attn::TmaGeo<HD, NSTG>;
   constexpr int G = attn::kWarps, NS = Gm::NS, NT = HD / 16;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -1237,30 +1240,57 @@ __global__ void k_attn_combine(int rows, const int* __restrict__ mpos, int H, in
 
 // Uniform-slot TMA path; false when the shape or pool does not fit it.
 // FUSE: q, k and v from the QKV partials (see k_attn_tma), Q unused.
-template <int HD, bool FUSE>
-static bool attn_tma(cudaStream_t s, const __nv_bfloat16* Q, int rows, const int* mslot, const int* mpos,
-                     const int* mdepth, int depth_uniform, KvGeom kv, int slot_base, int clamp, int H, int split,
-                     int max_splits, __nv_bfloat16* O, float* part_o, float* part_ml, int* status, Parts qkv,
-                     const float2* rope) {
-  using Gm = attn::TmaGeo<HD>;
+template <int HD, bool FUSE, int NSTG>
+static bool attn_tma_ns(cudaStream_t s, const CUtensorMap* tm, const __nv_bfloat16* Q, int rows, const int* mslot,
+                        const int* mpos, const int* mdepth, int depth_uniform, KvGeom kv, int slot_base, int clamp,
+                        int H, int split, int max_splits, __nv_bfloat16* O, float* part_o, float* part_ml,
+                        int* status, Parts qkv, const float2* rope) {
+  using Gm = attn::TmaGeo<HD, NSTG>;
   constexpr size_t smem = FUSE ? Gm::SMEM_FUSED : Gm::SMEM;
-  const uint64_t pool_rows = (uint64_t)kv.kv_blocks * kv.nsl * 2 * H * 16;
-  if (pool_rows + 16 * attn::kWarps >= (1ull << 31)) return false;  // tile row coordinates are int32
-  const CUtensorMap* tm = tmap_bf16_2d(kv.pool, HD, pool_rows, (uint64_t)HD * 2, Gm::XW, Gm::ROWS, Gm::SWB);
-  if (!tm) return false;
   static bool set[kMaxDevices] = {};
   const int dev = current_device();
   if (!set[dev]) {
-    if (cudaFuncSetAttribute(k_attn_tma<HD, FUSE>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
+    if (cudaFuncSetAttribute(k_attn_tma<HD, FUSE, NSTG>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
         cudaSuccess)
       return false;
     set[dev] = true;
   }
   dim3 grid(max_splits, (H + attn::kWarps - 1) / attn::kWarps, rows);
   count_launch();
-  launch_pdl(k_attn_tma<HD, FUSE>, grid, dim3((attn::kWarps + 1) * 32), smem, s, *tm, Q, rows, mslot, mpos, mdepth,
-             depth_uniform, kv, slot_base, clamp, H, split, max_splits, O, part_o, part_ml, status, qkv, rope);
+  launch_pdl(k_attn_tma<HD, FUSE, NSTG>, grid, dim3((attn::kWarps + 1) * 32), smem, s, *tm, Q, rows, mslot, mpos,
+             mdepth, depth_uniform, kv, slot_base, clamp, H, split, max_splits, O, part_o, part_ml, status, qkv, rope);
   return true;
+}
+
+static int attn_sm_count() {
+  static int n[kMaxDevices] = {};
+  const int dev = current_device();
+  if (!n[dev]) {
+    int v = 0;
+    if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || v <= 0) v = 1;
+    n[dev] = v;
+  }
+  return n[dev];
+}
+
+// The ring depth changes neither the order in which a CTA takes its pages
+// nor their arithmetic, so a row's result is the same with either.
+template <int HD, bool FUSE>
+static bool attn_tma(cudaStream_t s, const __nv_bfloat16* Q, int rows, const int* mslot, const int* mpos,
+                     const int* mdepth, int depth_uniform, KvGeom kv, int slot_base, int clamp, int H, int split,
+                     int max_splits, __nv_bfloat16* O, float* part_o, float* part_ml, int* status, Parts qkv,
+                     const float2* rope) {
+  using Gm = attn::TmaGeo<HD>;
+  const uint64_t pool_rows = (uint64_t)kv.kv_blocks * kv.nsl * 2 * H * 16;
+  if (pool_rows + 16 * attn::kWarps >= (1ull << 31)) return false;  // tile row coordinates are int32
+  const CUtensorMap* tm = tmap_bf16_2d(kv.pool, HD, pool_rows, (uint64_t)HD * 2, Gm::XW, Gm::ROWS, Gm::SWB);
+  if (!tm) return false;
+  const long long ctas = (long long)max_splits * ((H + attn::kWarps - 1) / attn::kWarps) * rows;
+  if (ctas <= attn_sm_count())
+    return attn_tma_ns<HD, FUSE, 6>(s, tm, Q, rows, mslot, mpos, mdepth, depth_uniform, kv, slot_base, clamp, H, split,
+                                    max_splits, O, part_o, part_ml, status, qkv, rope);
+  return attn_tma_ns<HD, FUSE, 2>(s, tm, Q, rows, mslot, mpos, mdepth, depth_uniform, kv, slot_base, clamp, H, split,
+                                  max_splits, O, part_o, part_ml, status, qkv, rope);
 }
 
 // Merge of the split partials (rows whose keys span more than one split).
