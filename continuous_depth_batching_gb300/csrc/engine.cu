@@ -579,6 +579,20 @@ class GpuExecutor : public Executor {
     if ((rc = upload(x, ls, a.data(), n * 4)) < 0) return rc;
     if ((rc = upload(x, lt, b.data(), n * 4)) < 0) return rc;
     if ((rc = upload(x, lp, c.data(), n * 4)) < 0) return rc;
+    if (x->m.n_prelude == 0 && !x->m.has_adapter) {
+      // No prelude layers: the embeddings are the refill rows themselves.
+      RowMeta pm = meta_at(x, L.meta[2]);
+      pm.slot += p.dst_off;
+      pm.pos += p.dst_off;
+      pm.t += p.dst_off;
+      pm.depth += p.dst_off;
+      pm.pend += p.dst_off;
+      launch_embed_prelude<T>(x->cs, (const T*)x->embed, d, x->m.vocab, ls, lt, lp, n, at<int>(x, L.out_tok),
+                              x->c.max_new_cap, at<float>(x, L.rows[2]) + (size_t)p.dst_off * d, pm, geom(),
+                              x->m.r_max, at<int>(x, L.status));
+      CK(cudaGetLastError());
+      return CDB_OK;
+    }
     float* Tp = at<float>(x, L.rows[4]);
     RowMeta tm = meta_at(x, L.meta[4]);
     launch_embed_prelude<T>(x->cs, (const T*)x->embed, d, x->m.vocab, ls, lt, lp, n, at<int>(x, L.out_tok),

@@ -572,9 +572,9 @@ __global__ void k_argmax(const float* __restrict__ logits, int rows, int V, RowM
       bi = j;
     }
   };
-  if ((V & 3) == 0) {  // rows are 16-byte aligned: four logits per load, all loads in flight
+  if ((V & 3) == 0) {  // rows are 16-byte aligned: four logits per load, eight loads in flight
     const float4* lg4 = reinterpret_cast<const float4*>(lg);
-#pragma unroll 4
+#pragma unroll 8
     for (int j = threadIdx.x; j < V / 4; j += blockDim.x) {
       const float4 v = lg4[j];
       take(v.x, 4 * j);
