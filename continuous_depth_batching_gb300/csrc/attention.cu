@@ -1176,8 +1176,11 @@ template <typename T>
 __global__ void k_attn_combine(int rows, const int* __restrict__ mpos, int H, int HDv, int d, int split,
                                int max_splits, int max_keys, const float* __restrict__ part_o,
                                const float* __restrict__ part_ml, T* __restrict__ O) {
-  pdl_wait();
+  // Trigger first: the O projection that follows reads only its weights
+  // before its own wait, so its CTAs can start streaming them on SMs the
+  // attention kernel's tail has freed.
   pdl_trigger();
+  pdl_wait();
   const int lane = threadIdx.x & 31;
   const int item = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   const int row = item / H, h = item % H;

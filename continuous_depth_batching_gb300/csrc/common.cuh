@@ -21,7 +21,10 @@ inline int current_device() {
 // calls pdl_wait() before its first access to memory another kernel writes
 // (and before any global write), which returns once the previous grid has
 // completed and its writes are visible.  pdl_trigger() lets the next kernel
-// be scheduled early (it will itself wait).
+// be scheduled early (it will itself wait).  Kernels trigger after their
+// wait, except where noted (the split-KV combine): a kernel may trigger first
+// only if the kernel after it touches nothing but immutable data before its
+// own wait.
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
