@@ -287,7 +287,7 @@ def live_core_costs(eng, stream, binding, n_steps):
            "boundary_calls_per_core_step": {k: len(v) / max(n_core, 1) for k, v in bound.items()}}
     for c in classes[1:]:
         out[c] = mean[c] - base
-    out["rowwise_note"] = "RoPE + KV write and the SwiGLU combine; RMSNorm folds are in other"
+    out["rowwise_note"] = "the SwiGLU combine (bf16 decode runs RoPE and the KV write inside attention); RMSNorm folds are in other"
     out["other"] = base - sum(out[c] for c in classes[1:])
     return out
 
