@@ -113,6 +113,7 @@ def lib(path: str | None = None) -> C.CDLL:
     L.cdb_last_error.restype = C.c_char_p
     L.cdb_trace_enable.argtypes = [C.c_void_p, C.c_int]
     L.cdb_profile_enable.argtypes = [C.c_void_p, C.c_int]
+    L.cdb_test_kv_pool.argtypes = [C.c_void_p, C.POINTER(C.c_void_p), C.POINTER(C.c_int), C.POINTER(C.c_int)]
     L.cdb_profile_repeat.argtypes = [C.c_void_p, C.c_int]
     L.cdb_profile_read.argtypes = [C.c_void_p, C.POINTER(KernelStat), C.c_int, C.POINTER(C.c_int)]
     L.cdb_kernel_launches.restype = C.c_int64
@@ -324,6 +325,19 @@ class Engine:
         a, b = C.c_int64(), C.c_int64()
         self._check(self.L.cdb_io_bytes(self.ctx, C.byref(a), C.byref(b)))
         return a.value, b.value
+
+    def kv_pool(self):
+        """The KV cache in the arena as a tensor view [kv_blocks, n_kv_slots, 2, H, 16, hd]."""
+        import torch
+        p, nb, ns = C.c_void_p(), C.c_int(), C.c_int()
+        self._check(self.L.cdb_test_kv_pool(self.ctx, C.byref(p), C.byref(nb), C.byref(ns)))
+        s = self.shape
+        es = 2 if s.dtype == "bf16" else 4
+        n = nb.value * ns.value * 2 * s.n_heads * 16 * s.head_dim
+        off = p.value - self.arena.data_ptr()
+        raw = self.arena[off:off + n * es]
+        t = raw.view(torch.bfloat16 if es == 2 else torch.float32)
+        return t.view(nb.value, ns.value, 2, s.n_heads, 16, s.head_dim)
 
     def trace_enable(self, on=True):
         self._check(self.L.cdb_trace_enable(self.ctx, int(on)))

@@ -1212,6 +1212,14 @@ int cdb_test_attention_prefill(const void* q, int rows, const int32_t* row_slot,
   return st ? CDB_ERR_DEVICE_BOUNDS : CDB_OK;
 }
 
+int cdb_test_kv_pool(const cdb_ctx* x, void** pool, int* kv_blocks, int* n_kv_slots) {
+  if (!x || !pool || !kv_blocks || !n_kv_slots) return CDB_ERR_ARG;
+  *pool = x->base + x->L.pool;
+  *kv_blocks = x->c.kv_blocks;
+  *n_kv_slots = x->L.nsl;
+  return CDB_OK;
+}
+
 int cdb_test_attention(const void* q, int rows, const int32_t* slot, const int32_t* pos, const int32_t* depth,
                        const void* kv_pool, const int32_t* block_table, int max_blocks, const uint8_t* exit_table,
                        int kv_blocks, int n_kv_slots, int slot_base, int n_heads, int head_dim, int dtype, int split,

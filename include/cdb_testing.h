@@ -8,6 +8,8 @@
 #include <stddef.h>
 #include <stdint.h>
 
+typedef struct cdb_ctx cdb_ctx; /* opaque engine context (cdb.h) */
+
 #ifdef __cplusplus
 extern "C" {
 #endif
@@ -115,6 +117,19 @@ int cdb_test_attention_prefill(const void *q, int rows, const int32_t *row_slot,
  * streams, other host threads) race; issue them one after another.  A row
  * whose position lies past max_ctx's block table or split partials is skipped
  * and the call returns CDB_ERR_DEVICE_BOUNDS.  Synchronizes the stream. */
+/* The KV cache inside an engine's arena, so that tests can read back what the
+ * engine cached ("Depth-adaptive Inference of Looped Language Models via
+ * Continuous Depth Batching", §4.2: one slot per core layer and loop step).
+ * *pool: device pointer to [kv_blocks][n_kv_slots][2][n_heads][16][head_dim]
+ * elements of the model's dtype (K then V per block and slot, each head's 16
+ * positions contiguous); core layer l, loop step r lives in slot
+ * n_prelude + l * s + min(r, s) - 1 (s the model's kv_slots, r_max for the
+ * depth-indexed cache).  A sequence's i-th block of 16 positions is the pool
+ * block its block table names; the engine hands out free blocks in increasing
+ * order, so the first sequence admitted to a new engine holds blocks 0, 1, ...
+ * The memory belongs to the caller's arena.  Returns CDB_OK or CDB_ERR_ARG. */
+int cdb_test_kv_pool(const cdb_ctx *ctx, void **pool, int *kv_blocks, int *n_kv_slots);
+
 int cdb_attention_noalloc(const void *q, int rows, const int32_t *slot, const int32_t *pos,
                           const int32_t *depth, const void *kv_pool, const int32_t *block_table,
                           int max_blocks, const uint8_t *exit_table, int kv_blocks, int n_kv_slots,
