@@ -339,7 +339,8 @@ struct PfCfg {
   static constexpr int STAGE = A_BYTES * (SW ? 2 : 1) + B_BYTES;
   static constexpr int STAGES = (196 * 1024) / STAGE > 8 ? 8 : (196 * 1024) / STAGE;
   static constexpr int ACC = BN * (SW ? 2 : 1);  // TMEM columns of one tile's accumulators
-  static constexpr int TMEM_COLS = 2 * ACC;      // two buffers
+  // Two buffers; an allocation is a power of two of at least 32 columns.
+  static constexpr int TMEM_COLS = 2 * ACC <= 128 ? 128 : 2 * ACC <= 256 ? 256 : 512;
   static constexpr int SMEM = STAGES * STAGE + 1024 + 256;
   static_assert(TMEM_COLS <= 512, "two accumulator buffers must fit TMEM");
 };
@@ -670,25 +671,33 @@ int launch_gemm_tc(cudaStream_t s, int epi, const __nv_bfloat16* A, int lda, int
   } else {
     // Persistent: one CTA per SM, double-buffered accumulators.  Prefill:
     // 256-row tiles where one accumulator fits, 128-row tiles for SwiGLU.
-    // Wide decode batches: 128-row tiles always.
     const bool wide = tiling == kTilePrefill && rows > 128;
     // Wide decode batches, narrow weights (fewer than 32 tiles of 128
     // features: the O and down projections): 64-row tiles, so the tiles
-    // outnumber the SMs.  Without split-K a row's result is the same for
-    // any tile width.
-    const bool narrow = tiling == kTileWide && (N + tc::BM - 1) / tc::BM < 32;
+    // outnumber the SMs.  Other wide decode GEMMs: the smallest of 128, 192
+    // and 256 rows whose tiles fit one wave of CTAs (else 128), so that each
+    // weight tile is read by fewer CTAs.  Without split-K a row's result is
+    // the same for any tile height.
     const int sm = sm_count();
+    const long long tiles_n = (N + tc::BM - 1) / tc::BM;
+    const bool narrow = tiling == kTileWide && tiles_n < 32;
+    int bn = wide ? 256 : narrow ? 64 : 128;
+    if (tiling == kTileWide && !narrow) {
+      for (int b : {128, 192, 256})
+        if (tiles_n * ((rows + b - 1) / b) <= sm) {
+          bn = b;
+          break;
+        }
+    }
+#define CDB_PF(E)                                                                                          \
+  ok = bn == 64    ? tc::launch_pf<64, E>(s, A, lda, a_rows, W, W2, N, K, rows, Cf, Ct, ldc, sm, status)  \
+       : bn == 192 ? tc::launch_pf<192, E>(s, A, lda, a_rows, W, W2, N, K, rows, Cf, Ct, ldc, sm, status) \
+       : bn == 256 ? tc::launch_pf<256, E>(s, A, lda, a_rows, W, W2, N, K, rows, Cf, Ct, ldc, sm, status) \
+                   : tc::launch_pf<128, E>(s, A, lda, a_rows, W, W2, N, K, rows, Cf, Ct, ldc, sm, status);
     switch (epi) {
-      case kEpiStore:
-        ok = wide     ? tc::launch_pf<256, kEpiStore>(s, A, lda, a_rows, W, W2, N, K, rows, Cf, Ct, ldc, sm, status)
-             : narrow ? tc::launch_pf<64, kEpiStore>(s, A, lda, a_rows, W, W2, N, K, rows, Cf, Ct, ldc, sm, status)
-                      : tc::launch_pf<128, kEpiStore>(s, A, lda, a_rows, W, W2, N, K, rows, Cf, Ct, ldc, sm, status);
-        break;
-      case kEpiResid:
-        ok = wide     ? tc::launch_pf<256, kEpiResid>(s, A, lda, a_rows, W, W2, N, K, rows, Cf, Ct, ldc, sm, status)
-             : narrow ? tc::launch_pf<64, kEpiResid>(s, A, lda, a_rows, W, W2, N, K, rows, Cf, Ct, ldc, sm, status)
-                      : tc::launch_pf<128, kEpiResid>(s, A, lda, a_rows, W, W2, N, K, rows, Cf, Ct, ldc, sm, status);
-        break;
+      case kEpiStore: CDB_PF(kEpiStore) break;
+      case kEpiResid: CDB_PF(kEpiResid) break;
+#undef CDB_PF
       default: ok = tc::launch_pf<128, kEpiSwiglu>(s, A, lda, a_rows, W, W2, N, K, rows, Cf, Ct, ldc, sm, status); break;
     }
   }

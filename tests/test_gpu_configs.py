@@ -189,9 +189,9 @@ def test_step_delta_repeats_leave_results_unchanged():
 
 def test_wide_engines_agree_bit_exactly():
     """Engines of 384 or more slots run the projections without split-K (the
-    persistent GEMM, 128-row tiles at any row count); a token's bits still do
-    not depend on the batch: W = 384 and W = 512 refill runs and a W = 448
-    no-refill run of the same requests agree bit for bit."""
+    persistent GEMM, its tile height chosen by the row count); a token's bits
+    still do not depend on the batch: W = 384 and W = 512 refill runs and a
+    W = 448 no-refill run of the same requests agree bit for bit."""
     from continuous_depth_batching_gb300 import binding
     shape = _shape(r_max=5)
     wts = make_weights(shape)

@@ -2,8 +2,8 @@
 
 Checks every epilogue (store, residual add, SwiGLU), every tensor-core tiling
 (decode: 64-, 128- or 256-row tiles with split-K fixed by the weight shape;
-prefill: 128- and 256-row tiles; wide decode: 128-row tiles, 64 for narrow
-weights),
+prefill: 128- and 256-row tiles; wide decode: 128-, 192- or 256-row tiles
+by the batch, 64 for narrow weights),
 ragged N and K tails, the split-K shapes of the Ouro-shaped core, agreement
 with the CUDA-core kernel, and that a row's result does not depend on how
 many other rows are in the batch (bit-exact).
@@ -58,7 +58,7 @@ def rnd(*shape, std=1.0, seed=0):
 
 
 SHAPES = [(5, 256, 192), (7, 200, 200), (64, 6144, 2048), (64, 2048, 5632), (33, 384, 1000), (300, 384, 256),
-          (100, 6144, 2048), (200, 2048, 5632)]
+          (100, 6144, 2048), (200, 2048, 5632), (500, 6144, 320), (700, 6144, 200)]
 
 
 @pytest.mark.parametrize("rows,N,K", SHAPES)
@@ -103,10 +103,12 @@ def test_matches_cuda_core_kernel(L):
 def test_row_result_independent_of_batch(L, N, K, tiling):
     # Decode tiling: 200 rows run on 256-row tiles, 1-64 rows on 64-row tiles
     # and 100 on 128-row tiles; the split count is the same for all of them.
-    rows = 200 if tiling == 0 else 300
+    # Wide tiling, N = 6144 (48 feature tiles): 700 rows on 256-row tiles,
+    # 500 on 192-row tiles, up to 384 on 128-row tiles; N = 2048: 64-row tiles.
+    rows = 200 if tiling == 0 else 700
     A = rnd(rows, K, seed=8)
     W = rnd(N, K, std=1.0 / np.sqrt(K), seed=9)
     full, _ = run(L, 0, tiling, A, W, a_rows=rows)
-    for r in (1, 17, 64, 100):
+    for r in (1, 17, 64, 100) + ((300, 500) if tiling == 3 else ()):
         part, _ = run(L, 0, tiling, A[:r].contiguous(), W, a_rows=rows)
         assert (part == full[:r]).all().item(), "row results must not depend on batch size"
