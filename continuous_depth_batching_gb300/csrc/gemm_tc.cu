@@ -328,7 +328,9 @@ __global__ void __launch_bounds__(128, DEEP ? 1 : 2)
 // accumulator buffers alternate between tiles, so the epilogue of one tile
 // overlaps the main loop of the next: the MMA warp waits for `tempty[b]`
 // (all four epilogue warps done with buffer b) before reusing it, the
-// epilogue warps wait for `tfull[b]` (the tile's last MMA committed).  An
+// epilogue warps wait for `tfull[b]` (the tile's last MMA committed).  When
+// the grid covers every tile once, buffer 1 is never used and only one is
+// allocated, which lets a SwiGLU tile of 192 or 256 rows fit TMEM.  An
 // epilogue warp reads the TMEM lane quadrant its warp index selects
 // (warp % 4), i.e. output features n0 + 32 * (warp % 4) + lane.
 // ---------------------------------------------------------------------------
@@ -339,10 +341,13 @@ struct PfCfg {
   static constexpr int STAGE = A_BYTES * (SW ? 2 : 1) + B_BYTES;
   static constexpr int STAGES = (196 * 1024) / STAGE > 8 ? 8 : (196 * 1024) / STAGE;
   static constexpr int ACC = BN * (SW ? 2 : 1);  // TMEM columns of one tile's accumulators
-  // Two buffers; an allocation is a power of two of at least 32 columns.
-  static constexpr int TMEM_COLS = 2 * ACC <= 128 ? 128 : 2 * ACC <= 256 ? 256 : 512;
+  // TMEM columns to allocate (a power of two, at least 32): one buffer when
+  // the grid covers every tile once, two when CTAs walk several tiles; 0 when
+  // two buffers do not fit, so that such a tile runs in a single pass only.
+  static constexpr int TMEM_ONE = ACC <= 32 ? 32 : ACC <= 64 ? 64 : ACC <= 128 ? 128 : ACC <= 256 ? 256 : 512;
+  static constexpr int TMEM_TWO = 2 * ACC <= 128 ? 128 : 2 * ACC <= 256 ? 256 : 2 * ACC <= 512 ? 512 : 0;
   static constexpr int SMEM = STAGES * STAGE + 1024 + 256;
-  static_assert(TMEM_COLS <= 512, "two accumulator buffers must fit TMEM");
+  static_assert(ACC <= 512, "one accumulator buffer must fit TMEM");
 };
 
 __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
@@ -368,6 +373,11 @@ __global__ void __launch_bounds__(192, 1)
   const int tiles_n = (N + BM - 1) / BM;
   const int tiles = tiles_n * ((rows + BN - 1) / BN);
   const int KT = (K + BK - 1) / BK;
+  const uint32_t tmem_cols = tiles <= (int)gridDim.x ? C::TMEM_ONE : C::TMEM_TWO;
+  if (tmem_cols == 0) {  // uniform over the grid: nothing allocated or waited on yet
+    if (threadIdx.x == 0) atomicOr(status, kStatusBadLaunch);
+    return;
+  }
 
   if (threadIdx.x == 0) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(&tmW) : "memory");
@@ -386,7 +396,7 @@ __global__ void __launch_bounds__(192, 1)
   }
   if (warp == 0) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(su32(tmem_slot)),
-                 "r"(C::TMEM_COLS));
+                 "r"(tmem_cols));
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
   }
   fence_before();
@@ -481,8 +491,7 @@ __global__ void __launch_bounds__(192, 1)
   fence_before();
   __syncthreads();
   if (fail && lane == 0) atomicOr(status, kStatusTimeout);
-  if (warp == 0)
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(C::TMEM_COLS));
+  if (warp == 0) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(tmem_cols));
 }
 
 // ---------------------------------------------------------------------------
@@ -689,6 +698,9 @@ int launch_gemm_tc(cudaStream_t s, int epi, const __nv_bfloat16* A, int lda, int
           break;
         }
     }
+    // SwiGLU (two accumulators per tile) takes 192- and 256-row tiles only
+    // in one wave, where each CTA needs one accumulator buffer.
+    const int sbn = tiling == kTileWide && !narrow ? bn : 128;
 #define CDB_PF(E)                                                                                          \
   ok = bn == 64    ? tc::launch_pf<64, E>(s, A, lda, a_rows, W, W2, N, K, rows, Cf, Ct, ldc, sm, status)  \
        : bn == 192 ? tc::launch_pf<192, E>(s, A, lda, a_rows, W, W2, N, K, rows, Cf, Ct, ldc, sm, status) \
@@ -698,7 +710,11 @@ int launch_gemm_tc(cudaStream_t s, int epi, const __nv_bfloat16* A, int lda, int
       case kEpiStore: CDB_PF(kEpiStore) break;
       case kEpiResid: CDB_PF(kEpiResid) break;
 #undef CDB_PF
-      default: ok = tc::launch_pf<128, kEpiSwiglu>(s, A, lda, a_rows, W, W2, N, K, rows, Cf, Ct, ldc, sm, status); break;
+      default:
+        ok = sbn == 192   ? tc::launch_pf<192, kEpiSwiglu>(s, A, lda, a_rows, W, W2, N, K, rows, Cf, Ct, ldc, sm, status)
+             : sbn == 256 ? tc::launch_pf<256, kEpiSwiglu>(s, A, lda, a_rows, W, W2, N, K, rows, Cf, Ct, ldc, sm, status)
+                          : tc::launch_pf<128, kEpiSwiglu>(s, A, lda, a_rows, W, W2, N, K, rows, Cf, Ct, ldc, sm, status);
+        break;
     }
   }
   if (!ok) return -1;

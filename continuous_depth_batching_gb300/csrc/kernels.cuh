@@ -43,7 +43,8 @@ enum : int {
   kStatusBadToken = 4,
   kStatusBadRow = 8,
   kStatusNaN = 16,
-  kStatusTimeout = 32,  // a bounded wait inside a kernel expired
+  kStatusTimeout = 32,   // a bounded wait inside a kernel expired
+  kStatusBadLaunch = 64, // a kernel was launched in a shape it does not support
 };
 // The status area is kStatusBytes of zeroed device memory: word 0 holds the
 // bits above; words kWorkCounter and kWorkCounter + 1 are the work queue of

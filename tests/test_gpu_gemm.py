@@ -75,7 +75,8 @@ def test_store_and_residual(L, rows, N, K, tiling):
     assert (Cr.double() - (ref + C0.double())).abs().max().item() <= TOL
 
 
-@pytest.mark.parametrize("rows,N,K", [(5, 256, 192), (64, 5632, 2048), (200, 300, 128)])
+@pytest.mark.parametrize("rows,N,K", [(5, 256, 192), (64, 5632, 2048), (200, 300, 128), (400, 5632, 256),
+                                      (700, 5632, 192), (2000, 5632, 128)])
 @pytest.mark.parametrize("tiling", [0, 1, 3])
 def test_swiglu(L, rows, N, K, tiling):
     import torch
@@ -111,4 +112,18 @@ def test_row_result_independent_of_batch(L, N, K, tiling):
     full, _ = run(L, 0, tiling, A, W, a_rows=rows)
     for r in (1, 17, 64, 100) + ((300, 500) if tiling == 3 else ()):
         part, _ = run(L, 0, tiling, A[:r].contiguous(), W, a_rows=rows)
+        assert (part == full[:r]).all().item(), "row results must not depend on batch size"
+
+
+def test_swiglu_row_result_independent_of_batch(L):
+    # Wide tiling, N = 5632 (44 feature tiles): 700 rows run in one wave of
+    # 256-row tiles, 400 of 192-row tiles, up to 384 rows of 128-row tiles
+    # (one accumulator buffer per CTA each time).
+    K, N, rows = 2048, 5632, 700
+    A = rnd(rows, K, seed=10)
+    W = rnd(N, K, std=1.0 / np.sqrt(K), seed=11)
+    W2 = rnd(N, K, std=1.0 / np.sqrt(K), seed=12)
+    _, full = run(L, 2, 3, A, W, W2, a_rows=rows)
+    for r in (1, 100, 300, 400):
+        _, part = run(L, 2, 3, A[:r].contiguous(), W, W2, a_rows=rows)
         assert (part == full[:r]).all().item(), "row results must not depend on batch size"
