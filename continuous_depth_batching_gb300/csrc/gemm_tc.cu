@@ -683,23 +683,30 @@ int launch_gemm_tc(cudaStream_t s, int epi, const __nv_bfloat16* A, int lda, int
     const bool wide = tiling == kTilePrefill && rows > 128;
     // Wide decode batches, narrow weights (fewer than 32 tiles of 128
     // features: the O and down projections): 64-row tiles, so the tiles
-    // outnumber the SMs.  Other wide decode GEMMs: the smallest of 128, 192
-    // and 256 rows whose tiles fit one wave of CTAs (else 128), so that each
-    // weight tile is read by fewer CTAs.  Without split-K a row's result is
-    // the same for any tile height.
+    // outnumber the SMs.  Other wide decode GEMMs: 128, 192 or 256 rows,
+    // whichever minimises waves x bytes per k-slab of a tile (128 weight
+    // rows, 256 for SwiGLU, plus the tile's activation rows), since a CTA
+    // streams a tile's slabs through a ring of fixed size; the smallest on a
+    // tie.  SwiGLU takes 192 or 256 rows only in one wave, where each CTA
+    // needs one accumulator buffer.  Without split-K a row's result is the
+    // same for any tile height.
     const int sm = sm_count();
     const long long tiles_n = (N + tc::BM - 1) / tc::BM;
     const bool narrow = tiling == kTileWide && tiles_n < 32;
     int bn = wide ? 256 : narrow ? 64 : 128;
     if (tiling == kTileWide && !narrow) {
-      for (int b : {128, 192, 256})
-        if (tiles_n * ((rows + b - 1) / b) <= sm) {
+      const int wrows = epi == kEpiSwiglu ? 2 * tc::BM : tc::BM;
+      long long best = -1;
+      for (int b : {128, 192, 256}) {
+        const long long waves = (tiles_n * ((rows + b - 1) / b) + sm - 1) / sm;
+        if (epi == kEpiSwiglu && b > 128 && waves > 1) continue;
+        const long long cost = waves * (wrows + b);
+        if (best < 0 || cost < best) {
+          best = cost;
           bn = b;
-          break;
         }
+      }
     }
-    // SwiGLU (two accumulators per tile) takes 192- and 256-row tiles only
-    // in one wave, where each CTA needs one accumulator buffer.
     const int sbn = tiling == kTileWide && !narrow ? bn : 128;
 #define CDB_PF(E)                                                                                          \
   ok = bn == 64    ? tc::launch_pf<64, E>(s, A, lda, a_rows, W, W2, N, K, rows, Cf, Ct, ldc, sm, status)  \

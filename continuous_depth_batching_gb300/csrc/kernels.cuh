@@ -231,8 +231,8 @@ __device__ __forceinline__ void rope_pair(float a, float b, float2 cs, float& lo
 // Tilings: kTileSplit = 64-row tiles with split-K (decode batches below the
 // wide threshold); kTilePrefill = persistent, 256-row tiles (128 for SwiGLU)
 // when rows > 128; kTileWide = persistent, no split-K (wide decode batches:
-// 64-row tiles for narrow weights, else 128, 192 or 256 rows, the smallest
-// whose tiles fit one wave).
+// 64-row tiles for narrow weights, else 128, 192 or 256 rows by waves x
+// operand bytes per tile).
 enum GemmTiling { kTileSplit = 0, kTilePrefill = 1, kTileWide = 2 };
 int gemm_tc_splits(int N, int K, bool decode);
 int launch_gemm_tc(cudaStream_t s, int epi, const __nv_bfloat16* A, int lda, int a_rows,

@@ -27,9 +27,9 @@ extern "C" {
  *   tiling 2: the CUDA-core kernel (fp32 FMA), for comparison
  *   tiling 3: tensor cores, persistent tiles at any row count, no split
  *             (what engines of 384 or more slots run in decode): 64 rows for
- *             weights of fewer than 32 tiles of 128 features; else the
- *             smallest of 128, 192 and 256 rows whose tiles fit one wave of
- *             CTAs, 128 when none does
+ *             weights of fewer than 32 tiles of 128 features; else 128, 192
+ *             or 256 rows, whichever needs the fewest waves of CTAs times
+ *             operand bytes per tile (SwiGLU: above 128 only in one wave)
  * a_rows: rows allocated in A (>= rows).  ws: device memory of at least
  * cdb_test_gemm_ws_bytes() bytes: the kernel's status word, then the split-K
  * partials.  stream: cudaStream_t or NULL.

@@ -104,8 +104,10 @@ def test_matches_cuda_core_kernel(L):
 def test_row_result_independent_of_batch(L, N, K, tiling):
     # Decode tiling: 200 rows run on 256-row tiles, 1-64 rows on 64-row tiles
     # and 100 on 128-row tiles; the split count is the same for all of them.
-    # Wide tiling, N = 6144 (48 feature tiles): 700 rows on 256-row tiles,
-    # 500 on 192-row tiles, up to 384 on 128-row tiles; N = 2048: 64-row tiles.
+    # Wide tiling, N = 6144 (48 feature tiles, one wave): 700 rows on 256-row
+    # tiles, 500 on 192-row tiles, up to 384 on 128-row tiles; N = 49152
+    # (several waves): 256 rows at 500 and 700, 192 at 300, 128 up to 100;
+    # N = 2048: 64-row tiles.
     rows = 200 if tiling == 0 else 700
     A = rnd(rows, K, seed=8)
     W = rnd(N, K, std=1.0 / np.sqrt(K), seed=9)
