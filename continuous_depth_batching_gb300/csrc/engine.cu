@@ -24,7 +24,7 @@
 namespace cdb {
 
 static constexpr int kRing = 8;           // lookahead flag ring (core steps)
-static constexpr int kWideBatch = 384;    // engines with at least this many slots skip split-K
+static constexpr int kWideBatch = 384;    // engines with at least this many slots split only narrow weights
 static constexpr size_t kAlign = 256;
 static constexpr size_t kStageSeg = 1 << 20;  // pinned upload segment
 static constexpr int kStageSegs = 8;
@@ -109,8 +109,9 @@ static bool plan_layout(const cdb_model_desc* m, const cdb_sched_cfg* c, Layout*
   L->part_o = take(W * H * L->max_splits * hd * 4);
   L->part_ml = take(W * H * L->max_splits * 2 * 4);
   // Split-K partials of one decode GEMM ([split][row][ldp], ldp <= max(3d, 2f)).
-  // Split-K partials exist only for engines below kWideBatch slots.
-  L->gpart_floats = W < kWideBatch ? (size_t)kGemmMaxSplits * W * std::max(3 * d, 2 * f) : 64;
+  // Split-K partials: every decode projection below kWideBatch slots, the
+  // narrow weights (at most kWideMaxSplits splits) from kWideBatch on.
+  L->gpart_floats = (size_t)(W < kWideBatch ? kGemmMaxSplits : kWideMaxSplits) * W * std::max(3 * d, 2 * f);
   L->gpart = take(L->gpart_floats * 4);
   L->total = o;
   return true;
@@ -328,18 +329,19 @@ class GpuExecutor : public Executor {
     const double es = sizeof(T), nw = W2 ? 2.0 : 1.0;
     const int h = prof_begin(x, decode_tiles_ ? 1 : 4);
     int ns = -1;
-    // Decode tiling (64-row tiles, split-K fixed by the weight shape) for
-    // engines of fewer than kWideBatch slots; wider engines run every
-    // projection on the persistent kernel without split partials, whose
-    // traffic grows with the rows (about 200 MB per Ouro-shaped layer at 512
-    // rows).  Either way a row's result does not depend on the other rows.
+    // Decode tiling (split-K fixed by the weight shape) for engines of fewer
+    // than kWideBatch slots; wider engines split only the narrow weights (at
+    // most kWideMaxSplits) and run the others on the persistent kernel
+    // without split partials, whose traffic grows with the rows (about 200 MB
+    // per Ouro-shaped layer at 512 rows with decode splits).  Either way a
+    // row's result does not depend on the other rows.
     const bool split_tiles = decode_tiles_ && x->c.W < kWideBatch;
     const int tiling = split_tiles ? kTileSplit : decode_tiles_ ? kTileWide : kTilePrefill;
+    float* const gp = parts && decode_tiles_ ? at<float>(x, x->L.gpart) : nullptr;
     if (sizeof(T) == 2)
       ns = launch_gemm_tc(x->cs, epi, (const __nv_bfloat16*)A, lda, x->L.R, (const __nv_bfloat16*)W,
-                          (const __nv_bfloat16*)W2, N, K, rows, Cf, (__nv_bfloat16*)Ct, ldc, tiling,
-                          parts && split_tiles ? at<float>(x, x->L.gpart) : nullptr, x->L.gpart_floats,
-                          at<int>(x, x->L.status));
+                          (const __nv_bfloat16*)W2, N, K, rows, Cf, (__nv_bfloat16*)Ct, ldc, tiling, gp,
+                          x->L.gpart_floats, at<int>(x, x->L.status));
     if (ns < 0) {
       launch_gemm<T>(x->cs, epi, A, lda, (const T*)W, (const T*)W2, N, K, rows, Cf, Ct, ldc);
       ns = 0;
@@ -347,9 +349,8 @@ class GpuExecutor : public Executor {
       // Step-delta timing: the same launch again writes the same partials
       // (or the same stored output); an in-place residual is not repeated.
       launch_gemm_tc(x->cs, epi, (const __nv_bfloat16*)A, lda, x->L.R, (const __nv_bfloat16*)W,
-                     (const __nv_bfloat16*)W2, N, K, rows, Cf, (__nv_bfloat16*)Ct, ldc, tiling,
-                     parts && split_tiles ? at<float>(x, x->L.gpart) : nullptr, x->L.gpart_floats,
-                     at<int>(x, x->L.status));
+                     (const __nv_bfloat16*)W2, N, K, rows, Cf, (__nv_bfloat16*)Ct, ldc, tiling, gp,
+                     x->L.gpart_floats, at<int>(x, x->L.status));
     }
     const double out_b = epi == kEpiSwiglu ? es : (epi == kEpiResid ? 8.0 : 4.0);
     prof_end(x, h, nw * N * (double)K * es + (double)rows * K * es + (double)rows * N * out_b,
@@ -1100,7 +1101,7 @@ size_t cdb_test_gemm_ws_bytes(int N, int K, int rows, int tiling, int epi) {
   if (N < 1 || K < 1 || rows < 0) return 0;
   (void)K;
   const size_t ldp = epi == 2 ? 2 * (size_t)N : (size_t)N;
-  return 256 + (tiling == 0 ? (size_t)kGemmMaxSplits * rows * ldp * 4 : 0);
+  return 256 + (tiling == 0 || tiling == 3 ? (size_t)kGemmMaxSplits * rows * ldp * 4 : 0);
 }
 
 int cdb_test_gemm(int epi, int tiling, const void* A, int lda, int a_rows, const void* W, const void* W2, int N,
@@ -1121,7 +1122,7 @@ int cdb_test_gemm(int epi, int tiling, const void* A, int lda, int a_rows, const
     const int ns = launch_gemm_tc(s, epi, (const __nv_bfloat16*)A, lda, a_rows, (const __nv_bfloat16*)W,
                                   (const __nv_bfloat16*)W2, N, K, rows, Cf, (__nv_bfloat16*)Ct, ldc,
                                   tiling == 0 ? kTileSplit : tiling == 1 ? kTilePrefill : kTileWide,
-                                  tiling == 0 ? parts : nullptr, (ws_bytes - 256) / 4, status);
+                                  tiling == 0 || tiling == 3 ? parts : nullptr, (ws_bytes - 256) / 4, status);
     if (ns < 0) return CDB_ERR_ARG;
     if (ns > 0) {
       if (epi == 2) launch_swiglu_combine<__nv_bfloat16>(s, parts, ns, rows, N, (__nv_bfloat16*)Ct);

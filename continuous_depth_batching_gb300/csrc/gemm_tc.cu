@@ -641,28 +641,61 @@ int gemm_tc_splits(int N, int K, bool decode) {
   return s < 1 ? 1 : s;
 }
 
+// Split count of a narrow weight (fewer than 32 tiles of 128 features) in a
+// wide decode batch: about one CTA per SM for two 256-row activation tiles,
+// at least four K slabs per split, at most kWideMaxSplits.  Depends only on
+// the weight shape (and the device), never on the number of rows.
+static int gemm_tc_wide_splits(int N, int K) {
+  const int tiles = (N + tc::BM - 1) / tc::BM;
+  const int KT = (K + tc::BK - 1) / tc::BK;
+  int s = sm_count() / (2 * tiles);
+  if (s > KT / 4) s = KT / 4;
+  if (s > kWideMaxSplits) s = kWideMaxSplits;
+  return s < 1 ? 1 : s;
+}
+
 int launch_gemm_tc(cudaStream_t s, int epi, const __nv_bfloat16* A, int lda, int a_rows, const __nv_bfloat16* W,
                    const __nv_bfloat16* W2, int N, int K, int rows, float* Cf, __nv_bfloat16* Ct, int ldc,
                    int tiling, float* ws, size_t ws_floats, int* status) {
   if (rows <= 0) return 0;
-  const bool decode = tiling == kTileSplit;
   if ((K * 2) % 16 != 0 || (lda * 2) % 16 != 0 || rows > a_rows) return -1;
-  int splits = ws ? gemm_tc_splits(N, K, decode) : 1;
+  const int sm = sm_count();
+  const long long tiles_n = (N + tc::BM - 1) / tc::BM;
+  // Narrow weights in wide decode batches (the O and down projections):
+  // their few feature tiles leave a CTA a long K loop of small tiles, so
+  // they split K instead (consumers fold the partials, as for decode).
+  const bool narrow = tiling == kTileWide && tiles_n < 32;
+  int splits = !ws ? 1 : tiling == kTileSplit ? gemm_tc_splits(N, K, true) : narrow ? gemm_tc_wide_splits(N, K) : 1;
   const size_t ldp = epi == kEpiSwiglu ? 2 * (size_t)N : (size_t)N;
   // Consumers fold partials four columns at a time.
   if (splits > 1 && ((size_t)splits * rows * ldp > ws_floats || N % 4 != 0)) splits = 1;
   float* P = splits > 1 ? ws : nullptr;
+  const bool decode = tiling == kTileSplit || (narrow && P);
   bool ok;
   if (decode) {
-    // Activation tile height: the smallest of 64, 128 and 256 rows that holds
-    // the batch, while the grid stays one wave (else 128-row tiles).  The
-    // split count comes from the weight shape alone and a tile's height does
-    // not change the order in which a row's products are summed, so a row's
-    // result is the same for every batch size.
-    const int sm = sm_count();
-    const long long one_wave = (long long)((N + tc::BM - 1) / tc::BM) * splits;
+    // Activation tile height.  Decode tiling: the smallest of 64, 128 and
+    // 256 rows that holds the batch, while the grid stays one wave (else
+    // 128-row tiles).  Split narrow weights of wide batches: 64, 128 or 256
+    // rows, whichever minimises waves x bytes per k-slab of a tile (weight
+    // rows plus activation rows; the smallest on a tie).  The split count
+    // comes from the weight shape alone and a tile's height does not change
+    // the order in which a row's products are summed, so a row's result is
+    // the same for every batch size.
+    const long long one_wave = tiles_n * splits;
     int bn = rows <= 64 ? 64 : rows <= 128 ? 128 : rows <= 256 ? 256 : 128;
     if (bn == 256 && one_wave > sm) bn = 128;
+    if (tiling == kTileWide) {
+      const int wrows = epi == kEpiSwiglu ? 2 * tc::BM : tc::BM;
+      long long best = -1;
+      for (int b : {64, 128, 256}) {
+        const long long waves = (one_wave * ((rows + b - 1) / b) + sm - 1) / sm;
+        const long long cost = waves * (wrows + b);
+        if (best < 0 || cost < best) {
+          best = cost;
+          bn = b;
+        }
+      }
+    }
 #define CDB_BN(B)                                                                                                \
   switch (epi) {                                                                                                 \
     case kEpiStore: ok = tc::launch_bn<B, kEpiStore>(s, A, lda, a_rows, W, W2, N, K, rows, splits, Cf, Ct, ldc, P, status, sm); break; \
@@ -681,18 +714,14 @@ int launch_gemm_tc(cudaStream_t s, int epi, const __nv_bfloat16* A, int lda, int
     // Persistent: one CTA per SM, double-buffered accumulators.  Prefill:
     // 256-row tiles where one accumulator fits, 128-row tiles for SwiGLU.
     const bool wide = tiling == kTilePrefill && rows > 128;
-    // Wide decode batches, narrow weights (fewer than 32 tiles of 128
-    // features: the O and down projections): 64-row tiles, so the tiles
-    // outnumber the SMs.  Other wide decode GEMMs: 128, 192 or 256 rows,
-    // whichever minimises waves x bytes per k-slab of a tile (128 weight
-    // rows, 256 for SwiGLU, plus the tile's activation rows), since a CTA
-    // streams a tile's slabs through a ring of fixed size; the smallest on a
-    // tie.  SwiGLU takes 192 or 256 rows only in one wave, where each CTA
-    // needs one accumulator buffer.  Without split-K a row's result is the
-    // same for any tile height.
-    const int sm = sm_count();
-    const long long tiles_n = (N + tc::BM - 1) / tc::BM;
-    const bool narrow = tiling == kTileWide && tiles_n < 32;
+    // Wide decode batches, narrow weights without a split workspace: 64-row
+    // tiles, so the tiles outnumber the SMs.  Other wide decode GEMMs: 128,
+    // 192 or 256 rows, whichever minimises waves x bytes per k-slab of a tile
+    // (128 weight rows, 256 for SwiGLU, plus the tile's activation rows),
+    // since a CTA streams a tile's slabs through a ring of fixed size; the
+    // smallest on a tie.  SwiGLU takes 192 or 256 rows only in one wave,
+    // where each CTA needs one accumulator buffer.  Without split-K a row's
+    // result is the same for any tile height.
     int bn = wide ? 256 : narrow ? 64 : 128;
     if (tiling == kTileWide && !narrow) {
       const int wrows = epi == kEpiSwiglu ? 2 * tc::BM : tc::BM;

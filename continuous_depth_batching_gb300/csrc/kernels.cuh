@@ -173,8 +173,9 @@ void launch_gemm(cudaStream_t s, int epi, const T* A, int lda, const T* W, const
                  int K, int rows, float* Cf, T* Ct, int ldc);
 
 // ---- tensor-core GEMM (gemm_tc.cu), bf16 only ----
-// decode: 64-row tiles with
-// split-K; otherwise 128-row tiles, one split.  With ws (room for ws_floats)
+// kTileSplit: split-K fixed by the weight shape; kTileWide: split-K (at most
+// kWideMaxSplits, fixed by the weight shape) for narrow weights only;
+// kTilePrefill: one split.  With ws (room for ws_floats)
 // and more than one split, each split's fp32 partial goes to
 // ws[split][row][ldp] (ldp = N, or 2N for SwiGLU with the up projection at
 // +N) and the epilogue is left to the consumer (sum the partials in split
@@ -182,6 +183,7 @@ void launch_gemm(cudaStream_t s, int epi, const T* A, int lda, const T* W, const
 // when the epilogue was applied in place, -1 when the shape is unsupported.
 // a_rows: rows allocated in A (TMA bounds).
 constexpr int kGemmMaxSplits = 16;
+constexpr int kWideMaxSplits = 4;
 
 // Split-K partials of a GEMM output: P[split][row][ld] with split stride ss;
 // their sum in split order (the reduction every consumer uses, so a value is
@@ -230,9 +232,9 @@ __device__ __forceinline__ void rope_pair(float a, float b, float2 cs, float& lo
 
 // Tilings: kTileSplit = 64-row tiles with split-K (decode batches below the
 // wide threshold); kTilePrefill = persistent, 256-row tiles (128 for SwiGLU)
-// when rows > 128; kTileWide = persistent, no split-K (wide decode batches:
-// 64-row tiles for narrow weights, else 128, 192 or 256 rows by waves x
-// operand bytes per tile).
+// when rows > 128; kTileWide = wide decode batches: narrow weights split-K
+// (with a workspace), else persistent, no split, 128, 192 or 256 rows by
+// waves x operand bytes per tile.
 enum GemmTiling { kTileSplit = 0, kTilePrefill = 1, kTileWide = 2 };
 int gemm_tc_splits(int N, int K, bool decode);
 int launch_gemm_tc(cudaStream_t s, int epi, const __nv_bfloat16* A, int lda, int a_rows,

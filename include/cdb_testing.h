@@ -25,11 +25,13 @@ extern "C" {
  *   tiling 1: tensor cores, persistent prefill tiles (256 rows, 128 for
  *             SwiGLU, when rows > 128; else 128), no split
  *   tiling 2: the CUDA-core kernel (fp32 FMA), for comparison
- *   tiling 3: tensor cores, persistent tiles at any row count, no split
- *             (what engines of 384 or more slots run in decode): 64 rows for
- *             weights of fewer than 32 tiles of 128 features; else 128, 192
- *             or 256 rows, whichever needs the fewest waves of CTAs times
- *             operand bytes per tile (SwiGLU: above 128 only in one wave)
+ *   tiling 3: what engines of 384 or more slots run in decode: weights of
+ *             fewer than 32 tiles of 128 features split K (at most 4 splits,
+ *             fixed by N and K; partials folded as for tiling 0) on 64-, 128-
+ *             or 256-row tiles; other weights run persistent tiles without
+ *             split, 128, 192 or 256 rows, whichever needs the fewest waves
+ *             of CTAs times operand bytes per tile (SwiGLU: above 128 only in
+ *             one wave)
  * a_rows: rows allocated in A (>= rows).  ws: device memory of at least
  * cdb_test_gemm_ws_bytes() bytes: the kernel's status word, then the split-K
  * partials.  stream: cudaStream_t or NULL.

@@ -3,7 +3,7 @@
 Checks every epilogue (store, residual add, SwiGLU), every tensor-core tiling
 (decode: 64-, 128- or 256-row tiles with split-K fixed by the weight shape;
 prefill: 128- and 256-row tiles; wide decode: 128-, 192- or 256-row tiles
-by the batch, 64 for narrow weights),
+by the batch, split-K on 64- to 256-row tiles for narrow weights),
 ragged N and K tails, the split-K shapes of the Ouro-shaped core, agreement
 with the CUDA-core kernel, and that a row's result does not depend on how
 many other rows are in the batch (bit-exact).
@@ -58,7 +58,7 @@ def rnd(*shape, std=1.0, seed=0):
 
 
 SHAPES = [(5, 256, 192), (7, 200, 200), (64, 6144, 2048), (64, 2048, 5632), (33, 384, 1000), (300, 384, 256),
-          (100, 6144, 2048), (200, 2048, 5632), (500, 6144, 320), (700, 6144, 200)]
+          (100, 6144, 2048), (200, 2048, 5632), (500, 6144, 320), (700, 6144, 200), (333, 1024, 1000)]
 
 
 @pytest.mark.parametrize("rows,N,K", SHAPES)
@@ -76,7 +76,7 @@ def test_store_and_residual(L, rows, N, K, tiling):
 
 
 @pytest.mark.parametrize("rows,N,K", [(5, 256, 192), (64, 5632, 2048), (200, 300, 128), (400, 5632, 256),
-                                      (700, 5632, 192), (2000, 5632, 128)])
+                                      (700, 5632, 192), (2000, 5632, 128), (200, 512, 1024)])
 @pytest.mark.parametrize("tiling", [0, 1, 3])
 def test_swiglu(L, rows, N, K, tiling):
     import torch
@@ -107,7 +107,7 @@ def test_row_result_independent_of_batch(L, N, K, tiling):
     # Wide tiling, N = 6144 (48 feature tiles, one wave): 700 rows on 256-row
     # tiles, 500 on 192-row tiles, up to 384 on 128-row tiles; N = 49152
     # (several waves): 256 rows at 500 and 700, 192 at 300, 128 up to 100;
-    # N = 2048: 64-row tiles.
+    # N = 2048 (narrow, four K splits): 256-row tiles at 500, 128 at 700.
     rows = 200 if tiling == 0 else 700
     A = rnd(rows, K, seed=8)
     W = rnd(N, K, std=1.0 / np.sqrt(K), seed=9)
