@@ -788,6 +788,24 @@ class GpuExecutor : public Executor {
   bool repeat(int cls) const { return x_->in_core && x_->prof_repeat == cls; }
 };
 
+// Names of the device status bits that are set, for the error message.
+static std::string status_text(int st) {
+  static const struct {
+    int bit;
+    const char* name;
+  } names[] = {{kStatusBadBlock, "block table entry out of range"},
+               {kStatusBadDepth, "loop depth out of range"},
+               {kStatusBadToken, "token id out of range"},
+               {kStatusBadRow, "row, slot or position out of range"},
+               {kStatusNaN, "non-finite value"},
+               {kStatusTimeout, "bounded wait expired"},
+               {kStatusBadLaunch, "unsupported launch shape"}};
+  std::string out;
+  for (const auto& n : names)
+    if (st & n.bit) out += (out.empty() ? "" : "; ") + std::string(n.name);
+  return out.empty() ? "unknown" : out;
+}
+
 static int check_status(cdb_ctx* x) {
   int st = 0;
   cudaError_t e = cudaMemcpyAsync(&st, at<int>(x, x->L.status), 4, cudaMemcpyDeviceToHost, x->cs);
@@ -796,7 +814,7 @@ static int check_status(cdb_ctx* x) {
   e = cudaStreamSynchronize(x->cs);
   if (e != cudaSuccess) return cuda_fail(x, e, "cudaStreamSynchronize");
   if (st != 0) {
-    x->err = "device bounds check failed (status " + std::to_string(st) + ")";
+    x->err = "device bounds check failed (status " + std::to_string(st) + ": " + status_text(st) + ")";
     x->dead = true;
     return CDB_ERR_DEVICE_BOUNDS;
   }
